@@ -1,0 +1,395 @@
+"""Pins for the CPU oracle: values printed on the pages, closed forms,
+invariants and brute force on tiny inputs.  None of these re-derives a value
+from the oracle's own formula; each would fail under a plausible slip (a
+dropped bias term, a swapped p/q, an off-by-one position, a missing +R)."""
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def gold(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+def uni24(rng, shape):
+    return rng.integers(0, 1 << 24, size=shape).astype(np.float64) * 2.0 ** -24
+
+
+# ---------------------------------------------------------------- Markov head
+
+def test_markov_two_token_toy():
+    g = gold("markov_two_token.json")
+    # V = 2, rank 1: E[A] = 1, W = (ln 9, 0): the previous token A adds ln 9 to A.
+    E = np.array([[1.0], [0.0]])
+    W = np.array([[math.log(9.0), 0.0]])
+    z = np.array(g["base_logits"]).reshape(1, 1, 2)
+    q = oracle.draft_distribution(z[:, 0, :], E, W, np.array([0]), 1.0)[0]
+    assert np.allclose(q, g["q_after"], atol=1e-12, rtol=0)
+    q0 = oracle.draft_distribution(z[:, 0, :], E, W, np.array([-1]), 1.0)[0]
+    assert np.allclose(q0, g["q_before"], atol=1e-15, rtol=0)
+    # The sampled token, its probability and the normaliser: closed forms.
+    for u, want in [(0.0, 0), (0.8999, 0), (0.9, 1), (0.99, 1)]:
+        tok, lse, qt = oracle.draft_sample(z, E, W, np.array([0]), np.array([[u]]), 1.0)
+        assert tok[0, 0] == want
+        assert abs(lse[0, 0] - math.log(10.0)) < 1e-12  # ln(e^{ln 9} + e^0)
+        assert abs(qt[0, 0] - (0.9 if want == 0 else 0.1)) < 1e-12
+
+
+def test_temperature_scales_logit_plus_bias():
+    E = np.array([[1.0], [0.0]])
+    W = np.array([[math.log(9.0), 0.0]])
+    z = np.zeros((1, 2))
+    for T in (0.5, 0.7, 2.0):
+        q = oracle.draft_distribution(z, E, W, np.array([0]), T)[0]
+        k = 9.0 ** (1.0 / T)
+        assert abs(q[0] - k / (k + 1.0)) < 1e-12
+
+
+def test_draft_feeds_previous_token_left_to_right():
+    # One-hot embedding (non-symmetric permutation) and a transition that
+    # strongly favours perm[prev]; base logits zero.  The draft must follow
+    # the chain anchor -> perm[anchor] -> perm[perm[anchor]] ...
+    V = 6
+    perm = np.array([3, 0, 5, 1, 2, 4])
+    E = np.eye(V)[[2, 0, 1, 5, 3, 4]]  # row v of E is one-hot at emb_idx[v]
+    emb_idx = np.argmax(E, axis=1)
+    W = np.full((V, V), -30.0)
+    for v in range(V):
+        W[emb_idx[v], perm[v]] = 30.0
+    G = 5
+    z = np.zeros((2, G, V))
+    u = np.full((2, G), 0.5)
+    tok, _, qt = oracle.draft_sample(z, E, W, np.array([1, 4]), u, 1.0)
+    for r, a0 in enumerate([1, 4]):
+        x = a0
+        for k in range(G):
+            x = perm[x]
+            assert tok[r, k] == x
+    assert np.all(qt > 1 - 1e-12)
+
+
+def test_anchor_minus_one_disables_first_bias():
+    E = np.array([[1.0], [0.0]])
+    W = np.array([[-50.0, 0.0]])
+    z = np.array([[[2.0, 0.0]]])
+    # with the anchor bias token 0 would be all but impossible
+    tok_b, _, _ = oracle.draft_sample(z, E, W, np.array([0]), np.array([[0.5]]), 1.0)
+    tok_n, _, _ = oracle.draft_sample(z, E, W, np.array([-1]), np.array([[0.5]]), 1.0)
+    assert tok_b[0, 0] == 1 and tok_n[0, 0] == 0
+
+
+def test_greedy_draft_lowest_index_on_ties():
+    z = np.array([[[1.0, 3.0, 3.0, 2.0], [5.0, 5.0, 0.0, 5.0]]])
+    E = np.zeros((4, 1))
+    W = np.zeros((1, 4))
+    tok, lse, qt = oracle.draft_sample(z, E, W, np.array([0]), np.zeros((1, 2)), 0.0)
+    assert tok.tolist() == [[1, 0]]
+    assert lse.tolist() == [[3.0, 5.0]] and qt.tolist() == [[1.0, 1.0]]
+
+
+# ---------------------------------------------------------------- inverse CDF
+
+def test_inverse_cdf_boundary_reading():
+    w = np.array([[1.0, 1.0, 1.0, 1.0]])
+    # smallest v with C_v > u * S: at u*S exactly on a boundary, the next token
+    assert oracle.inverse_cdf(w, np.array([0.25]))[0] == 1
+    assert oracle.inverse_cdf(w, np.array([0.25 - 2 ** -24]))[0] == 0
+    assert oracle.inverse_cdf(w, np.array([0.0]))[0] == 0
+    # zero-weight tokens are never drawn
+    w2 = np.array([[0.0, 2.0, 0.0, 0.0, 2.0, 0.0]])
+    got = [oracle.inverse_cdf(w2, np.array([u]))[0] for u in (0.0, 0.49, 0.5, 0.99)]
+    assert got == [1, 1, 4, 4]
+
+
+def test_inverse_cdf_brute_force_small_vocab():
+    rng = np.random.default_rng(7)
+    for V in range(1, 9):
+        for _ in range(20):
+            w = rng.integers(0, 5, size=V).astype(np.float64)
+            if w.sum() == 0:
+                w[rng.integers(V)] = 1.0
+            S = w.sum()
+            for k in range(0, 64):
+                u = k / 64.0
+                # explicit CDF table, integer arithmetic: first v with cum > u*S
+                want, cum = None, 0.0
+                for v in range(V):
+                    cum += w[v]
+                    if cum > u * S:
+                        want = v
+                        break
+                assert oracle.inverse_cdf(w[None, :], np.array([u]))[0] == want
+
+
+def test_softmax_two_token_closed_form():
+    rng = np.random.default_rng(3)
+    for _ in range(50):
+        a, b = rng.normal(0, 5, size=2)
+        e, lse = oracle.softmax_rows(np.array([[a, b]]))
+        want_lse = max(a, b) + math.log1p(math.exp(-abs(a - b)))
+        assert abs(lse[0] - want_lse) < 1e-12
+        p0 = math.exp(a - lse[0])
+        assert abs(p0 - 1.0 / (1.0 + math.exp(b - a))) < 1e-12
+
+
+# ---------------------------------------------------------------- confidence
+
+def test_confidence_closed_forms_and_indexing():
+    # d = 1, rank 1.  Feature vector [h_k ; E1[x_{k-1}]].
+    R, G, d, V = 1, 3, 1, 4
+    h = np.array([[[1.0], [0.0], [0.0]]])
+    E1 = np.array([[0.0], [1.0], [0.0], [2.0]])
+    w = np.array([math.log(3.0), -math.log(3.0)])
+    anchor = np.array([0])  # E1[0] = 0
+    tokens = np.array([[1, 3, 2]])  # x_1 = 1 (E1 = 1), x_2 = 3 (E1 = 2)
+    t = np.array([1.0, 1.0, 2.0])
+    c, a = oracle.confidence(h, w, E1, anchor, tokens, t)
+    # k=1: s = ln3 -> 0.75 ; k=2: s = -ln3 (E1[x_1]=1) -> 0.25 ;
+    # k=3: s = -2 ln3 (E1[x_2]=2), t=2 -> sigmoid(-ln3) = 0.25
+    assert np.allclose(c[0], [0.75, 0.25, 0.25], atol=1e-15)
+    assert np.allclose(a[0], [0.75, 0.1875, 0.046875], atol=1e-15)
+
+
+def test_survival_chain_page_values():
+    g = gold("survival_chain.json")
+    for case in g["cases"]:
+        c = np.array([[case["c1"]] + g["conditionals_after_first"]])
+        _, a = oracle.confidence(None, None, None, None, None, None, c_in=c)
+        assert np.allclose(a[0], case["a"], rtol=1e-14, atol=0)
+    g = gold("tutorial_worked_example.json")
+    _, a = oracle.confidence(None, None, None, None, None, None,
+                             c_in=np.array([g["confidences"]]))
+    assert np.allclose(a[0], g["survival_products"], rtol=1e-14, atol=0)
+
+
+def test_survival_never_increases():
+    rng = np.random.default_rng(11)
+    c = rng.uniform(0, 1, size=(64, 16))
+    c[:, 3] = 1.0  # c rounding to one
+    c[5, :] = 1.0
+    _, a = oracle.confidence(None, None, None, None, None, None, c_in=c)
+    assert np.all(np.diff(a, axis=1) <= 0)
+    assert np.all(a[5] == 1.0)
+
+
+# ---------------------------------------------------------------- scheduler
+
+def sps_from_cost_model(n, load=1.0):
+    g = gold("scheduler_cost_model.json")["T_ms"]
+    B = np.arange(n, dtype=np.float64)
+    T = g["const"] + (g["lin0"] + g["lin_load"] * load) * B + g["quad_load"] * load * B * B
+    return (1000.0 / T).astype(np.float32).astype(np.float64)
+
+
+def brute_force_best(a, sps):
+    """Enumerate every allocation l in {0..gamma}^R (prefixes per request);
+    Theta(l) = (R + sum of the first l_r survival values of each request)
+    * SPS[R + sum l].  Sums in the same 2^-40 integer units."""
+    R, G = a.shape
+    fx = oracle.to_fixed(a)
+    best, arg = None, []
+    for ell in itertools.product(range(G + 1), repeat=R):
+        s = sum(int(fx[r, :l].sum()) for r, l in enumerate(ell))
+        th = (float(R) + float(s) * 2.0 ** -40) * float(sps[R + sum(ell)])
+        if best is None or th > best:
+            best, arg = th, [ell]
+        elif th == best:
+            arg.append(ell)
+    return best, arg
+
+
+def random_survival(rng, R, G):
+    c = rng.uniform(0.05, 1.0, size=(R, G))
+    return np.cumprod(c, axis=1).astype(np.float32).astype(np.float64)
+
+
+def unimodal(theta):
+    i = int(np.argmax(theta))
+    return np.all(np.diff(theta[: i + 1]) > 0) and np.all(np.diff(theta[i:]) <= 0)
+
+
+@pytest.mark.parametrize("R,G", [(1, 4), (2, 3), (3, 2), (2, 4), (3, 3)])
+def test_scheduler_brute_force(R, G):
+    rng = np.random.default_rng(100 * R + G)
+    n_uni = 0
+    for trial in range(40):
+        a = random_survival(rng, R, G)
+        if trial % 2 == 0:
+            sps = sps_from_cost_model(R * (G + 1) + 1, load=rng.uniform(0.2, 30.0))
+        else:
+            sps = rng.uniform(1.0, 100.0, size=R * (G + 1) + 1)
+        best, args = brute_force_best(a, sps)
+        glob = oracle.schedule(a, sps, early_stop=False)
+        assert glob["theta"][glob["i_star"]] == best
+        if len(args) == 1:
+            assert tuple(glob["ell"].tolist()) == args[0]
+        es = oracle.schedule(a, sps, early_stop=True)
+        if unimodal(es["theta"]):
+            n_uni += 1
+            assert es["theta"][es["i_star"]] == best
+            assert es["i_star"] == glob["i_star"]
+        # prefix property: survival never increases within a request, so the
+        # chosen set is the first l_r positions of each request.
+        top = es["order"][: es["i_star"]]
+        for r in range(R):
+            js = sorted(int(o % G) for o in top if o // G == r)
+            assert js == list(range(len(js)))
+    assert n_uni > 0
+
+
+def test_scheduler_early_stop_differs_on_sawtooth():
+    # One request, four candidates of 0.9.  SPS dips at B = 2 then recovers:
+    # early stop keeps nothing, global search keeps all four.
+    a = np.array([[0.9, 0.81, 0.729, 0.6561]], dtype=np.float32).astype(np.float64)
+    sps = np.array([0.0, 100.0, 40.0, 60.0, 70.0, 80.0])
+    es = oracle.schedule(a, sps, early_stop=True)
+    gl = oracle.schedule(a, sps, early_stop=False)
+    assert es["ell"].tolist() == [0] and es["B"] == 1 and es["E"] == 1.0
+    assert gl["ell"].tolist() == [4] and gl["B"] == 5
+    assert abs(gl["E"] - (1.0 + a.sum())) < 1e-9
+
+
+def test_scheduler_plateau_stops():
+    # Throughput that stays flat is not rising: stop (strict comparison).
+    a = np.zeros((1, 3))
+    sps = np.full(5, 10.0)
+    es = oracle.schedule(a, sps, early_stop=True)
+    assert es["i_star"] == 0 and es["ell"].tolist() == [0]
+
+
+def test_scheduler_tie_order_request_then_position():
+    a = np.full((3, 2), 0.5)
+    sps = 1000.0 / (1.0 + 0.0 * np.arange(10))  # constant rate: only E matters
+    for i_cap, want in [(1, [1, 0, 0]), (2, [2, 0, 0]), (3, [2, 1, 0]), (5, [2, 2, 1])]:
+        out = oracle.schedule(a, sps, early_stop=False, max_B=3 + i_cap)
+        assert out["ell"].tolist() == want
+        assert out["row_off"].tolist() == [0, 1 + want[0], 2 + want[0] + want[1],
+                                            3 + sum(want)]
+
+
+def test_scheduler_sps_too_short_is_an_error():
+    with pytest.raises(ValueError):
+        oracle.schedule(np.full((2, 2), 0.5), np.ones(6), early_stop=True)
+
+
+def test_fixed_point_rounds_half_to_even():
+    u = 2.0 ** -40
+    assert oracle.to_fixed(np.array([0.5 * u, 1.5 * u, 2.5 * u, 1.0])).tolist() == \
+        [0, 2, 2, 1 << 40]
+
+
+# ---------------------------------------------------------------- verification
+
+def _two_token_step(q, p, n, rng):
+    """n independent one-position steps with draft q and target p (V = 2)."""
+    z = np.log(np.array(q)).reshape(1, 1, 2).repeat(n, axis=0)
+    E = np.zeros((2, 1))
+    W = np.zeros((1, 2))
+    anchor = np.zeros(n, dtype=np.int64)
+    tok, _, _ = oracle.draft_sample(z, E, W, anchor, uni24(rng, (n, 1)), 1.0)
+    target = np.tile(np.log(np.array(p)), (2 * n, 1))  # row 0: position 1, row 1: bonus
+    ell = np.ones(n, dtype=np.int64)
+    row_off = np.arange(n + 1, dtype=np.int64) * 2
+    out = oracle.verify(z, E, W, anchor, tok, 1.0, ell, row_off, target,
+                        uni24(rng, (n, 1)), uni24(rng, (n,)))
+    return tok, out
+
+
+@pytest.mark.parametrize("qi", [0, 1, 2, 3])
+def test_lossless_marginal_chi_square(qi):
+    g = gold("lossless_two_token.json")
+    p = np.array(g["p"])
+    q = np.array(g["q_cases"][qi])
+    n = g["trials"]
+    rng = np.random.default_rng(2024 + qi)
+    tok, out = _two_token_step(q, p, n, rng)
+    first = out["out_tokens"][:, 0]
+    counts = np.bincount(first, minlength=2).astype(np.float64)
+    expect = n * p
+    chi2 = float(np.sum((counts - expect) ** 2 / expect))
+    assert chi2 < 10.828  # chi-square, 1 dof, alpha = 1e-3
+    # acceptance rate equals sum_x min(p, q) within 4 sigma
+    acc = float(np.mean(out["n_acc"] == 1))
+    a_true = float(np.minimum(p, q).sum())
+    sd = math.sqrt(a_true * (1 - a_true) / n) + 1e-12
+    assert abs(acc - a_true) <= 4 * sd + 1e-12
+    # the failure mass is the complement, sum_x max(0, p - q)
+    assert abs((1 - acc) - float(np.maximum(0.0, p - q).sum())) <= 4 * sd + 1e-12
+    # emitted count: accepted -> bonus token too (2), rejected -> 1
+    assert np.all((out["out_tokens"][:, 1] >= 0) == (out["n_acc"] == 1))
+
+
+def test_identity_q_equals_p_accepts_everything():
+    rng = np.random.default_rng(5)
+    R, G, V = 8, 4, 16
+    z = rng.normal(0, 2, size=(R, G, V))
+    E = rng.normal(0, 0.3, size=(V, 3))
+    W = rng.normal(0, 0.3, size=(3, V))
+    anchor = rng.integers(0, V, size=R)
+    tok, _, _ = oracle.draft_sample(z, E, W, anchor, uni24(rng, (R, G)), 1.0)
+    # target row j = exactly the draft's logits for position j+1
+    target = np.zeros((R * (G + 1), V))
+    prev = anchor.copy()
+    for j in range(G):
+        target[np.arange(R) * (G + 1) + j] = z[:, j, :] + oracle.markov_bias(E, W, prev)
+        prev = tok[:, j]
+    target[np.arange(R) * (G + 1) + G] = rng.normal(0, 2, size=(R, V))
+    ell = np.full(R, G)
+    row_off = np.arange(R + 1) * (G + 1)
+    out = oracle.verify(z, E, W, anchor, tok, 1.0, ell, row_off, target,
+                        uni24(rng, (R, G)), uni24(rng, (R,)))
+    assert out["n_acc"].tolist() == [G] * R
+    assert np.all(out["out_tokens"][:, :G] == tok)
+    assert np.all(out["final_kind"] == 0)
+    # sum_x min(p, q) = 1 when q = p
+    q = oracle.draft_distribution(z[:, 0, :], E, W, anchor, 1.0)
+    assert np.allclose(np.minimum(q, q).sum(axis=1), 1.0, atol=1e-12)
+
+
+def test_greedy_verify_argmax_match():
+    V, G = 5, 3
+    z = np.zeros((3, G, V))
+    E = np.zeros((V, 1))
+    W = np.zeros((1, V))
+    anchor = np.zeros(3, dtype=np.int64)
+    tokens = np.array([[1, 2, 3], [1, 2, 3], [4, 4, 4]])
+    rows = []
+    # request 0: rows argmax 1, 2, 0 (mismatch at position 3), bonus unused
+    for am in (1, 2, 0, 4):
+        rows.append(np.eye(V)[am] * 3.0)
+    # request 1: all three match, bonus row argmax 0 (tie 0/3 -> lowest index)
+    for am in (1, 2, 3):
+        rows.append(np.eye(V)[am] * 3.0)
+    rows.append(np.array([7.0, 0.0, 0.0, 7.0, 0.0]))
+    # request 2: only two verified (l = 2); second mismatches
+    for am in (4, 1, 2):
+        rows.append(np.eye(V)[am] * 3.0)
+    target = np.array(rows)
+    ell = np.array([3, 3, 2])
+    row_off = np.array([0, 4, 8, 11])
+    out = oracle.verify(z, E, W, anchor, tokens, 0.0, ell, row_off, target,
+                        np.zeros((3, G)), np.zeros(3))
+    assert out["n_acc"].tolist() == [2, 3, 1]
+    assert out["out_tokens"].tolist() == [[1, 2, 0, -1], [1, 2, 3, 0], [4, 1, -1, -1]]
+
+
+def test_verify_rejection_never_accepts_zero_target_mass():
+    # p(x) = 0 for the drafted token: strict u < p/q never accepts, even u = 0
+    z = np.array([[[0.0, 0.0]]])
+    E = np.zeros((2, 1))
+    W = np.zeros((1, 2))
+    target = np.array([[0.0, -np.inf], [0.0, 0.0]])
+    out = oracle.verify(z, E, W, np.array([0]), np.array([[1]]), 1.0, np.array([1]),
+                        np.array([0, 2]), target, np.array([[0.0]]), np.array([0.7]))
+    assert out["n_acc"].tolist() == [0]
+    assert out["out_tokens"][0].tolist() == [0, -1]
