@@ -1,0 +1,308 @@
+// Device helpers and internal launch interfaces shared by the libdspark
+// kernels.  Nothing here is part of the C ABI.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dspark {
+
+// Vocabulary tile of the draft / final-sampling partial sums, and chunk of
+// the verification row pass.
+constexpr int kTileV = 256;
+constexpr int kChunkV = 4096;
+// Fixed-point fraction bits: weights relative to a tile's power-of-two
+// reference (each <= 1) are summed exactly as integers in units of 2^-kFixRel;
+// normalised weights (p, residual) in units of 2^-kFixAbs.
+constexpr int kFixRel = 40;
+constexpr int kFixAbs = 60;
+constexpr int kMaxGamma = 32;
+
+constexpr uint32_t kFlagTokenRange = 0x1u;
+constexpr uint32_t kFlagNonFinite = 0x2u;
+constexpr uint32_t kFlagRowRange = 0x4u;
+constexpr uint32_t kFlagSpsRange = 0x8u;
+
+// log2(e) as a double-float pair (hi = fp32 rounding, lo = remainder) so that
+// y * log2(e) / T carries no shared fp32 rounding of the constant.
+struct ScalePair {
+  float hi, lo;
+};
+
+__host__ inline ScalePair make_scale(double c) {
+  ScalePair s;
+  s.hi = (float)c;
+  s.lo = (float)(c - (double)s.hi);
+  return s;
+}
+
+__device__ __forceinline__ float scaled(float y, ScalePair s) {
+  return fmaf(y, s.hi, y * s.lo);
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T v);
+template <>
+__device__ __forceinline__ float to_f32<float>(float v) {
+  return v;
+}
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
+  return __bfloat162float(v);
+}
+
+template <typename T>
+__device__ __forceinline__ float ldf(const T* p, size_t i) {
+  return to_f32<T>(p[i]);
+}
+
+__device__ __forceinline__ void set_flag(uint32_t* status, uint32_t f) {
+  atomicOr(status, f);
+}
+
+// ---------------------------------------------------------------- reductions
+
+template <typename T>
+__device__ __forceinline__ T warp_sum(T v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// (value, index) arg-max with the lowest index winning ties.
+struct ArgMax {
+  float v;
+  int i;
+};
+
+__device__ __forceinline__ ArgMax better(ArgMax a, ArgMax b) {
+  if (b.v > a.v || (b.v == a.v && b.i < a.i)) return b;
+  return a;
+}
+
+__device__ __forceinline__ ArgMax warp_argmax(ArgMax a) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ArgMax b;
+    b.v = __shfl_xor_sync(0xffffffffu, a.v, o);
+    b.i = __shfl_xor_sync(0xffffffffu, a.i, o);
+    a = better(a, b);
+  }
+  return a;
+}
+
+// Block-wide reductions for blockDim.x a multiple of 32 (<= 1024).  `sh`
+// must hold 32 elements; every thread receives the result.
+template <typename T>
+__device__ T block_sum(T v, T* sh) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) sh[wid] = v;
+  __syncthreads();
+  T t = lane < nw ? sh[lane] : T(0);
+  return warp_sum(t);
+}
+
+__device__ inline float block_max(float v, float* sh) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_max(v);
+  __syncthreads();
+  if (lane == 0) sh[wid] = v;
+  __syncthreads();
+  float t = lane < nw ? sh[lane] : -INFINITY;
+  return warp_max(t);
+}
+
+__device__ inline ArgMax block_argmax(ArgMax a, ArgMax* sh) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  a = warp_argmax(a);
+  __syncthreads();
+  if (lane == 0) sh[wid] = a;
+  __syncthreads();
+  ArgMax t = lane < nw ? sh[lane] : ArgMax{-INFINITY, 0x7fffffff};
+  return warp_argmax(t);
+}
+
+__device__ inline int block_min_int(int v, int* sh) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();
+  if (lane == 0) sh[wid] = v;
+  __syncthreads();
+  int t = lane < nw ? sh[lane] : 0x7fffffff;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) t = min(t, __shfl_xor_sync(0xffffffffu, t, o));
+  return t;
+}
+
+__device__ inline int block_max_int(int v, int* sh) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();
+  if (lane == 0) sh[wid] = v;
+  __syncthreads();
+  int t = lane < nw ? sh[lane] : -0x7fffffff;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) t = max(t, __shfl_xor_sync(0xffffffffu, t, o));
+  return t;
+}
+
+// Inclusive block scan (Hillis-Steele over warps); `sh` holds 32 elements.
+template <typename T>
+__device__ T block_inclusive_scan(T v, T* sh) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    T n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  __syncthreads();
+  if (lane == 31) sh[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    T s = lane < nw ? sh[lane] : T(0);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      T n = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += n;
+    }
+    if (lane < nw) sh[lane] = s;
+  }
+  __syncthreads();
+  if (wid > 0) v += sh[wid - 1];
+  return v;
+}
+
+// ---------------------------------------------------------------- tracing
+// Kernel kinds, in the order of the names in trace.cu.
+enum KernelKind {
+  kKindBias = 0,
+  kKindDraftPartial,
+  kKindDraftFinish,
+  kKindConfidence,
+  kKindRank,
+  kKindSchedFinish,
+  kKindVerifyRows,
+  kKindVerifyDecide,
+  kKindFinalPartial,
+  kKindFinalPick,
+  kKindDraftFusedTc,
+  kKindCount
+};
+
+void trace_begin(int kind, cudaStream_t st);
+void trace_end(int kind, cudaStream_t st);
+
+// Every kernel launch: counted, and bracketed by trace events when tracing.
+#define DSPARK_LAUNCH(kind, st, ...)   \
+  do {                                 \
+    ::dspark::trace_begin((kind), (st)); \
+    __VA_ARGS__;                       \
+    ::dspark::trace_end((kind), (st));   \
+  } while (0)
+
+// ---------------------------------------------------------------- launchers
+// (defined in the kernel translation units; all enqueue on `st`)
+
+struct DraftArgs {
+  int R, gamma, V, r, dt;
+  float T;
+  const void* z;
+  const void* E;
+  const void* Wt;
+  const int32_t* anchor;
+  const float* u;
+  int32_t* tokens;
+  double* q_lse;
+  float* q_tok;
+  uint32_t* status;
+  float* bias;      // [R][V] scratch
+  double* part;     // [R][n_tiles] scratch (greedy: ArgMax pairs)
+};
+cudaError_t launch_draft(const DraftArgs& a, cudaStream_t st);
+
+struct ConfArgs {
+  int R, gamma, d, r, V, dt;
+  const void* h;
+  const float* w;
+  const void* E1;
+  const int32_t* anchor;
+  const int32_t* tokens;
+  const float* sts;
+  const float* c_in;
+  float* c_out;
+  float* a_out;
+  uint32_t* status;
+};
+cudaError_t launch_confidence(const ConfArgs& a, cudaStream_t st);
+
+struct SchedArgs {
+  int R, gamma, n_sps, early_stop, max_B;
+  const float* a;
+  const float* sps;
+  int32_t* ell;
+  int32_t* row_off;
+  int32_t* B_out;
+  double* E_out;
+  uint32_t* status;
+  int32_t* rank;      // [N] scratch
+  long long* sfix;    // [N] scratch: fixed-point value at sorted position
+  int32_t* sreq;      // [N] scratch: request id at sorted position
+};
+cudaError_t launch_schedule(const SchedArgs& a, cudaStream_t st);
+
+struct VerifyState {
+  int n_acc;
+  int mode;       // 0 bonus, 1 residual
+  int final_row;  // target row of the final draw
+  int prev;       // token before the rejected position (residual), -1 none
+  double Sp;      // sum_v exp(target_row / T) of the final row
+  double Sq;      // sum_v exp(y_draft) of the rejected position
+};
+
+struct VerifyArgs {
+  int R, gamma, V, r, dt;
+  float T;
+  const void* z;
+  const void* E;
+  const void* Wt;
+  const int32_t* anchor;
+  const int32_t* tokens;
+  const double* q_lse;
+  const float* q_tok;
+  const int32_t* ell;
+  const int32_t* row_off;
+  const void* target;
+  long long n_rows;
+  const float* u_acc;
+  const float* u_fin;
+  int32_t* n_acc;
+  int32_t* out_tokens;
+  double* p_lse;
+  uint32_t* status;
+  double* row_part;      // [R*(gamma+1)][n_chunks]
+  VerifyState* vstate;   // [R]
+  float* bias;           // [R][V]
+  long long* fin_part;   // [R][n_tiles][2]
+  int32_t* prev;         // [R]
+};
+cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t st);
+
+// CUDA-core Markov bias: bias[n][v] = sum_i E[prev[n]][i] * Wt[v][i] for the
+// n = 0..R-1 rows whose previous token is prev_base[n * prev_stride]
+// (negative = zero row).
+cudaError_t launch_bias(int R, int V, int r, int dt, const void* E, const void* Wt,
+                        const int32_t* prev_base, int prev_stride, float* bias,
+                        uint32_t* status, cudaStream_t st);
+
+}  // namespace dspark

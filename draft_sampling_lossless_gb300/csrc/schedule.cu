@@ -1,0 +1,217 @@
+// Hardware-aware prefix scheduler.
+//
+// News article "DSpark: Confidence-Scheduled Speculative Decoding with
+// Semi-Autoregressive Generation", section 2.2: maximise tau * SPS(B) over the
+// per-request verify lengths, B = sum_r (1 + l_r); sort every candidate by its
+// survival probability, add them greedily, stop as soon as throughput stops
+// rising (O(gamma R log gamma R)); challenge 2: the same search without early
+// stop.  Explainer "DSpark.让每一轮计算，多走几步", survival panel:
+// E = R + sum a, rate = E / T(B), candidates added in sorted order.
+//
+// Two launches:
+//   rank   -- the position of every candidate in the total order
+//             (a descending, then flat index n*gamma + j ascending), counted by
+//             comparisons against all others; ranks are a permutation because
+//             the order is strict, so no sort network or stable radix pass is
+//             needed and the result does not depend on thread timing.
+//   finish -- one block: scatter to sorted order, exact integer prefix sums of
+//             the 2^-40 fixed-point survival values, Theta_i in double with the
+//             same operation order as the oracle, the early-stop or argmax cut,
+//             then l_r, row_off, B and E.
+#include "common.cuh"
+
+namespace dspark {
+
+namespace {
+
+constexpr int kRankThreads = 256;
+constexpr int kRankChunk = 2048;
+constexpr int kFinThreads = 1024;
+
+__device__ __forceinline__ float clean_a(float a, uint32_t* status) {
+  if (!(a >= 0.0f) || a == INFINITY) {  // NaN, negative or infinite
+    set_flag(status, kFlagNonFinite);
+    return 0.0f;
+  }
+  return a;
+}
+
+__device__ __forceinline__ long long to_fixed(float a) {
+  return __double2ll_rn((double)a * 1099511627776.0);  // 2^40, exact scaling
+}
+
+// grid: (ceil(N / 256), n_split); block 256.  rank[] must be zero on entry.
+__global__ void __launch_bounds__(kRankThreads) rank_kernel(int N, int per_split,
+                                                            const float* __restrict__ a,
+                                                            int32_t* __restrict__ rank,
+                                                            uint32_t* status) {
+  __shared__ float as[kRankChunk];
+  const int e = blockIdx.x * kRankThreads + threadIdx.x;
+  const float ae = e < N ? clean_a(a[e], status) : 0.0f;
+  const int lo = blockIdx.y * per_split, hi = min(N, lo + per_split);
+  int cnt = 0;
+  for (int c0 = lo; c0 < hi; c0 += kRankChunk) {
+    const int c1 = min(hi, c0 + kRankChunk);
+    __syncthreads();
+    for (int i = c0 + threadIdx.x; i < c1; i += kRankThreads) {
+      float v = a[i];
+      as[i - c0] = (!(v >= 0.0f) || v == INFINITY) ? 0.0f : v;
+    }
+    __syncthreads();
+    if (e < N) {
+      for (int i = c0; i < c1; ++i) {
+        const float ai = as[i - c0];
+        cnt += (ai > ae) | ((ai == ae) & (i < e));
+      }
+    }
+  }
+  if (e < N && cnt) atomicAdd(&rank[e], cnt);
+}
+
+__global__ void __launch_bounds__(kFinThreads) schedule_finish_kernel(
+    int R, int gamma, int imax, int early_stop, const float* __restrict__ a,
+    const float* __restrict__ sps, const int32_t* __restrict__ rank, long long* __restrict__ sfix,
+    int32_t* __restrict__ ell, int32_t* __restrict__ row_off, int32_t* __restrict__ B_out,
+    double* __restrict__ E_out, uint32_t* status) {
+  __shared__ long long shl[32];
+  __shared__ int shi[32];
+  __shared__ double shd[32];
+  __shared__ int shidx[32];
+  __shared__ int istar_s;
+  const int N = R * gamma;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  // 1. scatter the fixed-point survival values to their sorted positions
+  for (int e = tid; e < N; e += nt) {
+    float v = a[e];
+    v = (!(v >= 0.0f) || v == INFINITY) ? 0.0f : v;
+    sfix[rank[e]] = to_fixed(v);
+  }
+  __syncthreads();
+  // 2. Theta_i for i in [0, imax]; thread chunk [i0, i1) over i
+  const int n_i = imax + 1;
+  const int seg = (n_i + nt - 1) / nt;
+  const int i0 = min(n_i, tid * seg), i1 = min(n_i, i0 + seg);
+  long long loc = 0;
+  for (int i = i0; i < i1; ++i)
+    if (i < N) loc += sfix[i];
+  long long incl = block_inclusive_scan(loc, shl);
+  const long long S0 = incl - loc;  // exact: integers
+  // Theta in the oracle's operation order: ((double)S * 2^-40 + R) * SPS
+  auto theta_at = [&](int i, long long S) -> double {
+    double e = __dadd_rn((double)R, __ll2double_rn(S) * 9.094947017729282e-13);  // 2^-40
+    float s = sps[R + i];
+    if (!isfinite(s)) set_flag(status, kFlagNonFinite);
+    return __dmul_rn(e, (double)s);
+  };
+  int my_stop = 0x7fffffff;
+  double best_v = -INFINITY;
+  int best_i = 0x7fffffff;
+  {
+    long long S = S0;
+    double prev_th = 0.0;
+    for (int i = i0; i < i1; ++i) {
+      const double th = theta_at(i, S);
+      if (i > i0 && !(th > prev_th) && my_stop == 0x7fffffff) my_stop = i - 1;
+      if (th > best_v) {
+        best_v = th;
+        best_i = i;
+      }
+      prev_th = th;
+      if (i < N) S += sfix[i];
+    }
+    // the pair that straddles the chunk boundary (i1 - 1, i1)
+    if (i1 > i0 && i1 < n_i && my_stop == 0x7fffffff) {
+      const double th = theta_at(i1, S);
+      if (!(th > prev_th)) my_stop = i1 - 1;
+    }
+  }
+  int istar;
+  if (early_stop) {
+    int s = block_min_int(my_stop, shi);
+    istar = s == 0x7fffffff ? imax : s;
+  } else {
+    // first argmax: max value, then lowest index
+    const int lane = tid & 31, wid = tid >> 5, nw = nt >> 5;
+    double v = best_v;
+    int bi = best_i;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      double ov = __shfl_xor_sync(0xffffffffu, v, o);
+      int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > v || (ov == v && oi < bi)) {
+        v = ov;
+        bi = oi;
+      }
+    }
+    __syncthreads();
+    if (lane == 0) {
+      shd[wid] = v;
+      shidx[wid] = bi;
+    }
+    __syncthreads();
+    if (wid == 0) {
+      v = lane < nw ? shd[lane] : -INFINITY;
+      bi = lane < nw ? shidx[lane] : 0x7fffffff;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        double ov = __shfl_xor_sync(0xffffffffu, v, o);
+        int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > v || (ov == v && oi < bi)) {
+          v = ov;
+          bi = oi;
+        }
+      }
+      if (lane == 0) istar_s = bi;
+    }
+    __syncthreads();
+    istar = istar_s;
+    if (istar == 0x7fffffff) istar = 0;
+  }
+  // 3. E = R + S_{i*}
+  if (istar >= i0 && istar < i1) {
+    long long S = S0;
+    for (int i = i0; i < istar; ++i) S += sfix[i];
+    E_out[0] = __dadd_rn((double)R, __ll2double_rn(S) * 9.094947017729282e-13);
+    B_out[0] = R + istar;
+  }
+  // 4. l_r = number of request r's candidates ranked below i*, and row_off
+  const int rseg = (R + nt - 1) / nt;
+  const int r0 = min(R, tid * rseg), r1 = min(R, r0 + rseg);
+  long long lsum = 0;
+  for (int r = r0; r < r1; ++r) {
+    int c = 0;
+    for (int j = 0; j < gamma; ++j) c += rank[(size_t)r * gamma + j] < istar;
+    ell[r] = c;
+    lsum += 1 + c;
+  }
+  long long rincl = block_inclusive_scan(lsum, shl);
+  long long run = rincl - lsum;
+  for (int r = r0; r < r1; ++r) {
+    row_off[r] = (int32_t)run;
+    run += 1 + ell[r];
+  }
+  if (tid == nt - 1) row_off[R] = (int32_t)rincl;
+}
+
+}  // namespace
+
+cudaError_t launch_schedule(const SchedArgs& s, cudaStream_t st) {
+  const int N = s.R * s.gamma;
+  cudaError_t e = cudaMemsetAsync(s.rank, 0, sizeof(int32_t) * (size_t)N, st);
+  if (e != cudaSuccess) return e;
+  const int bx = (N + kRankThreads - 1) / kRankThreads;
+  // split the comparison range so the grid has a few waves on 152 SMs
+  int n_split = 1;
+  while ((long long)bx * n_split < 1024 && N / (n_split * 2) >= kRankChunk) n_split *= 2;
+  const int per_split = (N + n_split - 1) / n_split;
+  DSPARK_LAUNCH(kKindRank, st, rank_kernel<<<dim3(bx, n_split), kRankThreads, 0, st>>>(N, per_split, s.a, s.rank, s.status));
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int imax = s.max_B > 0 ? (s.max_B - s.R < N ? s.max_B - s.R : N) : N;
+  DSPARK_LAUNCH(kKindSchedFinish, st, schedule_finish_kernel<<<1, kFinThreads, 0, st>>>(s.R, s.gamma, imax < 0 ? 0 : imax,
+                                                   s.early_stop, s.a, s.sps, s.rank, s.sfix,
+                                                   s.ell, s.row_off, s.B_out, s.E_out, s.status));
+  return cudaGetLastError();
+}
+
+}  // namespace dspark
