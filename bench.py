@@ -243,10 +243,6 @@ def run_ours(args, wl, world, rank, local):
     with torch.cuda.graph(tgraph):
         one_step()
     Bd.trace_stop()
-    tgraph.replay()
-    torch.cuda.synchronize()
-    Bd.trace_start()  # reset totals, keep the captured event pairs
-    Bd.trace_stop()
     for i in range(args.steps):
         flush.zero_()
         tgraph.replay()
