@@ -36,6 +36,7 @@ SYMBOLS = (
     "dspark_trace_collect",
     "dspark_trace_kinds",
     "dspark_trace_get",
+    "dspark_schedule_noalloc",
 )
 
 
@@ -78,6 +79,9 @@ def lib() -> ctypes.CDLL:
         L.dspark_verify.argtypes = [c_int, c_int, c_int, c_int, c_float, vp, vp, vp, c_int, vp,
                                     vp, vp, vp, vp, vp, vp, ctypes.c_int64, vp, vp, vp, vp, vp,
                                     vp, c_size, vp]
+        L.dspark_schedule_noalloc.restype = c_int
+        L.dspark_schedule_noalloc.argtypes = [c_int, c_int, vp, vp, c_int, c_int, c_int, vp, vp,
+                                              vp, vp, vp, vp]
         L.dspark_launch_count.restype = ctypes.c_longlong
         L.dspark_launch_count.argtypes = []
         for f in ("dspark_trace_start", "dspark_trace_stop", "dspark_trace_collect",
@@ -213,3 +217,14 @@ def dspark_verify(z, E, Wt, anchor, tokens, q_lse, q_tok, ell, row_off, target, 
         R, G, V, r, float(temperature), _p(z), _p(E), _p(Wt), _dt(z), _p(anchor), _p(tokens),
         _p(q_lse), _p(q_tok), _p(ell), _p(row_off), _p(target), target.shape[0], _p(u_acc),
         _p(u_fin), _p(n_acc), _p(out_tokens), _p(p_lse), _p(ws), ws.numel(), _stream(stream)))
+
+
+def dspark_schedule_noalloc(a, sps, early_stop, max_B, ell, row_off, B_out, E_out,
+                            dev_status=None, stream=None):
+    """The scheduler with library-internal static scratch (no workspace): for
+    callers that cannot allocate device memory.  Calls sharing a process must
+    not overlap on the GPU."""
+    R, G = a.shape
+    _check("dspark_schedule_noalloc", lib().dspark_schedule_noalloc(
+        R, G, _p(a), _p(sps), sps.numel(), int(early_stop), int(max_B), _p(ell), _p(row_off),
+        _p(B_out), _p(E_out), _p(dev_status), _stream(stream)))

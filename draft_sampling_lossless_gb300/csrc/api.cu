@@ -328,3 +328,8 @@ int dspark_verify(int R, int gamma, int V, int r, float temperature, const void*
 }
 
 }  // extern "C"
+
+namespace dspark {
+// Lets other translation units report a reason through dspark_last_error().
+void set_error_text(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+}  // namespace dspark

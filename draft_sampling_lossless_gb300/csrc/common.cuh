@@ -201,6 +201,7 @@ enum KernelKind {
 };
 
 void trace_begin(int kind, cudaStream_t st);
+void set_error_text(const char* msg);  // the text dspark_last_error() returns
 void trace_end(int kind, cudaStream_t st);
 
 // Every kernel launch: counted, and bracketed by trace events when tracing.

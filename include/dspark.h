@@ -218,6 +218,35 @@ int dspark_verify(int R, int gamma, int V, int r, float temperature,
                   double* p_lse, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * dspark_schedule_noalloc -- dspark_schedule for callers that cannot allocate
+ * device memory.  The paper has no counterpart: this is a deployment variant.
+ *
+ * Some callers cannot call cudaMalloc or pass a workspace: an engine that
+ * replays a fixed memory map reserved once at start-up (allocating inside the
+ * decode loop would break the plan, or the CUDA graph that replays it), or a
+ * plugin inside a host framework that owns the device heap.  This entry point
+ * runs the same scheduler with its scratch in a static device array inside
+ * the library instead of `ws`; it calls no cudaMalloc / cudaFree.
+ *
+ * Arguments and results are those of dspark_schedule, except:
+ *   dev_status  [1] uint32 or NULL   device status word the kernels OR
+ *                                    DSPARK_DEVFLAG_* bits into (caller-owned,
+ *                                    zero it first); NULL = not reported
+ * Limits:
+ *   R * gamma <= 32768, else DSPARK_ERR_INVALID_ARG with a reason in
+ *   dspark_last_error().  The static array (about 384 KiB) stays resident on
+ *   every GPU that loads the library until the process exits.
+ *   All calls share that array: calls that overlap on the GPU (different
+ *   streams or host threads) race and must be serialised by the caller.
+ *   The first call on each device resolves the array's address while that
+ *   device is current (cudaGetSymbolAddress); make it before any stream
+ *   capture.
+ */
+int dspark_schedule_noalloc(int R, int gamma, const float* a, const float* sps, int n_sps,
+                            int early_stop, int max_B, int32_t* ell, int32_t* row_off,
+                            int32_t* B_out, double* E_out, uint32_t* dev_status, void* stream);
+
+/*
  * Launch counting and kernel tracing (measurement support; no counterpart on
  * the pages).  Host-side only: these calls create CUDA events once and never
  * allocate device memory.
