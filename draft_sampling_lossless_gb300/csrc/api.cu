@@ -50,7 +50,7 @@ Layout layout(int R, int gamma, int V, int r) {
   L.bias = off;
   off += align_up((size_t)R * V * sizeof(float));
   L.part = off;
-  off += align_up((size_t)R * n_tiles * sizeof(double));
+  off += align_up((size_t)R * ((V + 127) / 128) * sizeof(double));  // 128-token partials (tensor-core path) or 256
   L.row_part = off;
   off += align_up((size_t)R * (gamma + 1) * n_chunks * sizeof(double));
   L.vstate = off;

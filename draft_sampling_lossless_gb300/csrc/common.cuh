@@ -37,8 +37,10 @@ __host__ inline ScalePair make_scale(double c) {
   return s;
 }
 
+// y * (hi + lo); -inf (a masked or impossible token) stays -inf, where the
+// two-term product would give inf - inf = NaN whenever lo < 0.
 __device__ __forceinline__ float scaled(float y, ScalePair s) {
-  return fmaf(y, s.hi, y * s.lo);
+  return y > -INFINITY ? fmaf(y, s.hi, y * s.lo) : -INFINITY;
 }
 
 template <typename T>
@@ -231,6 +233,17 @@ struct DraftArgs {
   double* part;     // [R][n_tiles] scratch (greedy: ArgMax pairs)
 };
 cudaError_t launch_draft(const DraftArgs& a, cudaStream_t st);
+
+// Tensor-core path of the draft (bf16, r % 8 == 0, r <= 256, 16-byte aligned
+// operands): the fused bias GEMM + partial pass for draft position k.
+bool draft_tc_supported(const DraftArgs& a);
+bool tc_shape_supported(int dt, int V, int r, const void* a, const void* b, const void* c);
+// bias[n][v] = E[prev[n * prev_stride]] . Wt[v] on the tensor cores.
+cudaError_t launch_bias_tc(int R, int V, int r, const void* E, const void* Wt,
+                           const int32_t* prev, int prev_stride, float* bias, uint32_t* status,
+                           cudaStream_t st);
+cudaError_t launch_draft_partial_tc(const DraftArgs& a, int k, const int32_t* prev,
+                                    int prev_stride, cudaStream_t st);
 
 struct ConfArgs {
   int R, gamma, d, r, V, dt;

@@ -149,21 +149,81 @@ __global__ void __launch_bounds__(kTileV) draft_partial_kernel(
   if (threadIdx.x == 0) part[(size_t)n * n_tiles + t] = S;
 }
 
+// Where the finish kernel gets the chosen tile's bias: the CUDA-core bias
+// array of the workspace (bias != nullptr), or recomputed on CUDA cores from
+// E, Wt and the previous token (the fused tensor-core pass stores no bias).
+struct BiasSrc {
+  const float* bias;
+  const __nv_bfloat16* E;
+  const __nv_bfloat16* Wt;
+  const int32_t* prev;
+  int prev_stride, r;
+};
+
+// bias_s[c] = E[prev] . Wt[v0 + c] for the TW columns of one tile: warp w
+// takes columns w*TW/8 .. +TW/8, lanes split the rank dimension (16-byte
+// loads of a Wt row, r a multiple of 8, r <= 256); all of a warp's row loads
+// are issued before the reductions so their L2 latencies overlap.
+template <int TW>
+__device__ void tile_bias_recompute(const BiasSrc& b, int n, int V, int v0, float* erow,
+                                    float* bias_s, uint32_t* status) {
+  constexpr int CPW = TW / 8;
+  int tok = b.prev[(size_t)n * b.prev_stride];
+  if (tok >= V || tok < -1) {
+    if (threadIdx.x == 0) set_flag(status, kFlagTokenRange);
+    tok = -1;
+  }
+  for (int i = threadIdx.x; i < b.r; i += blockDim.x)
+    erow[i] = tok >= 0 ? __bfloat162float(b.E[(size_t)tok * b.r + i]) : 0.f;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = lane * 8;
+  const bool lane_on = j < b.r;
+  uint4 raw[CPW];
+#pragma unroll
+  for (int c = 0; c < CPW; ++c) {
+    const int v = v0 + warp * CPW + c;
+    raw[c] = (lane_on && v < V) ? *reinterpret_cast<const uint4*>(b.Wt + (size_t)v * b.r + j)
+                                : make_uint4(0, 0, 0, 0);
+  }
+  float e8[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) e8[i] = lane_on ? erow[j + i] : 0.f;
+#pragma unroll
+  for (int c = 0; c < CPW; ++c) {
+    const uint32_t w4[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc = fmaf(__uint_as_float(w4[e] << 16), e8[2 * e], acc);
+      acc = fmaf(__uint_as_float(w4[e] & 0xffff0000u), e8[2 * e + 1], acc);
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) bias_s[warp * CPW + c] = acc;
+  }
+  __syncthreads();
+}
+
 // One block per request: choose the tile whose running sum crosses u*S, then
-// the token inside it by recomputing the tile's weights.
-template <typename T>
-__global__ void __launch_bounds__(kTileV) draft_finish_kernel(
-    int V, int gamma, int k, int n_tiles, const T* __restrict__ z, const float* __restrict__ bias,
-    ScalePair sc, int greedy, const double* __restrict__ part, const float* __restrict__ u,
+// the token inside it by recomputing the tile's weights.  With a recomputed
+// bias the tile's weights can differ from the partial pass in the last bits,
+// so the position inside the tile is taken as the same fraction of the
+// recomputed tile mass.
+template <typename T, int TW>
+__global__ void __launch_bounds__(256) draft_finish_kernel(
+    int V, int gamma, int k, int n_tiles, const T* __restrict__ z, BiasSrc bsrc, ScalePair sc,
+    int greedy, const double* __restrict__ part, const float* __restrict__ u,
     int32_t* __restrict__ tokens, double* __restrict__ q_lse, float* __restrict__ q_tok,
     uint32_t* status) {
   __shared__ double shd[32];
-  __shared__ double incl_s[kTileV];
+  __shared__ double incl_s[256];
   __shared__ long long shl[32];
   __shared__ float shf[32];
   __shared__ int shi[32];
   __shared__ ArgMax sha[32];
   __shared__ double base_s;
+  __shared__ float bias_s[TW];
+  __shared__ float erow[1024];
   const int n = blockIdx.x, tid = threadIdx.x;
   const size_t out = (size_t)n * gamma + k;
   if (greedy) {
@@ -223,11 +283,18 @@ __global__ void __launch_bounds__(kTileV) draft_finish_kernel(
   __syncthreads();
   const bool fallback = base_s < 0.0;
   base = base_s;
-  // Recompute the chosen tile exactly as the partial pass did.
-  const int v = tsel * kTileV + tid;
-  const bool ok = v < V;
+  // Recompute the chosen tile.
+  const int v = tsel * TW + tid;
+  const bool ok = tid < TW && v < V;
+  float bv = 0.f;
+  if (bsrc.bias != nullptr) {
+    if (ok) bv = bsrc.bias[(size_t)n * V + v];
+  } else {
+    tile_bias_recompute<TW>(bsrc, n, V, tsel * TW, erow, bias_s, status);
+    bv = tid < TW ? bias_s[tid] : 0.f;
+  }
   float y = -INFINITY;
-  if (ok) y = ldf(z, out * V + v) + bias[(size_t)n * V + v];
+  if (ok) y = ldf(z, out * V + v) + bv;
   if (ok && (isnan(y) || y == INFINITY)) y = -INFINITY;
   const float a = scaled(y, sc);
   const float amax = block_max(a, shf);
@@ -235,45 +302,72 @@ __global__ void __launch_bounds__(kTileV) draft_finish_kernel(
   float w = 0.f;
   long long f = (ok && a > -INFINITY && amax > -INFINITY) ? rel_fix(a, ref, &w) : 0ll;
   long long cum = block_inclusive_scan(f, shl);
+  __syncthreads();
+  if (tid == blockDim.x - 1) incl_s[0] = ldexp((double)cum, (int)ref - kFixRel);
+  __syncthreads();
+  const double tile_mass = incl_s[0];
+  // the crossing's position inside the tile, as a fraction of the tile mass
+  const double target = S[tsel] > 0.0 ? (thr - base) * (tile_mass / S[tsel]) : 0.0;
   int pick = 0x7fffffff;
-  if (!fallback && f > 0 && base + ldexp((double)cum, (int)ref - kFixRel) > thr) pick = tid;
+  if (!fallback && f > 0 && ldexp((double)cum, (int)ref - kFixRel) > target) pick = tid;
   int isel = block_min_int(pick, shi);
   if (isel == 0x7fffffff) isel = block_max_int(f > 0 ? tid : -1, shi);
   if (isel < 0) isel = 0;
   if (tid == isel) {
-    tokens[out] = tsel * kTileV + isel;
+    tokens[out] = tsel * TW + isel;
     if (!(total > 0.0) || !isfinite(total)) set_flag(status, kFlagNonFinite);
     q_lse[out] = log(total);
     q_tok[out] = (float)(ldexp((double)w, (int)ref) / total);
   }
 }
 
+template <typename T, int TW>
+cudaError_t launch_finish(const DraftArgs& a, int k, const BiasSrc& b, ScalePair sc, bool greedy,
+                          cudaStream_t st) {
+  const int n_tiles = (a.V + TW - 1) / TW;
+  DSPARK_LAUNCH(kKindDraftFinish, st,
+                draft_finish_kernel<T, TW><<<a.R, 256, 0, st>>>(
+                    a.V, a.gamma, k, n_tiles, (const T*)a.z, b, sc, greedy, a.part, a.u,
+                    a.tokens, a.q_lse, a.q_tok, a.status));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_draft(const DraftArgs& a, cudaStream_t st) {
   const int n_tiles = (a.V + kTileV - 1) / kTileV;
   const bool greedy = a.T == 0.0f;
   const ScalePair sc = make_scale(greedy ? 1.0 : 1.4426950408889634 / (double)a.T);
+  const bool tc = draft_tc_supported(a);
   for (int k = 0; k < a.gamma; ++k) {
     const int32_t* prev = k == 0 ? a.anchor : a.tokens + (k - 1);
     const int stride = k == 0 ? 1 : a.gamma;
-    cudaError_t e = launch_bias(a.R, a.V, a.r, a.dt, a.E, a.Wt, prev, stride, a.bias, a.status, st);
+    cudaError_t e;
+    if (tc) {
+      // bf16 on the tensor cores: fused bias GEMM + partial pass, then the
+      // finish recomputes the chosen tile's bias
+      e = launch_draft_partial_tc(a, k, prev, stride, st);
+      if (e != cudaSuccess) return e;
+      BiasSrc b{nullptr, (const __nv_bfloat16*)a.E, (const __nv_bfloat16*)a.Wt, prev, stride, a.r};
+      e = launch_finish<__nv_bfloat16, 128>(a, k, b, sc, greedy, st);
+      if (e != cudaSuccess) return e;
+      continue;
+    }
+    e = launch_bias(a.R, a.V, a.r, a.dt, a.E, a.Wt, prev, stride, a.bias, a.status, st);
     if (e != cudaSuccess) return e;
     dim3 g1(n_tiles, a.R);
+    BiasSrc b{a.bias, nullptr, nullptr, prev, stride, a.r};
     if (a.dt == 0) {
-      DSPARK_LAUNCH(kKindDraftPartial, st, draft_partial_kernel<__nv_bfloat16><<<g1, kTileV, 0, st>>>(
-          a.V, a.gamma, k, n_tiles, (const __nv_bfloat16*)a.z, a.bias, sc, greedy, a.part,
-          a.status));
-      DSPARK_LAUNCH(kKindDraftFinish, st, draft_finish_kernel<__nv_bfloat16><<<a.R, kTileV, 0, st>>>(
-          a.V, a.gamma, k, n_tiles, (const __nv_bfloat16*)a.z, a.bias, sc, greedy, a.part, a.u,
-          a.tokens, a.q_lse, a.q_tok, a.status));
+      DSPARK_LAUNCH(kKindDraftPartial, st,
+                    draft_partial_kernel<__nv_bfloat16><<<g1, kTileV, 0, st>>>(
+                        a.V, a.gamma, k, n_tiles, (const __nv_bfloat16*)a.z, a.bias, sc, greedy,
+                        a.part, a.status));
+      e = launch_finish<__nv_bfloat16, kTileV>(a, k, b, sc, greedy, st);
     } else {
-      DSPARK_LAUNCH(kKindDraftPartial, st, draft_partial_kernel<float><<<g1, kTileV, 0, st>>>(a.V, a.gamma, k, n_tiles,
-                                                         (const float*)a.z, a.bias, sc, greedy,
-                                                         a.part, a.status));
-      DSPARK_LAUNCH(kKindDraftFinish, st, draft_finish_kernel<float><<<a.R, kTileV, 0, st>>>(
-          a.V, a.gamma, k, n_tiles, (const float*)a.z, a.bias, sc, greedy, a.part, a.u,
-          a.tokens, a.q_lse, a.q_tok, a.status));
+      DSPARK_LAUNCH(kKindDraftPartial, st,
+                    draft_partial_kernel<float><<<g1, kTileV, 0, st>>>(
+                        a.V, a.gamma, k, n_tiles, (const float*)a.z, a.bias, sc, greedy, a.part,
+                        a.status));
+      e = launch_finish<float, kTileV>(a, k, b, sc, greedy, st);
     }
-    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -1,0 +1,515 @@
+// Fused Markov-bias GEMM + draft-sampler partial pass on the 5th-generation
+// tensor cores (tcgen05, TMEM accumulators, TMA operand loads).
+//
+// "DSpark.让每一轮计算，多走几步" (explainer), Markov head panel, and the news
+// article "DSpark: Confidence-Scheduled Speculative Decoding with
+// Semi-Autoregressive Generation", innovation 1, second stage: at draft
+// position k every request's previous token selects a row of the low-rank
+// table E, and bias = E[x_{k-1}] . W is added to the backbone logits before
+// the draw.
+//
+// One launch per draft position k.  The bias is never written to memory: per
+// (128-request tile, 256-token tile) the MMA
+//     D[m][v] = sum_i E[x_{k-1}(m)][i] * Wt[v][i]          (M=128, N=256, K=r)
+// lands in tensor memory, and the epilogue turns each thread's row of D plus
+// the matching slice of z into y = z + bias, a = y * log2(e)/T and, per
+// 128-token half tile, the exact fixed-point sum of 2^(a - ref) (greedy: the
+// half tile's max and argmax).  The per-request finish kernel consumes these
+// partials.
+//
+// Warp roles (352 threads, persistent over the CTA's vocabulary tiles):
+//   warps 0-7  epilogue: warp w reads TMEM lane quadrant w % 4 (requests
+//              32(w%4) .. +31 of the tile) and token half w / 4 of the tile
+//   warp 8     TMA producer of Wt K-chunks [256 tokens x 64] (3-stage ring)
+//   warp 9     TMEM allocation and the single MMA-issuing thread
+//   warp 10    TMA producer of z boxes [128 requests x 64 tokens] (4-box ring)
+// The A operand (the 128 gathered E rows) is built once per CTA in the
+// 128-byte swizzled K-major layout.  Two 256-column accumulators alternate so
+// the MMA of tile t+1 overlaps the epilogue of tile t.  Every mbarrier wait is
+// bounded (about one second); a timeout sets DSPARK_DEVFLAG_TIMEOUT, makes the
+// other waits of the CTA give up at once, and the kernel runs to completion.
+//
+// The same kernel in bias-out mode (no z stream) writes the fp32 bias rows
+// instead of partial sums; verification uses it for its residual draws.
+#include <climits>
+
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "sm100.cuh"
+
+namespace dspark {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int BM = 128;           // requests per tile (MMA M, TMEM lanes)
+constexpr int BN = 256;           // tokens per tile (MMA N)
+constexpr int BK = 64;            // K chunk = one 128-byte swizzle row of bf16
+constexpr int kHalf = BN / 2;     // tokens per epilogue warp per tile = partial width
+constexpr int kStagesB = 3;
+constexpr int kZBoxes = 4;        // 64-token boxes of z per tile
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = (kEpiWarps + 3) * 32;
+constexpr int kWarpW = kEpiWarps, kWarpMma = kEpiWarps + 1, kWarpZ = kEpiWarps + 2;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kABytesPerChunk = BM * BK * 2;  // 16 KiB
+constexpr uint32_t kBBytes = BN * BK * 2;          // 32 KiB
+constexpr uint32_t kZBytes = BM * 64 * 2;          // 16 KiB
+constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
+constexpr uint32_t kFlagTimeout = 0x10u;
+constexpr int kBars = 20;
+
+struct TcParams {
+  int R, gamma, V, r, k, nK, n_vt, n_parts;
+  int greedy;
+  ScalePair sc;
+  const __nv_bfloat16* E;
+  const int32_t* prev;
+  int prev_stride;
+  double* part;     // [R][n_parts] partials (draft mode)
+  float* bias_out;  // [R][V] (bias-out mode)
+  uint32_t* status;
+};
+
+size_t tc_smem_bytes(int nK) {
+  return 1024 + (size_t)nK * kABytesPerChunk + kStagesB * kBBytes + kZBoxes * kZBytes +
+         kBars * sizeof(uint64_t) + 16;
+}
+
+// Bounded wait that also gives up at once when another role of the CTA has
+// already timed out, so a broken pipeline ends the kernel quickly.
+__device__ __forceinline__ bool wait_abortable(uint32_t bar, uint32_t parity,
+                                               volatile int* abort_flag, uint32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > 1000000000ull) {
+      *abort_flag = 1;
+      set_flag(status, kFlagTimeout);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+// Per-thread running state of one (request, half tile) partial.
+struct Part {
+  long long acc;  // sum of 2^(a - ref) in units of 2^-40
+  int ref;        // power-of-two reference, INT_MIN = no mass yet
+  ArgMax best;    // greedy
+  float check;    // sum of every y: NaN or +inf exposes a non-finite input
+};
+
+// 32 consecutive tokens of one request row: y = z + bias, then the greedy
+// argmax or the fixed-point sum of 2^(a - ref) with a = y*log2(e)/T.  `lim`
+// = number of tokens of the 32 that lie below V.
+__device__ __forceinline__ void epi_chunk(const uint32_t (&b)[32], const uint4 (&zq)[4], int v0,
+                                          int lim, const TcParams& p, Part& s) {
+  float y[32];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t w4[4] = {zq[q].x, zq[q].y, zq[q].z, zq[q].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      y[q * 8 + 2 * e] = bf_lo(w4[e]) + __uint_as_float(b[q * 8 + 2 * e]);
+      y[q * 8 + 2 * e + 1] = bf_hi(w4[e]) + __uint_as_float(b[q * 8 + 2 * e + 1]);
+    }
+  }
+  if (lim < 32) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      if (e >= lim) y[e] = -INFINITY;
+  }
+  if (p.greedy) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      if (y[e] > s.best.v) s.best = ArgMax{y[e], v0 + e};
+      if (e < lim) s.check += y[e];
+    }
+    return;
+  }
+  // a = y * (hi + lo), clamped so that -inf (and NaN) become a finite
+  // "no mass" value instead of NaN
+  float cmax = -3.0e38f;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    if (e < lim) s.check += y[e];
+    y[e] = fmaxf(fmaf(y[e], p.sc.hi, y[e] * p.sc.lo), -3.0e38f);
+    cmax = fmaxf(cmax, y[e]);
+  }
+  if (cmax <= -1.0e38f) return;
+  const int cref = static_cast<int>(ceilf(cmax));
+  if (s.ref == INT_MIN) {
+    s.ref = cref;
+  } else if (cref > s.ref) {
+    const int d = cref - s.ref;
+    s.acc = d >= 63 ? 0 : (s.acc >> d);
+    s.ref = cref;
+  }
+  const float fref = static_cast<float>(s.ref);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float s8 = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s8 += ex2_approx(y[q * 8 + e] - fref);
+    s.acc += __float2ll_rn(s8 * 1099511627776.0f);  // 2^40
+  }
+}
+
+template <bool kBiasOut>
+__global__ void __launch_bounds__(kThreads, 1)
+    draft_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_w,
+                          const __grid_constant__ CUtensorMap tm_z, const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_abort;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + p.nK * kABytesPerChunk;
+  uint8_t* sZ = sB + kStagesB * kBBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sZ + kZBoxes * kZBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBars - 1);
+  const uint32_t b_fullB = smem_u32(bars + 0);      // [3]
+  const uint32_t b_emptyB = smem_u32(bars + 3);     // [3]
+  const uint32_t b_fullZ = smem_u32(bars + 6);      // [4]
+  const uint32_t b_emptyZ = smem_u32(bars + 10);    // [4]
+  const uint32_t b_accFull = smem_u32(bars + 14);   // [2]
+  const uint32_t b_accEmpty = smem_u32(bars + 16);  // [2]
+  const uint32_t b_drain = smem_u32(bars + 18);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = blockIdx.y * BM;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStagesB; ++i) {
+      mbar_init(b_fullB + 8 * i, 1);
+      mbar_init(b_emptyB + 8 * i, 1);
+    }
+    for (int i = 0; i < kZBoxes; ++i) {
+      mbar_init(b_fullZ + 8 * i, 1);
+      mbar_init(b_emptyZ + 8 * i, 4);  // the four warps of one token half
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b_accFull + 8 * i, 1);
+      mbar_init(b_accEmpty + 8 * i, kEpiWarps);
+    }
+    mbar_init(b_drain, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kWarpW && lane == 0) {
+    tma_prefetch(&tm_w);
+    if (!kBiasOut) tma_prefetch(&tm_z);
+  }
+  // A operand: the previous token's E row for each request of the tile, in
+  // the 128-byte swizzled K-major layout (row m at m*128 bytes of its K
+  // chunk, 16-byte granule g at position g ^ (m & 7)); rows past R are zero.
+  {
+    const int per_row = p.nK * 8;
+    for (int idx = threadIdx.x; idx < BM * per_row; idx += kThreads) {
+      const int m = idx / per_row, rem = idx - m * per_row;
+      const int c = rem >> 3, g = rem & 7;
+      const int n = r0 + m;
+      int tok = -1;
+      if (n < p.R) {
+        tok = p.prev[(size_t)n * p.prev_stride];
+        if (tok >= p.V || tok < -1) {
+          set_flag(p.status, kFlagTokenRange);
+          tok = -1;
+        }
+      }
+      uint4 val = make_uint4(0, 0, 0, 0);
+      const int col = c * BK + g * 8;
+      if (tok >= 0 && col < p.r)
+        val = *reinterpret_cast<const uint4*>(p.E + (size_t)tok * p.r + col);
+      *reinterpret_cast<uint4*>(sA + c * kABytesPerChunk + m * 128 + ((g ^ (m & 7)) << 4)) = val;
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kWarpW) {
+    // ---------------- Wt producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x) {
+        for (int c = 0; c < p.nK; ++c, ++it) {
+          const uint32_t s = it % kStagesB, ph = (it / kStagesB) & 1;
+          wait_abortable(b_emptyB + 8 * s, ph ^ 1, &s_abort, p.status);
+          mbar_arrive_expect_tx(b_fullB + 8 * s, kBBytes);
+          tma_load_2d(smem_u32(sB + s * kBBytes), &tm_w, b_fullB + 8 * s, c * BK, t * BN);
+        }
+      }
+    }
+  } else if (warp == kWarpZ) {
+    // ---------------- z producer
+    if (!kBiasOut && lane == 0) {
+      uint32_t it = 0;
+      for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x) {
+        for (int j = 0; j < kZBoxes; ++j, ++it) {
+          const uint32_t s = it % kZBoxes, ph = (it / kZBoxes) & 1;
+          wait_abortable(b_emptyZ + 8 * s, ph ^ 1, &s_abort, p.status);
+          mbar_arrive_expect_tx(b_fullZ + 8 * s, kZBytes);
+          tma_load_3d(smem_u32(sZ + s * kZBytes), &tm_z, b_fullZ + 8 * s, t * BN + j * 64, p.k,
+                      r0);
+        }
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, acc_it = 0;
+      for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x, ++acc_it) {
+        const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
+        wait_abortable(b_accEmpty + 8 * a, aph ^ 1, &s_abort, p.status);
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + a * BN;
+        for (int c = 0; c < p.nK; ++c, ++it) {
+          const uint32_t s = it % kStagesB, ph = (it / kStagesB) & 1;
+          wait_abortable(b_fullB + 8 * s, ph, &s_abort, p.status);
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + c * kABytesPerChunk);
+          const uint32_t b_base = smem_u32(sB + s * kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_bf16(d_tmem, desc_kmajor_sw128(a_base + kk * 32), desc_kmajor_sw128(b_base + kk * 32),
+                     kIdesc, (c | kk) != 0);
+          mma_commit(b_emptyB + 8 * s);
+        }
+        mma_commit(b_accFull + 8 * a);
+      }
+      // every MMA issued here completes before TMEM is released
+      mma_commit(b_drain);
+      if (!mbar_wait(b_drain, 0)) set_flag(p.status, kFlagTimeout);
+    }
+  } else {
+    // ---------------- epilogue, warps 0-7
+    const int quad = warp & 3, half = warp >> 2;
+    const int m = quad * 32 + lane;  // request row of the tile = TMEM lane
+    const int n = r0 + m;
+    const bool valid = n < p.R;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    uint32_t acc_it = 0, zit0 = 0;
+    for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x, ++acc_it, zit0 += kZBoxes) {
+      const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
+      wait_abortable(b_accFull + 8 * a, aph, &s_abort, p.status);
+      tc_fence_after();
+      Part s{0, INT_MIN, ArgMax{-INFINITY, 0x7fffffff}, 0.f};
+#pragma unroll 1
+      for (int jj = 0; jj < 2; ++jj) {
+        const int j = half * 2 + jj;  // z box (64 tokens) of this warp
+        const int col = j * 64;
+        uint32_t b0[32], b1[32];
+        __syncwarp();  // tcgen05.ld is warp-collective: reconverge first
+        tmem_ld_32x32b_x32(tmem + lane_base + a * BN + col, b0);
+        tmem_ld_32x32b_x32(tmem + lane_base + a * BN + col + 32, b1);
+        const int v0 = t * BN + col;
+        if (kBiasOut) {
+          tmem_wait_ld();
+          if (valid) {
+            float* dst = p.bias_out + (size_t)n * p.V;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              if (v0 + e + 4 <= p.V)
+                *reinterpret_cast<uint4*>(dst + v0 + e) = make_uint4(b0[e], b0[e + 1], b0[e + 2], b0[e + 3]);
+              if (v0 + 32 + e + 4 <= p.V)
+                *reinterpret_cast<uint4*>(dst + v0 + 32 + e) =
+                    make_uint4(b1[e], b1[e + 1], b1[e + 2], b1[e + 3]);
+            }
+          }
+          continue;
+        }
+        const uint32_t zs = (zit0 + j) % kZBoxes, zph = ((zit0 + j) / kZBoxes) & 1;
+        wait_abortable(b_fullZ + 8 * zs, zph, &s_abort, p.status);
+        uint4 z0[4], z1[4];
+        const uint8_t* zrow = sZ + zs * kZBytes + m * 128;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          z0[q] = *reinterpret_cast<const uint4*>(zrow + ((q ^ (m & 7)) << 4));
+          z1[q] = *reinterpret_cast<const uint4*>(zrow + (((q + 4) ^ (m & 7)) << 4));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_emptyZ + 8 * zs);
+        tmem_wait_ld();
+        if (valid) {
+          epi_chunk(b0, z0, v0, min(32, p.V - v0), p, s);
+          epi_chunk(b1, z1, v0 + 32, min(32, p.V - v0 - 32), p, s);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_accEmpty + 8 * a);
+      if (!kBiasOut && valid) {
+        if (s.check != s.check || s.check == INFINITY) set_flag(p.status, kFlagNonFinite);
+        const size_t o = (size_t)n * p.n_parts + t * 2 + half;
+        if (t * 2 + half < p.n_parts) {
+          if (p.greedy)
+            reinterpret_cast<ArgMax*>(p.part)[o] = s.best;
+          else
+            p.part[o] = (s.ref == INT_MIN) ? 0.0 : ldexp(static_cast<double>(s.acc), s.ref - kFixRel);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+int sm_count() {
+  static int n[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  if (n[dev] == 0) cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev);
+  return n[dev] > 0 ? n[dev] : 148;
+}
+
+cudaError_t encode_w(CUtensorMap* m, const void* Wt, int V, int r) {
+  cuuint64_t dims[2] = {(cuuint64_t)r, (cuuint64_t)V};
+  cuuint64_t strides[1] = {(cuuint64_t)r * 2};
+  cuuint32_t box[2] = {BK, BN};
+  cuuint32_t es[2] = {1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(Wt), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? cudaSuccess
+             : cudaErrorInvalidValue;
+}
+
+cudaError_t encode_z(CUtensorMap* m, const void* z, int R, int gamma, int V) {
+  cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)gamma, (cuuint64_t)R};
+  cuuint64_t strides[2] = {(cuuint64_t)V * 2, (cuuint64_t)gamma * V * 2};
+  cuuint32_t box[3] = {64, 1, BM};
+  cuuint32_t es[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(z), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? cudaSuccess
+             : cudaErrorInvalidValue;
+}
+
+template <bool kBiasOut>
+cudaError_t launch_tc(const CUtensorMap& tm_w, const CUtensorMap& tm_z, const TcParams& p,
+                      cudaStream_t st) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(draft_fused_tc_kernel<kBiasOut>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)tc_smem_bytes(4));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int n_rt = (p.R + BM - 1) / BM;
+  int gx = sm_count() / n_rt;
+  if (gx < 1) gx = 1;
+  if (gx > p.n_vt) gx = p.n_vt;
+  DSPARK_LAUNCH(kKindDraftFusedTc, st,
+                draft_fused_tc_kernel<kBiasOut>
+                <<<dim3(gx, n_rt), kThreads, tc_smem_bytes(p.nK), st>>>(tm_w, tm_z, p));
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_shape_supported(int dt, int V, int r, const void* a, const void* b, const void* c) {
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b) |
+                        reinterpret_cast<uintptr_t>(c);
+  return dt == 0 && r % 8 == 0 && r <= 256 && V % 8 == 0 && (mis & 15) == 0 &&
+         encode_fn() != nullptr;
+}
+
+bool draft_tc_supported(const DraftArgs& a) {
+  return tc_shape_supported(a.dt, a.V, a.r, a.z, a.E, a.Wt);
+}
+
+// Fused partial pass for draft position k (previous tokens at
+// prev[n * prev_stride]): partials per (request, 128-token half tile) in
+// a.part, ceil(V / 128) per request.
+cudaError_t launch_draft_partial_tc(const DraftArgs& a, int k, const int32_t* prev,
+                                    int prev_stride, cudaStream_t st) {
+  CUtensorMap tm_w, tm_z;
+  cudaError_t e = encode_w(&tm_w, a.Wt, a.V, a.r);
+  if (e == cudaSuccess) e = encode_z(&tm_z, a.z, a.R, a.gamma, a.V);
+  if (e != cudaSuccess) return e;
+  TcParams p;
+  p.R = a.R;
+  p.gamma = a.gamma;
+  p.V = a.V;
+  p.r = a.r;
+  p.k = k;
+  p.nK = (a.r + BK - 1) / BK;
+  p.n_vt = (a.V + BN - 1) / BN;
+  p.n_parts = (a.V + kHalf - 1) / kHalf;
+  p.greedy = a.T == 0.0f;
+  p.sc = make_scale(p.greedy ? 1.0 : 1.4426950408889634 / (double)a.T);
+  p.E = static_cast<const __nv_bfloat16*>(a.E);
+  p.prev = prev;
+  p.prev_stride = prev_stride;
+  p.part = a.part;
+  p.bias_out = nullptr;
+  p.status = a.status;
+  return launch_tc<false>(tm_w, tm_z, p, st);
+}
+
+// bias[n][v] = E[prev[n * prev_stride]] . Wt[v] on the tensor cores (rows of
+// requests with prev < 0 are zero).
+cudaError_t launch_bias_tc(int R, int V, int r, const void* E, const void* Wt,
+                           const int32_t* prev, int prev_stride, float* bias, uint32_t* status,
+                           cudaStream_t st) {
+  CUtensorMap tm_w;
+  cudaError_t e = encode_w(&tm_w, Wt, V, r);
+  if (e != cudaSuccess) return e;
+  TcParams p;
+  p.R = R;
+  p.gamma = 1;
+  p.V = V;
+  p.r = r;
+  p.k = 0;
+  p.nK = (r + BK - 1) / BK;
+  p.n_vt = (V + BN - 1) / BN;
+  p.n_parts = 0;
+  p.greedy = 0;
+  p.sc = ScalePair{1.f, 0.f};
+  p.E = static_cast<const __nv_bfloat16*>(E);
+  p.prev = prev;
+  p.prev_stride = prev_stride;
+  p.part = nullptr;
+  p.bias_out = bias;
+  p.status = status;
+  return launch_tc<true>(tm_w, tm_w, p, st);
+}
+
+}  // namespace dspark

@@ -186,38 +186,43 @@ __device__ __forceinline__ ScalePair norm_pair(float ref, double S) {
 
 // Weights of token v of request n's final draw: p (target, normalised) and
 // the residual max(0, p - q) (mode 1) -- recomputed identically by the pick
-// kernel.  Returns fixed-point units of 2^-60 for both.
+// kernel.  Returns fixed-point units of 2^-60 for both.  The tile's power-of-
+// two references and the double-float scales 2^ref / S are formed once per
+// block (thread 0) and shared through `shk`.
 template <typename T>
 __device__ void final_tile_weights(int gamma, int V, int t, const T* __restrict__ z,
                                    const float* __restrict__ bias, const T* __restrict__ target,
                                    ScalePair sc, const VerifyState& st, int n, float* shf,
-                                   long long* fr, long long* fp) {
+                                   ScalePair* shk, long long* fr, long long* fp) {
   const int v = t * kTileV + threadIdx.x;
   const bool ok = v < V;
   float tv = ok ? to_f32<T>(target[(size_t)st.final_row * V + v]) : -INFINITY;
   if (isnan(tv) || tv == INFINITY) tv = -INFINITY;
   const float ap = scaled(tv, sc);
+  float aq = -INFINITY;
+  if (st.mode == 1 && ok) {
+    float y = to_f32<T>(z[((size_t)n * gamma + st.n_acc) * V + v]) + bias[(size_t)n * V + v];
+    if (isnan(y) || y == INFINITY) y = -INFINITY;
+    aq = scaled(y, sc);
+  }
   const float mp = block_max(ap, shf);
+  const float mq = st.mode == 1 ? block_max(aq, shf) : -INFINITY;
+  if (threadIdx.x == 0) {
+    shk[0] = mp > -INFINITY ? norm_pair(ceilf(mp), st.Sp) : ScalePair{0.f, 0.f};
+    shk[1] = mq > -INFINITY ? norm_pair(ceilf(mq), st.Sq) : ScalePair{0.f, 0.f};
+  }
+  __syncthreads();
   float p = 0.f;
-  if (mp > -INFINITY && ap > -INFINITY) {
-    const float ref = ceilf(mp);
-    const ScalePair k = norm_pair(ref, st.Sp);
-    const float w = exp2f(ap - ref);
-    p = fmaf(w, k.hi, w * k.lo);
+  if (ap > -INFINITY) {
+    const float w = exp2f(ap - ceilf(mp));
+    p = fmaf(w, shk[0].hi, w * shk[0].lo);
   }
   float rho = p;
   if (st.mode == 1) {
-    float y = ok ? to_f32<T>(z[((size_t)n * gamma + st.n_acc) * V + v]) + bias[(size_t)n * V + v]
-                 : -INFINITY;
-    if (isnan(y) || y == INFINITY) y = -INFINITY;
-    const float aq = scaled(y, sc);
-    const float mq = block_max(aq, shf);
     float q = 0.f;
-    if (mq > -INFINITY && aq > -INFINITY) {
-      const float ref = ceilf(mq);
-      const ScalePair k = norm_pair(ref, st.Sq);
-      const float w = exp2f(aq - ref);
-      q = fmaf(w, k.hi, w * k.lo);
+    if (aq > -INFINITY) {
+      const float w = exp2f(aq - ceilf(mq));
+      q = fmaf(w, shk[1].hi, w * shk[1].lo);
     }
     rho = fmaxf(0.0f, p - q);
   }
@@ -233,6 +238,7 @@ __global__ void __launch_bounds__(kTileV) final_partial_kernel(
     long long* __restrict__ fin_part) {
   __shared__ float shf[32];
   __shared__ long long shl[32];
+  __shared__ ScalePair shk[2];
   const int t = blockIdx.x, n = blockIdx.y;
   const VerifyState st = vstate[n];
   long long* out = fin_part + ((size_t)n * n_tiles + t) * 2;
@@ -241,7 +247,7 @@ __global__ void __launch_bounds__(kTileV) final_partial_kernel(
     return;
   }
   long long fr, fp;
-  final_tile_weights<T>(gamma, V, t, z, bias, target, sc, st, n, shf, &fr, &fp);
+  final_tile_weights<T>(gamma, V, t, z, bias, target, sc, st, n, shf, shk, &fr, &fp);
   fr = block_sum(fr, shl);
   fp = block_sum(fp, shl);
   if (threadIdx.x == 0) {
@@ -276,6 +282,7 @@ __global__ void __launch_bounds__(kTileV) final_pick_kernel(
   __shared__ int shi[32];
   __shared__ long long incl_s[kTileV];
   __shared__ long long base_s;
+  __shared__ ScalePair shk[2];
   const int n = blockIdx.x, tid = threadIdx.x;
   const VerifyState st = vstate[n];
   if (st.mode < 0) return;
@@ -321,7 +328,7 @@ __global__ void __launch_bounds__(kTileV) final_pick_kernel(
   __syncthreads();
   base = base_s;
   long long fr, fp;
-  final_tile_weights<T>(gamma, V, tsel, z, bias, target, sc, st, n, shf, &fr, &fp);
+  final_tile_weights<T>(gamma, V, tsel, z, bias, target, sc, st, n, shf, shk, &fr, &fp);
   const long long f = col == 0 ? fr : fp;
   const long long cum = block_inclusive_scan(f, shl);
   int pick = (f > 0 && base + cum > thr) ? tid : 0x7fffffff;
@@ -347,7 +354,9 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t st) {
       a.status));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || greedy) return e;
-  e = launch_bias(a.R, a.V, a.r, a.dt, a.E, a.Wt, a.prev, 1, a.bias, a.status, st);
+  e = tc_shape_supported(a.dt, a.V, a.r, a.z, a.E, a.Wt)
+          ? launch_bias_tc(a.R, a.V, a.r, a.E, a.Wt, a.prev, 1, a.bias, a.status, st)
+          : launch_bias(a.R, a.V, a.r, a.dt, a.E, a.Wt, a.prev, 1, a.bias, a.status, st);
   if (e != cudaSuccess) return e;
   DSPARK_LAUNCH(kKindFinalPartial, st, final_partial_kernel<T><<<dim3(n_tiles, a.R), kTileV, 0, st>>>(
       a.gamma, a.V, n_tiles, z, a.bias, tg, sc, a.vstate, a.fin_part));

@@ -66,6 +66,7 @@ typedef enum { DSPARK_BF16 = 0, DSPARK_F32 = 1 } dspark_dtype;
 #define DSPARK_DEVFLAG_NONFINITE 0x2u   /* a NaN / inf logit, survival or SPS value */
 #define DSPARK_DEVFLAG_ROW_RANGE 0x4u   /* a target row index outside [0, n_target_rows) */
 #define DSPARK_DEVFLAG_SPS_RANGE 0x8u   /* the scheduler needed SPS[B] beyond the table */
+#define DSPARK_DEVFLAG_TIMEOUT 0x10u    /* a bounded on-chip wait gave up (results invalid) */
 
 /* Human-readable name of a status code.  Never NULL. */
 const char* dspark_status_string(int status);
