@@ -279,6 +279,8 @@ int dspark_verify(int R, int gamma, int V, int r, float temperature, const void*
   REQUIRE(target);
   REQUIRE(n_acc);
   REQUIRE(out_tokens);
+  if (((uintptr_t)target | (uintptr_t)z) & 15)
+    return fail(DSPARK_ERR_INVALID_ARG, "target and z must be 16-byte aligned");
   if (n_target_rows < 1 || n_target_rows > (int64_t)1 << 31)
     return fail(DSPARK_ERR_INVALID_ARG, "n_target_rows out of range");
   if (temperature > 0.0f) {

@@ -11,7 +11,7 @@ namespace dspark {
 // Vocabulary tile of the draft / final-sampling partial sums, and chunk of
 // the verification row pass.
 constexpr int kTileV = 256;
-constexpr int kChunkV = 4096;
+constexpr int kChunkV = 1024;  // tokens per warp item of the verification row pass
 // Fixed-point fraction bits: weights relative to a tile's power-of-two
 // reference (each <= 1) are summed exactly as integers in units of 2^-kFixRel;
 // normalised weights (p, residual) in units of 2^-kFixAbs.
@@ -282,7 +282,63 @@ struct VerifyState {
   int prev;       // token before the rejected position (residual), -1 none
   double Sp;      // sum_v exp(target_row / T) of the final row
   double Sq;      // sum_v exp(y_draft) of the rejected position
+  double inv_Sp;  // 1 / Sp
+  double inv_Sq;  // 1 / Sq (0 when not a residual draw)
 };
+
+// Fast base-2 exponential (MUFU ex2, flush-to-zero; results below 2^-126
+// are far below every fixed-point unit used here).
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// y * (hi + lo) clamped to >= -3e38: -inf and NaN inputs become a finite
+// "no mass" value (their exponential is 0) instead of NaN.
+__device__ __forceinline__ float scaled_clamped(float y, ScalePair s) {
+  return fmaxf(fmaf(y, s.hi, y * s.lo), -3.0e38f);
+}
+
+// Eight consecutive elements starting at p[v0] as fp32 (16/32-byte vector
+// loads when all eight lie below V, else masked scalar loads with `fill`).
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, int v0, int V, float (&o)[8], float fill);
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, int v0, int V,
+                                                     float (&o)[8], float fill) {
+  if (v0 + 8 <= V) {
+    const uint4 q = *reinterpret_cast<const uint4*>(p + v0);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = __uint_as_float(w[i] << 16);
+      o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = v0 + i < V ? __bfloat162float(p[v0 + i]) : fill;
+  }
+}
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, int v0, int V, float (&o)[8],
+                                             float fill) {
+  if (v0 + 8 <= V) {
+    const float4 a = *reinterpret_cast<const float4*>(p + v0);
+    const float4 b = *reinterpret_cast<const float4*>(p + v0 + 4);
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+    o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = v0 + i < V ? p[v0 + i] : fill;
+  }
+}
+
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
 
 struct VerifyArgs {
   int R, gamma, V, r, dt;

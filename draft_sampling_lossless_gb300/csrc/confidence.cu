@@ -7,16 +7,47 @@
 //
 // One block per request, one warp per draft position: the warp reads the
 // position's hidden state and the previous token's embedding row with
-// coalesced loads, reduces the dot product, applies sigma(s / t_k); lane 0 of
-// warp 0 then forms the running product along the block.
+// 16-byte loads (eight elements per lane per step), reduces the dot product,
+// applies sigma(s / t_k); thread 0 then forms the running product along the
+// block.  HBM-bound: R * gamma * (d + r) elements.
 #include "common.cuh"
 
 namespace dspark {
 
+namespace {
+
+// sum_i w[i] * x[i] over n elements, the warp's lanes taking eight at a time
+// (x 16-byte aligned and n a multiple of 8 for the vector path).
 template <typename T>
-__global__ void confidence_kernel(int gamma, int d, int r, int V, const T* __restrict__ h,
-                                  const float* __restrict__ w, const T* __restrict__ E1,
-                                  const int32_t* __restrict__ anchor,
+__device__ __forceinline__ float warp_dot(const float* __restrict__ w, const T* __restrict__ x,
+                                          int n, bool vec) {
+  const int lane = threadIdx.x & 31;
+  float s = 0.f;
+  if (vec) {
+    for (int i = lane * 8; i < n; i += 256) {
+      float xv[8];
+      load8<T>(x, i, n, xv, 0.f);
+      const float4 w0 = *reinterpret_cast<const float4*>(w + i);
+      const float4 w1 = *reinterpret_cast<const float4*>(w + i + 4);
+      s = fmaf(w0.x, xv[0], s);
+      s = fmaf(w0.y, xv[1], s);
+      s = fmaf(w0.z, xv[2], s);
+      s = fmaf(w0.w, xv[3], s);
+      s = fmaf(w1.x, xv[4], s);
+      s = fmaf(w1.y, xv[5], s);
+      s = fmaf(w1.z, xv[6], s);
+      s = fmaf(w1.w, xv[7], s);
+    }
+  } else {
+    for (int i = lane; i < n; i += 32) s = fmaf(w[i], to_f32<T>(x[i]), s);
+  }
+  return s;
+}
+
+template <typename T>
+__global__ void confidence_kernel(int gamma, int d, int r, int V, int vec,
+                                  const T* __restrict__ h, const float* __restrict__ w,
+                                  const T* __restrict__ E1, const int32_t* __restrict__ anchor,
                                   const int32_t* __restrict__ tokens,
                                   const float* __restrict__ sts, const float* __restrict__ c_in,
                                   float* __restrict__ c_out, float* __restrict__ a_out,
@@ -35,13 +66,8 @@ __global__ void confidence_kernel(int gamma, int d, int r, int V, const T* __res
         if (lane == 0) set_flag(status, kFlagTokenRange);
         prev = -1;
       }
-      float s = 0.f;
-      const T* hr = h + idx * d;
-      for (int i = lane; i < d; i += 32) s = fmaf(w[i], to_f32<T>(hr[i]), s);
-      if (prev >= 0) {
-        const T* er = E1 + (size_t)prev * r;
-        for (int i = lane; i < r; i += 32) s = fmaf(w[d + i], to_f32<T>(er[i]), s);
-      }
+      float s = warp_dot<T>(w, h + idx * d, d, vec);
+      if (prev >= 0) s += warp_dot<T>(w + d, E1 + (size_t)prev * r, r, vec);
       s = warp_sum(s);
       c = 1.0f / (1.0f + expf(-s / sts[k]));
     }
@@ -61,16 +87,27 @@ __global__ void confidence_kernel(int gamma, int d, int r, int V, const T* __res
   }
 }
 
+}  // namespace
+
 cudaError_t launch_confidence(const ConfArgs& a, cudaStream_t st) {
   const int threads = 32 * a.gamma;
+  // vector loads need 16-byte aligned rows and weights, d and r multiples of 8
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(a.h) | reinterpret_cast<uintptr_t>(a.E1) |
+                        reinterpret_cast<uintptr_t>(a.w);
+  const int esz = a.dt == 0 ? 2 : 4;
+  const int vec = a.c_in == nullptr && (mis & 15) == 0 && a.d % 8 == 0 && a.r % 8 == 0 &&
+                  ((size_t)a.d * esz) % 16 == 0 && ((size_t)a.d * 4) % 16 == 0;
   if (a.dt == 0)
-    DSPARK_LAUNCH(kKindConfidence, st, confidence_kernel<__nv_bfloat16><<<a.R, threads, 0, st>>>(
-        a.gamma, a.d, a.r, a.V, (const __nv_bfloat16*)a.h, a.w, (const __nv_bfloat16*)a.E1,
-        a.anchor, a.tokens, a.sts, a.c_in, a.c_out, a.a_out, a.status));
+    DSPARK_LAUNCH(kKindConfidence, st,
+                  confidence_kernel<__nv_bfloat16><<<a.R, threads, 0, st>>>(
+                      a.gamma, a.d, a.r, a.V, vec, (const __nv_bfloat16*)a.h, a.w,
+                      (const __nv_bfloat16*)a.E1, a.anchor, a.tokens, a.sts, a.c_in, a.c_out,
+                      a.a_out, a.status));
   else
-    DSPARK_LAUNCH(kKindConfidence, st, confidence_kernel<float><<<a.R, threads, 0, st>>>(
-        a.gamma, a.d, a.r, a.V, (const float*)a.h, a.w, (const float*)a.E1, a.anchor, a.tokens,
-        a.sts, a.c_in, a.c_out, a.a_out, a.status));
+    DSPARK_LAUNCH(kKindConfidence, st,
+                  confidence_kernel<float><<<a.R, threads, 0, st>>>(
+                      a.gamma, a.d, a.r, a.V, vec, (const float*)a.h, a.w, (const float*)a.E1,
+                      a.anchor, a.tokens, a.sts, a.c_in, a.c_out, a.a_out, a.status));
   return cudaGetLastError();
 }
 

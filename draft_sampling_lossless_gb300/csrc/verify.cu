@@ -8,74 +8,107 @@
 // tutorial, section 五: the first rejection ends the block.
 //
 // Launches (stochastic; greedy needs only the first two):
-//   rows    -- every verified target row streamed once in 4096-token chunks:
-//              exact chunk sums of 2^(t*log2e/T - ref) (greedy: chunk argmax)
+//   rows    -- every verified target row streamed once: a warp per 1024-token
+//              chunk, 16-byte loads, the chunk's exact sum of
+//              2^(t*log2e/T - ref) (greedy: the chunk's argmax)
 //   decide  -- per request: row normalisers, p_lse, the sequential accept test
 //              u < p(x)/q(x), n_acc, the accepted tokens and the final-draw setup
-//   bias    -- Markov bias of each rejected position (CUDA cores)
-//   final   -- per (request, 256-token tile): exact fixed-point sums of the
-//              residual max(0, p - q) and of p, both normalised
-//   pick    -- per request: inverse CDF over the tiles and inside the tile, with
-//              an exact integer comparison against u * total
+//   bias    -- Markov bias of each rejected position (tensor cores when the
+//              shapes allow, else CUDA cores)
+//   final   -- a warp per (request, 256-token tile): exact fixed-point sums of
+//              the residual max(0, p - q) and of p, both normalised
+//   pick    -- per request: inverse CDF over the tiles, then inside the tile by
+//              recomputing it with the same warp routine, compared with u*total
+//              in exact integer arithmetic
 #include "common.cuh"
 
 namespace dspark {
 
 namespace {
 
-constexpr int kRowThreads = 256;
-constexpr int kPerThread = kChunkV / kRowThreads;  // 16
+constexpr int kRowChunk = kChunkV;
+constexpr int kFinTile = 256;    // tokens per warp item of the final pass
+
+// ---------------------------------------------------------------- rows
+
+// Kahan-compensated fp32 running sum (the row normaliser scales every
+// residual weight of the final draw, so its error must stay far below the
+// per-element fp32 rounding).
+struct Kahan {
+  float s = 0.f, c = 0.f;
+  __device__ __forceinline__ void add(float x) {
+    const float y = x - c;
+    const float t = s + y;
+    c = (t - s) - y;
+    s = t;
+  }
+  // value in units of 2^-40
+  __device__ __forceinline__ long long fixed40() const {
+    return __float2ll_rn(s * 1099511627776.0f) - __float2ll_rn(c * 1099511627776.0f);
+  }
+};
 
 template <typename T>
-__global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(
-    int gamma, int V, int n_chunks, long long n_rows, const T* __restrict__ target,
+__global__ void __launch_bounds__(256) verify_rows_kernel(
+    int R, int gamma, int V, int n_chunks, long long n_rows, const T* __restrict__ target,
     const int32_t* __restrict__ ell, const int32_t* __restrict__ row_off, ScalePair sc,
     int greedy, double* __restrict__ row_part) {
-  __shared__ float shf[32];
-  __shared__ long long shl[32];
-  __shared__ ArgMax sha[32];
-  const int c = blockIdx.x, j = blockIdx.y, n = blockIdx.z;
-  const int L = ell[n];
-  if (j > L || L > gamma) return;
-  const long long row = (long long)row_off[n] + j;
-  if (row < 0 || row >= n_rows) return;  // reported by the decide kernel
-  const T* tr = target + (size_t)row * V;
-  const int base = c * kChunkV + threadIdx.x;
-  double* out = row_part + ((size_t)n * (gamma + 1) + j) * n_chunks + c;
-  if (greedy) {
-    ArgMax am{-INFINITY, 0x7fffffff};
+  const int lane = threadIdx.x & 31;
+  const long long total = (long long)R * (gamma + 1) * n_chunks;
+  const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long item = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       item < total; item += nwarps) {
+    const int c = (int)(item % n_chunks);
+    const long long nj = item / n_chunks;
+    const int j = (int)(nj % (gamma + 1));
+    const int n = (int)(nj / (gamma + 1));
+    const int L = ell[n];
+    if (j > L || L > gamma) continue;
+    const long long row = (long long)row_off[n] + j;
+    if (row < 0 || row >= n_rows) continue;  // reported by the decide kernel
+    const T* tr = target + (size_t)row * V;
+    double* out = row_part + ((size_t)n * (gamma + 1) + j) * n_chunks + c;
+    float x[4][8];
 #pragma unroll
-    for (int e = 0; e < kPerThread; ++e) {
-      const int v = base + e * kRowThreads;
-      if (v < V) am = better(am, ArgMax{to_f32<T>(tr[v]), v});
+    for (int i = 0; i < 4; ++i) load8<T>(tr, c * kRowChunk + i * 256 + lane * 8, V, x[i], -INFINITY);
+    if (greedy) {
+      ArgMax am{-INFINITY, 0x7fffffff};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int v = c * kRowChunk + i * 256 + lane * 8 + e;
+          if (v < V) am = better(am, ArgMax{x[i][e], v});
+        }
+      am = warp_argmax(am);
+      if (lane == 0) *reinterpret_cast<ArgMax*>(out) = am;
+      continue;
     }
-    am = block_argmax(am, sha);
-    if (threadIdx.x == 0) *reinterpret_cast<ArgMax*>(out) = am;
-    return;
-  }
-  float a[kPerThread];
-  float m = -INFINITY;
+    float m = -3.0e38f;
 #pragma unroll
-  for (int e = 0; e < kPerThread; ++e) {
-    const int v = base + e * kRowThreads;
-    float t = v < V ? to_f32<T>(tr[v]) : -INFINITY;
-    if (isnan(t) || t == INFINITY) t = -INFINITY;  // flagged by the decide kernel's checks
-    a[e] = scaled(t, sc);
-    m = fmaxf(m, a[e]);
-  }
-  m = block_max(m, shf);
-  double S = 0.0;
-  if (m > -INFINITY) {
-    const float ref = ceilf(m);
-    long long f = 0;
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int e = 0; e < kPerThread; ++e)
-      if (a[e] > -INFINITY) f += __float2ll_rn(exp2f(a[e] - ref) * 1099511627776.0f);
-    f = block_sum(f, shl);
-    S = ldexp((double)f, (int)ref - kFixRel);
+      for (int e = 0; e < 8; ++e) {
+        x[i][e] = scaled_clamped(x[i][e], sc);
+        m = fmaxf(m, x[i][e]);
+      }
+    m = warp_max(m);
+    double S = 0.0;
+    if (m > -1.0e38f) {
+      const float ref = ceilf(m);
+      Kahan k;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) k.add(ex2_fast(x[i][e] - ref));
+      const long long f = warp_sum(k.fixed40());
+      S = ldexp((double)f, (int)ref - kFixRel);
+    }
+    if (lane == 0) *out = S;
   }
-  if (threadIdx.x == 0) *out = S;
 }
+
+// ---------------------------------------------------------------- decide
 
 template <typename T>
 __global__ void __launch_bounds__(256) verify_decide_kernel(
@@ -103,7 +136,7 @@ __global__ void __launch_bounds__(256) verify_decide_kernel(
     for (int j = tid; j <= gamma; j += blockDim.x) ot[j] = -1;
     if (tid == 0) {
       n_acc_out[n] = 0;
-      VerifyState st{0, -1, 0, -1, 0.0, 0.0};
+      VerifyState st{0, -1, 0, -1, 0.0, 0.0, 0.0, 0.0};
       vstate[n] = st;
       prev_out[n] = -1;
     }
@@ -114,7 +147,8 @@ __global__ void __launch_bounds__(256) verify_decide_kernel(
     const double* pj = part + (size_t)j * n_chunks;
     if (greedy) {
       ArgMax am{-INFINITY, 0x7fffffff};
-      for (int c = lane; c < n_chunks; c += 32) am = better(am, reinterpret_cast<const ArgMax*>(pj)[c]);
+      for (int c = lane; c < n_chunks; c += 32)
+        am = better(am, reinterpret_cast<const ArgMax*>(pj)[c]);
       am = warp_argmax(am);
       if (lane == 0) {
         am_s[j] = am;
@@ -166,93 +200,120 @@ __global__ void __launch_bounds__(256) verify_decide_kernel(
   st.final_row = (int)(r0 + nacc);
   st.prev = -1;
   st.Sp = greedy ? 0.0 : Sp[nacc];
+  st.inv_Sp = greedy ? 0.0 : 1.0 / Sp[nacc];
   st.Sq = 0.0;
+  st.inv_Sq = 0.0;
   if (st.mode == 1) {
     st.prev = nacc == 0 ? anchor[n] : tokens[(size_t)n * gamma + nacc - 1];
     st.Sq = exp(q_lse[(size_t)n * gamma + nacc]);
+    st.inv_Sq = 1.0 / st.Sq;
   }
   vstate[n] = st;
   prev_out[n] = st.prev;
 }
 
-// Normalised weight split as (hi, lo) fp32 for k = 2^ref / S in double.
-__device__ __forceinline__ ScalePair norm_pair(float ref, double S) {
-  const double k = ldexp(1.0, (int)ref) / S;
+// ---------------------------------------------------------------- final draw
+
+// (hi, lo) fp32 split of 2^ref * inv_S (exact power-of-two scaling in double).
+__device__ __forceinline__ ScalePair norm_pair(int ref, double inv_S) {
+  const double k = ldexp(inv_S, ref);
   ScalePair p;
   p.hi = (float)k;
   p.lo = (float)(k - (double)p.hi);
   return p;
 }
 
-// Weights of token v of request n's final draw: p (target, normalised) and
-// the residual max(0, p - q) (mode 1) -- recomputed identically by the pick
-// kernel.  Returns fixed-point units of 2^-60 for both.  The tile's power-of-
-// two references and the double-float scales 2^ref / S are formed once per
-// block (thread 0) and shared through `shk`.
+// One warp, one 256-token tile of request n's final draw: per lane the eight
+// tokens t*256 + lane*8 .. +7.  fp / fr = the normalised target probability
+// p and the residual max(0, p - q) (= p for a bonus draw) in units of 2^-60.
+// The pick kernel calls this again for the chosen tile and gets identical
+// values.
 template <typename T>
-__device__ void final_tile_weights(int gamma, int V, int t, const T* __restrict__ z,
-                                   const float* __restrict__ bias, const T* __restrict__ target,
-                                   ScalePair sc, const VerifyState& st, int n, float* shf,
-                                   ScalePair* shk, long long* fr, long long* fp) {
-  const int v = t * kTileV + threadIdx.x;
-  const bool ok = v < V;
-  float tv = ok ? to_f32<T>(target[(size_t)st.final_row * V + v]) : -INFINITY;
-  if (isnan(tv) || tv == INFINITY) tv = -INFINITY;
-  const float ap = scaled(tv, sc);
-  float aq = -INFINITY;
-  if (st.mode == 1 && ok) {
-    float y = to_f32<T>(z[((size_t)n * gamma + st.n_acc) * V + v]) + bias[(size_t)n * V + v];
-    if (isnan(y) || y == INFINITY) y = -INFINITY;
-    aq = scaled(y, sc);
+__device__ __forceinline__ void final_warp_tile(int gamma, int V, int t,
+                                                const T* __restrict__ z,
+                                                const float* __restrict__ bias,
+                                                const T* __restrict__ target, ScalePair sc,
+                                                const VerifyState& st, int n, long long (&fr)[8],
+                                                long long (&fp)[8]) {
+  const int lane = threadIdx.x & 31;
+  const int v0 = t * kFinTile + lane * 8;
+  float ap[8], aq[8];
+  load8<T>(target + (size_t)st.final_row * V, v0, V, ap, -INFINITY);
+  float mp = -3.0e38f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    ap[e] = scaled_clamped(ap[e], sc);
+    mp = fmaxf(mp, ap[e]);
   }
-  const float mp = block_max(ap, shf);
-  const float mq = st.mode == 1 ? block_max(aq, shf) : -INFINITY;
-  if (threadIdx.x == 0) {
-    shk[0] = mp > -INFINITY ? norm_pair(ceilf(mp), st.Sp) : ScalePair{0.f, 0.f};
-    shk[1] = mq > -INFINITY ? norm_pair(ceilf(mq), st.Sq) : ScalePair{0.f, 0.f};
-  }
-  __syncthreads();
-  float p = 0.f;
-  if (ap > -INFINITY) {
-    const float w = exp2f(ap - ceilf(mp));
-    p = fmaf(w, shk[0].hi, w * shk[0].lo);
-  }
-  float rho = p;
+  mp = warp_max(mp);
+  float mq = -3.0e38f;
   if (st.mode == 1) {
-    float q = 0.f;
-    if (aq > -INFINITY) {
-      const float w = exp2f(aq - ceilf(mq));
-      q = fmaf(w, shk[1].hi, w * shk[1].lo);
+    float zz[8], bb[8];
+    load8<T>(z + ((size_t)n * gamma + st.n_acc) * V, v0, V, zz, -INFINITY);
+    load8<float>(bias + (size_t)n * V, v0, V, bb, 0.f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      aq[e] = scaled_clamped(zz[e] + bb[e], sc);
+      mq = fmaxf(mq, aq[e]);
     }
-    rho = fmaxf(0.0f, p - q);
+    mq = warp_max(mq);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) aq[e] = -3.0e38f;
   }
+  const int refp = mp > -1.0e38f ? (int)ceilf(mp) : 0;
+  const int refq = mq > -1.0e38f ? (int)ceilf(mq) : 0;
+  ScalePair kp{0.f, 0.f}, kq{0.f, 0.f};
+  if (lane == 0) {
+    if (mp > -1.0e38f) kp = norm_pair(refp, st.inv_Sp);
+    if (mq > -1.0e38f) kq = norm_pair(refq, st.inv_Sq);
+  }
+  kp.hi = __shfl_sync(0xffffffffu, kp.hi, 0);
+  kp.lo = __shfl_sync(0xffffffffu, kp.lo, 0);
+  kq.hi = __shfl_sync(0xffffffffu, kq.hi, 0);
+  kq.lo = __shfl_sync(0xffffffffu, kq.lo, 0);
   constexpr float k2_60 = 1152921504606846976.0f;  // 2^60
-  *fp = __float2ll_rn(p * k2_60);
-  *fr = __float2ll_rn(rho * k2_60);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float wp = ex2_fast(ap[e] - (float)refp);
+    const float p = fmaf(wp, kp.hi, wp * kp.lo);
+    float rho = p;
+    if (st.mode == 1) {
+      const float wq = ex2_fast(aq[e] - (float)refq);
+      rho = fmaxf(0.0f, p - fmaf(wq, kq.hi, wq * kq.lo));
+    }
+    fp[e] = __float2ll_rn(p * k2_60);
+    fr[e] = __float2ll_rn(rho * k2_60);
+  }
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kTileV) final_partial_kernel(
+__global__ void __launch_bounds__(256) final_partial_kernel(
     int gamma, int V, int n_tiles, const T* __restrict__ z, const float* __restrict__ bias,
     const T* __restrict__ target, ScalePair sc, const VerifyState* __restrict__ vstate,
     long long* __restrict__ fin_part) {
-  __shared__ float shf[32];
-  __shared__ long long shl[32];
-  __shared__ ScalePair shk[2];
-  const int t = blockIdx.x, n = blockIdx.y;
+  const int n = blockIdx.y;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= n_tiles) return;
   const VerifyState st = vstate[n];
   long long* out = fin_part + ((size_t)n * n_tiles + t) * 2;
   if (st.mode < 0) {
-    if (threadIdx.x == 0) out[0] = out[1] = 0;
+    if ((threadIdx.x & 31) == 0) out[0] = out[1] = 0;
     return;
   }
-  long long fr, fp;
-  final_tile_weights<T>(gamma, V, t, z, bias, target, sc, st, n, shf, shk, &fr, &fp);
-  fr = block_sum(fr, shl);
-  fp = block_sum(fp, shl);
-  if (threadIdx.x == 0) {
-    out[0] = fr;
-    out[1] = fp;
+  long long fr[8], fp[8];
+  final_warp_tile<T>(gamma, V, t, z, bias, target, sc, st, n, fr, fp);
+  long long sr = 0, sp = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    sr += fr[e];
+    sp += fp[e];
+  }
+  sr = warp_sum(sr);
+  sp = warp_sum(sp);
+  if ((threadIdx.x & 31) == 0) {
+    out[0] = sr;
+    out[1] = sp;
   }
 }
 
@@ -272,17 +333,16 @@ __device__ __forceinline__ long long floor_mul(float u, long long F) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kTileV) final_pick_kernel(
+__global__ void __launch_bounds__(256) final_pick_kernel(
     int gamma, int V, int n_tiles, const T* __restrict__ z, const float* __restrict__ bias,
     const T* __restrict__ target, ScalePair sc, const VerifyState* __restrict__ vstate,
     const long long* __restrict__ fin_part, const float* __restrict__ u_fin,
     int32_t* __restrict__ out_tokens, uint32_t* status) {
-  __shared__ float shf[32];
   __shared__ long long shl[32];
   __shared__ int shi[32];
-  __shared__ long long incl_s[kTileV];
+  __shared__ long long incl_s[256];
   __shared__ long long base_s;
-  __shared__ ScalePair shk[2];
+  __shared__ int tsel_s;
   const int n = blockIdx.x, tid = threadIdx.x;
   const VerifyState st = vstate[n];
   if (st.mode < 0) return;
@@ -324,45 +384,82 @@ __global__ void __launch_bounds__(kTileV) final_pick_kernel(
     }
   }
   const int tsel = block_min_int(cand, shi);  // always found: the total exceeds thr
-  if (cand == tsel) base_s = base;
+  if (cand == tsel) {
+    base_s = base;
+    tsel_s = tsel;
+  }
   __syncthreads();
-  base = base_s;
-  long long fr, fp;
-  final_tile_weights<T>(gamma, V, tsel, z, bias, target, sc, st, n, shf, shk, &fr, &fp);
-  const long long f = col == 0 ? fr : fp;
-  const long long cum = block_inclusive_scan(f, shl);
-  int pick = (f > 0 && base + cum > thr) ? tid : 0x7fffffff;
-  int isel = block_min_int(pick, shi);
-  if (isel == 0x7fffffff) isel = block_max_int(f > 0 ? tid : -1, shi);
-  if (isel < 0) isel = 0;
-  if (tid == 0) out_tokens[(size_t)n * (gamma + 1) + st.n_acc] = tsel * kTileV + isel;
+  if (tid >= 32) return;
+  // warp 0: the chosen tile again, then its inclusive prefix in token order
+  long long fr[8], fp[8];
+  final_warp_tile<T>(gamma, V, tsel_s, z, bias, target, sc, st, n, fr, fp);
+  long long w[8], lsum = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    w[e] = col == 0 ? fr[e] : fp[e];
+    lsum += w[e];
+  }
+  long long lincl = lsum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, lincl, o);
+    if (tid >= o) lincl += y;
+  }
+  long long run = base_s + (lincl - lsum);
+  int pick = 0x7fffffff, last = -1;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    run += w[e];
+    if (w[e] > 0) last = tid * 8 + e;
+    if (pick == 0x7fffffff && w[e] > 0 && run > thr) pick = tid * 8 + e;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    pick = min(pick, __shfl_xor_sync(0xffffffffu, pick, o));
+    last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+  }
+  if (tid == 0) {
+    const int idx = pick != 0x7fffffff ? pick : (last >= 0 ? last : 0);
+    out_tokens[(size_t)n * (gamma + 1) + st.n_acc] = tsel_s * kFinTile + idx;
+  }
+}
+
+int row_grid(long long items) {
+  const long long blocks = (items + 7) / 8;
+  return (int)(blocks < 152 * 16 ? blocks : 152 * 16);
 }
 
 template <typename T>
 cudaError_t run_verify(const VerifyArgs& a, cudaStream_t st) {
   const bool greedy = a.T == 0.0f;
   const ScalePair sc = make_scale(greedy ? 1.0 : 1.4426950408889634 / (double)a.T);
-  const int n_chunks = (a.V + kChunkV - 1) / kChunkV;
-  const int n_tiles = (a.V + kTileV - 1) / kTileV;
+  const int n_chunks = (a.V + kRowChunk - 1) / kRowChunk;
+  const int n_tiles = (a.V + kFinTile - 1) / kFinTile;
   const T* z = (const T*)a.z;
   const T* tg = (const T*)a.target;
-  DSPARK_LAUNCH(kKindVerifyRows, st, verify_rows_kernel<T><<<dim3(n_chunks, a.gamma + 1, a.R), kRowThreads, 0, st>>>(
-      a.gamma, a.V, n_chunks, a.n_rows, tg, a.ell, a.row_off, sc, greedy, a.row_part));
-  DSPARK_LAUNCH(kKindVerifyDecide, st, verify_decide_kernel<T><<<a.R, 256, 0, st>>>(
-      a.gamma, a.V, n_chunks, a.n_rows, tg, sc, greedy, a.anchor, a.tokens, a.q_lse, a.q_tok,
-      a.ell, a.row_off, a.u_acc, a.row_part, a.p_lse, a.n_acc, a.out_tokens, a.vstate, a.prev,
-      a.status));
+  const long long items = (long long)a.R * (a.gamma + 1) * n_chunks;
+  DSPARK_LAUNCH(kKindVerifyRows, st,
+                verify_rows_kernel<T><<<row_grid(items), 256, 0, st>>>(
+                    a.R, a.gamma, a.V, n_chunks, a.n_rows, tg, a.ell, a.row_off, sc, greedy,
+                    a.row_part));
+  DSPARK_LAUNCH(kKindVerifyDecide, st,
+                verify_decide_kernel<T><<<a.R, 256, 0, st>>>(
+                    a.gamma, a.V, n_chunks, a.n_rows, tg, sc, greedy, a.anchor, a.tokens,
+                    a.q_lse, a.q_tok, a.ell, a.row_off, a.u_acc, a.row_part, a.p_lse, a.n_acc,
+                    a.out_tokens, a.vstate, a.prev, a.status));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || greedy) return e;
   e = tc_shape_supported(a.dt, a.V, a.r, a.z, a.E, a.Wt)
           ? launch_bias_tc(a.R, a.V, a.r, a.E, a.Wt, a.prev, 1, a.bias, a.status, st)
           : launch_bias(a.R, a.V, a.r, a.dt, a.E, a.Wt, a.prev, 1, a.bias, a.status, st);
   if (e != cudaSuccess) return e;
-  DSPARK_LAUNCH(kKindFinalPartial, st, final_partial_kernel<T><<<dim3(n_tiles, a.R), kTileV, 0, st>>>(
-      a.gamma, a.V, n_tiles, z, a.bias, tg, sc, a.vstate, a.fin_part));
-  DSPARK_LAUNCH(kKindFinalPick, st, final_pick_kernel<T><<<a.R, kTileV, 0, st>>>(a.gamma, a.V, n_tiles, z, a.bias, tg, sc,
-                                               a.vstate, a.fin_part, a.u_fin, a.out_tokens,
-                                               a.status));
+  DSPARK_LAUNCH(kKindFinalPartial, st,
+                final_partial_kernel<T><<<dim3((n_tiles + 7) / 8, a.R), 256, 0, st>>>(
+                    a.gamma, a.V, n_tiles, z, a.bias, tg, sc, a.vstate, a.fin_part));
+  DSPARK_LAUNCH(kKindFinalPick, st,
+                final_pick_kernel<T><<<a.R, 256, 0, st>>>(a.gamma, a.V, n_tiles, z, a.bias, tg,
+                                                         sc, a.vstate, a.fin_part, a.u_fin,
+                                                         a.out_tokens, a.status));
   return cudaGetLastError();
 }
 
