@@ -167,15 +167,10 @@ struct BiasSrc {
 template <int TW>
 __device__ void tile_bias_recompute(const BiasSrc& b, int n, int V, int v0, float* erow,
                                     float* bias_s, uint32_t* status) {
+  // erow (the previous token's E row, fp32) was filled at kernel start
   constexpr int CPW = TW / 8;
-  int tok = b.prev[(size_t)n * b.prev_stride];
-  if (tok >= V || tok < -1) {
-    if (threadIdx.x == 0) set_flag(status, kFlagTokenRange);
-    tok = -1;
-  }
-  for (int i = threadIdx.x; i < b.r; i += blockDim.x)
-    erow[i] = tok >= 0 ? __bfloat162float(b.E[(size_t)tok * b.r + i]) : 0.f;
-  __syncthreads();
+  (void)n;
+  (void)status;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j = lane * 8;
   const bool lane_on = j < b.r;
@@ -243,6 +238,16 @@ __global__ void __launch_bounds__(256) draft_finish_kernel(
     }
     return;
   }
+  if (bsrc.bias == nullptr) {
+    // the previous token's E row, needed once the tile is chosen: load it now
+    int tok = bsrc.prev[(size_t)n * bsrc.prev_stride];
+    if (tok >= V || tok < -1) {
+      if (tid == 0) set_flag(status, kFlagTokenRange);
+      tok = -1;
+    }
+    for (int i = tid; i < bsrc.r; i += blockDim.x)
+      erow[i] = tok >= 0 ? __bfloat162float(bsrc.E[(size_t)tok * bsrc.r + i]) : 0.f;
+  }
   const double* S = part + (size_t)n * n_tiles;
   const int seg = (n_tiles + blockDim.x - 1) / blockDim.x;
   const int t0 = min(n_tiles, tid * seg), t1 = min(n_tiles, t0 + seg);
@@ -286,6 +291,7 @@ __global__ void __launch_bounds__(256) draft_finish_kernel(
   // Recompute the chosen tile.
   const int v = tsel * TW + tid;
   const bool ok = tid < TW && v < V;
+  const float zv = ok ? ldf(z, out * V + v) : 0.f;  // issued before the bias loads
   float bv = 0.f;
   if (bsrc.bias != nullptr) {
     if (ok) bv = bsrc.bias[(size_t)n * V + v];
@@ -294,7 +300,7 @@ __global__ void __launch_bounds__(256) draft_finish_kernel(
     bv = tid < TW ? bias_s[tid] : 0.f;
   }
   float y = -INFINITY;
-  if (ok) y = ldf(z, out * V + v) + bv;
+  if (ok) y = zv + bv;
   if (ok && (isnan(y) || y == INFINITY)) y = -INFINITY;
   const float a = scaled(y, sc);
   const float amax = block_max(a, shf);

@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const __grid_constant__ CUtensorMap tm_z, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_abort;
+  __shared__ int s_tok[BM];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
@@ -216,12 +217,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // A operand: the previous token's E row for each request of the tile, in
   // the 128-byte swizzled K-major layout (row m at m*128 bytes of its K
   // chunk, 16-byte granule g at position g ^ (m & 7)); rows past R are zero.
+  // The tokens go to shared memory first, then every thread issues all of
+  // its row loads before any store so the L2 latencies overlap.
   {
-    const int per_row = p.nK * 8;
-    for (int idx = threadIdx.x; idx < BM * per_row; idx += kThreads) {
-      const int m = idx / per_row, rem = idx - m * per_row;
-      const int c = rem >> 3, g = rem & 7;
-      const int n = r0 + m;
+    if (threadIdx.x < BM) {
+      const int n = r0 + threadIdx.x;
       int tok = -1;
       if (n < p.R) {
         tok = p.prev[(size_t)n * p.prev_stride];
@@ -230,11 +230,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           tok = -1;
         }
       }
-      uint4 val = make_uint4(0, 0, 0, 0);
-      const int col = c * BK + g * 8;
-      if (tok >= 0 && col < p.r)
-        val = *reinterpret_cast<const uint4*>(p.E + (size_t)tok * p.r + col);
-      *reinterpret_cast<uint4*>(sA + c * kABytesPerChunk + m * 128 + ((g ^ (m & 7)) << 4)) = val;
+      s_tok[threadIdx.x] = tok;
+    }
+    __syncthreads();
+    const int per_row = p.nK * 8;
+    constexpr int kPer = (BM * 32 + kThreads - 1) / kThreads;  // r <= 256: 32 granules a row
+    uint4 val[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int idx = threadIdx.x + i * kThreads;
+      val[i] = make_uint4(0, 0, 0, 0);
+      if (idx < BM * per_row) {
+        const int m = idx / per_row, rem = idx - m * per_row;
+        const int col = (rem >> 3) * BK + (rem & 7) * 8;
+        const int tok = s_tok[m];
+        if (tok >= 0 && col < p.r)
+          val[i] = *reinterpret_cast<const uint4*>(p.E + (size_t)tok * p.r + col);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int idx = threadIdx.x + i * kThreads;
+      if (idx < BM * per_row) {
+        const int m = idx / per_row, rem = idx - m * per_row;
+        const int c = rem >> 3, g = rem & 7;
+        *reinterpret_cast<uint4*>(sA + c * kABytesPerChunk + m * 128 + ((g ^ (m & 7)) << 4)) =
+            val[i];
+      }
     }
   }
   fence_proxy_async_smem();
@@ -246,27 +268,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpW) {
     // ---------------- Wt producer
     if (lane == 0) {
+      // W is re-read at every draft position: keep it resident in L2
+      const uint64_t pol = policy_evict_last();
       uint32_t it = 0;
       for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x) {
         for (int c = 0; c < p.nK; ++c, ++it) {
           const uint32_t s = it % kStagesB, ph = (it / kStagesB) & 1;
           wait_abortable(b_emptyB + 8 * s, ph ^ 1, &s_abort, p.status);
           mbar_arrive_expect_tx(b_fullB + 8 * s, kBBytes);
-          tma_load_2d(smem_u32(sB + s * kBBytes), &tm_w, b_fullB + 8 * s, c * BK, t * BN);
+          tma_load_2d_hint(smem_u32(sB + s * kBBytes), &tm_w, b_fullB + 8 * s, c * BK, t * BN,
+                           pol);
         }
       }
     }
   } else if (warp == kWarpZ) {
     // ---------------- z producer
     if (!kBiasOut && lane == 0) {
+      // each logit slice is read exactly once: do not let it displace W
+      const uint64_t pol = policy_evict_first();
       uint32_t it = 0;
       for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x) {
         for (int j = 0; j < kZBoxes; ++j, ++it) {
           const uint32_t s = it % kZBoxes, ph = (it / kZBoxes) & 1;
           wait_abortable(b_emptyZ + 8 * s, ph ^ 1, &s_abort, p.status);
           mbar_arrive_expect_tx(b_fullZ + 8 * s, kZBytes);
-          tma_load_3d(smem_u32(sZ + s * kZBytes), &tm_z, b_fullZ + 8 * s, t * BN + j * 64, p.k,
-                      r0);
+          tma_load_3d_hint(smem_u32(sZ + s * kZBytes), &tm_z, b_fullZ + 8 * s, t * BN + j * 64,
+                           p.k, r0, pol);
         }
       }
     }

@@ -237,8 +237,13 @@ __device__ __forceinline__ void final_warp_tile(int gamma, int V, int t,
                                                 long long (&fp)[8]) {
   const int lane = threadIdx.x & 31;
   const int v0 = t * kFinTile + lane * 8;
-  float ap[8], aq[8];
+  float ap[8], aq[8], bb[8];
+  // all loads first (one memory round trip), then the arithmetic
   load8<T>(target + (size_t)st.final_row * V, v0, V, ap, -INFINITY);
+  if (st.mode == 1) {
+    load8<T>(z + ((size_t)n * gamma + st.n_acc) * V, v0, V, aq, -INFINITY);
+    load8<float>(bias + (size_t)n * V, v0, V, bb, 0.f);
+  }
   float mp = -3.0e38f;
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
@@ -248,12 +253,9 @@ __device__ __forceinline__ void final_warp_tile(int gamma, int V, int t,
   mp = warp_max(mp);
   float mq = -3.0e38f;
   if (st.mode == 1) {
-    float zz[8], bb[8];
-    load8<T>(z + ((size_t)n * gamma + st.n_acc) * V, v0, V, zz, -INFINITY);
-    load8<float>(bias + (size_t)n * V, v0, V, bb, 0.f);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      aq[e] = scaled_clamped(zz[e] + bb[e], sc);
+      aq[e] = scaled_clamped(aq[e] + bb[e], sc);
       mq = fmaxf(mq, aq[e]);
     }
     mq = warp_max(mq);
