@@ -47,6 +47,8 @@ def algorithmic_bytes(kind, wl, B, n_rej):
         return B * V * e
     if kind in ("draft_partial", "draft_fused_tc"):
         return R * V * e + (r * V * e if kind == "draft_fused_tc" else 0)
+    if kind == "draft_persistent_tc":  # all gamma positions; W read once (L2-resident)
+        return wl.gamma * R * V * e + r * V * e
     if kind == "markov_bias":
         return r * V * e
     if kind == "final_partial":

@@ -169,6 +169,7 @@ int dspark_draft_sample(int R, int gamma, int V, int r, float temperature, const
   a.status = at<uint32_t>(ws, L.status);
   a.bias = at<float>(ws, L.bias);
   a.part = at<double>(ws, L.part);
+  a.grid_counter = at<unsigned>(ws, L.status + 64);
   cudaError_t e = launch_draft(a, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "dspark_draft_sample");
   return DSPARK_OK;

@@ -199,6 +199,7 @@ enum KernelKind {
   kKindFinalPartial,
   kKindFinalPick,
   kKindDraftFusedTc,
+  kKindDraftPersistent,
   kKindCount
 };
 
@@ -231,8 +232,10 @@ struct DraftArgs {
   uint32_t* status;
   float* bias;      // [R][V] scratch
   double* part;     // [R][n_tiles] scratch (greedy: ArgMax pairs)
+  unsigned* grid_counter;  // grid-barrier counter of the persistent draft kernel
 };
 cudaError_t launch_draft(const DraftArgs& a, cudaStream_t st);
+cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st);
 
 // Tensor-core path of the draft (bf16, r % 8 == 0, r <= 256, 16-byte aligned
 // operands): the fused bias GEMM + partial pass for draft position k.

@@ -36,6 +36,7 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "finish.cuh"
 #include "sm100.cuh"
 
 namespace dspark {
@@ -400,6 +401,285 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
 }
 
+// ---------------------------------------------------------------- persistent
+
+// All gamma draft positions in one cooperative launch.  Per position k:
+//   epilogue warps gather A(k) (E rows of x_{k-1}), release the MMA warp,
+//   run the partial pass over the CTA's tiles, grid barrier, run the finish
+//   of the CTA's requests (scratch aliased on the A tile, idle by then), grid
+//   barrier.  The Wt and z producers run ahead across positions through
+//   their rings (neither operand depends on the drafted tokens), so their
+//   loads overlap the finish and the barriers.  TMEM is allocated once.
+struct PersistParams {
+  TcParams p;
+  const __nv_bfloat16* z;
+  const __nv_bfloat16* Wt;
+  const int32_t* anchor;
+  int32_t* tokens;
+  double* q_lse;
+  float* q_tok;
+  const float* u;
+  unsigned* grid_counter;  // zeroed before the launch
+};
+
+// Grid-wide barrier among the 256 epilogue threads of every CTA (bounded:
+// gives up after about two seconds, setting the timeout flag).
+__device__ __forceinline__ void grid_sync(unsigned* ctr, unsigned target, volatile int* abort_flag,
+                                          uint32_t* status) {
+  NamedSync<2, 256>::sync();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(ctr, 1u);
+    if (!*abort_flag) {
+      const uint64_t t0 = globaltimer_ns();
+      while (*reinterpret_cast<volatile unsigned*>(ctr) < target) {
+        if (globaltimer_ns() - t0 > 2000000000ull) {
+          *abort_flag = 1;
+          set_flag(status, kFlagTimeout);
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    __threadfence();
+  }
+  NamedSync<2, 256>::sync();
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    draft_persistent_kernel(const __grid_constant__ CUtensorMap tm_w,
+                            const __grid_constant__ CUtensorMap tm_z, const PersistParams pp) {
+  const TcParams& p = pp.p;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_abort;
+  __shared__ int s_tok[BM];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + p.nK * kABytesPerChunk;
+  uint8_t* sZ = sB + kStagesB * kBBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sZ + kZBoxes * kZBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBars - 1);
+  const uint32_t b_fullB = smem_u32(bars + 0);
+  const uint32_t b_emptyB = smem_u32(bars + 3);
+  const uint32_t b_fullZ = smem_u32(bars + 6);
+  const uint32_t b_emptyZ = smem_u32(bars + 10);
+  const uint32_t b_accFull = smem_u32(bars + 14);
+  const uint32_t b_accEmpty = smem_u32(bars + 16);
+  const uint32_t b_drain = smem_u32(bars + 18);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = blockIdx.y * BM;
+  const unsigned n_ctas = gridDim.x * gridDim.y;
+  const int cta = blockIdx.y * gridDim.x + blockIdx.x;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStagesB; ++i) {
+      mbar_init(b_fullB + 8 * i, 1);
+      mbar_init(b_emptyB + 8 * i, 1);
+    }
+    for (int i = 0; i < kZBoxes; ++i) {
+      mbar_init(b_fullZ + 8 * i, 1);
+      mbar_init(b_emptyZ + 8 * i, 4);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b_accFull + 8 * i, 1);
+      mbar_init(b_accEmpty + 8 * i, kEpiWarps);
+    }
+    mbar_init(b_drain, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kWarpW && lane == 0) {
+    tma_prefetch(&tm_w);
+    tma_prefetch(&tm_z);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kWarpW) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_last();
+      uint32_t it = 0;
+      for (int k = 0; k < p.gamma; ++k)
+        for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x)
+          for (int c = 0; c < p.nK; ++c, ++it) {
+            const uint32_t s = it % kStagesB, ph = (it / kStagesB) & 1;
+            wait_abortable(b_emptyB + 8 * s, ph ^ 1, &s_abort, p.status);
+            mbar_arrive_expect_tx(b_fullB + 8 * s, kBBytes);
+            tma_load_2d_hint(smem_u32(sB + s * kBBytes), &tm_w, b_fullB + 8 * s, c * BK, t * BN,
+                             pol);
+          }
+    }
+  } else if (warp == kWarpZ) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      uint32_t it = 0;
+      for (int k = 0; k < p.gamma; ++k)
+        for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x)
+          for (int j = 0; j < kZBoxes; ++j, ++it) {
+            const uint32_t s = it % kZBoxes, ph = (it / kZBoxes) & 1;
+            wait_abortable(b_emptyZ + 8 * s, ph ^ 1, &s_abort, p.status);
+            mbar_arrive_expect_tx(b_fullZ + 8 * s, kZBytes);
+            tma_load_3d_hint(smem_u32(sZ + s * kZBytes), &tm_z, b_fullZ + 8 * s, t * BN + j * 64,
+                             k, r0, pol);
+          }
+    }
+  } else if (warp == kWarpMma) {
+    uint32_t it = 0, acc_it = 0;
+    for (int k = 0; k < p.gamma; ++k) {
+      NamedSync<1, 288>::sync();  // A(k) is in shared memory
+      if (lane == 0) {
+        for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x, ++acc_it) {
+          const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
+          wait_abortable(b_accEmpty + 8 * a, aph ^ 1, &s_abort, p.status);
+          tc_fence_after();
+          const uint32_t d_tmem = tmem + a * BN;
+          for (int c = 0; c < p.nK; ++c, ++it) {
+            const uint32_t s = it % kStagesB, ph = (it / kStagesB) & 1;
+            wait_abortable(b_fullB + 8 * s, ph, &s_abort, p.status);
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(sA + c * kABytesPerChunk);
+            const uint32_t b_base = smem_u32(sB + s * kBBytes);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              mma_bf16(d_tmem, desc_kmajor_sw128(a_base + kk * 32),
+                       desc_kmajor_sw128(b_base + kk * 32), kIdesc, (c | kk) != 0);
+            mma_commit(b_emptyB + 8 * s);
+          }
+          mma_commit(b_accFull + 8 * a);
+        }
+      }
+      __syncwarp();
+    }
+    if (lane == 0) {
+      mma_commit(b_drain);
+      if (!mbar_wait(b_drain, 0)) set_flag(p.status, kFlagTimeout);
+    }
+  } else {
+    // ---------------- epilogue warps 0-7 (also the gather and the finish)
+    const int quad = warp & 3, half = warp >> 2;
+    const int m = quad * 32 + lane;
+    const int n = r0 + m;
+    const bool valid = n < p.R;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    uint32_t acc_it = 0, zit0 = 0, epoch = 0;
+    FinishScratch& fs = *reinterpret_cast<FinishScratch*>(sA);
+    for (int k = 0; k < p.gamma; ++k) {
+      const int32_t* prev = k == 0 ? pp.anchor : pp.tokens + (k - 1);
+      const int stride = k == 0 ? 1 : p.gamma;
+      // gather A(k): the rows of E at the previous tokens
+      if (threadIdx.x < BM) {
+        const int nn = r0 + threadIdx.x;
+        int tok = -1;
+        if (nn < p.R) {
+          tok = __ldcg(prev + (size_t)nn * stride);
+          if (tok >= p.V || tok < -1) {
+            set_flag(p.status, kFlagTokenRange);
+            tok = -1;
+          }
+        }
+        s_tok[threadIdx.x] = tok;
+      }
+      NamedSync<3, 256>::sync();
+      {
+        const int per_row = p.nK * 8;
+        constexpr int kPer = BM * 32 / 256;
+        uint4 val[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int idx = threadIdx.x + i * 256;
+          val[i] = make_uint4(0, 0, 0, 0);
+          if (idx < BM * per_row) {
+            const int mm = idx / per_row, rem = idx - mm * per_row;
+            const int col = (rem >> 3) * BK + (rem & 7) * 8;
+            const int tok = s_tok[mm];
+            if (tok >= 0 && col < p.r)
+              val[i] = *reinterpret_cast<const uint4*>(p.E + (size_t)tok * p.r + col);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int idx = threadIdx.x + i * 256;
+          if (idx < BM * per_row) {
+            const int mm = idx / per_row, rem = idx - mm * per_row;
+            const int c = rem >> 3, g = rem & 7;
+            *reinterpret_cast<uint4*>(sA + c * kABytesPerChunk + mm * 128 + ((g ^ (mm & 7)) << 4)) =
+                val[i];
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      NamedSync<1, 288>::sync();  // release the MMA warp
+      // partial pass over this CTA's tiles
+      for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x, ++acc_it, zit0 += kZBoxes) {
+        const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
+        wait_abortable(b_accFull + 8 * a, aph, &s_abort, p.status);
+        tc_fence_after();
+        Part s{0, INT_MIN, ArgMax{-INFINITY, 0x7fffffff}, 0.f};
+#pragma unroll 1
+        for (int jj = 0; jj < 2; ++jj) {
+          const int j = half * 2 + jj;
+          const int col = j * 64;
+          uint32_t b0[32], b1[32];
+          __syncwarp();
+          tmem_ld_32x32b_x32(tmem + lane_base + a * BN + col, b0);
+          tmem_ld_32x32b_x32(tmem + lane_base + a * BN + col + 32, b1);
+          const int v0 = t * BN + col;
+          const uint32_t zs = (zit0 + j) % kZBoxes, zph = ((zit0 + j) / kZBoxes) & 1;
+          wait_abortable(b_fullZ + 8 * zs, zph, &s_abort, p.status);
+          uint4 z0[4], z1[4];
+          const uint8_t* zrow = sZ + zs * kZBytes + m * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            z0[q] = *reinterpret_cast<const uint4*>(zrow + ((q ^ (m & 7)) << 4));
+            z1[q] = *reinterpret_cast<const uint4*>(zrow + (((q + 4) ^ (m & 7)) << 4));
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_emptyZ + 8 * zs);
+          tmem_wait_ld();
+          if (valid) {
+            epi_chunk(b0, z0, v0, min(32, p.V - v0), p, s);
+            epi_chunk(b1, z1, v0 + 32, min(32, p.V - v0 - 32), p, s);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_accEmpty + 8 * a);
+        if (valid) {
+          if (s.check != s.check || s.check == INFINITY) set_flag(p.status, kFlagNonFinite);
+          const size_t o = (size_t)n * p.n_parts + t * 2 + half;
+          if (t * 2 + half < p.n_parts) {
+            if (p.greedy)
+              reinterpret_cast<ArgMax*>(p.part)[o] = s.best;
+            else
+              p.part[o] = (s.ref == INT_MIN) ? 0.0 : ldexp(static_cast<double>(s.acc), s.ref - kFixRel);
+          }
+        }
+      }
+      grid_sync(pp.grid_counter, (++epoch) * n_ctas, &s_abort, p.status);
+      // finish of this CTA's requests; scratch on the A tile (its MMAs are done)
+      const BiasSrc b{nullptr, p.E, pp.Wt, prev, stride, p.r};
+      for (int nn = cta; nn < p.R; nn += n_ctas)
+        finish_request<__nv_bfloat16, kHalf, NamedSync<3, 256>>(
+            fs, nn, p.V, p.gamma, k, p.n_parts, pp.z, b, p.sc, p.greedy, p.part, pp.u, pp.tokens,
+            pp.q_lse, pp.q_tok, p.status);
+      grid_sync(pp.grid_counter, (++epoch) * n_ctas, &s_abort, p.status);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (fn == nullptr) {
@@ -509,6 +789,75 @@ cudaError_t launch_draft_partial_tc(const DraftArgs& a, int k, const int32_t* pr
   p.bias_out = nullptr;
   p.status = a.status;
   return launch_tc<false>(tm_w, tm_z, p, st);
+}
+
+// Every draft position in one cooperative launch (see draft_persistent_kernel).
+// Returns cudaErrorNotSupported, launching nothing, when the GPU cannot hold
+// one CTA per SM for the whole grid (the caller then launches per position).
+cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st) {
+  if (a.grid_counter == nullptr) return cudaErrorNotSupported;
+  CUtensorMap tm_w, tm_z;
+  cudaError_t e = encode_w(&tm_w, a.Wt, a.V, a.r);
+  if (e == cudaSuccess) e = encode_z(&tm_z, a.z, a.R, a.gamma, a.V);
+  if (e != cudaSuccess) return e;
+  PersistParams pp;
+  TcParams& p = pp.p;
+  p.R = a.R;
+  p.gamma = a.gamma;
+  p.V = a.V;
+  p.r = a.r;
+  p.k = 0;
+  p.nK = (a.r + BK - 1) / BK;
+  p.n_vt = (a.V + BN - 1) / BN;
+  p.n_parts = (a.V + kHalf - 1) / kHalf;
+  p.greedy = a.T == 0.0f;
+  p.sc = make_scale(p.greedy ? 1.0 : 1.4426950408889634 / (double)a.T);
+  p.E = static_cast<const __nv_bfloat16*>(a.E);
+  p.prev = nullptr;
+  p.prev_stride = 0;
+  p.part = a.part;
+  p.bias_out = nullptr;
+  p.status = a.status;
+  pp.z = static_cast<const __nv_bfloat16*>(a.z);
+  pp.Wt = static_cast<const __nv_bfloat16*>(a.Wt);
+  pp.anchor = a.anchor;
+  pp.tokens = a.tokens;
+  pp.q_lse = a.q_lse;
+  pp.q_tok = a.q_tok;
+  pp.u = a.u;
+  pp.grid_counter = a.grid_counter;
+  static bool attr_set = false;
+  if (!attr_set) {
+    e = cudaFuncSetAttribute(draft_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)tc_smem_bytes(4));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const size_t smem = tc_smem_bytes(p.nK);
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, draft_persistent_kernel, kThreads,
+                                                    smem);
+  if (e != cudaSuccess || per_sm < 1) return cudaErrorNotSupported;
+  const int n_rt = (a.R + BM - 1) / BM;
+  int gx = sm_count() / n_rt;
+  if (gx < 1) return cudaErrorNotSupported;
+  if (gx > p.n_vt) gx = p.n_vt;
+  e = cudaMemsetAsync(a.grid_counter, 0, sizeof(unsigned), st);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(gx, n_rt);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  DSPARK_LAUNCH(kKindDraftPersistent, st,
+                e = cudaLaunchKernelEx(&cfg, draft_persistent_kernel, tm_w, tm_z, pp));
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 // bias[n][v] = E[prev[n * prev_stride]] . Wt[v] on the tensor cores (rows of

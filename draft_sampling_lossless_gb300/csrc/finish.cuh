@@ -1,0 +1,310 @@
+// Per-request finish of one draft position: from the per-tile partial sums,
+// choose the tile whose running sum crosses u*S, recompute that tile and
+// choose the token inside it.  Shared by the standalone finish kernel (a
+// 256-thread block) and the persistent draft kernel (its 256 epilogue
+// threads, synchronised by a named barrier).
+//
+// "DSpark.让每一轮计算，多走几步" (explainer), Markov head panel: the
+// left-to-right draw of each draft position from softmax((z + bias) / T).
+#pragma once
+
+#include "common.cuh"
+
+namespace dspark {
+
+struct BlockSync {
+  __device__ __forceinline__ static void sync() { __syncthreads(); }
+};
+
+template <int kId, int kThreads>
+struct NamedSync {
+  __device__ __forceinline__ static void sync() {
+    asm volatile("bar.sync %0, %1;" ::"n"(kId), "n"(kThreads) : "memory");
+  }
+};
+
+// Where the finish gets the chosen tile's bias: the CUDA-core bias array of
+// the workspace (bias != nullptr), or recomputed on CUDA cores from E, Wt and
+// the previous token (the fused tensor-core pass stores no bias).
+struct BiasSrc {
+  const float* bias;
+  const __nv_bfloat16* E;
+  const __nv_bfloat16* Wt;
+  const int32_t* prev;
+  int prev_stride, r;
+};
+
+// Shared-memory scratch of one finish (about 8 KiB).
+struct FinishScratch {
+  double incl[256];
+  double shd[8];
+  long long shl[8];
+  float shf[8];
+  int shi[8];
+  ArgMax sha[8];
+  double base;
+  float bias[256];
+  float erow[1024];
+};
+
+// ---- reductions over 256 threads (8 warps), every thread gets the result
+
+template <class S>
+__device__ __forceinline__ double g_scan_d(double v, double* sh) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  S::sync();
+  if (lane == 31) sh[wid] = v;
+  S::sync();
+  double off = 0.0;
+  for (int w = 0; w < wid; ++w) off += sh[w];
+  return v + off;
+}
+
+template <class S>
+__device__ __forceinline__ long long g_scan_ll(long long v, long long* sh) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  S::sync();
+  if (lane == 31) sh[wid] = v;
+  S::sync();
+  long long off = 0;
+  for (int w = 0; w < wid; ++w) off += sh[w];
+  return v + off;
+}
+
+template <class S>
+__device__ __forceinline__ int g_min_i(int v, int* sh) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  S::sync();
+  if (lane == 0) sh[wid] = v;
+  S::sync();
+  int r = sh[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) r = min(r, sh[w]);
+  return r;
+}
+
+template <class S>
+__device__ __forceinline__ int g_max_i(int v, int* sh) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  S::sync();
+  if (lane == 0) sh[wid] = v;
+  S::sync();
+  int r = sh[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) r = max(r, sh[w]);
+  return r;
+}
+
+template <class S>
+__device__ __forceinline__ float g_max_f(float v, float* sh) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  v = warp_max(v);
+  S::sync();
+  if (lane == 0) sh[wid] = v;
+  S::sync();
+  float r = sh[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) r = fmaxf(r, sh[w]);
+  return r;
+}
+
+template <class S>
+__device__ __forceinline__ ArgMax g_argmax(ArgMax a, ArgMax* sh) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  a = warp_argmax(a);
+  S::sync();
+  if (lane == 0) sh[wid] = a;
+  S::sync();
+  ArgMax r = sh[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) r = better(r, sh[w]);
+  return r;
+}
+
+// Weight of one token relative to the tile reference: 2^(a - ref) <= 1, in
+// fixed-point units of 2^-40, and the fp32 weight.
+__device__ __forceinline__ long long rel_fix(float a, float ref, float* w_out) {
+  const float w = exp2f(a - ref);
+  *w_out = w;
+  return __float2ll_rn(w * 1099511627776.0f);  // 2^40
+}
+
+// bias[c] = E[prev] . Wt[v0 + c] for the TW columns of one tile (erow holds
+// the previous token's E row in fp32): warp w takes columns w*TW/8 .. +TW/8,
+// lanes split the rank dimension with 16-byte loads of the Wt row (r a
+// multiple of 8, r <= 256); all of a warp's row loads are issued before the
+// reductions so their latencies overlap.
+template <int TW, class S>
+__device__ __forceinline__ void tile_bias_recompute(const BiasSrc& b, int V, int v0,
+                                                    const float* erow, float* bias) {
+  constexpr int CPW = TW / 8;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = lane * 8;
+  const bool lane_on = j < b.r;
+  uint4 raw[CPW];
+#pragma unroll
+  for (int c = 0; c < CPW; ++c) {
+    const int v = v0 + warp * CPW + c;
+    raw[c] = (lane_on && v < V) ? *reinterpret_cast<const uint4*>(b.Wt + (size_t)v * b.r + j)
+                                : make_uint4(0, 0, 0, 0);
+  }
+  float e8[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) e8[i] = lane_on ? erow[j + i] : 0.f;
+#pragma unroll
+  for (int c = 0; c < CPW; ++c) {
+    const uint32_t w4[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc = fmaf(__uint_as_float(w4[e] << 16), e8[2 * e], acc);
+      acc = fmaf(__uint_as_float(w4[e] & 0xffff0000u), e8[2 * e + 1], acc);
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) bias[warp * CPW + c] = acc;
+  }
+  S::sync();
+}
+
+// The finish of request n at draft position k, by 256 threads
+// (threadIdx.x < 256).  part: [R][n_tiles] tile partials (doubles; greedy:
+// ArgMax pairs) of width TW.  Writes tokens / q_lse / q_tok [n][k].
+// Partials and previous tokens may have been written by other blocks of the
+// same kernel, so they are read past L1 (ld.global.cg).
+template <typename T, int TW, class S>
+__device__ void finish_request(FinishScratch& s, int n, int V, int gamma, int k, int n_tiles,
+                               const T* __restrict__ z, const BiasSrc& bsrc, ScalePair sc,
+                               int greedy, const double* part, const float* __restrict__ u,
+                               int32_t* tokens, double* q_lse, float* q_tok, uint32_t* status) {
+  const int tid = threadIdx.x;
+  const size_t out = (size_t)n * gamma + k;
+  if (greedy) {
+    const ArgMax* P = reinterpret_cast<const ArgMax*>(part) + (size_t)n * n_tiles;
+    ArgMax best{-INFINITY, 0x7fffffff};
+    for (int t = tid; t < n_tiles; t += 256) {
+      const long long raw = __ldcg(reinterpret_cast<const long long*>(P + t));
+      ArgMax am;
+      am.v = __int_as_float((int)(raw & 0xffffffffll));
+      am.i = (int)(raw >> 32);
+      best = better(best, am);
+    }
+    best = g_argmax<S>(best, s.sha);
+    if (tid == 0) {
+      int tok = best.i;
+      if (tok < 0 || tok >= V) {
+        set_flag(status, kFlagNonFinite);
+        tok = 0;
+      }
+      tokens[out] = tok;
+      q_lse[out] = (double)best.v;
+      q_tok[out] = 1.0f;
+    }
+    S::sync();
+    return;
+  }
+  if (bsrc.bias == nullptr) {
+    // the previous token's E row, needed once the tile is chosen: load it now
+    int tok = __ldcg(bsrc.prev + (size_t)n * bsrc.prev_stride);
+    if (tok >= V || tok < -1) {
+      if (tid == 0) set_flag(status, kFlagTokenRange);
+      tok = -1;
+    }
+    for (int i = tid; i < bsrc.r; i += 256)
+      s.erow[i] = tok >= 0 ? __bfloat162float(bsrc.E[(size_t)tok * bsrc.r + i]) : 0.f;
+  }
+  const double* S_ = part + (size_t)n * n_tiles;
+  const int seg = (n_tiles + 255) / 256;
+  const int t0 = min(n_tiles, tid * seg), t1 = min(n_tiles, t0 + seg);
+  double loc = 0.0;
+  for (int t = t0; t < t1; ++t) loc += __ldcg(S_ + t);
+  const double incl = g_scan_d<S>(loc, s.shd);
+  s.incl[tid] = incl;
+  S::sync();
+  const double excl = tid > 0 ? s.incl[tid - 1] : 0.0;
+  const double total = s.incl[255];
+  const double thr = (double)u[out] * total;
+  int cand = 0x7fffffff;
+  double base = 0.0;
+  {
+    double run = excl;
+    for (int t = t0; t < t1; ++t) {
+      const double nx = run + __ldcg(S_ + t);
+      if (nx > thr) {
+        cand = t;
+        base = run;
+        break;
+      }
+      run = nx;
+    }
+  }
+  int tsel = g_min_i<S>(cand, s.shi);
+  if (tsel == 0x7fffffff) {
+    // rounding left no crossing: last tile with mass
+    int last = -1;
+    for (int t = t0; t < t1; ++t)
+      if (__ldcg(S_ + t) > 0.0) last = t;
+    tsel = g_max_i<S>(last, s.shi);
+    if (tsel < 0) tsel = 0;
+    if (tid == 0) s.base = -1.0;  // marks the fallback
+  } else if (cand == tsel) {
+    s.base = base;
+  }
+  S::sync();
+  const bool fallback = s.base < 0.0;
+  base = s.base;
+  const double S_sel = __ldcg(S_ + tsel);
+  // Recompute the chosen tile.
+  const int v = tsel * TW + tid;
+  const bool ok = tid < TW && v < V;
+  const float zv = ok ? ldf(z, out * V + v) : 0.f;  // issued before the bias loads
+  float bv = 0.f;
+  if (bsrc.bias != nullptr) {
+    if (ok) bv = bsrc.bias[(size_t)n * V + v];
+  } else {
+    tile_bias_recompute<TW, S>(bsrc, V, tsel * TW, s.erow, s.bias);
+    bv = tid < TW ? s.bias[tid] : 0.f;
+  }
+  float y = -INFINITY;
+  if (ok) y = zv + bv;
+  if (ok && (isnan(y) || y == INFINITY)) y = -INFINITY;
+  const float a = scaled(y, sc);
+  const float amax = g_max_f<S>(a, s.shf);
+  const float ref = ceilf(amax);
+  float w = 0.f;
+  const long long f = (ok && a > -INFINITY && amax > -INFINITY) ? rel_fix(a, ref, &w) : 0ll;
+  const long long cum = g_scan_ll<S>(f, s.shl);
+  S::sync();
+  if (tid == 255) s.incl[0] = ldexp((double)cum, (int)ref - kFixRel);
+  S::sync();
+  const double tile_mass = s.incl[0];
+  // the crossing's position inside the tile, as a fraction of the tile mass
+  const double target = S_sel > 0.0 ? (thr - base) * (tile_mass / S_sel) : 0.0;
+  int pick = 0x7fffffff;
+  if (!fallback && f > 0 && ldexp((double)cum, (int)ref - kFixRel) > target) pick = tid;
+  int isel = g_min_i<S>(pick, s.shi);
+  if (isel == 0x7fffffff) isel = g_max_i<S>(f > 0 ? tid : -1, s.shi);
+  if (isel < 0) isel = 0;
+  if (tid == isel) {
+    tokens[out] = tsel * TW + isel;
+    if (!(total > 0.0) || !isfinite(total)) set_flag(status, kFlagNonFinite);
+    q_lse[out] = log(total);
+    q_tok[out] = (float)(ldexp((double)w, (int)ref) / total);
+  }
+  S::sync();
+}
+
+}  // namespace dspark
