@@ -6,7 +6,7 @@
 #include <stdio.h>
 #include <string.h>
 
-#include "../../include/dspark.h"
+#include "dspark.h"
 #include "common.cuh"
 
 using namespace dspark;

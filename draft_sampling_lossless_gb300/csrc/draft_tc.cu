@@ -292,6 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < kZBoxes; ++j, ++it) {
           const uint32_t s = it % kZBoxes, ph = (it / kZBoxes) & 1;
           wait_abortable(b_emptyZ + 8 * s, ph ^ 1, &s_abort, p.status);
+          // the epilogue read this box through the generic proxy; order those
+          // reads before the async-proxy (TMA) write that refills it
+          fence_proxy_async_smem();
           mbar_arrive_expect_tx(b_fullZ + 8 * s, kZBytes);
           tma_load_3d_hint(smem_u32(sZ + s * kZBytes), &tm_z, b_fullZ + 8 * s, t * BN + j * 64,
                            p.k, r0, pol);
@@ -526,6 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < kZBoxes; ++j, ++it) {
             const uint32_t s = it % kZBoxes, ph = (it / kZBoxes) & 1;
             wait_abortable(b_emptyZ + 8 * s, ph ^ 1, &s_abort, p.status);
+            fence_proxy_async_smem();  // generic reads of the box before the TMA refill
             mbar_arrive_expect_tx(b_fullZ + 8 * s, kZBytes);
             tma_load_3d_hint(smem_u32(sZ + s * kZBytes), &tm_z, b_fullZ + 8 * s, t * BN + j * 64,
                              k, r0, pol);

@@ -24,7 +24,7 @@
 
 #include <mutex>
 
-#include "../../include/dspark.h"
+#include "dspark.h"
 #include "common.cuh"
 
 namespace dspark {

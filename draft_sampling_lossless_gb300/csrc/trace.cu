@@ -10,7 +10,7 @@
 #include <atomic>
 #include <mutex>
 
-#include "../../include/dspark.h"
+#include "dspark.h"
 #include "common.cuh"
 
 namespace dspark {
