@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <climits>
+
 namespace dspark {
 
 // Vocabulary tile of the draft / final-sampling partial sums, and chunk of
@@ -278,15 +280,22 @@ struct SchedArgs {
 };
 cudaError_t launch_schedule(const SchedArgs& a, cudaStream_t st);
 
+// 1/S for a row normaliser S, as (hi + lo) * 2^e with hi in [0.5, 1): the
+// final pass scales it by a tile's power-of-two reference with exponent
+// arithmetic only.  hi = lo = 0 means "no such row".
+struct InvPair {
+  float hi, lo;
+  int e;
+};
+
 struct VerifyState {
   int n_acc;
   int mode;       // 0 bonus, 1 residual
   int final_row;  // target row of the final draw
   int prev;       // token before the rejected position (residual), -1 none
-  double Sp;      // sum_v exp(target_row / T) of the final row
-  double Sq;      // sum_v exp(y_draft) of the rejected position
-  double inv_Sp;  // 1 / Sp
-  double inv_Sq;  // 1 / Sq (0 when not a residual draw)
+  InvPair ip;     // 1 / Sp, Sp = sum_v exp(target_row / T) of the final row
+  InvPair iq;     // 1 / Sq, Sq = sum_v exp(y_draft) of the rejected position
+                  // (zero when not a residual draw)
 };
 
 // Fast base-2 exponential (MUFU ex2, flush-to-zero; results below 2^-126
@@ -377,5 +386,86 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t st);
 cudaError_t launch_bias(int R, int V, int r, int dt, const void* E, const void* Wt,
                         const int32_t* prev_base, int prev_stride, float* bias,
                         uint32_t* status, cudaStream_t st);
+
+// ------------------------------------------------- integer-built doubles
+// The FP64 pipe of this part is narrow, so the hot paths build and take
+// apart doubles with integer operations only.
+
+// acc * 2^e2 as a double, for acc >= 0 (exact while acc < 2^53; wider values
+// are truncated to 53 bits).  Results below the normal range are 0.
+__device__ __forceinline__ double fix_to_double(long long acc, int e2) {
+  if (acc <= 0) return 0.0;
+  const int msb = 63 - __clzll(acc);
+  const int ex = msb + e2;
+  if (ex < -1022) return 0.0;
+  if (ex > 1023) return __longlong_as_double(0x7ff0000000000000ll);
+  unsigned long long m = (unsigned long long)acc;
+  m = msb >= 52 ? (m >> (msb - 52)) : (m << (52 - msb));
+  return __longlong_as_double((long long)(((unsigned long long)(ex + 1023) << 52) |
+                                          (m & 0x000fffffffffffffull)));
+}
+
+// Unbiased binary exponent of a finite x > 0 (x in [2^e, 2^(e+1))); INT_MIN
+// for zero, negative and subnormal x.
+__device__ __forceinline__ int double_exponent(double x) {
+  const long long b = __double_as_longlong(x);
+  const int be = (int)((b >> 52) & 0x7ff);
+  return (b <= 0 || be == 0) ? INT_MIN : be - 1023;
+}
+
+// floor(x / 2^g) for finite x >= 0; the caller keeps the result below 2^62.
+__device__ __forceinline__ long long double_to_fix(double x, int g) {
+  const long long b = __double_as_longlong(x);
+  const int be = (int)((b >> 52) & 0x7ff);
+  if (b <= 0 || be == 0) return 0;
+  const long long m = (b & 0x000fffffffffffffll) | 0x0010000000000000ll;
+  const int sh = be - 1075 - g;  // x = m * 2^(be - 1075)
+  if (sh >= 0) return sh > 9 ? 0x3fffffffffffffffll : (m << sh);
+  return -sh >= 63 ? 0 : (m >> -sh);
+}
+
+// x * 2^k for a finite fp32 x by exponent arithmetic; results below the
+// normal range flush to 0.
+__device__ __forceinline__ float scale_pow2(float x, int k) {
+  if (x == 0.0f || k < -252) return 0.0f;
+  if (k > 254) k = 254;
+  // two steps so that every k in range gives a normal factor
+  const int k1 = k / 2, k2 = k - k1;
+  return x * __int_as_float((k1 + 127) << 23) * __int_as_float((k2 + 127) << 23);
+}
+
+// floor(u * F) exactly, for u in [0, 1) and 0 <= F < 2^62.
+__device__ __forceinline__ long long floor_mul(float u, long long F) {
+  if (!(u > 0.0f)) return 0;
+  int e;
+  const float mf = frexpf(u, &e);  // u = mf * 2^e, mf in [0.5, 1)
+  const unsigned long long m = (unsigned long long)(mf * 16777216.0f);  // u = m * 2^(e-24)
+  const unsigned long long lo = m * (unsigned long long)F;
+  const unsigned long long hi = __umul64hi(m, (unsigned long long)F);
+  const int sh = 24 - e;
+  if (sh <= 0) return F;  // u >= 1: outside the contract, clamp
+  if (sh >= 128) return 0;
+  if (sh >= 64) return (long long)(hi >> (sh - 64));
+  return (long long)((lo >> sh) | (hi << (64 - sh)));
+}
+
+// a * b > c * d for non-negative 64-bit operands, exactly (128-bit products).
+__device__ __forceinline__ bool mul_gt(unsigned long long a, unsigned long long b,
+                                       unsigned long long c, unsigned long long d) {
+  const unsigned long long h1 = __umul64hi(a, b), h2 = __umul64hi(c, d);
+  return h1 != h2 ? h1 > h2 : a * b > c * d;
+}
+
+// x = 1/S as an InvPair (one thread; x > 0 finite, else the zero pair).
+__device__ __forceinline__ InvPair split_inv(double x) {
+  InvPair r{0.f, 0.f, 0};
+  if (!(x > 0.0) || !isfinite(x)) return r;
+  int e;
+  const double m = frexp(x, &e);  // x = m * 2^e, m in [0.5, 1)
+  r.hi = (float)m;
+  r.lo = (float)(m - (double)r.hi);
+  r.e = e;
+  return r;
+}
 
 }  // namespace dspark

@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(kTileV) draft_partial_kernel(
     float w;
     long long f = (a > -INFINITY) ? rel_fix(a, ref, &w) : 0ll;
     long long tot = block_sum(f, shl);
-    S = ldexp((double)tot, (int)ref - kFixRel);
+    S = fix_to_double(tot, (int)ref - kFixRel);
   }
   if (threadIdx.x == 0) part[(size_t)n * n_tiles + t] = S;
 }
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(256) draft_finish_kernel(
     int32_t* __restrict__ tokens, double* __restrict__ q_lse, float* __restrict__ q_tok,
     uint32_t* status) {
   __shared__ FinishScratch s;
-  finish_request<T, TW, BlockSync>(s, blockIdx.x, V, gamma, k, n_tiles, z, bsrc, sc, greedy, part,
+  finish_request<T, TW, BlockSync, false>(s, blockIdx.x, V, gamma, k, n_tiles, z, bsrc, sc, greedy, part,
                                    u, tokens, q_lse, q_tok, status);
 }
 

@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (p.greedy)
             reinterpret_cast<ArgMax*>(p.part)[o] = s.best;
           else
-            p.part[o] = (s.ref == INT_MIN) ? 0.0 : ldexp(static_cast<double>(s.acc), s.ref - kFixRel);
+            p.part[o] = (s.ref == INT_MIN) ? 0.0 : fix_to_double(s.acc, s.ref - kFixRel);
         }
       }
     }
@@ -663,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (p.greedy)
               reinterpret_cast<ArgMax*>(p.part)[o] = s.best;
             else
-              p.part[o] = (s.ref == INT_MIN) ? 0.0 : ldexp(static_cast<double>(s.acc), s.ref - kFixRel);
+              p.part[o] = (s.ref == INT_MIN) ? 0.0 : fix_to_double(s.acc, s.ref - kFixRel);
           }
         }
       }
@@ -671,10 +671,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       // finish of this CTA's requests; scratch on the A tile (its MMAs are done)
       const BiasSrc b{nullptr, p.E, pp.Wt, prev, stride, p.r};
       for (int nn = cta; nn < p.R; nn += n_ctas)
-        finish_request<__nv_bfloat16, kHalf, NamedSync<3, 256>>(
+        finish_request<__nv_bfloat16, kHalf, NamedSync<3, 256>, true>(
             fs, nn, p.V, p.gamma, k, p.n_parts, pp.z, b, p.sc, p.greedy, p.part, pp.u, pp.tokens,
             pp.q_lse, pp.q_tok, p.status);
       grid_sync(pp.grid_counter, (++epoch) * n_ctas, &s_abort, p.status);
+    }
+    // The finishes left each q_lse entry holding its normaliser; take the
+    // logarithms here, off the per-position path (same CTA, same requests).
+    if (!p.greedy) {
+      const int mine = p.R > cta ? (p.R - cta + (int)n_ctas - 1) / (int)n_ctas : 0;
+      for (int i = threadIdx.x; i < mine * p.gamma; i += 256) {
+        const size_t o = (size_t)(cta + (i / p.gamma) * (int)n_ctas) * p.gamma + i % p.gamma;
+        const double tot = pp.q_lse[o];
+        pp.q_lse[o] = tot > 0.0 ? log(tot) : -INFINITY;
+      }
     }
   }
 

@@ -36,34 +36,19 @@ struct BiasSrc {
 
 // Shared-memory scratch of one finish (about 8 KiB).
 struct FinishScratch {
-  double incl[256];
-  double shd[8];
+  long long incl[256];
   long long shl[8];
   float shf[8];
   int shi[8];
   ArgMax sha[8];
-  double base;
+  long long base;
+  long long mass;
+  int fallback;
   float bias[256];
   float erow[1024];
 };
 
 // ---- reductions over 256 threads (8 warps), every thread gets the result
-
-template <class S>
-__device__ __forceinline__ double g_scan_d(double v, double* sh) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const double n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
-  }
-  S::sync();
-  if (lane == 31) sh[wid] = v;
-  S::sync();
-  double off = 0.0;
-  for (int w = 0; w < wid; ++w) off += sh[w];
-  return v + off;
-}
 
 template <class S>
 __device__ __forceinline__ long long g_scan_ll(long long v, long long* sh) {
@@ -185,7 +170,7 @@ __device__ __forceinline__ void tile_bias_recompute(const BiasSrc& b, int V, int
 // ArgMax pairs) of width TW.  Writes tokens / q_lse / q_tok [n][k].
 // Partials and previous tokens may have been written by other blocks of the
 // same kernel, so they are read past L1 (ld.global.cg).
-template <typename T, int TW, class S>
+template <typename T, int TW, class S, bool kDeferLog>
 __device__ void finish_request(FinishScratch& s, int n, int V, int gamma, int k, int n_tiles,
                                const T* __restrict__ z, const BiasSrc& bsrc, ScalePair sc,
                                int greedy, const double* part, const float* __restrict__ u,
@@ -229,20 +214,38 @@ __device__ void finish_request(FinishScratch& s, int n, int V, int gamma, int k,
   const double* S_ = part + (size_t)n * n_tiles;
   const int seg = (n_tiles + 255) / 256;
   const int t0 = min(n_tiles, tid * seg), t1 = min(n_tiles, t0 + seg);
-  double loc = 0.0;
-  for (int t = t0; t < t1; ++t) loc += __ldcg(S_ + t);
-  const double incl = g_scan_d<S>(loc, s.shd);
+  // The partials are exact doubles; sum them exactly as integers in units of
+  // 2^g, g chosen from the largest partial's exponent so that the sum of all
+  // n_tiles partials stays below 2^62.
+  int emax = INT_MIN;
+  for (int t = t0; t < t1; ++t) emax = max(emax, double_exponent(__ldcg(S_ + t)));
+  emax = g_max_i<S>(emax, s.shi);
+  if (emax == INT_MIN) {  // no token has mass
+    if (tid == 0) {
+      set_flag(status, kFlagNonFinite);
+      tokens[out] = 0;
+      q_lse[out] = kDeferLog ? 0.0 : -INFINITY;
+      q_tok[out] = 0.0f;
+    }
+    S::sync();
+    return;
+  }
+  const int g = emax + 2 + (32 - __clz(n_tiles)) - 62;
+  long long loc = 0;
+  for (int t = t0; t < t1; ++t) loc += double_to_fix(__ldcg(S_ + t), g);
+  const long long incl = g_scan_ll<S>(loc, s.shl);
   s.incl[tid] = incl;
   S::sync();
-  const double excl = tid > 0 ? s.incl[tid - 1] : 0.0;
-  const double total = s.incl[255];
-  const double thr = (double)u[out] * total;
+  const long long F = s.incl[255];
+  // the draw is the first token whose running sum exceeds u*F; for integer
+  // running sums that is "exceeds floor(u*F)"
+  const long long thr = floor_mul(u[out], F);
   int cand = 0x7fffffff;
-  double base = 0.0;
+  long long base = 0;
   {
-    double run = excl;
+    long long run = incl - loc;
     for (int t = t0; t < t1; ++t) {
-      const double nx = run + __ldcg(S_ + t);
+      const long long nx = run + double_to_fix(__ldcg(S_ + t), g);
       if (nx > thr) {
         cand = t;
         base = run;
@@ -253,20 +256,21 @@ __device__ void finish_request(FinishScratch& s, int n, int V, int gamma, int k,
   }
   int tsel = g_min_i<S>(cand, s.shi);
   if (tsel == 0x7fffffff) {
-    // rounding left no crossing: last tile with mass
+    // u outside [0, 1): the last tile with mass
     int last = -1;
     for (int t = t0; t < t1; ++t)
       if (__ldcg(S_ + t) > 0.0) last = t;
     tsel = g_max_i<S>(last, s.shi);
     if (tsel < 0) tsel = 0;
-    if (tid == 0) s.base = -1.0;  // marks the fallback
+    if (tid == 0) s.fallback = 1;
   } else if (cand == tsel) {
     s.base = base;
+    s.fallback = 0;
   }
   S::sync();
-  const bool fallback = s.base < 0.0;
+  const bool fallback = s.fallback != 0;
   base = s.base;
-  const double S_sel = __ldcg(S_ + tsel);
+  const long long S_sel = double_to_fix(__ldcg(S_ + tsel), g);
   // Recompute the chosen tile.
   const int v = tsel * TW + tid;
   const bool ok = tid < TW && v < V;
@@ -287,22 +291,27 @@ __device__ void finish_request(FinishScratch& s, int n, int V, int gamma, int k,
   float w = 0.f;
   const long long f = (ok && a > -INFINITY && amax > -INFINITY) ? rel_fix(a, ref, &w) : 0ll;
   const long long cum = g_scan_ll<S>(f, s.shl);
+  if (tid == 255) s.mass = cum;
   S::sync();
-  if (tid == 255) s.incl[0] = ldexp((double)cum, (int)ref - kFixRel);
-  S::sync();
-  const double tile_mass = s.incl[0];
-  // the crossing's position inside the tile, as a fraction of the tile mass
-  const double target = S_sel > 0.0 ? (thr - base) * (tile_mass / S_sel) : 0.0;
+  const long long mass = s.mass;
+  // The recomputed tile can differ from its partial in the last bits, so the
+  // crossing is placed at the same fraction of the recomputed tile:
+  //   cum / mass > (thr - base) / S_sel  <=>  cum * S_sel > (thr - base) * mass
+  // compared exactly in 128-bit products.
+  const unsigned long long need = (unsigned long long)(thr - base);
   int pick = 0x7fffffff;
-  if (!fallback && f > 0 && ldexp((double)cum, (int)ref - kFixRel) > target) pick = tid;
+  if (!fallback && f > 0 &&
+      mul_gt((unsigned long long)cum, (unsigned long long)S_sel, need, (unsigned long long)mass))
+    pick = tid;
   int isel = g_min_i<S>(pick, s.shi);
   if (isel == 0x7fffffff) isel = g_max_i<S>(f > 0 ? tid : -1, s.shi);
   if (isel < 0) isel = 0;
   if (tid == isel) {
     tokens[out] = tsel * TW + isel;
-    if (!(total > 0.0) || !isfinite(total)) set_flag(status, kFlagNonFinite);
-    q_lse[out] = log(total);
-    q_tok[out] = (float)(ldexp((double)w, (int)ref) / total);
+    const double total = fix_to_double(F, g);  // sum_v 2^a_v
+    q_lse[out] = kDeferLog ? total : log(total);
+    // q(x) = 2^a / total = w * 2^ref / (F * 2^g)
+    q_tok[out] = scale_pow2(w / (float)F, (int)ref - g);
   }
   S::sync();
 }

@@ -102,13 +102,26 @@ __global__ void __launch_bounds__(256) verify_rows_kernel(
 #pragma unroll
         for (int e = 0; e < 8; ++e) k.add(ex2_fast(x[i][e] - ref));
       const long long f = warp_sum(k.fixed40());
-      S = ldexp((double)f, (int)ref - kFixRel);
+      S = fix_to_double(f, (int)ref - kFixRel);
     }
     if (lane == 0) *out = S;
   }
 }
 
 // ---------------------------------------------------------------- decide
+
+// u < p(x) / q(x) with p(x) = 2^a / Sp, a = t_x * log2(e) / T, in fp32
+// (Sp = m * 2^e taken apart by its bits, m to 24 bits): the result can differ
+// from the exact comparison only when u lies within about 1e-6 of the ratio.
+__device__ __forceinline__ bool accept_test(float tx, ScalePair sc, double Sp, float qx, float u) {
+  const int es = double_exponent(Sp);
+  if (es == INT_MIN || !isfinite(Sp)) return false;
+  const long long b = __double_as_longlong(Sp);
+  const float ms = __int_as_float(0x3f800000 | (int)((b >> 29) & 0x7fffff));  // [1, 2)
+  const float p = exp2f(scaled(tx, sc) - (float)es) / ms;
+  return u < p / qx;
+}
+
 
 template <typename T>
 __global__ void __launch_bounds__(256) verify_decide_kernel(
@@ -136,7 +149,7 @@ __global__ void __launch_bounds__(256) verify_decide_kernel(
     for (int j = tid; j <= gamma; j += blockDim.x) ot[j] = -1;
     if (tid == 0) {
       n_acc_out[n] = 0;
-      VerifyState st{0, -1, 0, -1, 0.0, 0.0, 0.0, 0.0};
+      VerifyState st{0, -1, 0, -1, {0.f, 0.f, 0}, {0.f, 0.f, 0}};
       vstate[n] = st;
       prev_out[n] = -1;
     }
@@ -166,47 +179,43 @@ __global__ void __launch_bounds__(256) verify_decide_kernel(
     }
   }
   __syncthreads();
-  if (tid != 0) return;
-  int nacc = L;
-  for (int j = 0; j < L; ++j) {
-    const int x = tokens[(size_t)n * gamma + j];
-    bool acc;
+  if (wid != 0) return;
+  // warp 0: the accept tests of the L drafted positions, one lane each, then
+  // n_acc = the first rejection
+  bool acc = true;
+  if (lane < L) {
+    const int x = tokens[(size_t)n * gamma + lane];
     if (x < 0 || x >= V) {
       set_flag(status, kFlagTokenRange);
       acc = false;
     } else if (greedy) {
-      acc = (x == am_s[j].i);
+      acc = (x == am_s[lane].i);
     } else {
-      const float tx = to_f32<T>(target[(size_t)(r0 + j) * V + x]);
-      const double px = exp2((double)scaled(tx, sc)) / Sp[j];
-      const double ratio = px / (double)q_tok[(size_t)n * gamma + j];
-      acc = (double)u_acc[(size_t)n * gamma + j] < ratio;
-    }
-    if (!acc) {
-      nacc = j;
-      break;
+      acc = accept_test(to_f32<T>(target[(size_t)(r0 + lane) * V + x]), sc, Sp[lane],
+                        q_tok[(size_t)n * gamma + lane], u_acc[(size_t)n * gamma + lane]);
     }
   }
-  n_acc_out[n] = nacc;
-  for (int j = 0; j <= gamma; ++j) {
+  const unsigned live = L >= 32 ? 0xffffffffu : ((1u << L) - 1u);
+  const unsigned rej = __ballot_sync(0xffffffffu, !acc) & live;
+  const int nacc = rej ? __ffs(rej) - 1 : L;
+  for (int j = lane; j <= gamma; j += 32) {
     int v = -1;
     if (j < nacc) v = tokens[(size_t)n * gamma + j];
     else if (j == nacc && greedy) v = am_s[nacc].i;
     ot[j] = v;
   }
+  if (lane != 0) return;
+  n_acc_out[n] = nacc;
   VerifyState st;
   st.n_acc = nacc;
   st.mode = greedy ? -1 : (nacc == L ? 0 : 1);
   st.final_row = (int)(r0 + nacc);
   st.prev = -1;
-  st.Sp = greedy ? 0.0 : Sp[nacc];
-  st.inv_Sp = greedy ? 0.0 : 1.0 / Sp[nacc];
-  st.Sq = 0.0;
-  st.inv_Sq = 0.0;
+  st.ip = greedy ? InvPair{0.f, 0.f, 0} : split_inv(1.0 / Sp[nacc]);
+  st.iq = InvPair{0.f, 0.f, 0};
   if (st.mode == 1) {
     st.prev = nacc == 0 ? anchor[n] : tokens[(size_t)n * gamma + nacc - 1];
-    st.Sq = exp(q_lse[(size_t)n * gamma + nacc]);
-    st.inv_Sq = 1.0 / st.Sq;
+    st.iq = split_inv(exp(-q_lse[(size_t)n * gamma + nacc]));
   }
   vstate[n] = st;
   prev_out[n] = st.prev;
@@ -214,13 +223,9 @@ __global__ void __launch_bounds__(256) verify_decide_kernel(
 
 // ---------------------------------------------------------------- final draw
 
-// (hi, lo) fp32 split of 2^ref * inv_S (exact power-of-two scaling in double).
-__device__ __forceinline__ ScalePair norm_pair(int ref, double inv_S) {
-  const double k = ldexp(inv_S, ref);
-  ScalePair p;
-  p.hi = (float)k;
-  p.lo = (float)(k - (double)p.hi);
-  return p;
+// (hi, lo) fp32 pair of 2^ref / S from the request's InvPair of 1/S.
+__device__ __forceinline__ ScalePair norm_pair(int ref, InvPair ip) {
+  return ScalePair{scale_pow2(ip.hi, ref + ip.e), scale_pow2(ip.lo, ref + ip.e)};
 }
 
 // One warp, one 256-token tile of request n's final draw: per lane the eight
@@ -265,15 +270,8 @@ __device__ __forceinline__ void final_warp_tile(int gamma, int V, int t,
   }
   const int refp = mp > -1.0e38f ? (int)ceilf(mp) : 0;
   const int refq = mq > -1.0e38f ? (int)ceilf(mq) : 0;
-  ScalePair kp{0.f, 0.f}, kq{0.f, 0.f};
-  if (lane == 0) {
-    if (mp > -1.0e38f) kp = norm_pair(refp, st.inv_Sp);
-    if (mq > -1.0e38f) kq = norm_pair(refq, st.inv_Sq);
-  }
-  kp.hi = __shfl_sync(0xffffffffu, kp.hi, 0);
-  kp.lo = __shfl_sync(0xffffffffu, kp.lo, 0);
-  kq.hi = __shfl_sync(0xffffffffu, kq.hi, 0);
-  kq.lo = __shfl_sync(0xffffffffu, kq.lo, 0);
+  const ScalePair kp = mp > -1.0e38f ? norm_pair(refp, st.ip) : ScalePair{0.f, 0.f};
+  const ScalePair kq = mq > -1.0e38f ? norm_pair(refq, st.iq) : ScalePair{0.f, 0.f};
   constexpr float k2_60 = 1152921504606846976.0f;  // 2^60
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
@@ -317,21 +315,6 @@ __global__ void __launch_bounds__(256) final_partial_kernel(
     out[0] = sr;
     out[1] = sp;
   }
-}
-
-// floor(u * F) exactly, for u in [0, 1) and 0 <= F < 2^62.
-__device__ __forceinline__ long long floor_mul(float u, long long F) {
-  if (!(u > 0.0f)) return 0;
-  int e;
-  const float mf = frexpf(u, &e);  // u = mf * 2^e, mf in [0.5, 1)
-  const unsigned long long m = (unsigned long long)(mf * 16777216.0f);  // u = m * 2^(e-24)
-  const unsigned long long lo = m * (unsigned long long)F;
-  const unsigned long long hi = __umul64hi(m, (unsigned long long)F);
-  const int sh = 24 - e;
-  if (sh <= 0) return F;  // u >= 1: outside the contract, clamp
-  if (sh >= 128) return 0;
-  if (sh >= 64) return (long long)(hi >> (sh - 64));
-  return (long long)((lo >> sh) | (hi << (64 - sh)));
 }
 
 template <typename T>
