@@ -423,7 +423,30 @@ struct PersistParams {
   float* q_tok;
   const float* u;
   unsigned* grid_counter;  // zeroed before the launch
+  int pair;                // R <= 64: two vocabulary tiles per accumulator
 };
+
+// Paired layout (R <= 64).  A 128-row accumulator holds two vocabulary tiles:
+// rows 0-63 the requests against tile t1, rows 64-127 the same requests
+// against tile t2.  The A operand lives in 8 KiB blocks of 64 swizzled rows,
+// [0, E_0, 0, E_1, ..., E_{nK-1}, 0] (E_c = K-chunk c of the gathered E rows,
+// 0 = zero rows): the descriptor starting at E_c reads [E_c; 0] and the one
+// starting at the zero block before it reads [0; E_c], so one accumulator
+// receives E W(t1) in its top half and E W(t2) in its bottom half from two
+// K-passes, with no more MMA work than two unpaired tiles and every TMEM
+// lane quadrant (hence every epilogue warp) holding live rows.
+constexpr uint32_t kPairBlk = 64 * 128;  // 64 rows x 128 bytes
+static_assert(sizeof(FinishScratch) <= kPairBlk, "finish scratch must fit one A block");
+
+__host__ __device__ inline uint32_t persist_a_bytes(int nK, int pair) {
+  return pair ? (uint32_t)(2 * nK + 1) * kPairBlk : (uint32_t)nK * kABytesPerChunk;
+}
+__host__ __device__ inline int persist_z_slots(int pair) { return pair ? 3 : kZBoxes; }
+
+size_t persist_smem_bytes(int nK, int pair) {
+  return 1024 + (size_t)persist_a_bytes(nK, pair) + kStagesB * kBBytes +
+         (size_t)persist_z_slots(pair) * kZBytes + kBars * sizeof(uint64_t) + 16;
+}
 
 // Grid-wide barrier among the 256 epilogue threads of every CTA (bounded:
 // gives up after about two seconds, setting the timeout flag).
@@ -453,15 +476,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     draft_persistent_kernel(const __grid_constant__ CUtensorMap tm_w,
                             const __grid_constant__ CUtensorMap tm_z, const PersistParams pp) {
   const TcParams& p = pp.p;
+  const bool pair = pp.pair != 0;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_abort;
   __shared__ int s_tok[BM];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = sA + p.nK * kABytesPerChunk;
+  uint8_t* sB = sA + persist_a_bytes(p.nK, pp.pair);
   uint8_t* sZ = sB + kStagesB * kBBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sZ + kZBoxes * kZBytes);
+  const int nzs = persist_z_slots(pp.pair);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sZ + nzs * kZBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBars - 1);
   const uint32_t b_fullB = smem_u32(bars + 0);
   const uint32_t b_emptyB = smem_u32(bars + 3);
@@ -475,15 +500,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int r0 = blockIdx.y * BM;
   const unsigned n_ctas = gridDim.x * gridDim.y;
   const int cta = blockIdx.y * gridDim.x + blockIdx.x;
+  // work units: one tile, or (paired) tiles 2u and 2u + 1
+  const int n_units = pair ? (p.n_vt + 1) / 2 : p.n_vt;
+  const int nW = pair ? 2 * p.nK : p.nK;  // W chunks per unit
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStagesB; ++i) {
       mbar_init(b_fullB + 8 * i, 1);
       mbar_init(b_emptyB + 8 * i, 1);
     }
-    for (int i = 0; i < kZBoxes; ++i) {
+    for (int i = 0; i < nzs; ++i) {
       mbar_init(b_fullZ + 8 * i, 1);
-      mbar_init(b_emptyZ + 8 * i, 4);
+      mbar_init(b_emptyZ + 8 * i, 4);  // the four warps of one token half
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_accFull + 8 * i, 1);
@@ -501,6 +529,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch(&tm_w);
     tma_prefetch(&tm_z);
   }
+  if (pair && threadIdx.x < 256) {
+    // the zero blocks of the paired A operand, written once
+    for (int c = 0; c <= p.nK; ++c) {
+      uint4* blk = reinterpret_cast<uint4*>(sA + (size_t)(2 * c) * kPairBlk);
+      for (int i = threadIdx.x; i < (int)(kPairBlk / 16); i += 256) blk[i] = make_uint4(0, 0, 0, 0);
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -511,13 +546,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol = policy_evict_last();
       uint32_t it = 0;
       for (int k = 0; k < p.gamma; ++k)
-        for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x)
-          for (int c = 0; c < p.nK; ++c, ++it) {
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x)
+          for (int i = 0; i < nW; ++i, ++it) {
+            const int t = pair ? 2 * u + i / p.nK : u, c = i % p.nK;
             const uint32_t s = it % kStagesB, ph = (it / kStagesB) & 1;
             wait_abortable(b_emptyB + 8 * s, ph ^ 1, &s_abort, p.status);
-            mbar_arrive_expect_tx(b_fullB + 8 * s, kBBytes);
-            tma_load_2d_hint(smem_u32(sB + s * kBBytes), &tm_w, b_fullB + 8 * s, c * BK, t * BN,
-                             pol);
+            if (t < p.n_vt) {
+              mbar_arrive_expect_tx(b_fullB + 8 * s, kBBytes);
+              tma_load_2d_hint(smem_u32(sB + s * kBBytes), &tm_w, b_fullB + 8 * s, c * BK, t * BN,
+                               pol);
+            } else {
+              // the odd last unit's second tile lies past V: no load, its
+              // accumulator rows are never read
+              mbar_arrive(b_fullB + 8 * s);
+            }
           }
     }
   } else if (warp == kWarpZ) {
@@ -525,14 +567,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol = policy_evict_first();
       uint32_t it = 0;
       for (int k = 0; k < p.gamma; ++k)
-        for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x)
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x)
           for (int j = 0; j < kZBoxes; ++j, ++it) {
-            const uint32_t s = it % kZBoxes, ph = (it / kZBoxes) & 1;
+            const uint32_t s = it % nzs, ph = (it / nzs) & 1;
             wait_abortable(b_emptyZ + 8 * s, ph ^ 1, &s_abort, p.status);
-            fence_proxy_async_smem();  // generic reads of the box before the TMA refill
-            mbar_arrive_expect_tx(b_fullZ + 8 * s, kZBytes);
-            tma_load_3d_hint(smem_u32(sZ + s * kZBytes), &tm_z, b_fullZ + 8 * s, t * BN + j * 64,
-                             k, r0, pol);
+            fence_proxy_async_smem();  // generic reads of the slot before the TMA refill
+            const uint32_t dst = smem_u32(sZ + s * kZBytes);
+            if (pair) {
+              // rows 0-63: the requests' logits of tile 2u; rows 64-127: of tile 2u + 1
+              const bool second = 2 * u + 1 < p.n_vt;
+              mbar_arrive_expect_tx(b_fullZ + 8 * s, second ? kZBytes : kZBytes / 2);
+              tma_load_3d_hint(dst, &tm_z, b_fullZ + 8 * s, (2 * u) * BN + j * 64, k, 0, pol);
+              if (second)
+                tma_load_3d_hint(dst + kZBytes / 2, &tm_z, b_fullZ + 8 * s,
+                                 (2 * u + 1) * BN + j * 64, k, 0, pol);
+            } else {
+              mbar_arrive_expect_tx(b_fullZ + 8 * s, kZBytes);
+              tma_load_3d_hint(dst, &tm_z, b_fullZ + 8 * s, u * BN + j * 64, k, r0, pol);
+            }
           }
     }
   } else if (warp == kWarpMma) {
@@ -540,21 +592,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0; k < p.gamma; ++k) {
       NamedSync<1, 288>::sync();  // A(k) is in shared memory
       if (lane == 0) {
-        for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x, ++acc_it) {
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++acc_it) {
           const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
           wait_abortable(b_accEmpty + 8 * a, aph ^ 1, &s_abort, p.status);
           tc_fence_after();
           const uint32_t d_tmem = tmem + a * BN;
-          for (int c = 0; c < p.nK; ++c, ++it) {
+          for (int i = 0; i < nW; ++i, ++it) {
             const uint32_t s = it % kStagesB, ph = (it / kStagesB) & 1;
             wait_abortable(b_fullB + 8 * s, ph, &s_abort, p.status);
             tc_fence_after();
-            const uint32_t a_base = smem_u32(sA + c * kABytesPerChunk);
+            const int c = i % p.nK;
+            // paired: first pass [E_c; 0] against tile 2u, second [0; E_c] against 2u + 1
+            const uint32_t a_base =
+                pair ? smem_u32(sA + (size_t)(2 * c + (i < p.nK ? 1 : 0)) * kPairBlk)
+                     : smem_u32(sA + c * kABytesPerChunk);
             const uint32_t b_base = smem_u32(sB + s * kBBytes);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
               mma_bf16(d_tmem, desc_kmajor_sw128(a_base + kk * 32),
-                       desc_kmajor_sw128(b_base + kk * 32), kIdesc, (c | kk) != 0);
+                       desc_kmajor_sw128(b_base + kk * 32), kIdesc, (i | kk) != 0);
             mma_commit(b_emptyB + 8 * s);
           }
           mma_commit(b_accFull + 8 * a);
@@ -569,18 +625,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- epilogue warps 0-7 (also the gather and the finish)
     const int quad = warp & 3, half = warp >> 2;
-    const int m = quad * 32 + lane;
-    const int n = r0 + m;
+    const int m = quad * 32 + lane;  // TMEM lane = row of the z slot
+    // paired: lanes 0-63 are requests 0-63 on tile 2u, lanes 64-127 on 2u + 1
+    const int n = pair ? (m & 63) : r0 + m;
+    const int tsub = pair ? (m >> 6) : 0;
     const bool valid = n < p.R;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    uint32_t acc_it = 0, zit0 = 0, epoch = 0;
-    FinishScratch& fs = *reinterpret_cast<FinishScratch*>(sA);
+    const int rows = pair ? 64 : BM;  // gathered A rows
+    uint32_t acc_it = 0, zit = 0, epoch = 0;
+    FinishScratch& fs = *reinterpret_cast<FinishScratch*>(pair ? sA + kPairBlk : sA);
     for (int k = 0; k < p.gamma; ++k) {
       const int32_t* prev = k == 0 ? pp.anchor : pp.tokens + (k - 1);
       const int stride = k == 0 ? 1 : p.gamma;
       // gather A(k): the rows of E at the previous tokens
-      if (threadIdx.x < BM) {
-        const int nn = r0 + threadIdx.x;
+      if (threadIdx.x < rows) {
+        const int nn = (pair ? 0 : r0) + threadIdx.x;
         int tok = -1;
         if (nn < p.R) {
           tok = __ldcg(prev + (size_t)nn * stride);
@@ -600,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kPer; ++i) {
           const int idx = threadIdx.x + i * 256;
           val[i] = make_uint4(0, 0, 0, 0);
-          if (idx < BM * per_row) {
+          if (idx < rows * per_row) {
             const int mm = idx / per_row, rem = idx - mm * per_row;
             const int col = (rem >> 3) * BK + (rem & 7) * 8;
             const int tok = s_tok[mm];
@@ -611,19 +670,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kPer; ++i) {
           const int idx = threadIdx.x + i * 256;
-          if (idx < BM * per_row) {
+          if (idx < rows * per_row) {
             const int mm = idx / per_row, rem = idx - mm * per_row;
             const int c = rem >> 3, g = rem & 7;
-            *reinterpret_cast<uint4*>(sA + c * kABytesPerChunk + mm * 128 + ((g ^ (mm & 7)) << 4)) =
-                val[i];
+            uint8_t* blk = pair ? sA + (size_t)(2 * c + 1) * kPairBlk : sA + c * kABytesPerChunk;
+            *reinterpret_cast<uint4*>(blk + mm * 128 + ((g ^ (mm & 7)) << 4)) = val[i];
           }
         }
       }
       fence_proxy_async_smem();
       NamedSync<1, 288>::sync();  // release the MMA warp
-      // partial pass over this CTA's tiles
-      for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x, ++acc_it, zit0 += kZBoxes) {
+      // partial pass over this CTA's units
+      for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++acc_it, zit += kZBoxes) {
         const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
+        const int t = pair ? 2 * u + tsub : u;
         wait_abortable(b_accFull + 8 * a, aph, &s_abort, p.status);
         tc_fence_after();
         Part s{0, INT_MIN, ArgMax{-INFINITY, 0x7fffffff}, 0.f};
@@ -636,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_32x32b_x32(tmem + lane_base + a * BN + col, b0);
           tmem_ld_32x32b_x32(tmem + lane_base + a * BN + col + 32, b1);
           const int v0 = t * BN + col;
-          const uint32_t zs = (zit0 + j) % kZBoxes, zph = ((zit0 + j) / kZBoxes) & 1;
+          const uint32_t zs = (zit + j) % nzs, zph = ((zit + j) / nzs) & 1;
           wait_abortable(b_fullZ + 8 * zs, zph, &s_abort, p.status);
           uint4 z0[4], z1[4];
           const uint8_t* zrow = sZ + zs * kZBytes + m * 128;
@@ -656,19 +716,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(b_accEmpty + 8 * a);
-        if (valid) {
+        if (valid && t * 2 + half < p.n_parts) {
           if (s.check != s.check || s.check == INFINITY) set_flag(p.status, kFlagNonFinite);
           const size_t o = (size_t)n * p.n_parts + t * 2 + half;
-          if (t * 2 + half < p.n_parts) {
-            if (p.greedy)
-              reinterpret_cast<ArgMax*>(p.part)[o] = s.best;
-            else
-              p.part[o] = (s.ref == INT_MIN) ? 0.0 : fix_to_double(s.acc, s.ref - kFixRel);
-          }
+          if (p.greedy)
+            reinterpret_cast<ArgMax*>(p.part)[o] = s.best;
+          else
+            p.part[o] = (s.ref == INT_MIN) ? 0.0 : fix_to_double(s.acc, s.ref - kFixRel);
         }
       }
       grid_sync(pp.grid_counter, (++epoch) * n_ctas, &s_abort, p.status);
-      // finish of this CTA's requests; scratch on the A tile (its MMAs are done)
+      // finish of this CTA's requests; scratch on an A block (its MMAs are
+      // done: order their async-proxy reads before these generic writes)
+      fence_proxy_async_smem();
       const BiasSrc b{nullptr, p.E, pp.Wt, prev, stride, p.r};
       for (int nn = cta; nn < p.R; nn += n_ctas)
         finish_request<__nv_bfloat16, kHalf, NamedSync<3, 256>, true>(
@@ -729,10 +789,10 @@ cudaError_t encode_w(CUtensorMap* m, const void* Wt, int V, int r) {
              : cudaErrorInvalidValue;
 }
 
-cudaError_t encode_z(CUtensorMap* m, const void* z, int R, int gamma, int V) {
+cudaError_t encode_z(CUtensorMap* m, const void* z, int R, int gamma, int V, int box_rows = BM) {
   cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)gamma, (cuuint64_t)R};
   cuuint64_t strides[2] = {(cuuint64_t)V * 2, (cuuint64_t)gamma * V * 2};
-  cuuint32_t box[3] = {64, 1, BM};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
   cuuint32_t es[3] = {1, 1, 1};
   return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(z), dims, strides,
                      box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -810,9 +870,10 @@ cudaError_t launch_draft_partial_tc(const DraftArgs& a, int k, const int32_t* pr
 // one CTA per SM for the whole grid (the caller then launches per position).
 cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st) {
   if (a.grid_counter == nullptr) return cudaErrorNotSupported;
+  const int pair = a.R <= 64 ? 1 : 0;
   CUtensorMap tm_w, tm_z;
   cudaError_t e = encode_w(&tm_w, a.Wt, a.V, a.r);
-  if (e == cudaSuccess) e = encode_z(&tm_z, a.z, a.R, a.gamma, a.V);
+  if (e == cudaSuccess) e = encode_z(&tm_z, a.z, a.R, a.gamma, a.V, pair ? 64 : BM);
   if (e != cudaSuccess) return e;
   PersistParams pp;
   TcParams& p = pp.p;
@@ -840,6 +901,7 @@ cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st) {
   pp.q_tok = a.q_tok;
   pp.u = a.u;
   pp.grid_counter = a.grid_counter;
+  pp.pair = pair;
   static bool attr_set = false;
   if (!attr_set) {
     e = cudaFuncSetAttribute(draft_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -847,15 +909,16 @@ cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const size_t smem = tc_smem_bytes(p.nK);
+  const size_t smem = persist_smem_bytes(p.nK, pair);
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, draft_persistent_kernel, kThreads,
                                                     smem);
   if (e != cudaSuccess || per_sm < 1) return cudaErrorNotSupported;
   const int n_rt = (a.R + BM - 1) / BM;
+  const int n_units = pair ? (p.n_vt + 1) / 2 : p.n_vt;
   int gx = sm_count() / n_rt;
   if (gx < 1) return cudaErrorNotSupported;
-  if (gx > p.n_vt) gx = p.n_vt;
+  if (gx > n_units) gx = n_units;
   e = cudaMemsetAsync(a.grid_counter, 0, sizeof(unsigned), st);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};

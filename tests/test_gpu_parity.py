@@ -23,6 +23,13 @@ SMALL = {
                                        n_sps=0),
     "one_request": W["qwen3_4b"].scaled(name="one_request", R=1, gamma=1, V=264, r=16, d=8,
                                         n_sps=0),
+    # an odd number of 256-token tiles: with R <= 64 the last tile pair of the
+    # tensor-core draft has no second tile
+    "odd_tiles": W["qwen3_4b"].scaled(name="odd_tiles", R=40, gamma=3, V=2800, r=64, d=32,
+                                      n_sps=0),
+    # more than 64 requests on one 128-row tile (the unpaired tensor-core layout)
+    "rows_100": W["qwen3_4b"].scaled(name="rows_100", R=100, gamma=3, V=4000, r=128, d=32,
+                                     n_sps=0),
 }
 
 pytestmark = pytest.mark.gpu
