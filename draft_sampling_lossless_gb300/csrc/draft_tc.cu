@@ -105,48 +105,80 @@ __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 
 struct Part {
   long long acc;  // sum of 2^(a - ref) in units of 2^-40
   int ref;        // power-of-two reference, INT_MIN = no mass yet
+  int bad;        // a NaN or +inf input was seen
   ArgMax best;    // greedy
-  float check;    // sum of every y: NaN or +inf exposes a non-finite input
 };
 
-// 32 consecutive tokens of one request row: y = z + bias, then the greedy
-// argmax or the fixed-point sum of 2^(a - ref) with a = y*log2(e)/T.  `lim`
-// = number of tokens of the 32 that lie below V.
-__device__ __forceinline__ void epi_chunk(const uint32_t (&b)[32], const uint4 (&zq)[4], int v0,
+// max(a, b) that returns NaN when either operand is NaN.
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// 64 consecutive tokens of one request row (two 32-column accumulator loads
+// and their z values): y = z + bias, then the greedy argmax or the
+// fixed-point sum of 2^(a - ref) with a = y*log2(e)/T.  `lim` = number of the
+// 64 tokens that lie below V.  The maxima and sums are trees, so a warp has
+// independent work to issue while MUFU and FMA results come back.
+__device__ __forceinline__ void epi_block(const uint32_t (&b0)[32], const uint32_t (&b1)[32],
+                                          const uint4 (&z0)[4], const uint4 (&z1)[4], int v0,
                                           int lim, const TcParams& p, Part& s) {
-  float y[32];
+  float y[64];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const uint32_t w4[4] = {zq[q].x, zq[q].y, zq[q].z, zq[q].w};
+    const uint32_t w0[4] = {z0[q].x, z0[q].y, z0[q].z, z0[q].w};
+    const uint32_t w1[4] = {z1[q].x, z1[q].y, z1[q].z, z1[q].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      y[q * 8 + 2 * e] = bf_lo(w4[e]) + __uint_as_float(b[q * 8 + 2 * e]);
-      y[q * 8 + 2 * e + 1] = bf_hi(w4[e]) + __uint_as_float(b[q * 8 + 2 * e + 1]);
+      y[q * 8 + 2 * e] = bf_lo(w0[e]) + __uint_as_float(b0[q * 8 + 2 * e]);
+      y[q * 8 + 2 * e + 1] = bf_hi(w0[e]) + __uint_as_float(b0[q * 8 + 2 * e + 1]);
+      y[32 + q * 8 + 2 * e] = bf_lo(w1[e]) + __uint_as_float(b1[q * 8 + 2 * e]);
+      y[32 + q * 8 + 2 * e + 1] = bf_hi(w1[e]) + __uint_as_float(b1[q * 8 + 2 * e + 1]);
     }
   }
-  if (lim < 32) {
+  if (lim < 64) {
 #pragma unroll
-    for (int e = 0; e < 32; ++e)
+    for (int e = 0; e < 64; ++e)
       if (e >= lim) y[e] = -INFINITY;
   }
   if (p.greedy) {
+    ArgMax t[32];
+    float chk = -INFINITY;
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
-      if (y[e] > s.best.v) s.best = ArgMax{y[e], v0 + e};
-      if (e < lim) s.check += y[e];
+      t[e] = better(ArgMax{y[e], v0 + e}, ArgMax{y[e + 32], v0 + e + 32});
+      chk = fmax_nan(chk, fmax_nan(y[e], y[e + 32]));
     }
+#pragma unroll
+    for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+      for (int e = 0; e < w; ++e) t[e] = better(t[e], t[e + w]);
+    s.best = better(s.best, t[0]);
+    if (!(chk < INFINITY)) s.bad = 1;
     return;
   }
-  // a = y * (hi + lo), clamped so that -inf (and NaN) become a finite
-  // "no mass" value instead of NaN
-  float cmax = -3.0e38f;
+  // a = y * (hi + lo).  -inf (a masked token) is first clamped to a finite
+  // value so that the two-term product cannot form inf - inf; NaN and +inf
+  // pass through and surface in the block maximum.
 #pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    if (e < lim) s.check += y[e];
-    y[e] = fmaxf(fmaf(y[e], p.sc.hi, y[e] * p.sc.lo), -3.0e38f);
-    cmax = fmaxf(cmax, y[e]);
+  for (int e = 0; e < 64; ++e) {
+    const float yc = fmax_nan(y[e], -3.0e38f);
+    y[e] = fmaf(yc, p.sc.hi, yc * p.sc.lo);
   }
-  if (cmax <= -1.0e38f) return;
+  float mx[32];
+#pragma unroll
+  for (int e = 0; e < 32; ++e) mx[e] = fmax_nan(y[e], y[e + 32]);
+#pragma unroll
+  for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+    for (int e = 0; e < w; ++e) mx[e] = fmax_nan(mx[e], mx[e + w]);
+  const float cmax = mx[0];
+  if (!(cmax < 3.0e38f)) {  // NaN or +inf among the inputs
+    s.bad = 1;
+    return;
+  }
+  if (cmax <= -1.0e38f) return;  // no mass in these tokens
   const int cref = static_cast<int>(ceilf(cmax));
   if (s.ref == INT_MIN) {
     s.ref = cref;
@@ -156,13 +188,19 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&b)[32], const uint4 (
     s.ref = cref;
   }
   const float fref = static_cast<float>(s.ref);
+  long long add = 0;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    float s8 = 0.f;
+  for (int g = 0; g < 4; ++g) {
+    float t[16];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) s8 += ex2_approx(y[q * 8 + e] - fref);
-    s.acc += __float2ll_rn(s8 * 1099511627776.0f);  // 2^40
+    for (int e = 0; e < 16; ++e) t[e] = ex2_approx(y[g * 16 + e] - fref);
+#pragma unroll
+    for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+      for (int e = 0; e < w; ++e) t[e] += t[e + w];
+    add += __float2ll_rn(t[0] * 1099511627776.0f);  // 2^40
   }
+  s.acc += add;
 }
 
 template <bool kBiasOut>
@@ -340,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
       wait_abortable(b_accFull + 8 * a, aph, &s_abort, p.status);
       tc_fence_after();
-      Part s{0, INT_MIN, ArgMax{-INFINITY, 0x7fffffff}, 0.f};
+      Part s{0, INT_MIN, 0, ArgMax{-INFINITY, 0x7fffffff}};
 #pragma unroll 1
       for (int jj = 0; jj < 2; ++jj) {
         const int j = half * 2 + jj;  // z box (64 tokens) of this warp
@@ -377,16 +415,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(b_emptyZ + 8 * zs);
         tmem_wait_ld();
-        if (valid) {
-          epi_chunk(b0, z0, v0, min(32, p.V - v0), p, s);
-          epi_chunk(b1, z1, v0 + 32, min(32, p.V - v0 - 32), p, s);
-        }
+        if (valid) epi_block(b0, b1, z0, z1, v0, min(64, p.V - v0), p, s);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_accEmpty + 8 * a);
       if (!kBiasOut && valid) {
-        if (s.check != s.check || s.check == INFINITY) set_flag(p.status, kFlagNonFinite);
+        if (s.bad) set_flag(p.status, kFlagNonFinite);
         const size_t o = (size_t)n * p.n_parts + t * 2 + half;
         if (t * 2 + half < p.n_parts) {
           if (p.greedy)
@@ -686,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = pair ? 2 * u + tsub : u;
         wait_abortable(b_accFull + 8 * a, aph, &s_abort, p.status);
         tc_fence_after();
-        Part s{0, INT_MIN, ArgMax{-INFINITY, 0x7fffffff}, 0.f};
+        Part s{0, INT_MIN, 0, ArgMax{-INFINITY, 0x7fffffff}};
 #pragma unroll 1
         for (int jj = 0; jj < 2; ++jj) {
           const int j = half * 2 + jj;
@@ -708,16 +743,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(b_emptyZ + 8 * zs);
           tmem_wait_ld();
-          if (valid) {
-            epi_chunk(b0, z0, v0, min(32, p.V - v0), p, s);
-            epi_chunk(b1, z1, v0 + 32, min(32, p.V - v0 - 32), p, s);
-          }
+          if (valid) epi_block(b0, b1, z0, z1, v0, min(64, p.V - v0), p, s);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(b_accEmpty + 8 * a);
         if (valid && t * 2 + half < p.n_parts) {
-          if (s.check != s.check || s.check == INFINITY) set_flag(p.status, kFlagNonFinite);
+          if (s.bad) set_flag(p.status, kFlagNonFinite);
           const size_t o = (size_t)n * p.n_parts + t * 2 + half;
           if (p.greedy)
             reinterpret_cast<ArgMax*>(p.part)[o] = s.best;

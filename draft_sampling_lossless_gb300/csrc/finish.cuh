@@ -36,13 +36,12 @@ struct BiasSrc {
 
 // Shared-memory scratch of one finish (about 8 KiB).
 struct FinishScratch {
-  long long incl[256];
   long long shl[8];
   float shf[8];
   int shi[8];
   ArgMax sha[8];
   long long base;
-  long long mass;
+  long long ssel;
   int fallback;
   float bias[256];
   float erow[1024];
@@ -50,8 +49,9 @@ struct FinishScratch {
 
 // ---- reductions over 256 threads (8 warps), every thread gets the result
 
+// Inclusive scan over the 256 threads; *total receives the sum of all.
 template <class S>
-__device__ __forceinline__ long long g_scan_ll(long long v, long long* sh) {
+__device__ __forceinline__ long long g_scan_ll(long long v, long long* sh, long long* total) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -61,8 +61,14 @@ __device__ __forceinline__ long long g_scan_ll(long long v, long long* sh) {
   S::sync();
   if (lane == 31) sh[wid] = v;
   S::sync();
-  long long off = 0;
-  for (int w = 0; w < wid; ++w) off += sh[w];
+  long long off = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const long long x = sh[w];
+    if (w < wid) off += x;
+    tot += x;
+  }
+  *total = tot;
   return v + off;
 }
 
@@ -211,14 +217,27 @@ __device__ void finish_request(FinishScratch& s, int n, int V, int gamma, int k,
     for (int i = tid; i < bsrc.r; i += 256)
       s.erow[i] = tok >= 0 ? __bfloat162float(bsrc.E[(size_t)tok * bsrc.r + i]) : 0.f;
   }
+  // The partials are exact doubles; they are summed exactly as integers in
+  // units of 2^g, g chosen from the largest partial's exponent so that the
+  // sum of all n_tiles partials stays below 2^62.  Thread tid owns the
+  // contiguous tiles [t0, t0 + seg); up to kMaxSeg of them (V <= 2^18 on
+  // the tensor-core path) are loaded once into registers, longer segments
+  // are re-read from L2 in each pass.
+  constexpr int kMaxSeg = 8;
   const double* S_ = part + (size_t)n * n_tiles;
   const int seg = (n_tiles + 255) / 256;
+  const bool fast = seg <= kMaxSeg;
   const int t0 = min(n_tiles, tid * seg), t1 = min(n_tiles, t0 + seg);
-  // The partials are exact doubles; sum them exactly as integers in units of
-  // 2^g, g chosen from the largest partial's exponent so that the sum of all
-  // n_tiles partials stays below 2^62.
+  double pv[kMaxSeg];
   int emax = INT_MIN;
-  for (int t = t0; t < t1; ++t) emax = max(emax, double_exponent(__ldcg(S_ + t)));
+  if (fast) {
+#pragma unroll
+    for (int i = 0; i < kMaxSeg; ++i) pv[i] = t0 + i < t1 ? __ldcg(S_ + t0 + i) : 0.0;
+#pragma unroll
+    for (int i = 0; i < kMaxSeg; ++i) emax = max(emax, double_exponent(pv[i]));
+  } else {
+    for (int t = t0; t < t1; ++t) emax = max(emax, double_exponent(__ldcg(S_ + t)));
+  }
   emax = g_max_i<S>(emax, s.shi);
   if (emax == INT_MIN) {  // no token has mass
     if (tid == 0) {
@@ -231,46 +250,66 @@ __device__ void finish_request(FinishScratch& s, int n, int V, int gamma, int k,
     return;
   }
   const int g = emax + 2 + (32 - __clz(n_tiles)) - 62;
-  long long loc = 0;
-  for (int t = t0; t < t1; ++t) loc += double_to_fix(__ldcg(S_ + t), g);
-  const long long incl = g_scan_ll<S>(loc, s.shl);
-  s.incl[tid] = incl;
-  S::sync();
-  const long long F = s.incl[255];
+  long long fx[kMaxSeg], loc = 0;
+  if (fast) {
+#pragma unroll
+    for (int i = 0; i < kMaxSeg; ++i) {
+      fx[i] = double_to_fix(pv[i], g);
+      loc += fx[i];
+    }
+  } else {
+    for (int t = t0; t < t1; ++t) loc += double_to_fix(__ldcg(S_ + t), g);
+  }
+  long long F;
+  const long long incl = g_scan_ll<S>(loc, s.shl, &F);
   // the draw is the first token whose running sum exceeds u*F; for integer
   // running sums that is "exceeds floor(u*F)"
   const long long thr = floor_mul(u[out], F);
-  int cand = 0x7fffffff;
-  long long base = 0;
+  int cand = 0x7fffffff, last = -1;
+  long long base = 0, ssel = 0;
   {
     long long run = incl - loc;
-    for (int t = t0; t < t1; ++t) {
-      const long long nx = run + double_to_fix(__ldcg(S_ + t), g);
-      if (nx > thr) {
-        cand = t;
-        base = run;
-        break;
+    if (fast) {
+#pragma unroll
+      for (int i = 0; i < kMaxSeg; ++i) {
+        const long long nx = run + fx[i];
+        if (cand == 0x7fffffff && t0 + i < t1 && nx > thr) {
+          cand = t0 + i;
+          base = run;
+          ssel = fx[i];
+        }
+        if (fx[i] > 0) last = t0 + i;
+        run = nx;
       }
-      run = nx;
+    } else {
+      for (int t = t0; t < t1; ++t) {
+        const long long f = double_to_fix(__ldcg(S_ + t), g);
+        const long long nx = run + f;
+        if (cand == 0x7fffffff && nx > thr) {
+          cand = t;
+          base = run;
+          ssel = f;
+        }
+        if (f > 0) last = t;
+        run = nx;
+      }
     }
   }
   int tsel = g_min_i<S>(cand, s.shi);
   if (tsel == 0x7fffffff) {
     // u outside [0, 1): the last tile with mass
-    int last = -1;
-    for (int t = t0; t < t1; ++t)
-      if (__ldcg(S_ + t) > 0.0) last = t;
     tsel = g_max_i<S>(last, s.shi);
     if (tsel < 0) tsel = 0;
     if (tid == 0) s.fallback = 1;
   } else if (cand == tsel) {
     s.base = base;
+    s.ssel = ssel;
     s.fallback = 0;
   }
   S::sync();
   const bool fallback = s.fallback != 0;
   base = s.base;
-  const long long S_sel = double_to_fix(__ldcg(S_ + tsel), g);
+  const long long S_sel = s.ssel;
   // Recompute the chosen tile.
   const int v = tsel * TW + tid;
   const bool ok = tid < TW && v < V;
@@ -290,10 +329,8 @@ __device__ void finish_request(FinishScratch& s, int n, int V, int gamma, int k,
   const float ref = ceilf(amax);
   float w = 0.f;
   const long long f = (ok && a > -INFINITY && amax > -INFINITY) ? rel_fix(a, ref, &w) : 0ll;
-  const long long cum = g_scan_ll<S>(f, s.shl);
-  if (tid == 255) s.mass = cum;
-  S::sync();
-  const long long mass = s.mass;
+  long long mass;
+  const long long cum = g_scan_ll<S>(f, s.shl, &mass);
   // The recomputed tile can differ from its partial in the last bits, so the
   // crossing is placed at the same fraction of the recomputed tile:
   //   cum / mass > (thr - base) / S_sel  <=>  cum * S_sel > (thr - base) * mass

@@ -27,6 +27,9 @@ SMALL = {
     # tensor-core draft has no second tile
     "odd_tiles": W["qwen3_4b"].scaled(name="odd_tiles", R=40, gamma=3, V=2800, r=64, d=32,
                                       n_sps=0),
+    # more than 2048 partials per request: the finish re-reads its segments
+    "big_vocab": W["qwen3_4b"].scaled(name="big_vocab", R=3, gamma=2, V=300000, r=64, d=16,
+                                      n_sps=0),
     # more than 64 requests on one 128-row tile (the unpaired tensor-core layout)
     "rows_100": W["qwen3_4b"].scaled(name="rows_100", R=100, gamma=3, V=4000, r=128, d=32,
                                      n_sps=0),
