@@ -41,7 +41,6 @@ bool sizes_ok(int R, int gamma, int V, int r) {
 Layout layout(int R, int gamma, int V, int r) {
   (void)r;
   Layout L;
-  const size_t n_tiles = (V + kTileV - 1) / kTileV;
   const size_t n_chunks = (V + kChunkV - 1) / kChunkV;
   const size_t N = (size_t)R * gamma;
   size_t off = 0;
@@ -56,7 +55,8 @@ Layout layout(int R, int gamma, int V, int r) {
   L.vstate = off;
   off += align_up((size_t)R * sizeof(VerifyState));
   L.fin_part = off;
-  off += align_up((size_t)R * n_tiles * 2 * sizeof(long long));
+  // 128-token halves (tensor-core path) or 256-token tiles
+  off += align_up((size_t)R * ((V + 127) / 128) * 2 * sizeof(long long));
   L.prev = off;
   off += align_up((size_t)R * sizeof(int32_t));
   L.rank = off;

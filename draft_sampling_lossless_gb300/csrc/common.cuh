@@ -202,6 +202,7 @@ enum KernelKind {
   kKindFinalPick,
   kKindDraftFusedTc,
   kKindDraftPersistent,
+  kKindFinalTc,
   kKindCount
 };
 
@@ -379,6 +380,11 @@ struct VerifyArgs {
   int32_t* prev;         // [R]
 };
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t st);
+// Final-draw partial sums on the tensor cores: fin_part[R][ceil(V / 128)][2]
+// (residual, p) in units of 2^-60, the bias of each rejected position formed
+// in TMEM (bf16, tensor-core shapes only).
+cudaError_t launch_final_tc(const VerifyArgs& a, const VerifyState* vstate, long long* fin_part,
+                            cudaStream_t st);
 
 // CUDA-core Markov bias: bias[n][v] = sum_i E[prev[n]][i] * Wt[v][i] for the
 // n = 0..R-1 rows whose previous token is prev_base[n * prev_stride]

@@ -60,7 +60,9 @@ constexpr uint32_t kBBytes = BN * BK * 2;          // 32 KiB
 constexpr uint32_t kZBytes = BM * 64 * 2;          // 16 KiB
 constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
 constexpr uint32_t kFlagTimeout = 0x10u;
-constexpr int kBars = 20;
+// mbarriers: fullB[3] @0, emptyB[3] @3, fullZ[2][4] @6, emptyZ[2][4] @14,
+// accFull[2] @22, accEmpty[2] @24, drain @26; the TMEM address word @27
+constexpr int kBars = 28;
 
 struct TcParams {
   int R, gamma, V, r, k, nK, n_vt, n_parts;
@@ -97,6 +99,27 @@ __device__ __forceinline__ bool wait_abortable(uint32_t bar, uint32_t parity,
     }
   }
 }
+
+// The z ring.  Slot s holding a box that token half h reads is guarded by
+// the barrier pair (fullZ[h][s], emptyZ[h][s]).  With fewer slots than boxes
+// per tile a slot is read alternately by both halves; one barrier pair per
+// (half, slot) keeps each barrier's phases consecutive for its only reader,
+// so a parity wait can never match an older phase.  The producer remembers
+// which half read each slot last and waits for that half's release.
+struct ZRing {
+  uint32_t epar = 0;  // bit h*4+s: parity of the next release of (h, s) to wait for
+  uint32_t last = 0;  // two bits per slot: 1 + the half that read it last, 0 = unused
+  __device__ __forceinline__ void acquire(uint32_t b_emptyZ, int s, int h, volatile int* abort_flag,
+                                          uint32_t* status) {
+    const uint32_t lu = (last >> (2 * s)) & 3u;
+    if (lu != 0) {
+      const int bit = (int)(lu - 1) * 4 + s;
+      wait_abortable(b_emptyZ + 8 * bit, (epar >> bit) & 1u, abort_flag, status);
+      epar ^= 1u << bit;
+    }
+    last = (last & ~(3u << (2 * s))) | ((uint32_t)(h + 1) << (2 * s));
+  }
+};
 
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
@@ -219,11 +242,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBars - 1);
   const uint32_t b_fullB = smem_u32(bars + 0);      // [3]
   const uint32_t b_emptyB = smem_u32(bars + 3);     // [3]
-  const uint32_t b_fullZ = smem_u32(bars + 6);      // [4]
-  const uint32_t b_emptyZ = smem_u32(bars + 10);    // [4]
-  const uint32_t b_accFull = smem_u32(bars + 14);   // [2]
-  const uint32_t b_accEmpty = smem_u32(bars + 16);  // [2]
-  const uint32_t b_drain = smem_u32(bars + 18);
+  const uint32_t b_fullZ = smem_u32(bars + 6);      // [2 halves][4 slots]
+  const uint32_t b_emptyZ = smem_u32(bars + 14);    // [2 halves][4 slots]
+  const uint32_t b_accFull = smem_u32(bars + 22);   // [2]
+  const uint32_t b_accEmpty = smem_u32(bars + 24);  // [2]
+  const uint32_t b_drain = smem_u32(bars + 26);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r0 = blockIdx.y * BM;
@@ -233,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(b_fullB + 8 * i, 1);
       mbar_init(b_emptyB + 8 * i, 1);
     }
-    for (int i = 0; i < kZBoxes; ++i) {
+    for (int i = 0; i < 2 * kZBoxes; ++i) {
       mbar_init(b_fullZ + 8 * i, 1);
       mbar_init(b_emptyZ + 8 * i, 4);  // the four warps of one token half
     }
@@ -326,16 +349,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // each logit slice is read exactly once: do not let it displace W
       const uint64_t pol = policy_evict_first();
       uint32_t it = 0;
+      ZRing zr;
       for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x) {
         for (int j = 0; j < kZBoxes; ++j, ++it) {
-          const uint32_t s = it % kZBoxes, ph = (it / kZBoxes) & 1;
-          wait_abortable(b_emptyZ + 8 * s, ph ^ 1, &s_abort, p.status);
+          const int s = it % kZBoxes;
+          zr.acquire(b_emptyZ, s, j >> 1, &s_abort, p.status);
           // the epilogue read this box through the generic proxy; order those
           // reads before the async-proxy (TMA) write that refills it
           fence_proxy_async_smem();
-          mbar_arrive_expect_tx(b_fullZ + 8 * s, kZBytes);
-          tma_load_3d_hint(smem_u32(sZ + s * kZBytes), &tm_z, b_fullZ + 8 * s, t * BN + j * 64,
-                           p.k, r0, pol);
+          const uint32_t fb = b_fullZ + 8 * ((j >> 1) * 4 + s);
+          mbar_arrive_expect_tx(fb, kZBytes);
+          tma_load_3d_hint(smem_u32(sZ + s * kZBytes), &tm_z, fb, t * BN + j * 64, p.k, r0, pol);
         }
       }
     }
@@ -373,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n = r0 + m;
     const bool valid = n < p.R;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    uint32_t acc_it = 0, zit0 = 0;
+    uint32_t acc_it = 0, zit0 = 0, cpar = 0;
     for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x, ++acc_it, zit0 += kZBoxes) {
       const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
       wait_abortable(b_accFull + 8 * a, aph, &s_abort, p.status);
@@ -403,8 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           continue;
         }
-        const uint32_t zs = (zit0 + j) % kZBoxes, zph = ((zit0 + j) / kZBoxes) & 1;
-        wait_abortable(b_fullZ + 8 * zs, zph, &s_abort, p.status);
+        const uint32_t zs = (zit0 + j) % kZBoxes;
+        wait_abortable(b_fullZ + 8 * (half * 4 + zs), (cpar >> zs) & 1u, &s_abort, p.status);
+        cpar ^= 1u << zs;
         uint4 z0[4], z1[4];
         const uint8_t* zrow = sZ + zs * kZBytes + m * 128;
 #pragma unroll
@@ -413,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           z1[q] = *reinterpret_cast<const uint4*>(zrow + (((q + 4) ^ (m & 7)) << 4));
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(b_emptyZ + 8 * zs);
+        if (lane == 0) mbar_arrive(b_emptyZ + 8 * (half * 4 + zs));
         tmem_wait_ld();
         if (valid) epi_block(b0, b1, z0, z1, v0, min(64, p.V - v0), p, s);
       }
@@ -525,11 +550,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBars - 1);
   const uint32_t b_fullB = smem_u32(bars + 0);
   const uint32_t b_emptyB = smem_u32(bars + 3);
-  const uint32_t b_fullZ = smem_u32(bars + 6);
-  const uint32_t b_emptyZ = smem_u32(bars + 10);
-  const uint32_t b_accFull = smem_u32(bars + 14);
-  const uint32_t b_accEmpty = smem_u32(bars + 16);
-  const uint32_t b_drain = smem_u32(bars + 18);
+  const uint32_t b_fullZ = smem_u32(bars + 6);    // [2 halves][4 slots]
+  const uint32_t b_emptyZ = smem_u32(bars + 14);  // [2 halves][4 slots]
+  const uint32_t b_accFull = smem_u32(bars + 22);
+  const uint32_t b_accEmpty = smem_u32(bars + 24);
+  const uint32_t b_drain = smem_u32(bars + 26);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r0 = blockIdx.y * BM;
@@ -544,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(b_fullB + 8 * i, 1);
       mbar_init(b_emptyB + 8 * i, 1);
     }
-    for (int i = 0; i < nzs; ++i) {
+    for (int i = 0; i < 2 * kZBoxes; ++i) {
       mbar_init(b_fullZ + 8 * i, 1);
       mbar_init(b_emptyZ + 8 * i, 4);  // the four warps of one token half
     }
@@ -601,24 +626,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       uint32_t it = 0;
+      ZRing zr;
       for (int k = 0; k < p.gamma; ++k)
         for (int u = blockIdx.x; u < n_units; u += gridDim.x)
           for (int j = 0; j < kZBoxes; ++j, ++it) {
-            const uint32_t s = it % nzs, ph = (it / nzs) & 1;
-            wait_abortable(b_emptyZ + 8 * s, ph ^ 1, &s_abort, p.status);
+            const int s = it % nzs;
+            zr.acquire(b_emptyZ, s, j >> 1, &s_abort, p.status);
+            const uint32_t fb = b_fullZ + 8 * ((j >> 1) * 4 + s);
             fence_proxy_async_smem();  // generic reads of the slot before the TMA refill
             const uint32_t dst = smem_u32(sZ + s * kZBytes);
             if (pair) {
               // rows 0-63: the requests' logits of tile 2u; rows 64-127: of tile 2u + 1
               const bool second = 2 * u + 1 < p.n_vt;
-              mbar_arrive_expect_tx(b_fullZ + 8 * s, second ? kZBytes : kZBytes / 2);
-              tma_load_3d_hint(dst, &tm_z, b_fullZ + 8 * s, (2 * u) * BN + j * 64, k, 0, pol);
+              mbar_arrive_expect_tx(fb, second ? kZBytes : kZBytes / 2);
+              tma_load_3d_hint(dst, &tm_z, fb, (2 * u) * BN + j * 64, k, 0, pol);
               if (second)
-                tma_load_3d_hint(dst + kZBytes / 2, &tm_z, b_fullZ + 8 * s,
-                                 (2 * u + 1) * BN + j * 64, k, 0, pol);
+                tma_load_3d_hint(dst + kZBytes / 2, &tm_z, fb, (2 * u + 1) * BN + j * 64, k, 0,
+                                 pol);
             } else {
-              mbar_arrive_expect_tx(b_fullZ + 8 * s, kZBytes);
-              tma_load_3d_hint(dst, &tm_z, b_fullZ + 8 * s, u * BN + j * 64, k, r0, pol);
+              mbar_arrive_expect_tx(fb, kZBytes);
+              tma_load_3d_hint(dst, &tm_z, fb, u * BN + j * 64, k, r0, pol);
             }
           }
     }
@@ -667,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool valid = n < p.R;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const int rows = pair ? 64 : BM;  // gathered A rows
-    uint32_t acc_it = 0, zit = 0, epoch = 0;
+    uint32_t acc_it = 0, zit = 0, epoch = 0, cpar = 0;
     FinishScratch& fs = *reinterpret_cast<FinishScratch*>(pair ? sA + kPairBlk : sA);
     for (int k = 0; k < p.gamma; ++k) {
       const int32_t* prev = k == 0 ? pp.anchor : pp.tokens + (k - 1);
@@ -731,8 +758,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_32x32b_x32(tmem + lane_base + a * BN + col, b0);
           tmem_ld_32x32b_x32(tmem + lane_base + a * BN + col + 32, b1);
           const int v0 = t * BN + col;
-          const uint32_t zs = (zit + j) % nzs, zph = ((zit + j) / nzs) & 1;
-          wait_abortable(b_fullZ + 8 * zs, zph, &s_abort, p.status);
+          const uint32_t zs = (zit + j) % nzs;
+          wait_abortable(b_fullZ + 8 * (half * 4 + zs), (cpar >> zs) & 1u, &s_abort, p.status);
+          cpar ^= 1u << zs;
           uint4 z0[4], z1[4];
           const uint8_t* zrow = sZ + zs * kZBytes + m * 128;
 #pragma unroll
@@ -741,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             z1[q] = *reinterpret_cast<const uint4*>(zrow + (((q + 4) ^ (m & 7)) << 4));
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(b_emptyZ + 8 * zs);
+          if (lane == 0) mbar_arrive(b_emptyZ + 8 * (half * 4 + zs));
           tmem_wait_ld();
           if (valid) epi_block(b0, b1, z0, z1, v0, min(64, p.V - v0), p, s);
         }
@@ -776,6 +804,355 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t o = (size_t)(cta + (i / p.gamma) * (int)n_ctas) * p.gamma + i % p.gamma;
         const double tot = pp.q_lse[o];
         pp.q_lse[o] = tot > 0.0 ? log(tot) : -INFINITY;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------- final draw
+
+// Final draw of the verification (the residual max(0, p - q) after a
+// rejection, p itself for the bonus token): per (request, 128-token half
+// tile) the exact fixed-point sums of both, in units of 2^-60 of the
+// normalised probabilities.  The draft logits at the rejected position need
+// the Markov bias of the token before it, which the tensor cores produce in
+// TMEM as in the draft.  The z and target rows sit at request-dependent
+// positions, so the producer warp copies them granule by granule (cp.async,
+// 16 bytes each, all 32 lanes) into the swizzled slot layout the epilogue
+// reads without bank conflicts.
+struct FinalParams {
+  int R, V, r, nK, n_vt, n_halves, gamma;
+  long long n_rows;
+  ScalePair sc;
+  const __nv_bfloat16* E;
+  const __nv_bfloat16* z;       // [R][gamma][V]
+  const __nv_bfloat16* target;  // [n_rows][V]
+  const int32_t* prev;          // [R] token before the rejected position, -1 none
+  const VerifyState* vstate;    // [R]
+  long long* fin_part;          // [R][n_halves][2]: residual, p
+  uint32_t* status;
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// Arrive on `bar` once this thread's earlier cp.async copies have landed
+// (counts as one of the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// 64 consecutive tokens of one request's final row: p = 2^(a_p) / Sp from the
+// target logits and, for a residual draw, q = 2^(a_q) / Sq from the draft
+// logits z + bias; adds the fixed-point sums of max(0, p - q) (p itself for a
+// bonus draw) and of p.
+__device__ __forceinline__ void fin_block(const uint32_t (&b0)[32], const uint32_t (&b1)[32],
+                                          const uint4 (&zq)[8], const uint4 (&tq)[8], int lim,
+                                          bool resid, ScalePair sc, InvPair ip, InvPair iq,
+                                          long long& fr, long long& fp) {
+  float ap[64], aq[64];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint32_t wt[4] = {tq[q].x, tq[q].y, tq[q].z, tq[q].w};
+    const uint32_t wz[4] = {zq[q].x, zq[q].y, zq[q].z, zq[q].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = q * 8 + 2 * e;
+      const uint32_t bl = i < 32 ? b0[i] : b1[i - 32], bh = i < 32 ? b0[i + 1] : b1[i - 31];
+      ap[i] = bf_lo(wt[e]);
+      ap[i + 1] = bf_hi(wt[e]);
+      aq[i] = bf_lo(wz[e]) + __uint_as_float(bl);
+      aq[i + 1] = bf_hi(wz[e]) + __uint_as_float(bh);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 64; ++e) {
+    const bool in = e < lim;
+    ap[e] = in ? scaled_clamped(ap[e], sc) : -3.0e38f;
+    aq[e] = in && resid ? scaled_clamped(aq[e], sc) : -3.0e38f;
+  }
+  float mp[32], mq[32];
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    mp[e] = fmaxf(ap[e], ap[e + 32]);
+    mq[e] = fmaxf(aq[e], aq[e + 32]);
+  }
+#pragma unroll
+  for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+    for (int e = 0; e < w; ++e) {
+      mp[e] = fmaxf(mp[e], mp[e + w]);
+      mq[e] = fmaxf(mq[e], mq[e + w]);
+    }
+  if (mp[0] <= -1.0e38f) return;  // no target mass here: both sums stay 0
+  const int refp = static_cast<int>(ceilf(mp[0]));
+  const int refq = mq[0] > -1.0e38f ? static_cast<int>(ceilf(mq[0])) : 0;
+  const ScalePair kp{scale_pow2(ip.hi, refp + ip.e), scale_pow2(ip.lo, refp + ip.e)};
+  const ScalePair kq = mq[0] > -1.0e38f
+                           ? ScalePair{scale_pow2(iq.hi, refq + iq.e), scale_pow2(iq.lo, refq + iq.e)}
+                           : ScalePair{0.f, 0.f};
+  const float fp_ref = static_cast<float>(refp), fq_ref = static_cast<float>(refq);
+  constexpr float k2_60 = 1152921504606846976.0f;  // 2^60
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    float sp[16], sr[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const float wp = ex2_fast(ap[g * 16 + e] - fp_ref);
+      const float pv = fmaf(wp, kp.hi, wp * kp.lo);
+      float rho = pv;
+      if (resid) {
+        const float wq = ex2_fast(aq[g * 16 + e] - fq_ref);
+        rho = fmaxf(0.0f, pv - fmaf(wq, kq.hi, wq * kq.lo));
+      }
+      sp[e] = pv;
+      sr[e] = rho;
+    }
+#pragma unroll
+    for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+      for (int e = 0; e < w; ++e) {
+        sp[e] += sp[e + w];
+        sr[e] += sr[e + w];
+      }
+    fp += __float2ll_rn(sp[0] * k2_60);
+    fr += __float2ll_rn(sr[0] * k2_60);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    final_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const FinalParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_abort;
+  __shared__ int s_tok[BM];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + p.nK * kABytesPerChunk;
+  uint8_t* sZ = sB + kStagesB * kBBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sZ + kZBoxes * kZBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBars - 1);
+  const uint32_t b_fullB = smem_u32(bars + 0);
+  const uint32_t b_emptyB = smem_u32(bars + 3);
+  const uint32_t b_fullZ = smem_u32(bars + 6);    // [2 halves][4 slots]
+  const uint32_t b_emptyZ = smem_u32(bars + 14);  // [2 halves][4 slots]
+  const uint32_t b_accFull = smem_u32(bars + 22);
+  const uint32_t b_accEmpty = smem_u32(bars + 24);
+  const uint32_t b_drain = smem_u32(bars + 26);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = blockIdx.y * BM;
+  // a slot holds one 64-token block of the z rows and of the target rows of
+  // the tile's requests: 64 rows when R - r0 <= 64, else 128
+  const int srows = p.R - r0 <= 64 ? 64 : BM;
+  const uint32_t slot_bytes = (uint32_t)srows * 128 * 2;
+  const int nslots = (int)((kZBoxes * kZBytes) / slot_bytes);  // 4 or 2
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStagesB; ++i) {
+      mbar_init(b_fullB + 8 * i, 1);
+      mbar_init(b_emptyB + 8 * i, 1);
+    }
+    for (int i = 0; i < 2 * kZBoxes; ++i) {
+      mbar_init(b_fullZ + 8 * i, 32);  // every producer lane's copies
+      mbar_init(b_emptyZ + 8 * i, 4);  // the four warps of one token half
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b_accFull + 8 * i, 1);
+      mbar_init(b_accEmpty + 8 * i, kEpiWarps);
+    }
+    mbar_init(b_drain, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kWarpW && lane == 0) tma_prefetch(&tm_w);
+  // A operand: E rows of the token before each request's rejected position
+  {
+    if (threadIdx.x < BM) {
+      const int n = r0 + threadIdx.x;
+      int tok = -1;
+      if (n < p.R) {
+        tok = p.prev[n];
+        if (tok >= p.V || tok < -1) {
+          set_flag(p.status, kFlagTokenRange);
+          tok = -1;
+        }
+      }
+      s_tok[threadIdx.x] = tok;
+    }
+    __syncthreads();
+    const int per_row = p.nK * 8;
+    constexpr int kPer = (BM * 32 + kThreads - 1) / kThreads;
+    uint4 val[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int idx = threadIdx.x + i * kThreads;
+      val[i] = make_uint4(0, 0, 0, 0);
+      if (idx < BM * per_row) {
+        const int m = idx / per_row, rem = idx - m * per_row;
+        const int col = (rem >> 3) * BK + (rem & 7) * 8;
+        const int tok = s_tok[m];
+        if (tok >= 0 && col < p.r)
+          val[i] = *reinterpret_cast<const uint4*>(p.E + (size_t)tok * p.r + col);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int idx = threadIdx.x + i * kThreads;
+      if (idx < BM * per_row) {
+        const int m = idx / per_row, rem = idx - m * per_row;
+        const int c = rem >> 3, g = rem & 7;
+        *reinterpret_cast<uint4*>(sA + c * kABytesPerChunk + m * 128 + ((g ^ (m & 7)) << 4)) =
+            val[i];
+      }
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kWarpW) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_last();
+      uint32_t it = 0;
+      for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x)
+        for (int c = 0; c < p.nK; ++c, ++it) {
+          const uint32_t s = it % kStagesB, ph = (it / kStagesB) & 1;
+          wait_abortable(b_emptyB + 8 * s, ph ^ 1, &s_abort, p.status);
+          mbar_arrive_expect_tx(b_fullB + 8 * s, kBBytes);
+          tma_load_2d_hint(smem_u32(sB + s * kBBytes), &tm_w, b_fullB + 8 * s, c * BK, t * BN,
+                           pol);
+        }
+    }
+  } else if (warp == kWarpZ) {
+    // row copier: lane l copies rows l, l + 32, ... of every block
+    const __nv_bfloat16* zr[4];
+    const __nv_bfloat16* tr[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      zr[i] = nullptr;
+      tr[i] = nullptr;
+      const int m = lane + 32 * i, n = r0 + m;
+      if (m < srows && n < p.R) {
+        const VerifyState st = p.vstate[n];
+        if (st.mode >= 0 && st.final_row >= 0 && st.final_row < p.n_rows)
+          tr[i] = p.target + (size_t)st.final_row * p.V;
+        if (st.mode == 1 && st.n_acc >= 0 && st.n_acc < p.gamma)
+          zr[i] = p.z + ((size_t)n * p.gamma + st.n_acc) * p.V;
+      }
+    }
+    uint32_t it = 0;
+    ZRing zring;
+    for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x)
+      for (int j = 0; j < kZBoxes; ++j, ++it) {
+        const int s = it % nslots;
+        zring.acquire(b_emptyZ, s, j >> 1, &s_abort, p.status);
+        fence_proxy_async_smem();
+        const uint32_t zdst = smem_u32(sZ + s * slot_bytes);
+        const uint32_t tdst = zdst + slot_bytes / 2;
+        const int v0 = t * BN + j * 64;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int m = lane + 32 * i;
+          const uint32_t row = (uint32_t)m * 128;
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const int v = v0 + g * 8;  // V is a multiple of 8: a granule is all in or all out
+            const uint32_t off = row + ((uint32_t)(g ^ (m & 7)) << 4);
+            if (tr[i] != nullptr && v < p.V) cp_async16(tdst + off, tr[i] + v);
+            if (zr[i] != nullptr && v < p.V) cp_async16(zdst + off, zr[i] + v);
+          }
+        }
+        cp_async_arrive(b_fullZ + 8 * ((j >> 1) * 4 + s));
+      }
+  } else if (warp == kWarpMma) {
+    if (lane == 0) {
+      uint32_t it = 0, acc_it = 0;
+      for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x, ++acc_it) {
+        const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
+        wait_abortable(b_accEmpty + 8 * a, aph ^ 1, &s_abort, p.status);
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + a * BN;
+        for (int c = 0; c < p.nK; ++c, ++it) {
+          const uint32_t s = it % kStagesB, ph = (it / kStagesB) & 1;
+          wait_abortable(b_fullB + 8 * s, ph, &s_abort, p.status);
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + c * kABytesPerChunk);
+          const uint32_t b_base = smem_u32(sB + s * kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_bf16(d_tmem, desc_kmajor_sw128(a_base + kk * 32), desc_kmajor_sw128(b_base + kk * 32),
+                     kIdesc, (c | kk) != 0);
+          mma_commit(b_emptyB + 8 * s);
+        }
+        mma_commit(b_accFull + 8 * a);
+      }
+      mma_commit(b_drain);
+      if (!mbar_wait(b_drain, 0)) set_flag(p.status, kFlagTimeout);
+    }
+  } else {
+    // ---------------- epilogue, warps 0-7
+    const int quad = warp & 3, half = warp >> 2;
+    const int m = quad * 32 + lane;
+    const int n = r0 + m;
+    VerifyState st{0, -1, 0, -1, {0.f, 0.f, 0}, {0.f, 0.f, 0}};
+    if (n < p.R) st = p.vstate[n];
+    const bool valid = m < srows && n < p.R && st.mode >= 0;
+    const bool resid = st.mode == 1;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    uint32_t acc_it = 0, zit = 0, cpar = 0;
+    for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x, ++acc_it, zit += kZBoxes) {
+      const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
+      wait_abortable(b_accFull + 8 * a, aph, &s_abort, p.status);
+      tc_fence_after();
+      long long fr = 0, fp = 0;
+#pragma unroll 1
+      for (int jj = 0; jj < 2; ++jj) {
+        const int j = half * 2 + jj;
+        const int col = j * 64;
+        uint32_t b0[32], b1[32];
+        __syncwarp();
+        tmem_ld_32x32b_x32(tmem + lane_base + a * BN + col, b0);
+        tmem_ld_32x32b_x32(tmem + lane_base + a * BN + col + 32, b1);
+        const int v0 = t * BN + col;
+        const uint32_t zs = (zit + j) % nslots;
+        wait_abortable(b_fullZ + 8 * (half * 4 + zs), (cpar >> zs) & 1u, &s_abort, p.status);
+        cpar ^= 1u << zs;
+        uint4 zq[8], tq[8];
+        const uint8_t* zrow = sZ + zs * slot_bytes + m * 128;
+        const uint8_t* trow = zrow + slot_bytes / 2;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          zq[q] = make_uint4(0, 0, 0, 0);
+          tq[q] = make_uint4(0, 0, 0, 0);
+          if (valid) {
+            tq[q] = *reinterpret_cast<const uint4*>(trow + ((q ^ (m & 7)) << 4));
+            if (resid) zq[q] = *reinterpret_cast<const uint4*>(zrow + ((q ^ (m & 7)) << 4));
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_emptyZ + 8 * (half * 4 + zs));
+        tmem_wait_ld();
+        if (valid)
+          fin_block(b0, b1, zq, tq, min(64, p.V - v0), resid, p.sc, st.ip, st.iq, fr, fp);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_accEmpty + 8 * a);
+      if (n < p.R && m < srows && t * 2 + half < p.n_halves) {
+        long long* o = p.fin_part + ((size_t)n * p.n_halves + t * 2 + half) * 2;
+        o[0] = fr;
+        o[1] = fp;
       }
     }
   }
@@ -995,6 +1372,46 @@ cudaError_t launch_bias_tc(int R, int V, int r, const void* E, const void* Wt,
   p.bias_out = bias;
   p.status = status;
   return launch_tc<true>(tm_w, tm_w, p, st);
+}
+
+// Final-draw partial sums on the tensor cores (see final_tc_kernel):
+// fin_part[R][ceil(V / 128)][2].
+cudaError_t launch_final_tc(const VerifyArgs& a, const VerifyState* vstate, long long* fin_part,
+                            cudaStream_t st) {
+  CUtensorMap tm_w;
+  cudaError_t e = encode_w(&tm_w, a.Wt, a.V, a.r);
+  if (e != cudaSuccess) return e;
+  FinalParams p;
+  p.R = a.R;
+  p.V = a.V;
+  p.r = a.r;
+  p.nK = (a.r + BK - 1) / BK;
+  p.n_vt = (a.V + BN - 1) / BN;
+  p.n_halves = (a.V + kHalf - 1) / kHalf;
+  p.gamma = a.gamma;
+  p.n_rows = a.n_rows;
+  p.sc = make_scale(1.4426950408889634 / (double)a.T);
+  p.E = static_cast<const __nv_bfloat16*>(a.E);
+  p.z = static_cast<const __nv_bfloat16*>(a.z);
+  p.target = static_cast<const __nv_bfloat16*>(a.target);
+  p.prev = a.prev;
+  p.vstate = vstate;
+  p.fin_part = fin_part;
+  p.status = a.status;
+  static bool attr_set = false;
+  if (!attr_set) {
+    e = cudaFuncSetAttribute(final_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)tc_smem_bytes(4));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int n_rt = (a.R + BM - 1) / BM;
+  int gx = sm_count() / n_rt;
+  if (gx < 1) gx = 1;
+  if (gx > p.n_vt) gx = p.n_vt;
+  DSPARK_LAUNCH(kKindFinalTc, st,
+                final_tc_kernel<<<dim3(gx, n_rt), kThreads, tc_smem_bytes(p.nK), st>>>(tm_w, p));
+  return cudaGetLastError();
 }
 
 }  // namespace dspark

@@ -22,7 +22,7 @@ constexpr int kPairs = 8192;
 const char* const kNames[kKindCount] = {
     "markov_bias",       "draft_partial",  "draft_finish", "confidence",  "schedule_rank",
     "schedule_finish",   "verify_rows",    "verify_decide", "final_partial", "final_pick",
-    "draft_fused_tc",    "draft_persistent_tc",
+    "draft_fused_tc",    "draft_persistent_tc", "final_tc",
 };
 
 std::mutex g_mu;

@@ -21,6 +21,7 @@
 //              recomputing it with the same warp routine, compared with u*total
 //              in exact integer arithmetic
 #include "common.cuh"
+#include "finish.cuh"
 
 namespace dspark {
 
@@ -409,6 +410,117 @@ __global__ void __launch_bounds__(256) final_pick_kernel(
   }
 }
 
+// Pick of the final draw on the tensor-core path.  The partials are per
+// 128-token half tile and were formed with the tensor-core bias; the chosen
+// half tile is recomputed here with the bias on CUDA cores, so its running
+// sums can differ from its partial in the last bits.  The crossing is placed
+// at the same fraction of the recomputed half tile (exact 128-bit
+// cross-multiplication), as in the draft finish.
+__global__ void __launch_bounds__(256) final_pick_tc_kernel(
+    int gamma, int V, int r, int n_halves, const __nv_bfloat16* __restrict__ z,
+    const __nv_bfloat16* __restrict__ target, const __nv_bfloat16* __restrict__ E,
+    const __nv_bfloat16* __restrict__ Wt, ScalePair sc, const VerifyState* __restrict__ vstate,
+    const long long* __restrict__ fin_part, const float* __restrict__ u_fin,
+    int32_t* __restrict__ out_tokens, uint32_t* status) {
+  __shared__ FinishScratch s;
+  const int n = blockIdx.x, tid = threadIdx.x;
+  const VerifyState st = vstate[n];
+  if (st.mode < 0) return;
+  const bool resid = st.mode == 1;
+  if (resid) {  // the previous token's E row, needed once the half tile is known
+    for (int i = tid; i < r; i += 256)
+      s.erow[i] = st.prev >= 0 ? __bfloat162float(E[(size_t)st.prev * r + i]) : 0.f;
+  }
+  const long long* P = fin_part + (size_t)n * n_halves * 2;
+  const int seg = (n_halves + 255) / 256;
+  const int t0 = min(n_halves, tid * seg), t1 = min(n_halves, t0 + seg);
+  long long lr = 0, lp = 0;
+  for (int t = t0; t < t1; ++t) {
+    lr += P[2 * t];
+    lp += P[2 * t + 1];
+  }
+  long long Fr;
+  g_scan_ll<BlockSync>(lr, s.shl, &Fr);
+  // the residual column, unless p and q agree everywhere (then p itself)
+  const int col = (resid && Fr > 0) ? 0 : 1;
+  const long long loc = col == 0 ? lr : lp;
+  long long F;
+  const long long incl = g_scan_ll<BlockSync>(loc, s.shl, &F);
+  if (F <= 0) {
+    if (tid == 0) {
+      set_flag(status, kFlagNonFinite);
+      out_tokens[(size_t)n * (gamma + 1) + st.n_acc] = 0;
+    }
+    return;
+  }
+  const long long thr = floor_mul(u_fin[n], F);  // C > u*F  <=>  C > floor(u*F)
+  int cand = 0x7fffffff;
+  long long base = 0, ssel = 0;
+  {
+    long long run = incl - loc;
+    for (int t = t0; t < t1; ++t) {
+      const long long x = P[2 * t + col];
+      const long long nx = run + x;
+      if (cand == 0x7fffffff && nx > thr) {
+        cand = t;
+        base = run;
+        ssel = x;
+      }
+      run = nx;
+    }
+  }
+  const int hsel = g_min_i<BlockSync>(cand, s.shi);  // found: F > thr
+  if (cand == hsel) {
+    s.base = base;
+    s.ssel = ssel;
+  }
+  __syncthreads();
+  base = s.base;
+  ssel = s.ssel;
+  // recompute the chosen half tile: thread tid < 128 takes token hsel*128 + tid
+  const int v = hsel * 128 + tid;
+  const bool ok = tid < 128 && v < V;
+  const float tv = ok ? __bfloat162float(target[(size_t)st.final_row * V + v]) : -INFINITY;
+  float zv = 0.f;
+  if (resid && ok) zv = __bfloat162float(z[((size_t)n * gamma + st.n_acc) * V + v]);
+  float bv = 0.f;
+  if (resid) {
+    const BiasSrc b{nullptr, E, Wt, nullptr, 0, r};
+    tile_bias_recompute<128, BlockSync>(b, V, hsel * 128, s.erow, s.bias);
+    bv = tid < 128 ? s.bias[tid] : 0.f;
+  }
+  const float ap = ok ? scaled_clamped(tv, sc) : -3.0e38f;
+  const float aq = ok && resid ? scaled_clamped(zv + bv, sc) : -3.0e38f;
+  const float mp = g_max_f<BlockSync>(ap, s.shf);
+  const float mq = g_max_f<BlockSync>(aq, s.shf);
+  long long f = 0;
+  if (ok && mp > -1.0e38f) {
+    const int refp = (int)ceilf(mp);
+    const float wp = ex2_fast(ap - (float)refp);
+    const float pv = fmaf(wp, scale_pow2(st.ip.hi, refp + st.ip.e),
+                          wp * scale_pow2(st.ip.lo, refp + st.ip.e));
+    float rho = pv;
+    if (resid && mq > -1.0e38f) {
+      const int refq = (int)ceilf(mq);
+      const float wq = ex2_fast(aq - (float)refq);
+      rho = fmaxf(0.0f, pv - fmaf(wq, scale_pow2(st.iq.hi, refq + st.iq.e),
+                                  wq * scale_pow2(st.iq.lo, refq + st.iq.e)));
+    }
+    f = __float2ll_rn((col == 0 ? rho : pv) * 1152921504606846976.0f);  // 2^60
+  }
+  long long mass;
+  const long long cum = g_scan_ll<BlockSync>(f, s.shl, &mass);
+  //   cum / mass > (thr - base) / ssel  <=>  cum * ssel > (thr - base) * mass
+  int pick = 0x7fffffff;
+  if (f > 0 && mul_gt((unsigned long long)cum, (unsigned long long)ssel,
+                      (unsigned long long)(thr - base), (unsigned long long)mass))
+    pick = tid;
+  int isel = g_min_i<BlockSync>(pick, s.shi);
+  if (isel == 0x7fffffff) isel = g_max_i<BlockSync>(f > 0 ? tid : -1, s.shi);
+  if (isel < 0) isel = 0;
+  if (tid == 0) out_tokens[(size_t)n * (gamma + 1) + st.n_acc] = hsel * 128 + isel;
+}
+
 int row_grid(long long items) {
   const long long blocks = (items + 7) / 8;
   return (int)(blocks < 152 * 16 ? blocks : 152 * 16);
@@ -434,6 +546,21 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t st) {
                     a.out_tokens, a.vstate, a.prev, a.status));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || greedy) return e;
+  if (tc_shape_supported(a.dt, a.V, a.r, a.z, a.E, a.Wt) &&
+      (((uintptr_t)a.target & 15) == 0)) {
+    // bias, p and the residual in one tensor-core pass; the pick recomputes
+    // its half tile
+    e = launch_final_tc(a, a.vstate, a.fin_part, st);
+    if (e != cudaSuccess) return e;
+    const int n_halves = (a.V + 127) / 128;
+    DSPARK_LAUNCH(kKindFinalPick, st,
+                  final_pick_tc_kernel<<<a.R, 256, 0, st>>>(
+                      a.gamma, a.V, a.r, n_halves, (const __nv_bfloat16*)a.z,
+                      (const __nv_bfloat16*)a.target, (const __nv_bfloat16*)a.E,
+                      (const __nv_bfloat16*)a.Wt, sc, a.vstate, a.fin_part, a.u_fin,
+                      a.out_tokens, a.status));
+    return cudaGetLastError();
+  }
   e = tc_shape_supported(a.dt, a.V, a.r, a.z, a.E, a.Wt)
           ? launch_bias_tc(a.R, a.V, a.r, a.E, a.Wt, a.prev, 1, a.bias, a.status, st)
           : launch_bias(a.R, a.V, a.r, a.dt, a.E, a.Wt, a.prev, 1, a.bias, a.status, st);
