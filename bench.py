@@ -53,6 +53,8 @@ def algorithmic_bytes(kind, wl, B, n_rej):
         return r * V * e
     if kind == "final_partial":
         return R * V * e + n_rej * V * e
+    if kind == "final_tc":  # target row of every request, z row of each rejection, W once
+        return R * V * e + n_rej * V * e + r * V * e
     return None
 
 
