@@ -17,14 +17,39 @@ namespace dspark {
 namespace {
 
 // sum_i w[i] * x[i] over n elements, the warp's lanes taking eight at a time
-// (x 16-byte aligned and n a multiple of 8 for the vector path).
+// (x 16-byte aligned and n a multiple of 8 for the vector path).  The vector
+// path issues four steps' loads before their multiply-adds, so a lane has up
+// to four 16-byte loads in flight instead of one dependent chain.
 template <typename T>
 __device__ __forceinline__ float warp_dot(const float* __restrict__ w, const T* __restrict__ x,
                                           int n, bool vec) {
   const int lane = threadIdx.x & 31;
   float s = 0.f;
   if (vec) {
-    for (int i = lane * 8; i < n; i += 256) {
+    constexpr int kU = 4;
+    int i = lane * 8;
+    for (; i + (kU - 1) * 256 < n; i += kU * 256) {
+      float xv[kU][8];
+      float4 wv[kU][2];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        load8<T>(x, i + u * 256, n, xv[u], 0.f);
+        wv[u][0] = *reinterpret_cast<const float4*>(w + i + u * 256);
+        wv[u][1] = *reinterpret_cast<const float4*>(w + i + u * 256 + 4);
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        s = fmaf(wv[u][0].x, xv[u][0], s);
+        s = fmaf(wv[u][0].y, xv[u][1], s);
+        s = fmaf(wv[u][0].z, xv[u][2], s);
+        s = fmaf(wv[u][0].w, xv[u][3], s);
+        s = fmaf(wv[u][1].x, xv[u][4], s);
+        s = fmaf(wv[u][1].y, xv[u][5], s);
+        s = fmaf(wv[u][1].z, xv[u][6], s);
+        s = fmaf(wv[u][1].w, xv[u][7], s);
+      }
+    }
+    for (; i < n; i += 256) {
       float xv[8];
       load8<T>(x, i, n, xv, 0.f);
       const float4 w0 = *reinterpret_cast<const float4*>(w + i);

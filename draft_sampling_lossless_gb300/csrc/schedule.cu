@@ -68,9 +68,11 @@ __global__ void __launch_bounds__(kRankThreads) rank_kernel(int N, int per_split
   if (e < N && cnt) atomicAdd(&rank[e], cnt);
 }
 
-__global__ void __launch_bounds__(kFinThreads) schedule_finish_kernel(
+// The cut and the per-request outputs, by one block of kFinThreads threads,
+// given every candidate's rank.
+__device__ __forceinline__ void schedule_finish(
     int R, int gamma, int imax, int early_stop, const float* __restrict__ a,
-    const float* __restrict__ sps, const int32_t* __restrict__ rank, long long* __restrict__ sfix,
+    const float* __restrict__ sps, const int32_t* rank, long long* __restrict__ sfix,
     int32_t* __restrict__ ell, int32_t* __restrict__ row_off, int32_t* __restrict__ B_out,
     double* __restrict__ E_out, uint32_t* status) {
   __shared__ long long shl[32];
@@ -193,10 +195,58 @@ __global__ void __launch_bounds__(kFinThreads) schedule_finish_kernel(
   if (tid == nt - 1) row_off[R] = (int32_t)rincl;
 }
 
+__global__ void __launch_bounds__(kFinThreads) schedule_finish_kernel(
+    int R, int gamma, int imax, int early_stop, const float* __restrict__ a,
+    const float* __restrict__ sps, const int32_t* __restrict__ rank, long long* __restrict__ sfix,
+    int32_t* __restrict__ ell, int32_t* __restrict__ row_off, int32_t* __restrict__ B_out,
+    double* __restrict__ E_out, uint32_t* status) {
+  schedule_finish(R, gamma, imax, early_stop, a, sps, rank, sfix, ell, row_off, B_out, E_out,
+                  status);
+}
+
+// Small batches (N <= kFusedMax candidates, one per thread): the ranks and the cut in one
+// block.  The candidates' survival values go to shared memory, every thread
+// ranks its candidates by counting comparisons against all N (no atomics, no
+// zeroing pass), and the finish reads the ranks from shared memory.
+constexpr int kFusedMax = 1024;
+
+__global__ void __launch_bounds__(kFinThreads) schedule_fused_kernel(
+    int R, int gamma, int imax, int early_stop, const float* __restrict__ a,
+    const float* __restrict__ sps, long long* __restrict__ sfix, int32_t* __restrict__ rank_out,
+    int32_t* __restrict__ ell, int32_t* __restrict__ row_off, int32_t* __restrict__ B_out,
+    double* __restrict__ E_out, uint32_t* status) {
+  __shared__ float as[kFusedMax];
+  __shared__ int32_t rk[kFusedMax];
+  const int N = R * gamma;
+  for (int e = threadIdx.x; e < N; e += blockDim.x) as[e] = clean_a(a[e], status);
+  __syncthreads();
+  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+    const float ae = as[e];
+    int cnt = 0;
+    for (int i = 0; i < N; ++i) {
+      const float ai = as[i];
+      cnt += (ai > ae) | ((ai == ae) & (i < e));
+    }
+    rk[e] = cnt;
+    rank_out[e] = cnt;
+  }
+  __syncthreads();
+  schedule_finish(R, gamma, imax, early_stop, a, sps, rk, sfix, ell, row_off, B_out, E_out,
+                  status);
+}
+
 }  // namespace
 
 cudaError_t launch_schedule(const SchedArgs& s, cudaStream_t st) {
   const int N = s.R * s.gamma;
+  const int imax0 = s.max_B > 0 ? (s.max_B - s.R < N ? s.max_B - s.R : N) : N;
+  if (N <= kFusedMax) {
+    DSPARK_LAUNCH(kKindSchedFinish, st,
+                  schedule_fused_kernel<<<1, kFinThreads, 0, st>>>(
+                      s.R, s.gamma, imax0 < 0 ? 0 : imax0, s.early_stop, s.a, s.sps, s.sfix,
+                      s.rank, s.ell, s.row_off, s.B_out, s.E_out, s.status));
+    return cudaGetLastError();
+  }
   cudaError_t e = cudaMemsetAsync(s.rank, 0, sizeof(int32_t) * (size_t)N, st);
   if (e != cudaSuccess) return e;
   const int bx = (N + kRankThreads - 1) / kRankThreads;
