@@ -30,7 +30,7 @@ int cuda_fail(cudaError_t e, const char* where) {
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-  size_t status, bias, part, row_part, vstate, fin_part, prev, rank, sfix, total;
+  size_t status, bias, part, row_part, vstate, fin_part, prev, stage, rank, sfix, total;
 };
 
 bool sizes_ok(int R, int gamma, int V, int r) {
@@ -39,7 +39,6 @@ bool sizes_ok(int R, int gamma, int V, int r) {
 }
 
 Layout layout(int R, int gamma, int V, int r) {
-  (void)r;
   Layout L;
   const size_t n_chunks = (V + kChunkV - 1) / kChunkV;
   const size_t N = (size_t)R * gamma;
@@ -59,6 +58,8 @@ Layout layout(int R, int gamma, int V, int r) {
   off += align_up((size_t)R * ((V + 127) / 128) * 2 * sizeof(long long));
   L.prev = off;
   off += align_up((size_t)R * sizeof(int32_t));
+  L.stage = off;
+  off += align_up((size_t)R * r * 2);
   L.rank = off;
   off += align_up(N * sizeof(int32_t));
   L.sfix = off;
@@ -170,6 +171,7 @@ int dspark_draft_sample(int R, int gamma, int V, int r, float temperature, const
   a.bias = at<float>(ws, L.bias);
   a.part = at<double>(ws, L.part);
   a.grid_counter = at<unsigned>(ws, L.status + 64);
+  a.stage = at<void>(ws, L.stage);
   cudaError_t e = launch_draft(a, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "dspark_draft_sample");
   return DSPARK_OK;

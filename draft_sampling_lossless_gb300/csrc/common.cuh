@@ -236,6 +236,7 @@ struct DraftArgs {
   float* bias;      // [R][V] scratch
   double* part;     // [R][n_tiles] scratch (greedy: ArgMax pairs)
   unsigned* grid_counter;  // grid-barrier counter of the persistent draft kernel
+  void* stage;             // [R][r] bf16: E rows of the latest drafted tokens
 };
 cudaError_t launch_draft(const DraftArgs& a, cudaStream_t st);
 cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st);

@@ -61,8 +61,9 @@ constexpr uint32_t kZBytes = BM * 64 * 2;          // 16 KiB
 constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
 constexpr uint32_t kFlagTimeout = 0x10u;
 // mbarriers: fullB[3] @0, emptyB[3] @3, fullZ[2][4] @6, emptyZ[2][4] @14,
-// accFull[2] @22, accEmpty[2] @24, drain @26; the TMEM address word @27
-constexpr int kBars = 28;
+// accFull[2] @22, accEmpty[2] @24, drain @26, aFull @27 (persistent kernel:
+// the staged A operand); the TMEM address word @28
+constexpr int kBars = 29;
 
 struct TcParams {
   int R, gamma, V, r, k, nK, n_vt, n_parts;
@@ -484,6 +485,7 @@ struct PersistParams {
   const float* u;
   unsigned* grid_counter;  // zeroed before the launch
   int pair;                // R <= 64: two vocabulary tiles per accumulator
+  __nv_bfloat16* stage;    // [R][r]: E rows of the tokens drawn at the last position
 };
 
 // Paired layout (R <= 64).  A 128-row accumulator holds two vocabulary tiles:
@@ -534,7 +536,8 @@ __device__ __forceinline__ void grid_sync(unsigned* ctr, unsigned target, volati
 
 __global__ void __launch_bounds__(kThreads, 1)
     draft_persistent_kernel(const __grid_constant__ CUtensorMap tm_w,
-                            const __grid_constant__ CUtensorMap tm_z, const PersistParams pp) {
+                            const __grid_constant__ CUtensorMap tm_z,
+                            const __grid_constant__ CUtensorMap tm_a, const PersistParams pp) {
   const TcParams& p = pp.p;
   const bool pair = pp.pair != 0;
   extern __shared__ uint8_t smem_raw[];
@@ -555,6 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t b_accFull = smem_u32(bars + 22);
   const uint32_t b_accEmpty = smem_u32(bars + 24);
   const uint32_t b_drain = smem_u32(bars + 26);
+  const uint32_t b_aFull = smem_u32(bars + 27);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r0 = blockIdx.y * BM;
@@ -578,6 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(b_accEmpty + 8 * i, kEpiWarps);
     }
     mbar_init(b_drain, 1);
+    mbar_init(b_aFull, 1);
     s_abort = 0;
     fence_mbar_init();
   }
@@ -588,6 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpW && lane == 0) {
     tma_prefetch(&tm_w);
     tma_prefetch(&tm_z);
+    tma_prefetch(&tm_a);
   }
   if (pair && threadIdx.x < 256) {
     // the zero blocks of the paired A operand, written once
@@ -652,8 +658,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMma) {
     uint32_t it = 0, acc_it = 0;
     for (int k = 0; k < p.gamma; ++k) {
-      NamedSync<1, 288>::sync();  // A(k) is in shared memory
+      NamedSync<1, 288>::sync();  // A(k) is in shared memory, or on its way by TMA
       if (lane == 0) {
+        if (k > 0) wait_abortable(b_aFull, (k - 1) & 1, &s_abort, p.status);
         for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++acc_it) {
           const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
           wait_abortable(b_accEmpty + 8 * a, aph ^ 1, &s_abort, p.status);
@@ -699,7 +706,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0; k < p.gamma; ++k) {
       const int32_t* prev = k == 0 ? pp.anchor : pp.tokens + (k - 1);
       const int stride = k == 0 ? 1 : p.gamma;
-      // gather A(k): the rows of E at the previous tokens
+      if (k > 0) {
+        // A(k) = the E rows the finishes staged at position k - 1: four TMA
+        // boxes straight into the swizzled A blocks
+        if (threadIdx.x == 0) {
+          fence_proxy_async_all();
+          const uint32_t box = pair ? kPairBlk : kABytesPerChunk;
+          mbar_arrive_expect_tx(b_aFull, box * p.nK);
+          for (int c = 0; c < p.nK; ++c)
+            tma_load_2d(smem_u32(pair ? sA + (size_t)(2 * c + 1) * kPairBlk
+                                      : sA + (size_t)c * kABytesPerChunk),
+                        &tm_a, b_aFull, c * BK, pair ? 0 : r0);
+        }
+      } else {
+      // gather A(0): the rows of E at the anchors
       if (threadIdx.x < rows) {
         const int nn = (pair ? 0 : r0) + threadIdx.x;
         int tok = -1;
@@ -739,6 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(blk + mm * 128 + ((g ^ (mm & 7)) << 4)) = val[i];
           }
         }
+      }
       }
       fence_proxy_async_smem();
       NamedSync<1, 288>::sync();  // release the MMA warp
@@ -793,7 +814,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int nn = cta; nn < p.R; nn += n_ctas)
         finish_request<__nv_bfloat16, kHalf, NamedSync<3, 256>, true>(
             fs, nn, p.V, p.gamma, k, p.n_parts, pp.z, b, p.sc, p.greedy, p.part, pp.u, pp.tokens,
-            pp.q_lse, pp.q_tok, p.status);
+            pp.q_lse, pp.q_tok, p.status, k + 1 < p.gamma ? pp.stage : nullptr);
+      // the finish scratch (generic) is overwritten by the next A's TMA
+      fence_proxy_async_smem();
       grid_sync(pp.grid_counter, (++epoch) * n_ctas, &s_abort, p.status);
     }
     // The finishes left each q_lse entry holding its normaliser; take the
@@ -1211,6 +1234,21 @@ cudaError_t encode_z(CUtensorMap* m, const void* z, int R, int gamma, int V, int
              : cudaErrorInvalidValue;
 }
 
+// The staged A rows, [R][r] bf16, as 64-element (128-byte) K chunks of
+// box_rows rows, 128-byte swizzled like the A blocks they land in.
+cudaError_t encode_stage(CUtensorMap* m, const void* stage, int R, int r, int box_rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)r, (cuuint64_t)R};
+  cuuint64_t strides[1] = {(cuuint64_t)r * 2};
+  cuuint32_t box[2] = {BK, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(stage), dims,
+                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? cudaSuccess
+             : cudaErrorInvalidValue;
+}
+
 template <bool kBiasOut>
 cudaError_t launch_tc(const CUtensorMap& tm_w, const CUtensorMap& tm_z, const TcParams& p,
                       cudaStream_t st) {
@@ -1283,6 +1321,8 @@ cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st) {
   CUtensorMap tm_w, tm_z;
   cudaError_t e = encode_w(&tm_w, a.Wt, a.V, a.r);
   if (e == cudaSuccess) e = encode_z(&tm_z, a.z, a.R, a.gamma, a.V, pair ? 64 : BM);
+  CUtensorMap tm_a;
+  if (e == cudaSuccess) e = encode_stage(&tm_a, a.stage, a.R, a.r, pair ? 64 : BM);
   if (e != cudaSuccess) return e;
   PersistParams pp;
   TcParams& p = pp.p;
@@ -1311,6 +1351,7 @@ cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st) {
   pp.u = a.u;
   pp.grid_counter = a.grid_counter;
   pp.pair = pair;
+  pp.stage = static_cast<__nv_bfloat16*>(a.stage);
   static bool attr_set = false;
   if (!attr_set) {
     e = cudaFuncSetAttribute(draft_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1341,7 +1382,7 @@ cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   DSPARK_LAUNCH(kKindDraftPersistent, st,
-                e = cudaLaunchKernelEx(&cfg, draft_persistent_kernel, tm_w, tm_z, pp));
+                e = cudaLaunchKernelEx(&cfg, draft_persistent_kernel, tm_w, tm_z, tm_a, pp));
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -9,6 +9,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace dspark {
 
@@ -43,6 +44,7 @@ struct FinishScratch {
   long long base;
   long long ssel;
   int fallback;
+  int tok;
   float bias[256];
   float erow[1024];
 };
@@ -171,6 +173,25 @@ __device__ __forceinline__ void tile_bias_recompute(const BiasSrc& b, int V, int
   S::sync();
 }
 
+// With a stage buffer: copy the drawn token's E row (s.tok, set by the
+// drawing thread before the last sync) to stage[n], where the next position's
+// A operand is loaded from by TMA; the proxy fence orders these generic
+// stores before that async-proxy read (r a multiple of 8, rows 16-byte aligned).
+template <class S>
+__device__ __forceinline__ void stage_row(FinishScratch& s, __nv_bfloat16* stage,
+                                          const BiasSrc& b, int n) {
+  if (stage == nullptr) return;
+  const int tok = s.tok;
+  const int tid = threadIdx.x;
+  if (tid < b.r / 8) {
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (tok >= 0) v = *reinterpret_cast<const uint4*>(b.E + (size_t)tok * b.r + tid * 8);
+    *reinterpret_cast<uint4*>(stage + (size_t)n * b.r + tid * 8) = v;
+  }
+  sm100::fence_proxy_async_all();
+  S::sync();
+}
+
 // The finish of request n at draft position k, by 256 threads
 // (threadIdx.x < 256).  part: [R][n_tiles] tile partials (doubles; greedy:
 // ArgMax pairs) of width TW.  Writes tokens / q_lse / q_tok [n][k].
@@ -180,7 +201,8 @@ template <typename T, int TW, class S, bool kDeferLog>
 __device__ void finish_request(FinishScratch& s, int n, int V, int gamma, int k, int n_tiles,
                                const T* __restrict__ z, const BiasSrc& bsrc, ScalePair sc,
                                int greedy, const double* part, const float* __restrict__ u,
-                               int32_t* tokens, double* q_lse, float* q_tok, uint32_t* status) {
+                               int32_t* tokens, double* q_lse, float* q_tok, uint32_t* status,
+                               __nv_bfloat16* stage = nullptr) {
   const int tid = threadIdx.x;
   const size_t out = (size_t)n * gamma + k;
   if (greedy) {
@@ -203,8 +225,10 @@ __device__ void finish_request(FinishScratch& s, int n, int V, int gamma, int k,
       tokens[out] = tok;
       q_lse[out] = (double)best.v;
       q_tok[out] = 1.0f;
+      s.tok = tok;
     }
     S::sync();
+    stage_row<S>(s, stage, bsrc, n);
     return;
   }
   if (bsrc.bias == nullptr) {
@@ -349,8 +373,10 @@ __device__ void finish_request(FinishScratch& s, int n, int V, int gamma, int k,
     q_lse[out] = kDeferLog ? total : log(total);
     // q(x) = 2^a / total = w * 2^ref / (F * 2^g)
     q_tok[out] = scale_pow2(w / (float)F, (int)ref - g);
+    s.tok = tsel * TW + isel;
   }
   S::sync();
+  stage_row<S>(s, stage, bsrc, n);
 }
 
 }  // namespace dspark
