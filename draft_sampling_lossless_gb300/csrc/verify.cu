@@ -49,12 +49,51 @@ struct Kahan {
   }
 };
 
+// load8 with an L2 evict-first cache policy: the row pass streams every
+// verified target row once, and should not push the draft's W (kept with an
+// evict-last policy for the final draw) out of L2.
+template <typename T>
+__device__ __forceinline__ void load8_stream(const T* p, int v0, int V, float (&o)[8], float fill,
+                                             uint64_t pol);
+template <>
+__device__ __forceinline__ void load8_stream<__nv_bfloat16>(const __nv_bfloat16* p, int v0, int V,
+                                                            float (&o)[8], float fill,
+                                                            uint64_t pol) {
+  if (v0 + 8 <= V) {
+    uint32_t w[4];
+    asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                 : "l"(p + v0), "l"(pol));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = __uint_as_float(w[i] << 16);
+      o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  } else {
+    load8<__nv_bfloat16>(p, v0, V, o, fill);
+  }
+}
+template <>
+__device__ __forceinline__ void load8_stream<float>(const float* p, int v0, int V, float (&o)[8],
+                                                    float fill, uint64_t pol) {
+  if (v0 + 8 <= V) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      asm volatile("ld.global.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+                   : "=f"(o[4 * h]), "=f"(o[4 * h + 1]), "=f"(o[4 * h + 2]), "=f"(o[4 * h + 3])
+                   : "l"(p + v0 + 4 * h), "l"(pol));
+  } else {
+    load8<float>(p, v0, V, o, fill);
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) verify_rows_kernel(
     int R, int gamma, int V, int n_chunks, long long n_rows, const T* __restrict__ target,
     const int32_t* __restrict__ ell, const int32_t* __restrict__ row_off, ScalePair sc,
     int greedy, double* __restrict__ row_part) {
   const int lane = threadIdx.x & 31;
+  const uint64_t pol = sm100::policy_evict_first();
   const long long total = (long long)R * (gamma + 1) * n_chunks;
   const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
   for (long long item = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -71,7 +110,8 @@ __global__ void __launch_bounds__(256) verify_rows_kernel(
     double* out = row_part + ((size_t)n * (gamma + 1) + j) * n_chunks + c;
     float x[4][8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) load8<T>(tr, c * kRowChunk + i * 256 + lane * 8, V, x[i], -INFINITY);
+    for (int i = 0; i < 4; ++i)
+      load8_stream<T>(tr, c * kRowChunk + i * 256 + lane * 8, V, x[i], -INFINITY, pol);
     if (greedy) {
       ArgMax am{-INFINITY, 0x7fffffff};
 #pragma unroll
