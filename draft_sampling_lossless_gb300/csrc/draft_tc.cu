@@ -844,12 +844,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // tile) the exact fixed-point sums of both, in units of 2^-60 of the
 // normalised probabilities.  The draft logits at the rejected position need
 // the Markov bias of the token before it, which the tensor cores produce in
-// TMEM as in the draft.  The z and target rows sit at request-dependent
-// positions, so the producer warp copies them granule by granule (cp.async,
-// 16 bytes each, all 32 lanes) into the swizzled slot layout the epilogue
-// reads without bank conflicts.
+// TMEM as in the draft (with the paired accumulator layout when R <= 64).
+// The z and target rows sit at request-dependent positions: the producer
+// warp copies them 32 tokens (64 bytes) at a time with cp.async, four lanes
+// per row so that every 16-byte copy of an instruction falls in one of eight
+// row segments, into 64-byte slot rows whose 16-byte granules are permuted
+// by row so that the epilogue's 16-byte reads across 32 rows hit distinct
+// banks.
 struct FinalParams {
-  int R, V, r, nK, n_vt, n_halves, gamma;
+  int R, V, r, nK, n_vt, n_halves, gamma, pair;
   long long n_rows;
   ScalePair sc;
   const __nv_bfloat16* E;
@@ -861,6 +864,22 @@ struct FinalParams {
   uint32_t* status;
 };
 
+constexpr int kFinSteps = BN / 32;            // 32-token blocks per tile
+constexpr uint32_t kRowPart = BM * 64;         // one tensor's 128 rows of 64 bytes
+constexpr uint32_t kRowSlot = 2 * kRowPart;    // z rows + target rows of one block
+constexpr int kFinSlots = 3;
+
+size_t final_smem_bytes(int nK, int pair) {
+  const size_t a = pair ? (size_t)(2 * nK + 1) * kPairBlk : (size_t)nK * kABytesPerChunk;
+  return 1024 + a + (size_t)kStagesB * kBBytes + (size_t)kFinSlots * kRowSlot +
+         kBars * sizeof(uint64_t) + 16;
+}
+
+// byte offset of 16-byte granule g (0..3) of slot row m
+__device__ __forceinline__ uint32_t row_granule(int m, int g) {
+  return (uint32_t)m * 64 + ((uint32_t)(g ^ ((m >> 1) & 3)) << 4);
+}
+
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -870,43 +889,41 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// 64 consecutive tokens of one request's final row: p = 2^(a_p) / Sp from the
+// 32 consecutive tokens of one request's final row: p = 2^(a_p) / Sp from the
 // target logits and, for a residual draw, q = 2^(a_q) / Sq from the draft
 // logits z + bias; adds the fixed-point sums of max(0, p - q) (p itself for a
 // bonus draw) and of p.
-__device__ __forceinline__ void fin_block(const uint32_t (&b0)[32], const uint32_t (&b1)[32],
-                                          const uint4 (&zq)[8], const uint4 (&tq)[8], int lim,
-                                          bool resid, ScalePair sc, InvPair ip, InvPair iq,
-                                          long long& fr, long long& fp) {
-  float ap[64], aq[64];
+__device__ __forceinline__ void fin_block(const uint32_t (&b)[32], const uint4 (&zq)[4],
+                                          const uint4 (&tq)[4], int lim, bool resid, ScalePair sc,
+                                          InvPair ip, InvPair iq, long long& fr, long long& fp) {
+  float ap[32], aq[32];
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
+  for (int q = 0; q < 4; ++q) {
     const uint32_t wt[4] = {tq[q].x, tq[q].y, tq[q].z, tq[q].w};
     const uint32_t wz[4] = {zq[q].x, zq[q].y, zq[q].z, zq[q].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int i = q * 8 + 2 * e;
-      const uint32_t bl = i < 32 ? b0[i] : b1[i - 32], bh = i < 32 ? b0[i + 1] : b1[i - 31];
       ap[i] = bf_lo(wt[e]);
       ap[i + 1] = bf_hi(wt[e]);
-      aq[i] = bf_lo(wz[e]) + __uint_as_float(bl);
-      aq[i + 1] = bf_hi(wz[e]) + __uint_as_float(bh);
+      aq[i] = bf_lo(wz[e]) + __uint_as_float(b[i]);
+      aq[i + 1] = bf_hi(wz[e]) + __uint_as_float(b[i + 1]);
     }
   }
 #pragma unroll
-  for (int e = 0; e < 64; ++e) {
+  for (int e = 0; e < 32; ++e) {
     const bool in = e < lim;
     ap[e] = in ? scaled_clamped(ap[e], sc) : -3.0e38f;
     aq[e] = in && resid ? scaled_clamped(aq[e], sc) : -3.0e38f;
   }
-  float mp[32], mq[32];
+  float mp[16], mq[16];
 #pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    mp[e] = fmaxf(ap[e], ap[e + 32]);
-    mq[e] = fmaxf(aq[e], aq[e + 32]);
+  for (int e = 0; e < 16; ++e) {
+    mp[e] = fmaxf(ap[e], ap[e + 16]);
+    mq[e] = fmaxf(aq[e], aq[e + 16]);
   }
 #pragma unroll
-  for (int w = 16; w > 0; w >>= 1)
+  for (int w = 8; w > 0; w >>= 1)
 #pragma unroll
     for (int e = 0; e < w; ++e) {
       mp[e] = fmaxf(mp[e], mp[e + w]);
@@ -922,7 +939,7 @@ __device__ __forceinline__ void fin_block(const uint32_t (&b0)[32], const uint32
   const float fp_ref = static_cast<float>(refp), fq_ref = static_cast<float>(refq);
   constexpr float k2_60 = 1152921504606846976.0f;  // 2^60
 #pragma unroll
-  for (int g = 0; g < 4; ++g) {
+  for (int g = 0; g < 2; ++g) {
     float sp[16], sr[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
@@ -953,12 +970,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_abort;
   __shared__ int s_tok[BM];
+  const bool pair = p.pair != 0;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = sA + p.nK * kABytesPerChunk;
+  uint8_t* sB = sA + (pair ? (size_t)(2 * p.nK + 1) * kPairBlk : (size_t)p.nK * kABytesPerChunk);
   uint8_t* sZ = sB + kStagesB * kBBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sZ + kZBoxes * kZBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sZ + kFinSlots * kRowSlot);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBars - 1);
   const uint32_t b_fullB = smem_u32(bars + 0);
   const uint32_t b_emptyB = smem_u32(bars + 3);
@@ -969,11 +987,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t b_drain = smem_u32(bars + 26);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r0 = blockIdx.y * BM;
-  // a slot holds one 64-token block of the z rows and of the target rows of
-  // the tile's requests: 64 rows when R - r0 <= 64, else 128
-  const int srows = p.R - r0 <= 64 ? 64 : BM;
-  const uint32_t slot_bytes = (uint32_t)srows * 128 * 2;
-  const int nslots = (int)((kZBoxes * kZBytes) / slot_bytes);  // 4 or 2
+  // units: one tile, or (paired) tiles 2u and 2u + 1
+  const int n_units = pair ? (p.n_vt + 1) / 2 : p.n_vt;
+  const int nW = pair ? 2 * p.nK : p.nK;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStagesB; ++i) {
@@ -981,7 +997,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(b_emptyB + 8 * i, 1);
     }
     for (int i = 0; i < 2 * kZBoxes; ++i) {
-      mbar_init(b_fullZ + 8 * i, 32);  // every producer lane's copies
+      mbar_init(b_fullZ + 8 * i, 32);  // every copier lane's arrival
       mbar_init(b_emptyZ + 8 * i, 4);  // the four warps of one token half
     }
     for (int i = 0; i < 2; ++i) {
@@ -999,7 +1015,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpW && lane == 0) tma_prefetch(&tm_w);
   // A operand: E rows of the token before each request's rejected position
   {
-    if (threadIdx.x < BM) {
+    const int rows = pair ? 64 : BM;
+    if (pair && threadIdx.x < 256) {
+      for (int c = 0; c <= p.nK; ++c) {
+        uint4* blk = reinterpret_cast<uint4*>(sA + (size_t)(2 * c) * kPairBlk);
+        for (int i = threadIdx.x; i < (int)(kPairBlk / 16); i += 256) blk[i] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    if (threadIdx.x < rows) {
       const int n = r0 + threadIdx.x;
       int tok = -1;
       if (n < p.R) {
@@ -1019,7 +1042,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kPer; ++i) {
       const int idx = threadIdx.x + i * kThreads;
       val[i] = make_uint4(0, 0, 0, 0);
-      if (idx < BM * per_row) {
+      if (idx < rows * per_row) {
         const int m = idx / per_row, rem = idx - m * per_row;
         const int col = (rem >> 3) * BK + (rem & 7) * 8;
         const int tok = s_tok[m];
@@ -1030,11 +1053,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
       const int idx = threadIdx.x + i * kThreads;
-      if (idx < BM * per_row) {
+      if (idx < rows * per_row) {
         const int m = idx / per_row, rem = idx - m * per_row;
         const int c = rem >> 3, g = rem & 7;
-        *reinterpret_cast<uint4*>(sA + c * kABytesPerChunk + m * 128 + ((g ^ (m & 7)) << 4)) =
-            val[i];
+        uint8_t* blk = pair ? sA + (size_t)(2 * c + 1) * kPairBlk : sA + c * kABytesPerChunk;
+        *reinterpret_cast<uint4*>(blk + m * 128 + ((g ^ (m & 7)) << 4)) = val[i];
       }
     }
   }
@@ -1048,74 +1071,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t pol = policy_evict_last();
       uint32_t it = 0;
-      for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x)
-        for (int c = 0; c < p.nK; ++c, ++it) {
+      for (int u = blockIdx.x; u < n_units; u += gridDim.x)
+        for (int i = 0; i < nW; ++i, ++it) {
+          const int t = pair ? 2 * u + i / p.nK : u, c = i % p.nK;
           const uint32_t s = it % kStagesB, ph = (it / kStagesB) & 1;
           wait_abortable(b_emptyB + 8 * s, ph ^ 1, &s_abort, p.status);
-          mbar_arrive_expect_tx(b_fullB + 8 * s, kBBytes);
-          tma_load_2d_hint(smem_u32(sB + s * kBBytes), &tm_w, b_fullB + 8 * s, c * BK, t * BN,
-                           pol);
+          if (t < p.n_vt) {
+            mbar_arrive_expect_tx(b_fullB + 8 * s, kBBytes);
+            tma_load_2d_hint(smem_u32(sB + s * kBBytes), &tm_w, b_fullB + 8 * s, c * BK, t * BN,
+                             pol);
+          } else {
+            mbar_arrive(b_fullB + 8 * s);  // past V: nothing to load, rows never read
+          }
         }
     }
   } else if (warp == kWarpZ) {
-    // row copier: lane l copies rows l, l + 32, ... of every block
-    const __nv_bfloat16* zr[4];
-    const __nv_bfloat16* tr[4];
+    // row copier: an instruction moves 8 slot rows, lanes 4i..4i+3 the four
+    // 16-byte granules of row 8c + i
+    const int sub = lane >> 2, g = lane & 3;
+    const __nv_bfloat16* zr[16];
+    const __nv_bfloat16* tr[16];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      zr[i] = nullptr;
-      tr[i] = nullptr;
-      const int m = lane + 32 * i, n = r0 + m;
-      if (m < srows && n < p.R) {
+    for (int c = 0; c < 16; ++c) {
+      zr[c] = nullptr;
+      tr[c] = nullptr;
+      const int m = 8 * c + sub;
+      const int n = pair ? (m & 63) : r0 + m;
+      if (n < p.R) {
         const VerifyState st = p.vstate[n];
         if (st.mode >= 0 && st.final_row >= 0 && st.final_row < p.n_rows)
-          tr[i] = p.target + (size_t)st.final_row * p.V;
+          tr[c] = p.target + (size_t)st.final_row * p.V;
         if (st.mode == 1 && st.n_acc >= 0 && st.n_acc < p.gamma)
-          zr[i] = p.z + ((size_t)n * p.gamma + st.n_acc) * p.V;
+          zr[c] = p.z + ((size_t)n * p.gamma + st.n_acc) * p.V;
       }
     }
     uint32_t it = 0;
     ZRing zring;
-    for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x)
-      for (int j = 0; j < kZBoxes; ++j, ++it) {
-        const int s = it % nslots;
-        zring.acquire(b_emptyZ, s, j >> 1, &s_abort, p.status);
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x)
+      for (int j = 0; j < kFinSteps; ++j, ++it) {
+        const int s = it % kFinSlots, h = j / (kFinSteps / 2);
+        zring.acquire(b_emptyZ, s, h, &s_abort, p.status);
         fence_proxy_async_smem();
-        const uint32_t zdst = smem_u32(sZ + s * slot_bytes);
-        const uint32_t tdst = zdst + slot_bytes / 2;
-        const int v0 = t * BN + j * 64;
+        const uint32_t zdst = smem_u32(sZ + s * kRowSlot), tdst = zdst + kRowPart;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int m = lane + 32 * i;
-          const uint32_t row = (uint32_t)m * 128;
-#pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            const int v = v0 + g * 8;  // V is a multiple of 8: a granule is all in or all out
-            const uint32_t off = row + ((uint32_t)(g ^ (m & 7)) << 4);
-            if (tr[i] != nullptr && v < p.V) cp_async16(tdst + off, tr[i] + v);
-            if (zr[i] != nullptr && v < p.V) cp_async16(zdst + off, zr[i] + v);
+        for (int c = 0; c < 16; ++c) {
+          const int m = 8 * c + sub;
+          const int t = pair ? 2 * u + (m >> 6) : u;
+          const int v = t * BN + j * 32 + g * 8;  // V is a multiple of 8: a granule is all in or out
+          if (v < p.V) {
+            const uint32_t off = row_granule(m, g);
+            if (tr[c] != nullptr) cp_async16(tdst + off, tr[c] + v);
+            if (zr[c] != nullptr) cp_async16(zdst + off, zr[c] + v);
           }
         }
-        cp_async_arrive(b_fullZ + 8 * ((j >> 1) * 4 + s));
+        cp_async_arrive(b_fullZ + 8 * (h * 4 + s));
       }
   } else if (warp == kWarpMma) {
     if (lane == 0) {
       uint32_t it = 0, acc_it = 0;
-      for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x, ++acc_it) {
+      for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++acc_it) {
         const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
         wait_abortable(b_accEmpty + 8 * a, aph ^ 1, &s_abort, p.status);
         tc_fence_after();
         const uint32_t d_tmem = tmem + a * BN;
-        for (int c = 0; c < p.nK; ++c, ++it) {
+        for (int i = 0; i < nW; ++i, ++it) {
           const uint32_t s = it % kStagesB, ph = (it / kStagesB) & 1;
           wait_abortable(b_fullB + 8 * s, ph, &s_abort, p.status);
           tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + c * kABytesPerChunk);
+          const int c = i % p.nK;
+          const uint32_t a_base =
+              pair ? smem_u32(sA + (size_t)(2 * c + (i < p.nK ? 1 : 0)) * kPairBlk)
+                   : smem_u32(sA + c * kABytesPerChunk);
           const uint32_t b_base = smem_u32(sB + s * kBBytes);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             mma_bf16(d_tmem, desc_kmajor_sw128(a_base + kk * 32), desc_kmajor_sw128(b_base + kk * 32),
-                     kIdesc, (c | kk) != 0);
+                     kIdesc, (i | kk) != 0);
           mma_commit(b_emptyB + 8 * s);
         }
         mma_commit(b_accFull + 8 * a);
@@ -1126,53 +1157,54 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- epilogue, warps 0-7
     const int quad = warp & 3, half = warp >> 2;
-    const int m = quad * 32 + lane;
-    const int n = r0 + m;
+    const int m = quad * 32 + lane;  // TMEM lane = slot row
+    const int n = pair ? (m & 63) : r0 + m;
+    const int tsub = pair ? (m >> 6) : 0;
     VerifyState st{0, -1, 0, -1, {0.f, 0.f, 0}, {0.f, 0.f, 0}};
     if (n < p.R) st = p.vstate[n];
-    const bool valid = m < srows && n < p.R && st.mode >= 0;
+    const bool live = n < p.R && st.mode >= 0;
     const bool resid = st.mode == 1;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     uint32_t acc_it = 0, zit = 0, cpar = 0;
-    for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x, ++acc_it, zit += kZBoxes) {
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++acc_it, zit += kFinSteps) {
       const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
+      const int t = pair ? 2 * u + tsub : u;
+      const bool valid = live && t < p.n_vt;
       wait_abortable(b_accFull + 8 * a, aph, &s_abort, p.status);
       tc_fence_after();
       long long fr = 0, fp = 0;
 #pragma unroll 1
-      for (int jj = 0; jj < 2; ++jj) {
-        const int j = half * 2 + jj;
-        const int col = j * 64;
-        uint32_t b0[32], b1[32];
+      for (int jj = 0; jj < kFinSteps / 2; ++jj) {
+        const int j = half * (kFinSteps / 2) + jj;
+        const int col = j * 32;
+        uint32_t b[32];
         __syncwarp();
-        tmem_ld_32x32b_x32(tmem + lane_base + a * BN + col, b0);
-        tmem_ld_32x32b_x32(tmem + lane_base + a * BN + col + 32, b1);
+        tmem_ld_32x32b_x32(tmem + lane_base + a * BN + col, b);
         const int v0 = t * BN + col;
-        const uint32_t zs = (zit + j) % nslots;
+        const uint32_t zs = (zit + j) % kFinSlots;
         wait_abortable(b_fullZ + 8 * (half * 4 + zs), (cpar >> zs) & 1u, &s_abort, p.status);
         cpar ^= 1u << zs;
-        uint4 zq[8], tq[8];
-        const uint8_t* zrow = sZ + zs * slot_bytes + m * 128;
-        const uint8_t* trow = zrow + slot_bytes / 2;
+        uint4 zq[4], tq[4];
+        const uint8_t* zslot = sZ + zs * kRowSlot;
+        const uint8_t* tslot = zslot + kRowPart;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < 4; ++q) {
           zq[q] = make_uint4(0, 0, 0, 0);
           tq[q] = make_uint4(0, 0, 0, 0);
           if (valid) {
-            tq[q] = *reinterpret_cast<const uint4*>(trow + ((q ^ (m & 7)) << 4));
-            if (resid) zq[q] = *reinterpret_cast<const uint4*>(zrow + ((q ^ (m & 7)) << 4));
+            tq[q] = *reinterpret_cast<const uint4*>(tslot + row_granule(m, q));
+            if (resid) zq[q] = *reinterpret_cast<const uint4*>(zslot + row_granule(m, q));
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(b_emptyZ + 8 * (half * 4 + zs));
         tmem_wait_ld();
-        if (valid)
-          fin_block(b0, b1, zq, tq, min(64, p.V - v0), resid, p.sc, st.ip, st.iq, fr, fp);
+        if (valid) fin_block(b, zq, tq, min(32, p.V - v0), resid, p.sc, st.ip, st.iq, fr, fp);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_accEmpty + 8 * a);
-      if (n < p.R && m < srows && t * 2 + half < p.n_halves) {
+      if (n < p.R && t < p.n_vt && t * 2 + half < p.n_halves) {
         long long* o = p.fin_part + ((size_t)n * p.n_halves + t * 2 + half) * 2;
         o[0] = fr;
         o[1] = fp;
@@ -1439,19 +1471,22 @@ cudaError_t launch_final_tc(const VerifyArgs& a, const VerifyState* vstate, long
   p.vstate = vstate;
   p.fin_part = fin_part;
   p.status = a.status;
+  p.pair = a.R <= 64 ? 1 : 0;
   static bool attr_set = false;
   if (!attr_set) {
     e = cudaFuncSetAttribute(final_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)tc_smem_bytes(4));
+                             (int)final_smem_bytes(4, 1));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const int n_rt = (a.R + BM - 1) / BM;
+  const int n_units = p.pair ? (p.n_vt + 1) / 2 : p.n_vt;
   int gx = sm_count() / n_rt;
   if (gx < 1) gx = 1;
-  if (gx > p.n_vt) gx = p.n_vt;
+  if (gx > n_units) gx = n_units;
   DSPARK_LAUNCH(kKindFinalTc, st,
-                final_tc_kernel<<<dim3(gx, n_rt), kThreads, tc_smem_bytes(p.nK), st>>>(tm_w, p));
+                final_tc_kernel<<<dim3(gx, n_rt), kThreads, final_smem_bytes(p.nK, p.pair), st>>>(
+                    tm_w, p));
   return cudaGetLastError();
 }
 

@@ -205,6 +205,7 @@ __device__ void finish_request(FinishScratch& s, int n, int V, int gamma, int k,
                                __nv_bfloat16* stage = nullptr) {
   const int tid = threadIdx.x;
   const size_t out = (size_t)n * gamma + k;
+  const float u_out = greedy ? 0.0f : u[out];  // issued early: needed after the scan
   if (greedy) {
     const ArgMax* P = reinterpret_cast<const ArgMax*>(part) + (size_t)n * n_tiles;
     ArgMax best{-INFINITY, 0x7fffffff};
@@ -288,7 +289,7 @@ __device__ void finish_request(FinishScratch& s, int n, int V, int gamma, int k,
   const long long incl = g_scan_ll<S>(loc, s.shl, &F);
   // the draw is the first token whose running sum exceeds u*F; for integer
   // running sums that is "exceeds floor(u*F)"
-  const long long thr = floor_mul(u[out], F);
+  const long long thr = floor_mul(u_out, F);
   int cand = 0x7fffffff, last = -1;
   long long base = 0, ssel = 0;
   {
