@@ -206,6 +206,30 @@ enum KernelKind {
   kKindCount
 };
 
+// Programmatic dependent launch: a kernel launched with launch_pdl may start
+// while the previous kernel on its stream is still draining; it calls
+// grid_dependency_wait() before reading anything that kernel wrote (a no-op
+// when launched without the attribute).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 void trace_begin(int kind, cudaStream_t st);
 void set_error_text(const char* msg);  // the text dspark_last_error() returns
 void trace_end(int kind, cudaStream_t st);

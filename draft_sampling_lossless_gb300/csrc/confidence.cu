@@ -78,6 +78,7 @@ __global__ void confidence_kernel(int gamma, int d, int r, int V, int vec,
                                   float* __restrict__ c_out, float* __restrict__ a_out,
                                   uint32_t* status) {
   __shared__ float c_s[kMaxGamma];
+  grid_dependency_wait();  // the drafted tokens
   const int n = blockIdx.x;
   const int k = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (k < gamma) {
@@ -124,15 +125,15 @@ cudaError_t launch_confidence(const ConfArgs& a, cudaStream_t st) {
                   ((size_t)a.d * esz) % 16 == 0 && ((size_t)a.d * 4) % 16 == 0;
   if (a.dt == 0)
     DSPARK_LAUNCH(kKindConfidence, st,
-                  confidence_kernel<__nv_bfloat16><<<a.R, threads, 0, st>>>(
-                      a.gamma, a.d, a.r, a.V, vec, (const __nv_bfloat16*)a.h, a.w,
-                      (const __nv_bfloat16*)a.E1, a.anchor, a.tokens, a.sts, a.c_in, a.c_out,
-                      a.a_out, a.status));
+                  launch_pdl(confidence_kernel<__nv_bfloat16>, dim3(a.R), dim3(threads), 0, st,
+                             a.gamma, a.d, a.r, a.V, vec, (const __nv_bfloat16*)a.h, a.w,
+                             (const __nv_bfloat16*)a.E1, a.anchor, a.tokens, a.sts, a.c_in,
+                             a.c_out, a.a_out, a.status));
   else
     DSPARK_LAUNCH(kKindConfidence, st,
-                  confidence_kernel<float><<<a.R, threads, 0, st>>>(
-                      a.gamma, a.d, a.r, a.V, vec, (const float*)a.h, a.w, (const float*)a.E1,
-                      a.anchor, a.tokens, a.sts, a.c_in, a.c_out, a.a_out, a.status));
+                  launch_pdl(confidence_kernel<float>, dim3(a.R), dim3(threads), 0, st, a.gamma,
+                             a.d, a.r, a.V, vec, (const float*)a.h, a.w, (const float*)a.E1,
+                             a.anchor, a.tokens, a.sts, a.c_in, a.c_out, a.a_out, a.status));
   return cudaGetLastError();
 }
 

@@ -1013,6 +1013,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (warp == kWarpW && lane == 0) tma_prefetch(&tm_w);
+  grid_dependency_wait();  // the verification state and previous tokens
   // A operand: E rows of the token before each request's rejected position
   {
     const int rows = pair ? 64 : BM;
@@ -1485,8 +1486,9 @@ cudaError_t launch_final_tc(const VerifyArgs& a, const VerifyState* vstate, long
   if (gx < 1) gx = 1;
   if (gx > n_units) gx = n_units;
   DSPARK_LAUNCH(kKindFinalTc, st,
-                final_tc_kernel<<<dim3(gx, n_rt), kThreads, final_smem_bytes(p.nK, p.pair), st>>>(
-                    tm_w, p));
+                e = launch_pdl(final_tc_kernel, dim3(gx, n_rt), dim3(kThreads),
+                               final_smem_bytes(p.nK, p.pair), st, tm_w, p));
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

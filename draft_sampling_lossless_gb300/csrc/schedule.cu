@@ -217,6 +217,7 @@ __global__ void __launch_bounds__(kFinThreads) schedule_fused_kernel(
     double* __restrict__ E_out, uint32_t* status) {
   __shared__ float as[kFusedMax];
   __shared__ int32_t rk[kFusedMax];
+  grid_dependency_wait();  // the survival values
   const int N = R * gamma;
   for (int e = threadIdx.x; e < N; e += blockDim.x) as[e] = clean_a(a[e], status);
   __syncthreads();
@@ -242,9 +243,9 @@ cudaError_t launch_schedule(const SchedArgs& s, cudaStream_t st) {
   const int imax0 = s.max_B > 0 ? (s.max_B - s.R < N ? s.max_B - s.R : N) : N;
   if (N <= kFusedMax) {
     DSPARK_LAUNCH(kKindSchedFinish, st,
-                  schedule_fused_kernel<<<1, kFinThreads, 0, st>>>(
-                      s.R, s.gamma, imax0 < 0 ? 0 : imax0, s.early_stop, s.a, s.sps, s.sfix,
-                      s.rank, s.ell, s.row_off, s.B_out, s.E_out, s.status));
+                  launch_pdl(schedule_fused_kernel, dim3(1), dim3(kFinThreads), 0, st, s.R,
+                             s.gamma, imax0 < 0 ? 0 : imax0, s.early_stop, s.a, s.sps, s.sfix,
+                             s.rank, s.ell, s.row_off, s.B_out, s.E_out, s.status));
     return cudaGetLastError();
   }
   cudaError_t e = cudaMemsetAsync(s.rank, 0, sizeof(int32_t) * (size_t)N, st);

@@ -94,6 +94,7 @@ __global__ void __launch_bounds__(256) verify_rows_kernel(
     int greedy, double* __restrict__ row_part) {
   const int lane = threadIdx.x & 31;
   const uint64_t pol = sm100::policy_evict_first();
+  grid_dependency_wait();  // ell, row_off
   const long long total = (long long)R * (gamma + 1) * n_chunks;
   const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
   for (long long item = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -177,6 +178,7 @@ __global__ void __launch_bounds__(256) verify_decide_kernel(
   __shared__ double Sp[kMaxGamma + 1];
   __shared__ ArgMax am_s[kMaxGamma + 1];
   __shared__ int bad_s;
+  grid_dependency_wait();  // the row partials
   const int n = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int L = ell[n];
   const long long r0 = row_off[n];
@@ -463,6 +465,7 @@ __global__ void __launch_bounds__(256) final_pick_tc_kernel(
     const long long* __restrict__ fin_part, const float* __restrict__ u_fin,
     int32_t* __restrict__ out_tokens, uint32_t* status) {
   __shared__ FinishScratch s;
+  grid_dependency_wait();  // the final partials
   const int n = blockIdx.x, tid = threadIdx.x;
   const VerifyState st = vstate[n];
   if (st.mode < 0) return;
@@ -576,14 +579,14 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t st) {
   const T* tg = (const T*)a.target;
   const long long items = (long long)a.R * (a.gamma + 1) * n_chunks;
   DSPARK_LAUNCH(kKindVerifyRows, st,
-                verify_rows_kernel<T><<<row_grid(items), 256, 0, st>>>(
-                    a.R, a.gamma, a.V, n_chunks, a.n_rows, tg, a.ell, a.row_off, sc, greedy,
-                    a.row_part));
+                launch_pdl(verify_rows_kernel<T>, dim3(row_grid(items)), dim3(256), 0, st, a.R,
+                           a.gamma, a.V, n_chunks, a.n_rows, tg, a.ell, a.row_off, sc,
+                           (int)greedy, a.row_part));
   DSPARK_LAUNCH(kKindVerifyDecide, st,
-                verify_decide_kernel<T><<<a.R, 256, 0, st>>>(
-                    a.gamma, a.V, n_chunks, a.n_rows, tg, sc, greedy, a.anchor, a.tokens,
-                    a.q_lse, a.q_tok, a.ell, a.row_off, a.u_acc, a.row_part, a.p_lse, a.n_acc,
-                    a.out_tokens, a.vstate, a.prev, a.status));
+                launch_pdl(verify_decide_kernel<T>, dim3(a.R), dim3(256), 0, st, a.gamma, a.V,
+                           n_chunks, a.n_rows, tg, sc, (int)greedy, a.anchor, a.tokens, a.q_lse,
+                           a.q_tok, a.ell, a.row_off, a.u_acc, (const double*)a.row_part, a.p_lse,
+                           a.n_acc, a.out_tokens, a.vstate, a.prev, a.status));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || greedy) return e;
   if (tc_shape_supported(a.dt, a.V, a.r, a.z, a.E, a.Wt) &&
@@ -594,11 +597,11 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     const int n_halves = (a.V + 127) / 128;
     DSPARK_LAUNCH(kKindFinalPick, st,
-                  final_pick_tc_kernel<<<a.R, 256, 0, st>>>(
-                      a.gamma, a.V, a.r, n_halves, (const __nv_bfloat16*)a.z,
-                      (const __nv_bfloat16*)a.target, (const __nv_bfloat16*)a.E,
-                      (const __nv_bfloat16*)a.Wt, sc, a.vstate, a.fin_part, a.u_fin,
-                      a.out_tokens, a.status));
+                  launch_pdl(final_pick_tc_kernel, dim3(a.R), dim3(256), 0, st, a.gamma, a.V,
+                             a.r, n_halves, (const __nv_bfloat16*)a.z,
+                             (const __nv_bfloat16*)a.target, (const __nv_bfloat16*)a.E,
+                             (const __nv_bfloat16*)a.Wt, sc, (const VerifyState*)a.vstate,
+                             (const long long*)a.fin_part, a.u_fin, a.out_tokens, a.status));
     return cudaGetLastError();
   }
   e = tc_shape_supported(a.dt, a.V, a.r, a.z, a.E, a.Wt)
