@@ -122,6 +122,28 @@ struct ZRing {
   }
 };
 
+// Slot and phase of a stage ring, advanced by increment and wrap so that
+// the single MMA-issuing thread spends no cycles on divisions.
+struct RingPos {
+  uint32_t s = 0, ph = 0;
+  __device__ __forceinline__ void next(uint32_t n) {
+    if (++s == n) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+};
+
+// The four K=16 MMAs of one 64-wide K chunk.  Both descriptors start at
+// their operand's chunk and advance 32 bytes (2 in the descriptor's 16-byte
+// address units) per step inside the 128-byte swizzle row.
+__device__ __forceinline__ void mma_chunk(uint32_t d_tmem, uint64_t da, uint64_t db,
+                                          bool accumulate) {
+  mma_bf16(d_tmem, da, db, kIdesc, accumulate ? 1u : 0u);
+#pragma unroll
+  for (int kk = 1; kk < BK / 16; ++kk) mma_bf16(d_tmem, da + 2 * kk, db + 2 * kk, kIdesc, 1u);
+}
+
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
@@ -333,14 +355,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // W is re-read at every draft position: keep it resident in L2
       const uint64_t pol = policy_evict_last();
-      uint32_t it = 0;
+      RingPos rb;
       for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x) {
-        for (int c = 0; c < p.nK; ++c, ++it) {
-          const uint32_t s = it % kStagesB, ph = (it / kStagesB) & 1;
-          wait_abortable(b_emptyB + 8 * s, ph ^ 1, &s_abort, p.status);
-          mbar_arrive_expect_tx(b_fullB + 8 * s, kBBytes);
-          tma_load_2d_hint(smem_u32(sB + s * kBBytes), &tm_w, b_fullB + 8 * s, c * BK, t * BN,
-                           pol);
+        for (int c = 0; c < p.nK; ++c, rb.next(kStagesB)) {
+          wait_abortable(b_emptyB + 8 * rb.s, rb.ph ^ 1, &s_abort, p.status);
+          mbar_arrive_expect_tx(b_fullB + 8 * rb.s, kBBytes);
+          tma_load_2d_hint(smem_u32(sB + rb.s * kBBytes), &tm_w, b_fullB + 8 * rb.s, c * BK,
+                           t * BN, pol);
         }
       }
     }
@@ -367,23 +388,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMma) {
     // ---------------- MMA issuer
     if (lane == 0) {
-      uint32_t it = 0, acc_it = 0;
+      const uint64_t da0 = desc_kmajor_sw128(smem_u32(sA));
+      const uint64_t db0 = desc_kmajor_sw128(smem_u32(sB));
+      RingPos rb;
+      uint32_t acc_it = 0;
       for (int t = blockIdx.x; t < p.n_vt; t += gridDim.x, ++acc_it) {
         const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
         wait_abortable(b_accEmpty + 8 * a, aph ^ 1, &s_abort, p.status);
         tc_fence_after();
         const uint32_t d_tmem = tmem + a * BN;
-        for (int c = 0; c < p.nK; ++c, ++it) {
-          const uint32_t s = it % kStagesB, ph = (it / kStagesB) & 1;
-          wait_abortable(b_fullB + 8 * s, ph, &s_abort, p.status);
+        for (int c = 0; c < p.nK; ++c, rb.next(kStagesB)) {
+          wait_abortable(b_fullB + 8 * rb.s, rb.ph, &s_abort, p.status);
           tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + c * kABytesPerChunk);
-          const uint32_t b_base = smem_u32(sB + s * kBBytes);
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            mma_bf16(d_tmem, desc_kmajor_sw128(a_base + kk * 32), desc_kmajor_sw128(b_base + kk * 32),
-                     kIdesc, (c | kk) != 0);
-          mma_commit(b_emptyB + 8 * s);
+          mma_chunk(d_tmem, da0 + ((uint32_t)c * (kABytesPerChunk >> 4)),
+                    db0 + (rb.s * (kBBytes >> 4)), c != 0);
+          mma_commit(b_emptyB + 8 * rb.s);
         }
         mma_commit(b_accFull + 8 * a);
       }
@@ -566,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int cta = blockIdx.y * gridDim.x + blockIdx.x;
   // work units: one tile, or (paired) tiles 2u and 2u + 1
   const int n_units = pair ? (p.n_vt + 1) / 2 : p.n_vt;
-  const int nW = pair ? 2 * p.nK : p.nK;  // W chunks per unit
+  const int passes = pair ? 2 : 1;  // K passes per unit (one per tile)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStagesB; ++i) {
@@ -610,23 +629,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpW) {
     if (lane == 0) {
       const uint64_t pol = policy_evict_last();
-      uint32_t it = 0;
+      RingPos rb;
       for (int k = 0; k < p.gamma; ++k)
         for (int u = blockIdx.x; u < n_units; u += gridDim.x)
-          for (int i = 0; i < nW; ++i, ++it) {
-            const int t = pair ? 2 * u + i / p.nK : u, c = i % p.nK;
-            const uint32_t s = it % kStagesB, ph = (it / kStagesB) & 1;
-            wait_abortable(b_emptyB + 8 * s, ph ^ 1, &s_abort, p.status);
-            if (t < p.n_vt) {
-              mbar_arrive_expect_tx(b_fullB + 8 * s, kBBytes);
-              tma_load_2d_hint(smem_u32(sB + s * kBBytes), &tm_w, b_fullB + 8 * s, c * BK, t * BN,
-                               pol);
-            } else {
-              // the odd last unit's second tile lies past V: no load, its
-              // accumulator rows are never read
-              mbar_arrive(b_fullB + 8 * s);
+          for (int pass = 0; pass < passes; ++pass)
+            for (int c = 0; c < p.nK; ++c, rb.next(kStagesB)) {
+              const int t = pair ? 2 * u + pass : u;
+              wait_abortable(b_emptyB + 8 * rb.s, rb.ph ^ 1, &s_abort, p.status);
+              if (t < p.n_vt) {
+                mbar_arrive_expect_tx(b_fullB + 8 * rb.s, kBBytes);
+                tma_load_2d_hint(smem_u32(sB + rb.s * kBBytes), &tm_w, b_fullB + 8 * rb.s, c * BK,
+                                 t * BN, pol);
+              } else {
+                // the odd last unit's second tile lies past V: no load, its
+                // accumulator rows are never read
+                mbar_arrive(b_fullB + 8 * rb.s);
+              }
             }
-          }
     }
   } else if (warp == kWarpZ) {
     if (lane == 0) {
@@ -656,7 +675,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
     }
   } else if (warp == kWarpMma) {
-    uint32_t it = 0, acc_it = 0;
+    const uint64_t da0 = desc_kmajor_sw128(smem_u32(sA));
+    const uint64_t db0 = desc_kmajor_sw128(smem_u32(sB));
+    // A chunk c of pass 0 / pass 1, in 16-byte descriptor units: paired, the
+    // first pass reads [E_c; 0] (block 2c + 1) against tile 2u and the
+    // second [0; E_c] (block 2c) against tile 2u + 1
+    const uint32_t a_step = (pair ? 2 * kPairBlk : kABytesPerChunk) >> 4;
+    const uint32_t a_pass0 = pair ? kPairBlk >> 4 : 0;
+    RingPos rb;
+    uint32_t acc_it = 0;
     for (int k = 0; k < p.gamma; ++k) {
       NamedSync<1, 288>::sync();  // A(k) is in shared memory, or on its way by TMA
       if (lane == 0) {
@@ -666,21 +693,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           wait_abortable(b_accEmpty + 8 * a, aph ^ 1, &s_abort, p.status);
           tc_fence_after();
           const uint32_t d_tmem = tmem + a * BN;
-          for (int i = 0; i < nW; ++i, ++it) {
-            const uint32_t s = it % kStagesB, ph = (it / kStagesB) & 1;
-            wait_abortable(b_fullB + 8 * s, ph, &s_abort, p.status);
-            tc_fence_after();
-            const int c = i % p.nK;
-            // paired: first pass [E_c; 0] against tile 2u, second [0; E_c] against 2u + 1
-            const uint32_t a_base =
-                pair ? smem_u32(sA + (size_t)(2 * c + (i < p.nK ? 1 : 0)) * kPairBlk)
-                     : smem_u32(sA + c * kABytesPerChunk);
-            const uint32_t b_base = smem_u32(sB + s * kBBytes);
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              mma_bf16(d_tmem, desc_kmajor_sw128(a_base + kk * 32),
-                       desc_kmajor_sw128(b_base + kk * 32), kIdesc, (i | kk) != 0);
-            mma_commit(b_emptyB + 8 * s);
+          for (int pass = 0; pass < passes; ++pass) {
+            uint64_t da = da0 + (pass == 0 ? a_pass0 : 0);
+            for (int c = 0; c < p.nK; ++c, da += a_step, rb.next(kStagesB)) {
+              wait_abortable(b_fullB + 8 * rb.s, rb.ph, &s_abort, p.status);
+              tc_fence_after();
+              mma_chunk(d_tmem, da, db0 + rb.s * (kBBytes >> 4), (pass | c) != 0);
+              mma_commit(b_emptyB + 8 * rb.s);
+            }
           }
           mma_commit(b_accFull + 8 * a);
         }
@@ -989,7 +1009,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int r0 = blockIdx.y * BM;
   // units: one tile, or (paired) tiles 2u and 2u + 1
   const int n_units = pair ? (p.n_vt + 1) / 2 : p.n_vt;
-  const int nW = pair ? 2 * p.nK : p.nK;
+  const int passes = pair ? 2 : 1;  // K passes per unit (one per tile)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStagesB; ++i) {
@@ -1071,20 +1091,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpW) {
     if (lane == 0) {
       const uint64_t pol = policy_evict_last();
-      uint32_t it = 0;
+      RingPos rb;
       for (int u = blockIdx.x; u < n_units; u += gridDim.x)
-        for (int i = 0; i < nW; ++i, ++it) {
-          const int t = pair ? 2 * u + i / p.nK : u, c = i % p.nK;
-          const uint32_t s = it % kStagesB, ph = (it / kStagesB) & 1;
-          wait_abortable(b_emptyB + 8 * s, ph ^ 1, &s_abort, p.status);
-          if (t < p.n_vt) {
-            mbar_arrive_expect_tx(b_fullB + 8 * s, kBBytes);
-            tma_load_2d_hint(smem_u32(sB + s * kBBytes), &tm_w, b_fullB + 8 * s, c * BK, t * BN,
-                             pol);
-          } else {
-            mbar_arrive(b_fullB + 8 * s);  // past V: nothing to load, rows never read
+        for (int pass = 0; pass < passes; ++pass)
+          for (int c = 0; c < p.nK; ++c, rb.next(kStagesB)) {
+            const int t = pair ? 2 * u + pass : u;
+            wait_abortable(b_emptyB + 8 * rb.s, rb.ph ^ 1, &s_abort, p.status);
+            if (t < p.n_vt) {
+              mbar_arrive_expect_tx(b_fullB + 8 * rb.s, kBBytes);
+              tma_load_2d_hint(smem_u32(sB + rb.s * kBBytes), &tm_w, b_fullB + 8 * rb.s, c * BK,
+                               t * BN, pol);
+            } else {
+              mbar_arrive(b_fullB + 8 * rb.s);  // past V: nothing to load, rows never read
+            }
           }
-        }
     }
   } else if (warp == kWarpZ) {
     // row copier: an instruction moves 8 slot rows, lanes 4i..4i+3 the four
@@ -1129,26 +1149,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
   } else if (warp == kWarpMma) {
     if (lane == 0) {
-      uint32_t it = 0, acc_it = 0;
+      const uint64_t da0 = desc_kmajor_sw128(smem_u32(sA));
+      const uint64_t db0 = desc_kmajor_sw128(smem_u32(sB));
+      // paired A chunks: pass 0 reads [E_c; 0] at block 2c + 1, pass 1 [0; E_c] at 2c
+      const uint32_t a_step = (pair ? 2 * kPairBlk : kABytesPerChunk) >> 4;
+      const uint32_t a_pass0 = pair ? kPairBlk >> 4 : 0;
+      RingPos rb;
+      uint32_t acc_it = 0;
       for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++acc_it) {
         const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
         wait_abortable(b_accEmpty + 8 * a, aph ^ 1, &s_abort, p.status);
         tc_fence_after();
         const uint32_t d_tmem = tmem + a * BN;
-        for (int i = 0; i < nW; ++i, ++it) {
-          const uint32_t s = it % kStagesB, ph = (it / kStagesB) & 1;
-          wait_abortable(b_fullB + 8 * s, ph, &s_abort, p.status);
-          tc_fence_after();
-          const int c = i % p.nK;
-          const uint32_t a_base =
-              pair ? smem_u32(sA + (size_t)(2 * c + (i < p.nK ? 1 : 0)) * kPairBlk)
-                   : smem_u32(sA + c * kABytesPerChunk);
-          const uint32_t b_base = smem_u32(sB + s * kBBytes);
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            mma_bf16(d_tmem, desc_kmajor_sw128(a_base + kk * 32), desc_kmajor_sw128(b_base + kk * 32),
-                     kIdesc, (i | kk) != 0);
-          mma_commit(b_emptyB + 8 * s);
+        for (int pass = 0; pass < passes; ++pass) {
+          uint64_t da = da0 + (pass == 0 ? a_pass0 : 0);
+          for (int c = 0; c < p.nK; ++c, da += a_step, rb.next(kStagesB)) {
+            wait_abortable(b_fullB + 8 * rb.s, rb.ph, &s_abort, p.status);
+            tc_fence_after();
+            mma_chunk(d_tmem, da, db0 + rb.s * (kBBytes >> 4), (pass | c) != 0);
+            mma_commit(b_emptyB + 8 * rb.s);
+          }
         }
         mma_commit(b_accFull + 8 * a);
       }
