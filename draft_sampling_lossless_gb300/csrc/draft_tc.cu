@@ -204,14 +204,10 @@ __device__ __forceinline__ void epi_block(const uint32_t (&b0)[32], const uint32
     if (!(chk < INFINITY)) s.bad = 1;
     return;
   }
-  // a = y * (hi + lo).  -inf (a masked token) is first clamped to a finite
-  // value so that the two-term product cannot form inf - inf; NaN and +inf
-  // pass through and surface in the block maximum.
-#pragma unroll
-  for (int e = 0; e < 64; ++e) {
-    const float yc = fmax_nan(y[e], -3.0e38f);
-    y[e] = fmaf(yc, p.sc.hi, yc * p.sc.lo);
-  }
+  // a = y * c with c = log2(e)/T rounded to fp32.  The block maximum is taken
+  // on y: the rounded product is monotone in y (c > 0), so the largest a is
+  // the product of the largest y.  NaN and +inf surface in that maximum;
+  // -inf (a masked token) stays -inf through the product and weighs 0.
   float mx[32];
 #pragma unroll
   for (int e = 0; e < 32; ++e) mx[e] = fmax_nan(y[e], y[e + 32]);
@@ -219,13 +215,13 @@ __device__ __forceinline__ void epi_block(const uint32_t (&b0)[32], const uint32
   for (int w = 16; w > 0; w >>= 1)
 #pragma unroll
     for (int e = 0; e < w; ++e) mx[e] = fmax_nan(mx[e], mx[e + w]);
-  const float cmax = mx[0];
+  const float cmax = mx[0] * p.sc.hi;
   if (!(cmax < 3.0e38f)) {  // NaN or +inf among the inputs
     s.bad = 1;
     return;
   }
   if (cmax <= -1.0e38f) return;  // no mass in these tokens
-  const int cref = static_cast<int>(ceilf(cmax));
+  const int cref = static_cast<int>(ceilf(fmaxf(cmax, -2.0e9f)));
   if (s.ref == INT_MIN) {
     s.ref = cref;
   } else if (cref > s.ref) {
@@ -239,7 +235,7 @@ __device__ __forceinline__ void epi_block(const uint32_t (&b0)[32], const uint32
   for (int g = 0; g < 4; ++g) {
     float t[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) t[e] = ex2_approx(y[g * 16 + e] - fref);
+    for (int e = 0; e < 16; ++e) t[e] = ex2_approx(fmaf(y[g * 16 + e], p.sc.hi, -fref));
 #pragma unroll
     for (int w = 8; w > 0; w >>= 1)
 #pragma unroll
