@@ -30,7 +30,7 @@ int cuda_fail(cudaError_t e, const char* where) {
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-  size_t status, bias, part, row_part, vstate, fin_part, prev, stage, rank, sfix, total;
+  size_t status, bias, part, sub, row_part, vstate, fin_part, prev, stage, rank, sfix, total;
 };
 
 bool sizes_ok(int R, int gamma, int V, int r) {
@@ -49,6 +49,8 @@ Layout layout(int R, int gamma, int V, int r) {
   off += align_up((size_t)R * V * sizeof(float));
   L.part = off;
   off += align_up((size_t)R * ((V + 127) / 128) * sizeof(double));  // 128-token partials (tensor-core path) or 256
+  L.sub = off;
+  off += align_up((size_t)R * ((V + 127) / 128) * 8 * sizeof(float));  // their 16-token group sums
   L.row_part = off;
   off += align_up((size_t)R * (gamma + 1) * n_chunks * sizeof(double));
   L.vstate = off;
@@ -170,6 +172,7 @@ int dspark_draft_sample(int R, int gamma, int V, int r, float temperature, const
   a.status = at<uint32_t>(ws, L.status);
   a.bias = at<float>(ws, L.bias);
   a.part = at<double>(ws, L.part);
+  a.sub = at<float>(ws, L.sub);
   a.grid_counter = at<unsigned>(ws, L.status + 64);
   a.stage = at<void>(ws, L.stage);
   cudaError_t e = launch_draft(a, (cudaStream_t)stream);

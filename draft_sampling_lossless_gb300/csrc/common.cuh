@@ -259,6 +259,7 @@ struct DraftArgs {
   uint32_t* status;
   float* bias;      // [R][V] scratch
   double* part;     // [R][n_tiles] scratch (greedy: ArgMax pairs)
+  float* sub;       // [R][n_tiles][8] 16-token group sums of 128-token partials
   unsigned* grid_counter;  // grid-barrier counter of the persistent draft kernel
   void* stage;             // [R][r] bf16: E rows of the latest drafted tokens
 };

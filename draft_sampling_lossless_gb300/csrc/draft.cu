@@ -149,10 +149,10 @@ __global__ void __launch_bounds__(256) draft_finish_kernel(
     int V, int gamma, int k, int n_tiles, const T* __restrict__ z, BiasSrc bsrc, ScalePair sc,
     int greedy, const double* __restrict__ part, const float* __restrict__ u,
     int32_t* __restrict__ tokens, double* __restrict__ q_lse, float* __restrict__ q_tok,
-    uint32_t* status) {
+    uint32_t* status, const float* __restrict__ sub) {
   __shared__ FinishScratch s;
   finish_request<T, TW, BlockSync, false>(s, blockIdx.x, V, gamma, k, n_tiles, z, bsrc, sc, greedy, part,
-                                   u, tokens, q_lse, q_tok, status);
+                                   u, tokens, q_lse, q_tok, status, nullptr, sub);
 }
 
 template <typename T, int TW>
@@ -162,7 +162,7 @@ cudaError_t launch_finish(const DraftArgs& a, int k, const BiasSrc& b, ScalePair
   DSPARK_LAUNCH(kKindDraftFinish, st,
                 draft_finish_kernel<T, TW><<<a.R, 256, 0, st>>>(
                     a.V, a.gamma, k, n_tiles, (const T*)a.z, b, sc, greedy, a.part, a.u,
-                    a.tokens, a.q_lse, a.q_tok, a.status));
+                    a.tokens, a.q_lse, a.q_tok, a.status, TW == 128 ? a.sub : nullptr));
   return cudaGetLastError();
 }
 

@@ -73,6 +73,7 @@ struct TcParams {
   const int32_t* prev;
   int prev_stride;
   double* part;     // [R][n_parts] partials (draft mode)
+  float* sub;       // [R][n_parts][8] 16-token group sums of each partial (sampling)
   float* bias_out;  // [R][V] (bias-out mode)
   uint32_t* status;
 };
@@ -165,11 +166,15 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
 // 64 consecutive tokens of one request row (two 32-column accumulator loads
 // and their z values): y = z + bias, then the greedy argmax or the
 // fixed-point sum of 2^(a - ref) with a = y*log2(e)/T.  `lim` = number of the
-// 64 tokens that lie below V.  The maxima and sums are trees, so a warp has
-// independent work to issue while MUFU and FMA results come back.
+// 64 tokens that lie below V.  gs receives the sums of the four 16-token
+// groups in units of 2^ref (s.ref on return; 0 where a group has no mass).
+// The maxima and sums are trees, so a warp has independent work to issue
+// while MUFU and FMA results come back.
 __device__ __forceinline__ void epi_block(const uint32_t (&b0)[32], const uint32_t (&b1)[32],
                                           const uint4 (&z0)[4], const uint4 (&z1)[4], int v0,
-                                          int lim, const TcParams& p, Part& s) {
+                                          int lim, const TcParams& p, Part& s, float (&gs)[4]) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) gs[g] = 0.f;
   float y[64];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -240,9 +245,25 @@ __device__ __forceinline__ void epi_block(const uint32_t (&b0)[32], const uint32
     for (int w = 8; w > 0; w >>= 1)
 #pragma unroll
       for (int e = 0; e < w; ++e) t[e] += t[e + w];
+    gs[g] = t[0];
     add += __float2ll_rn(t[0] * 1099511627776.0f);  // 2^40
   }
   s.acc += add;
+}
+
+// Stores the four 16-token group sums gs of block jj (0, 1) of a 128-token
+// partial, all eight in one unit: block 0's reference ref0 (the first block
+// with mass).  Block 1's sums, in units of 2^ref, are scaled up by
+// 2^(ref - ref0) (capped at 2^100: block 0 then weighs under 2^-100).
+__device__ __forceinline__ void store_groups(float* dst, int jj, const float (&gs)[4], int ref,
+                                             int& ref0) {
+  float sc = 1.f;
+  if (jj == 0) {
+    ref0 = ref;
+  } else if (ref0 != INT_MIN && ref > ref0) {
+    sc = __int_as_float((127 + min(ref - ref0, 100)) << 23);
+  }
+  *reinterpret_cast<float4*>(dst + jj * 4) = make_float4(gs[0] * sc, gs[1] * sc, gs[2] * sc, gs[3] * sc);
 }
 
 template <bool kBiasOut>
@@ -419,6 +440,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_abortable(b_accFull + 8 * a, aph, &s_abort, p.status);
       tc_fence_after();
       Part s{0, INT_MIN, 0, ArgMax{-INFINITY, 0x7fffffff}};
+      int ref0 = INT_MIN;
+      const size_t o = (size_t)n * p.n_parts + t * 2 + half;
+      const bool own = !kBiasOut && valid && t * 2 + half < p.n_parts;
 #pragma unroll 1
       for (int jj = 0; jj < 2; ++jj) {
         const int j = half * 2 + jj;  // z box (64 tokens) of this warp
@@ -456,20 +480,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(b_emptyZ + 8 * (half * 4 + zs));
         tmem_wait_ld();
-        if (valid) epi_block(b0, b1, z0, z1, v0, min(64, p.V - v0), p, s);
+        float gs[4] = {0.f, 0.f, 0.f, 0.f};
+        if (valid) epi_block(b0, b1, z0, z1, v0, min(64, p.V - v0), p, s, gs);
+        if (own && !p.greedy) store_groups(p.sub + o * 8, jj, gs, s.ref, ref0);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_accEmpty + 8 * a);
-      if (!kBiasOut && valid) {
+      if (own) {
         if (s.bad) set_flag(p.status, kFlagNonFinite);
-        const size_t o = (size_t)n * p.n_parts + t * 2 + half;
-        if (t * 2 + half < p.n_parts) {
-          if (p.greedy)
-            reinterpret_cast<ArgMax*>(p.part)[o] = s.best;
-          else
-            p.part[o] = (s.ref == INT_MIN) ? 0.0 : fix_to_double(s.acc, s.ref - kFixRel);
-        }
+        if (p.greedy)
+          reinterpret_cast<ArgMax*>(p.part)[o] = s.best;
+        else
+          p.part[o] = (s.ref == INT_MIN) ? 0.0 : fix_to_double(s.acc, s.ref - kFixRel);
       }
     }
   }
@@ -786,6 +809,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_abortable(b_accFull + 8 * a, aph, &s_abort, p.status);
         tc_fence_after();
         Part s{0, INT_MIN, 0, ArgMax{-INFINITY, 0x7fffffff}};
+        int ref0 = INT_MIN;
+        const size_t o = (size_t)n * p.n_parts + t * 2 + half;
+        const bool own = valid && t * 2 + half < p.n_parts;
 #pragma unroll 1
         for (int jj = 0; jj < 2; ++jj) {
           const int j = half * 2 + jj;
@@ -808,14 +834,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(b_emptyZ + 8 * (half * 4 + zs));
           tmem_wait_ld();
-          if (valid) epi_block(b0, b1, z0, z1, v0, min(64, p.V - v0), p, s);
+          float gs[4] = {0.f, 0.f, 0.f, 0.f};
+          if (valid) epi_block(b0, b1, z0, z1, v0, min(64, p.V - v0), p, s, gs);
+          if (own && !p.greedy) store_groups(p.sub + o * 8, jj, gs, s.ref, ref0);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(b_accEmpty + 8 * a);
-        if (valid && t * 2 + half < p.n_parts) {
+        if (own) {
           if (s.bad) set_flag(p.status, kFlagNonFinite);
-          const size_t o = (size_t)n * p.n_parts + t * 2 + half;
           if (p.greedy)
             reinterpret_cast<ArgMax*>(p.part)[o] = s.best;
           else
@@ -830,7 +857,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int nn = cta; nn < p.R; nn += n_ctas)
         finish_request<__nv_bfloat16, kHalf, NamedSync<3, 256>, true>(
             fs, nn, p.V, p.gamma, k, p.n_parts, pp.z, b, p.sc, p.greedy, p.part, pp.u, pp.tokens,
-            pp.q_lse, pp.q_tok, p.status, k + 1 < p.gamma ? pp.stage : nullptr);
+            pp.q_lse, pp.q_tok, p.status, k + 1 < p.gamma ? pp.stage : nullptr, p.sub);
       // the finish scratch (generic) is overwritten by the next A's TMA
       fence_proxy_async_smem();
       grid_sync(pp.grid_counter, (++epoch) * n_ctas, &s_abort, p.status);
@@ -1356,6 +1383,7 @@ cudaError_t launch_draft_partial_tc(const DraftArgs& a, int k, const int32_t* pr
   p.prev = prev;
   p.prev_stride = prev_stride;
   p.part = a.part;
+  p.sub = a.sub;
   p.bias_out = nullptr;
   p.status = a.status;
   return launch_tc<false>(tm_w, tm_z, p, st);
@@ -1389,6 +1417,7 @@ cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st) {
   p.prev = nullptr;
   p.prev_stride = 0;
   p.part = a.part;
+  p.sub = a.sub;
   p.bias_out = nullptr;
   p.status = a.status;
   pp.z = static_cast<const __nv_bfloat16*>(a.z);
@@ -1459,6 +1488,7 @@ cudaError_t launch_bias_tc(int R, int V, int r, const void* E, const void* Wt,
   p.prev = prev;
   p.prev_stride = prev_stride;
   p.part = nullptr;
+  p.sub = nullptr;
   p.bias_out = bias;
   p.status = status;
   return launch_tc<true>(tm_w, tm_w, p, st);

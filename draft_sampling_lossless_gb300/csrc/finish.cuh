@@ -45,6 +45,8 @@ struct FinishScratch {
   long long ssel;
   int fallback;
   int tok;
+  int grp;      // 16-token group of the chosen tile holding the draw
+  float f2;     // position of the draw inside that group, as a fraction of its mass
   float bias[256];
   float erow[1024];
 };
@@ -192,17 +194,81 @@ __device__ __forceinline__ void stage_row(FinishScratch& s, __nv_bfloat16* stage
   S::sync();
 }
 
+// The draw inside tile tsel from its 16-token group sums: the group (placed
+// by the caller, or the last group with mass after a fallback) is recomputed
+// exactly (warp w takes the group's tokens 2w and 2w + 1; lanes split the
+// rank with 16-byte loads) together with those tokens' E rows, so the drawn
+// token's row is staged from registers.  F, g: the fixed-point total of the
+// request's partials (sum_v 2^a_v = F * 2^g).
+template <typename T, class S, bool kDeferLog>
+__device__ __forceinline__ void finish_group(FinishScratch& s, int n, int V, int tsel, bool fallback,
+                                          size_t out, long long F, int g, const T* __restrict__ z,
+                                          const BiasSrc& bsrc, ScalePair sc, const float* sub,
+                                          int n_tiles, int32_t* tokens, double* q_lse,
+                                          float* q_tok, __nv_bfloat16* stage);
+
+// Where the draw falls inside a tile, from the tile's eight 16-token group
+// sums gs (any common unit) and the fraction f in [0, 1) of the tile's mass
+// below the draw: the first group whose running sum exceeds f * total, and
+// the fraction of that group's mass below the draw (fp32 throughout: a
+// group boundary moves by rounding only for draws within ~1e-7 of it).  No
+// group crossed: the last group with mass and *f_in = 2 (its last token).
+__device__ __forceinline__ int pick_group(const float (&gs)[8], float f, float* f_in) {
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) tot += gs[i];
+  const float tgt = f * tot;
+  float cum = 0.f, before = 0.f, gsel = 1.f;
+  int j = -1, lastg = -1;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float g = gs[i];
+    if (g > 0.f) {
+      if (j < 0 && cum + g > tgt) {
+        j = i;
+        before = cum;
+        gsel = g;
+      }
+      lastg = i;
+    }
+    cum += g;
+  }
+  if (j < 0) {
+    *f_in = 2.0f;
+    return lastg;
+  }
+  *f_in = fminf(fmaxf((tgt - before) / gsel, 0.f), 1.f);
+  return j;
+}
+
+// num / den for 0 <= num < den < 2^63, to fp32 precision, from the top 24
+// bits of both (integer shifts: no 64-bit conversions).
+__device__ __forceinline__ float ratio_ll(long long num, long long den) {
+  const int sh = max(0, 40 - __clzll(den));  // den >> sh < 2^24
+  return (float)(unsigned)(num >> sh) / (float)(unsigned)(den >> sh);
+}
+
+__device__ __forceinline__ void load_groups(const float* sub, float (&gs)[8]) {
+  const float4 a = __ldcg(reinterpret_cast<const float4*>(sub));
+  const float4 b = __ldcg(reinterpret_cast<const float4*>(sub) + 1);
+  gs[0] = a.x; gs[1] = a.y; gs[2] = a.z; gs[3] = a.w;
+  gs[4] = b.x; gs[5] = b.y; gs[6] = b.z; gs[7] = b.w;
+}
+
 // The finish of request n at draft position k, by 256 threads
 // (threadIdx.x < 256).  part: [R][n_tiles] tile partials (doubles; greedy:
 // ArgMax pairs) of width TW.  Writes tokens / q_lse / q_tok [n][k].
-// Partials and previous tokens may have been written by other blocks of the
-// same kernel, so they are read past L1 (ld.global.cg).
+// With sub ([R][n_tiles][8] group sums of 128-token partials) the draw is
+// placed in a 16-token group first and only that group is recomputed;
+// without, the whole tile is.  Partials and previous tokens may have been
+// written by other blocks of the same kernel, so they are read past L1
+// (ld.global.cg).
 template <typename T, int TW, class S, bool kDeferLog>
 __device__ void finish_request(FinishScratch& s, int n, int V, int gamma, int k, int n_tiles,
                                const T* __restrict__ z, const BiasSrc& bsrc, ScalePair sc,
                                int greedy, const double* part, const float* __restrict__ u,
                                int32_t* tokens, double* q_lse, float* q_tok, uint32_t* status,
-                               __nv_bfloat16* stage = nullptr) {
+                               __nv_bfloat16* stage = nullptr, const float* sub = nullptr) {
   const int tid = threadIdx.x;
   const size_t out = (size_t)n * gamma + k;
   const float u_out = greedy ? 0.0f : u[out];  // issued early: needed after the scan
@@ -320,19 +386,38 @@ __device__ void finish_request(FinishScratch& s, int n, int V, int gamma, int k,
       }
     }
   }
+  // With group sums, the thread whose segment holds the crossing places it
+  // in a group now, so that load overlaps the reduction that picks the tile.
+  int grp = -1;
+  float f2 = 2.0f;
+  if (TW == 128 && sub != nullptr && cand != 0x7fffffff) {
+    float gs[8];
+    load_groups(sub + ((size_t)n * n_tiles + cand) * 8, gs);
+    grp = pick_group(gs, ratio_ll(thr - base, ssel), &f2);
+  }
   int tsel = g_min_i<S>(cand, s.shi);
   if (tsel == 0x7fffffff) {
     // u outside [0, 1): the last tile with mass
     tsel = g_max_i<S>(last, s.shi);
     if (tsel < 0) tsel = 0;
-    if (tid == 0) s.fallback = 1;
+    if (tid == 0) {
+      s.fallback = 1;
+      s.grp = -1;
+    }
   } else if (cand == tsel) {
     s.base = base;
     s.ssel = ssel;
     s.fallback = 0;
+    s.grp = grp;
+    s.f2 = f2;
   }
   S::sync();
   const bool fallback = s.fallback != 0;
+  if (TW == 128 && sub != nullptr) {
+    finish_group<T, S, kDeferLog>(s, n, V, tsel, fallback, out, F, g, z, bsrc, sc, sub, n_tiles,
+                                  tokens, q_lse, q_tok, stage);
+    return;
+  }
   base = s.base;
   const long long S_sel = s.ssel;
   // Recompute the chosen tile.
@@ -378,6 +463,103 @@ __device__ void finish_request(FinishScratch& s, int n, int V, int gamma, int k,
   }
   S::sync();
   stage_row<S>(s, stage, bsrc, n);
+}
+
+template <typename T, class S, bool kDeferLog>
+__device__ __forceinline__ void finish_group(FinishScratch& s, int n, int V, int tsel, bool fallback,
+                                          size_t out, long long F, int g, const T* __restrict__ z,
+                                          const BiasSrc& bsrc, ScalePair sc, const float* sub,
+                                          int n_tiles, int32_t* tokens, double* q_lse,
+                                          float* q_tok, __nv_bfloat16* stage) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int grp0 = s.grp;
+  if (fallback || grp0 < 0) {
+    // the last group with mass, its last token with mass
+    S::sync();  // every thread has read s.grp before it is rewritten
+    if (tid == 0) {
+      float gs[8];
+      load_groups(sub + ((size_t)n * n_tiles + tsel) * 8, gs);
+      int lastg = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (gs[i] > 0.f) lastg = i;
+      s.grp = lastg;
+      s.f2 = 2.0f;
+    }
+    S::sync();
+  }
+  const int gv0 = tsel * 128 + s.grp * 16;
+  const float f2 = s.f2;
+  // bias of tokens gv0 + 2w + c; the E rows of the same tokens ride along
+  const int j = lane * 8;
+  const bool lane_on = j < bsrc.r;
+  uint4 wr[2], er[2];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int v = gv0 + 2 * w + c;
+    const bool ok = lane_on && v < V;
+    wr[c] = ok ? *reinterpret_cast<const uint4*>(bsrc.Wt + (size_t)v * bsrc.r + j)
+               : make_uint4(0, 0, 0, 0);
+    er[c] = (ok && stage != nullptr)
+                ? *reinterpret_cast<const uint4*>(bsrc.E + (size_t)v * bsrc.r + j)
+                : make_uint4(0, 0, 0, 0);
+  }
+  const int vz = gv0 + lane;
+  const float zv = (w == 0 && lane < 16 && vz < V) ? ldf(z, out * V + vz) : 0.f;
+  float e8[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) e8[i] = lane_on ? s.erow[j + i] : 0.f;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const uint32_t w4[4] = {wr[c].x, wr[c].y, wr[c].z, wr[c].w};
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc = fmaf(__uint_as_float(w4[e] << 16), e8[2 * e], acc);
+      acc = fmaf(__uint_as_float(w4[e] & 0xffff0000u), e8[2 * e + 1], acc);
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) s.bias[2 * w + c] = acc;
+  }
+  S::sync();
+  if (w == 0) {
+    const bool ok = lane < 16 && vz < V;
+    float y = ok ? zv + s.bias[lane] : -INFINITY;
+    if (ok && (isnan(y) || y == INFINITY)) y = -INFINITY;
+    const float a = scaled(y, sc);
+    const float amax = warp_max(a);
+    const float ref = ceilf(amax);
+    float wt = 0.f;
+    const long long f = (ok && a > -INFINITY && amax > -INFINITY) ? rel_fix(a, ref, &wt) : 0ll;
+    long long cum = f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long x = __shfl_up_sync(0xffffffffu, cum, o);
+      if (lane >= o) cum += x;
+    }
+    const long long mass = __shfl_sync(0xffffffffu, cum, 31);
+    // the draw is the first token whose running sum exceeds f2 * mass
+    const long long thr_g = f2 < 1.5f ? floor_mul(f2, mass) : LLONG_MAX;
+    const unsigned hit = __ballot_sync(0xffffffffu, f > 0 && cum > thr_g);
+    const unsigned has = __ballot_sync(0xffffffffu, f > 0);
+    const int isel = hit ? __ffs(hit) - 1 : (has ? 31 - __clz(has) : 0);
+    if (lane == isel) {
+      const int tok = gv0 + isel;
+      tokens[out] = tok;
+      const double total = fix_to_double(F, g);  // sum_v 2^a_v
+      q_lse[out] = kDeferLog ? total : log(total);
+      q_tok[out] = scale_pow2(wt / (float)F, (int)ref - g);
+      s.tok = isel;
+    }
+  }
+  S::sync();
+  if (stage != nullptr) {
+    const int isel = s.tok;
+    if (w == (isel >> 1) && lane_on)
+      *reinterpret_cast<uint4*>(stage + (size_t)n * bsrc.r + j) = (isel & 1) ? er[1] : er[0];
+    sm100::fence_proxy_async_all();
+    S::sync();
+  }
 }
 
 }  // namespace dspark
