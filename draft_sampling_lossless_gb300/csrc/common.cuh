@@ -488,15 +488,132 @@ __device__ __forceinline__ bool mul_gt(unsigned long long a, unsigned long long 
   return h1 != h2 ? h1 > h2 : a * b > c * d;
 }
 
-// x = 1/S as an InvPair (one thread; x > 0 finite, else the zero pair).
-__device__ __forceinline__ InvPair split_inv(double x) {
+// ---- Without double instructions.  The FP64 pipe of this GPU is narrow: a
+// dependent double division, logarithm or exponential costs on the order of
+// a microsecond, so paths that feed a per-request decision use the integer
+// and fp32 forms below.
+
+// v * 2^e2 as a float, v's top 24 bits (truncated); below the normal range: 0.
+__device__ __forceinline__ float fix_to_float(long long v, int e2) {
+  if (v == 0) return 0.f;
+  const bool neg = v < 0;
+  const unsigned long long a = neg ? 0ull - (unsigned long long)v : (unsigned long long)v;
+  const int msb = 63 - __clzll(a);
+  const uint32_t top = msb >= 23 ? (uint32_t)(a >> (msb - 23)) : (uint32_t)(a << (23 - msb));
+  const int ex = msb + e2;  // |value| = 1.top * 2^ex
+  if (ex < -126) return 0.f;
+  if (ex > 127) return neg ? -INFINITY : INFINITY;
+  return __uint_as_float((neg ? 0x80000000u : 0u) | ((uint32_t)(ex + 127) << 23) | (top & 0x7fffffu));
+}
+
+// Natural logarithm of F * 2^g (F > 0) in fp32 arithmetic, to about 3e-7
+// relative.  Away from 1 (value outside [0.5, 2), |log| > 0.69): the binary
+// exponent times ln 2 (split so that the large product is exact) plus the
+// logarithm of F's top 24 bits normalised to [1, 2).  Near 1: log1p of
+// value - 1, formed exactly in fixed point, so a logarithm near 0 keeps
+// its relative precision.
+__device__ __forceinline__ float fix_log(long long F, int g) {
+  const int msb = 63 - __clzll(F);
+  if ((msb + g == 0 || msb + g == -1) && g <= 0 && g >= -62) {
+    const long long u = F - (1ll << -g);  // (value - 1) * 2^-g, exact
+    return log1pf(fix_to_float(u, g));
+  }
+  const uint32_t top =
+      msb >= 23 ? (uint32_t)(F >> (msb - 23)) : (uint32_t)((unsigned long long)F << (23 - msb));
+  const float m = __uint_as_float(0x3f800000u | (top & 0x7fffffu));  // [1, 2)
+  const float A = (float)(msb + g);
+  constexpr float kLn2Hi = 0.693115234375f;        // 2839 / 4096: A * kLn2Hi is exact
+  constexpr float kLn2Lo = 3.1946184945309417e-05f;  // ln 2 - kLn2Hi
+  return fmaf(A, kLn2Hi, fmaf(A, kLn2Lo, logf(m)));
+}
+
+// Natural logarithm of a positive finite double x (as fix_log, from its
+// bits); 0 or negative: -inf.
+__device__ __forceinline__ float dbl_log(double x) {
+  const long long b = __double_as_longlong(x);
+  const int be = (int)((b >> 52) & 0x7ff);
+  if (b <= 0 || be == 0) return -INFINITY;
+  return fix_log((b & 0x000fffffffffffffll) | 0x0010000000000000ll, be - 1075);
+}
+
+// 1 / (F * 2^g) as an InvPair (F > 0; else the zero pair): an fp32
+// reciprocal of F's top bits, corrected by the exactly computed residual
+// 1 - x * r0 (128-bit integer product), relative error about 2^-45.
+__device__ __forceinline__ InvPair inv_fix(long long F, int g) {
   InvPair r{0.f, 0.f, 0};
-  if (!(x > 0.0) || !isfinite(x)) return r;
-  int e;
-  const double m = frexp(x, &e);  // x = m * 2^e, m in [0.5, 1)
-  r.hi = (float)m;
-  r.lo = (float)(m - (double)r.hi);
-  r.e = e;
+  if (F <= 0) return r;
+  const int msb = 63 - __clzll(F);
+  const unsigned long long Fn = (unsigned long long)F << (63 - msb);  // x = Fn / 2^64 in [0.5, 1)
+  const float xf = (float)(uint32_t)(Fn >> 40) * 5.9604644775390625e-08f;  // top 24 bits * 2^-24
+  const float r0 = 1.0f / xf;                                             // (1, 2]
+  const unsigned long long Mr = (unsigned long long)__float_as_uint(r0) == 0x40000000u
+                                    ? (1ull << 24)
+                                    : (((__float_as_uint(r0) & 0x7fffffu) | 0x800000u));  // r0 = Mr * 2^-23
+  // D = 2^87 - Fn * Mr = (1 - x * r0) * 2^87, |D| < 2^66
+  const unsigned long long plo = Fn * Mr, phi = __umul64hi(Fn, Mr);
+  const unsigned long long dlo = 0ull - plo;
+  const unsigned long long dhi = (1ull << 23) - phi - (plo != 0 ? 1ull : 0ull);
+  const long long d35 = (long long)((dlo >> 35) | (dhi << 29));  // D >> 35 (arithmetic)
+  const float eps = (float)(int)d35 * 2.220446049250313e-16f;    // D * 2^-87 = (D >> 35) * 2^-52
+  r.hi = 0.5f * r0;
+  r.lo = 0.5f * r0 * eps;
+  r.e = -(msb + g);  // 1 / (F 2^g) = (r0 + r0 eps) / 2 * 2^-(msb + g)
+  if (r.hi >= 1.0f) {
+    r.hi *= 0.5f;
+    r.lo *= 0.5f;
+    r.e += 1;
+  }
+  return r;
+}
+
+// exp(-x) for a double x as an InvPair (hi in [0.5, 1), lo = 0, e), without
+// double instructions: t = x log2(e) formed in fixed point from x's bits
+// (64-bit constant, 128-bit product, 32 fraction bits), then
+// 2^-t = 2^(1 - frac) / 2 * 2^-floor(t) with exp2f.  Relative error about
+// 3e-7.  x = NaN, +-inf or |x log2 e| >= 2^31: the zero pair.
+__device__ __forceinline__ InvPair exp_neg_pair(double x) {
+  InvPair r{0.f, 0.f, 0};
+  const unsigned long long xb = (unsigned long long)__double_as_longlong(x);
+  const int E = (int)((xb >> 52) & 0x7ff);
+  if (E == 0x7ff) return r;
+  if (E == 0) {  // zero or subnormal: exp(-x) = 1 to fp32 precision
+    r.hi = 0.5f;
+    r.e = 1;
+    return r;
+  }
+  const unsigned long long xm = (xb & 0x000fffffffffffffull) | 0x0010000000000000ull;
+  constexpr unsigned long long kLog2E = 6653256548922161246ull;  // round(log2(e) * 2^62)
+  const unsigned long long plo = xm * kLog2E, phi = __umul64hi(xm, kLog2E);
+  // t * 2^32 = P * 2^(E - 1075 - 62 + 32) = P >> (1105 - E)
+  const int sh = 1105 - E;
+  if (sh < 33) return r;  // t >= 2^31
+  unsigned long long T;
+  if (sh >= 128) {
+    T = 0;
+  } else if (sh >= 64) {
+    T = phi >> (sh - 64);
+  } else {
+    if ((phi >> sh) != 0) return r;  // P >> sh does not fit 64 bits: t >= 2^32
+    T = (plo >> sh) | (phi << (64 - sh));
+  }
+  if (T >> 63) return r;  // t >= 2^31
+  const long long k = (long long)(T >> 32);
+  const uint32_t f = (uint32_t)T;  // fraction of t in 2^-32 units
+  const bool neg = (xb >> 63) != 0;  // x < 0: exp(-x) = 2^+t
+  if (!neg) {
+    // 2^-t = (2^(1 - f 2^-32) / 2) * 2^-k, 2^(1 - .) in (1, 2]
+    const float fp = 1.0f - (float)f * 2.3283064365386963e-10f;
+    r.hi = 0.5f * exp2f(fp);
+    r.e = (int)-k;
+  } else {
+    // 2^t = (2^(f 2^-32) / 2) * 2^(k + 1), 2^(.) in [1, 2)
+    r.hi = 0.5f * exp2f((float)f * 2.3283064365386963e-10f);
+    r.e = (int)k + 1;
+  }
+  if (r.hi >= 1.0f) {
+    r.hi *= 0.5f;
+    r.e += 1;
+  }
   return r;
 }
 

@@ -869,7 +869,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = threadIdx.x; i < mine * p.gamma; i += 256) {
         const size_t o = (size_t)(cta + (i / p.gamma) * (int)n_ctas) * p.gamma + i % p.gamma;
         const double tot = pp.q_lse[o];
-        pp.q_lse[o] = tot > 0.0 ? log(tot) : -INFINITY;
+        pp.q_lse[o] = (double)dbl_log(tot);
       }
     }
   }

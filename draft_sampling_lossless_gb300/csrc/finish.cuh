@@ -456,7 +456,7 @@ __device__ void finish_request(FinishScratch& s, int n, int V, int gamma, int k,
   if (tid == isel) {
     tokens[out] = tsel * TW + isel;
     const double total = fix_to_double(F, g);  // sum_v 2^a_v
-    q_lse[out] = kDeferLog ? total : log(total);
+    q_lse[out] = kDeferLog ? total : (double)fix_log(F, g);
     // q(x) = 2^a / total = w * 2^ref / (F * 2^g)
     q_tok[out] = scale_pow2(w / (float)F, (int)ref - g);
     s.tok = tsel * TW + isel;
@@ -547,7 +547,7 @@ __device__ __forceinline__ void finish_group(FinishScratch& s, int n, int V, int
       const int tok = gv0 + isel;
       tokens[out] = tok;
       const double total = fix_to_double(F, g);  // sum_v 2^a_v
-      q_lse[out] = kDeferLog ? total : log(total);
+      q_lse[out] = kDeferLog ? total : (double)fix_log(F, g);
       q_tok[out] = scale_pow2(wt / (float)F, (int)ref - g);
       s.tok = isel;
     }

@@ -15,9 +15,12 @@
 //             the order is strict, so no sort network or stable radix pass is
 //             needed and the result does not depend on thread timing.
 //   finish -- one block: scatter to sorted order, exact integer prefix sums of
-//             the 2^-40 fixed-point survival values, Theta_i in double with the
-//             same operation order as the oracle, the early-stop or argmax cut,
-//             then l_r, row_off, B and E.
+//             the 2^-40 fixed-point survival values, Theta_i rounded exactly as
+//             the oracle's double arithmetic rounds it, the early-stop or
+//             argmax cut, then l_r, row_off, B and E.
+// No floating-point double instruction runs here: the double roundings are
+// reproduced with integer arithmetic (round to nearest, ties to even), which
+// gives the same bits and avoids the narrow FP64 pipe.
 #include "common.cuh"
 
 namespace dspark {
@@ -36,8 +39,104 @@ __device__ __forceinline__ float clean_a(float a, uint32_t* status) {
   return a;
 }
 
+// Nearest multiple of 2^-40 (ties to even) of a finite a >= 0, in 2^-40
+// units: the same integer as rounding the double a * 2^40.
 __device__ __forceinline__ long long to_fixed(float a) {
-  return __double2ll_rn((double)a * 1099511627776.0);  // 2^40, exact scaling
+  const uint32_t b = __float_as_uint(a);
+  const int E = (int)(b >> 23) & 0xff;
+  if (E == 0) return 0;  // subnormal: below 2^-126, rounds to 0
+  const unsigned long long m = (b & 0x7fffffu) | 0x800000u;  // a = m * 2^(E - 150)
+  const int sh = E - 110;                                     // a * 2^40 = m * 2^sh
+  if (sh >= 0) return sh > 39 ? LLONG_MAX : (long long)(m << sh);
+  const int k = -sh;
+  if (k > 25) return 0;
+  const unsigned long long q = m >> k, r = m & ((1ull << k) - 1), half = 1ull << (k - 1);
+  return (long long)(q + ((r > half || (r == half && (q & 1))) ? 1 : 0));
+}
+
+// x rounded to 53 significant bits (ties to even), for x < 2^63: the value
+// of the double nearest to x, as an integer.
+__device__ __forceinline__ unsigned long long rne53(unsigned long long x) {
+  const int msb = 63 - __clzll(x | 1);
+  if (msb <= 52) return x;
+  const int k = msb - 52;
+  const unsigned long long q = x >> k, r = x & ((1ull << k) - 1), half = 1ull << (k - 1);
+  return (q + ((r > half || (r == half && (q & 1))) ? 1 : 0)) << k;
+}
+
+// Bits of the double x * 2^e2 for an integer x < 2^63 with at most 53
+// significant bits (exact), x > 0.
+__device__ __forceinline__ unsigned long long dbl_bits(unsigned long long x, int e2) {
+  const int msb = 63 - __clzll(x);
+  const unsigned long long mant = msb <= 52 ? x << (52 - msb) : x >> (msb - 52);
+  return ((unsigned long long)(msb + e2 + 1023) << 52) | (mant & 0x000fffffffffffffull);
+}
+
+// Bits of the double product d * s rounded to nearest (ties to even), d a
+// positive normal double (bits), s a finite float; the result is a normal
+// double for every such pair met here (d in [1, 2^23]).  Zero: +0.
+__device__ __forceinline__ unsigned long long dbl_mul_float(unsigned long long d, float s) {
+  const uint32_t fb = __float_as_uint(s);
+  const int fe = (int)(fb >> 23) & 0xff;
+  unsigned long long fm = fb & 0x7fffffu;
+  if (fe == 0 && fm == 0) return 0;
+  int fexp;  // s = fm * 2^fexp
+  if (fe == 0) {
+    fexp = -149;
+  } else {
+    fm |= 0x800000u;
+    fexp = fe - 150;
+  }
+  const unsigned long long dm = (d & 0x000fffffffffffffull) | 0x0010000000000000ull;
+  const int dexp = (int)((d >> 52) & 0x7ff) - 1075;  // d = dm * 2^dexp
+  // exact product dm * fm (< 2^77) as hi:lo
+  const unsigned long long lo = dm * fm, hi = __umul64hi(dm, fm);
+  const int msb = hi ? 127 - __clzll(hi) : 63 - __clzll(lo);
+  const int k = msb - 52;  // bits below the 53 kept (k >= 0: dm alone has 53)
+  unsigned long long q, rlo, rhi;  // kept bits; remainder below them (hi:lo)
+  if (k >= 64) {
+    q = hi >> (k - 64);
+    rhi = hi & ((1ull << (k - 64)) - 1);
+    rlo = lo;
+  } else if (k > 0) {
+    q = (lo >> k) | (hi << (64 - k));
+    rhi = 0;
+    rlo = lo & ((1ull << k) - 1);
+  } else {
+    q = lo;
+    rhi = 0;
+    rlo = 0;
+  }
+  bool up = false;
+  if (k > 0) {
+    // compare the remainder with half = 2^(k-1)
+    bool gt, eq;
+    if (k - 1 >= 64) {
+      const unsigned long long hh = 1ull << (k - 1 - 64);
+      gt = rhi > hh || (rhi == hh && rlo > 0);
+      eq = rhi == hh && rlo == 0;
+    } else {
+      const unsigned long long hl = 1ull << (k - 1);
+      gt = rhi > 0 || rlo > hl;
+      eq = rhi == 0 && rlo == hl;
+    }
+    up = gt || (eq && (q & 1));
+  }
+  q += up ? 1 : 0;
+  int ex = msb + dexp + fexp;  // value = q * 2^(ex - 52)
+  if (q >> 53) {
+    q >>= 1;
+    ++ex;
+  }
+  const unsigned long long sign = (unsigned long long)(fb >> 31) << 63;
+  return sign | ((unsigned long long)(ex + 1023) << 52) | (q & 0x000fffffffffffffull);
+}
+
+// Unsigned key with the numeric order of the double whose bits are b (b not
+// NaN; -0 compares equal to +0).
+__device__ __forceinline__ unsigned long long dbl_key(unsigned long long b) {
+  if ((b << 1) == 0) b = 0;
+  return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
 }
 
 // grid: (ceil(N / 256), n_split); block 256.  rank[] must be zero on entry.
@@ -77,7 +176,7 @@ __device__ __forceinline__ void schedule_finish(
     double* __restrict__ E_out, uint32_t* status) {
   __shared__ long long shl[32];
   __shared__ int shi[32];
-  __shared__ double shd[32];
+  __shared__ unsigned long long shk[32];
   __shared__ int shidx[32];
   __shared__ int istar_s;
   const int N = R * gamma;
@@ -98,23 +197,29 @@ __device__ __forceinline__ void schedule_finish(
     if (i < N) loc += sfix[i];
   long long incl = block_inclusive_scan(loc, shl);
   const long long S0 = incl - loc;  // exact: integers
-  // Theta in the oracle's operation order: ((double)S * 2^-40 + R) * SPS
-  auto theta_at = [&](int i, long long S) -> double {
-    double e = __dadd_rn((double)R, __ll2double_rn(S) * 9.094947017729282e-13);  // 2^-40
+  // Theta in the oracle's operation order, ((double)S * 2^-40 + R) * SPS:
+  // S rounded to a double, the sum rounded, the product rounded; returned as
+  // an order key of the double's bits.
+  auto theta_key = [&](int i, long long S) -> unsigned long long {
+    const unsigned long long e =
+        rne53(((unsigned long long)R << 40) + rne53((unsigned long long)S));  // (R + S 2^-40) 2^40
     float s = sps[R + i];
-    if (!isfinite(s)) set_flag(status, kFlagNonFinite);
-    return __dmul_rn(e, (double)s);
+    if (!isfinite(s)) {
+      set_flag(status, kFlagNonFinite);
+      s = 0.0f;
+    }
+    return dbl_key(dbl_mul_float(dbl_bits(e, -40), s));
   };
   int my_stop = 0x7fffffff;
-  double best_v = -INFINITY;
+  unsigned long long best_v = 0;
   int best_i = 0x7fffffff;
   {
     long long S = S0;
-    double prev_th = 0.0;
+    unsigned long long prev_th = 0;
     for (int i = i0; i < i1; ++i) {
-      const double th = theta_at(i, S);
+      const unsigned long long th = theta_key(i, S);
       if (i > i0 && !(th > prev_th) && my_stop == 0x7fffffff) my_stop = i - 1;
-      if (th > best_v) {
+      if (best_i == 0x7fffffff || th > best_v) {
         best_v = th;
         best_i = i;
       }
@@ -123,7 +228,7 @@ __device__ __forceinline__ void schedule_finish(
     }
     // the pair that straddles the chunk boundary (i1 - 1, i1)
     if (i1 > i0 && i1 < n_i && my_stop == 0x7fffffff) {
-      const double th = theta_at(i1, S);
+      const unsigned long long th = theta_key(i1, S);
       if (!(th > prev_th)) my_stop = i1 - 1;
     }
   }
@@ -133,13 +238,14 @@ __device__ __forceinline__ void schedule_finish(
     istar = s == 0x7fffffff ? imax : s;
   } else {
     // first argmax: max value, then lowest index
+    // (key 0 is below every double's key: a thread with no i never wins)
     const int lane = tid & 31, wid = tid >> 5, nw = nt >> 5;
-    double v = best_v;
+    unsigned long long v = best_v;
     int bi = best_i;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      double ov = __shfl_xor_sync(0xffffffffu, v, o);
-      int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      const unsigned long long ov = __shfl_xor_sync(0xffffffffu, v, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
       if (ov > v || (ov == v && oi < bi)) {
         v = ov;
         bi = oi;
@@ -147,17 +253,17 @@ __device__ __forceinline__ void schedule_finish(
     }
     __syncthreads();
     if (lane == 0) {
-      shd[wid] = v;
+      shk[wid] = v;
       shidx[wid] = bi;
     }
     __syncthreads();
     if (wid == 0) {
-      v = lane < nw ? shd[lane] : -INFINITY;
+      v = lane < nw ? shk[lane] : 0ull;
       bi = lane < nw ? shidx[lane] : 0x7fffffff;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
-        double ov = __shfl_xor_sync(0xffffffffu, v, o);
-        int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        const unsigned long long ov = __shfl_xor_sync(0xffffffffu, v, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
         if (ov > v || (ov == v && oi < bi)) {
           v = ov;
           bi = oi;
@@ -173,7 +279,9 @@ __device__ __forceinline__ void schedule_finish(
   if (istar >= i0 && istar < i1) {
     long long S = S0;
     for (int i = i0; i < istar; ++i) S += sfix[i];
-    E_out[0] = __dadd_rn((double)R, __ll2double_rn(S) * 9.094947017729282e-13);
+    const unsigned long long e =
+        rne53(((unsigned long long)R << 40) + rne53((unsigned long long)S));
+    E_out[0] = __longlong_as_double((long long)dbl_bits(e, -40));
     B_out[0] = R + istar;
   }
   // 4. l_r = number of request r's candidates ranked below i*, and row_off

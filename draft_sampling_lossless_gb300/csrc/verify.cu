@@ -153,15 +153,65 @@ __global__ void __launch_bounds__(256) verify_rows_kernel(
 // ---------------------------------------------------------------- decide
 
 // u < p(x) / q(x) with p(x) = 2^a / Sp, a = t_x * log2(e) / T, in fp32
-// (Sp = m * 2^e taken apart by its bits, m to 24 bits): the result can differ
-// from the exact comparison only when u lies within about 1e-6 of the ratio.
-__device__ __forceinline__ bool accept_test(float tx, ScalePair sc, double Sp, float qx, float u) {
-  const int es = double_exponent(Sp);
-  if (es == INT_MIN || !isfinite(Sp)) return false;
-  const long long b = __double_as_longlong(Sp);
-  const float ms = __int_as_float(0x3f800000 | (int)((b >> 29) & 0x7fffff));  // [1, 2)
-  const float p = exp2f(scaled(tx, sc) - (float)es) / ms;
+// (Sp = F * 2^g = m * 2^e with m = F's top 24 bits in [1, 2)): the result can
+// differ from the exact comparison only when u lies within about 1e-6 of the
+// ratio.
+__device__ __forceinline__ bool accept_test(float tx, ScalePair sc, long long F, int g, float qx,
+                                            float u) {
+  if (F <= 0) return false;
+  const int msb = 63 - __clzll(F);
+  const uint32_t top =
+      msb >= 23 ? (uint32_t)(F >> (msb - 23)) : (uint32_t)((unsigned long long)F << (23 - msb));
+  const float ms = __uint_as_float(0x3f800000u | (top & 0x7fffffu));  // [1, 2)
+  const float p = exp2f(scaled(tx, sc) - (float)(msb + g)) / ms;
   return u < p / qx;
+}
+
+// A row's chunk partials are exact doubles of fixed-point sums: their total
+// F * 2^g is formed exactly as an integer sum in units of 2^g, g from the
+// largest exponent so that n_chunks of them stay below 2^62 (one warp; every
+// lane gets F and g).  No double instruction is used.  Non-finite partials
+// are counted as 0 and reported in *bad.
+__device__ __forceinline__ long long warp_fix_total(const double* __restrict__ pj, int n_chunks,
+                                                    int* g_out, bool* bad) {
+  const int lane = threadIdx.x & 31;
+  constexpr int kReg = 8;  // chunks per lane kept in registers (n_chunks <= 256)
+  const bool fast = n_chunks <= 32 * kReg;
+  auto clean = [&](double x) -> double {
+    if (((__double_as_longlong(x) >> 52) & 0x7ff) == 0x7ff) {
+      *bad = true;
+      return 0.0;
+    }
+    return x;
+  };
+  double pv[kReg];
+  int emax = INT_MIN;
+  if (fast) {
+#pragma unroll
+    for (int i = 0; i < kReg; ++i) {
+      const int c = lane + 32 * i;
+      pv[i] = c < n_chunks ? clean(pj[c]) : 0.0;
+      emax = max(emax, double_exponent(pv[i]));
+    }
+  } else {
+    for (int c = lane; c < n_chunks; c += 32) emax = max(emax, double_exponent(clean(pj[c])));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
+  if (emax == INT_MIN) {
+    *g_out = 0;
+    return 0;
+  }
+  const int g = emax + 2 + (32 - __clz(n_chunks)) - 62;
+  long long loc = 0;
+  if (fast) {
+#pragma unroll
+    for (int i = 0; i < kReg; ++i) loc += double_to_fix(pv[i], g);
+  } else {
+    for (int c = lane; c < n_chunks; c += 32) loc += double_to_fix(clean(pj[c]), g);
+  }
+  *g_out = g;
+  return warp_sum(loc);
 }
 
 
@@ -175,7 +225,8 @@ __global__ void __launch_bounds__(256) verify_decide_kernel(
     const double* __restrict__ row_part, double* __restrict__ p_lse,
     int32_t* __restrict__ n_acc_out, int32_t* __restrict__ out_tokens,
     VerifyState* __restrict__ vstate, int32_t* __restrict__ prev_out, uint32_t* status) {
-  __shared__ double Sp[kMaxGamma + 1];
+  __shared__ long long SpF[kMaxGamma + 1];  // target row totals F * 2^g
+  __shared__ int Spg[kMaxGamma + 1];
   __shared__ ArgMax am_s[kMaxGamma + 1];
   __shared__ int bad_s;
   grid_dependency_wait();  // the row partials
@@ -211,13 +262,15 @@ __global__ void __launch_bounds__(256) verify_decide_kernel(
         if (p_lse) p_lse[r0 + j] = (double)am.v;
       }
     } else {
-      double s = 0.0;
-      for (int c = lane; c < n_chunks; c += 32) s += pj[c];
-      s = warp_sum(s);
+      int g;
+      bool bad = false;
+      const long long F = warp_fix_total(pj, n_chunks, &g, &bad);
+      if (bad) set_flag(status, kFlagNonFinite);
       if (lane == 0) {
-        Sp[j] = s;
-        if (!(s > 0.0) || !isfinite(s)) set_flag(status, kFlagNonFinite);
-        if (p_lse) p_lse[r0 + j] = log(s);
+        SpF[j] = F;
+        Spg[j] = g;
+        if (F <= 0) set_flag(status, kFlagNonFinite);
+        if (p_lse) p_lse[r0 + j] = F > 0 ? (double)fix_log(F, g) : -INFINITY;
       }
     }
   }
@@ -234,7 +287,7 @@ __global__ void __launch_bounds__(256) verify_decide_kernel(
     } else if (greedy) {
       acc = (x == am_s[lane].i);
     } else {
-      acc = accept_test(to_f32<T>(target[(size_t)(r0 + lane) * V + x]), sc, Sp[lane],
+      acc = accept_test(to_f32<T>(target[(size_t)(r0 + lane) * V + x]), sc, SpF[lane], Spg[lane],
                         q_tok[(size_t)n * gamma + lane], u_acc[(size_t)n * gamma + lane]);
     }
   }
@@ -254,11 +307,11 @@ __global__ void __launch_bounds__(256) verify_decide_kernel(
   st.mode = greedy ? -1 : (nacc == L ? 0 : 1);
   st.final_row = (int)(r0 + nacc);
   st.prev = -1;
-  st.ip = greedy ? InvPair{0.f, 0.f, 0} : split_inv(1.0 / Sp[nacc]);
+  st.ip = greedy ? InvPair{0.f, 0.f, 0} : inv_fix(SpF[nacc], Spg[nacc]);
   st.iq = InvPair{0.f, 0.f, 0};
   if (st.mode == 1) {
     st.prev = nacc == 0 ? anchor[n] : tokens[(size_t)n * gamma + nacc - 1];
-    st.iq = split_inv(exp(-q_lse[(size_t)n * gamma + nacc]));
+    st.iq = exp_neg_pair(q_lse[(size_t)n * gamma + nacc]);
   }
   vstate[n] = st;
   prev_out[n] = st.prev;
