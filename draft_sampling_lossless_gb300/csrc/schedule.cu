@@ -169,9 +169,10 @@ __global__ void __launch_bounds__(kRankThreads) rank_kernel(int N, int per_split
 
 // The cut and the per-request outputs, by one block of kFinThreads threads,
 // given every candidate's rank.
+// a, rank and sfix may point to shared or global memory.
 __device__ __forceinline__ void schedule_finish(
-    int R, int gamma, int imax, int early_stop, const float* __restrict__ a,
-    const float* __restrict__ sps, const int32_t* rank, long long* __restrict__ sfix,
+    int R, int gamma, int imax, int early_stop, const float* a,
+    const float* __restrict__ sps, const int32_t* rank, long long* sfix,
     int32_t* __restrict__ ell, int32_t* __restrict__ row_off, int32_t* __restrict__ B_out,
     double* __restrict__ E_out, uint32_t* status) {
   __shared__ long long shl[32];
@@ -312,36 +313,49 @@ __global__ void __launch_bounds__(kFinThreads) schedule_finish_kernel(
                   status);
 }
 
-// Small batches (N <= kFusedMax candidates, one per thread): the ranks and the cut in one
-// block.  The candidates' survival values go to shared memory, every thread
-// ranks its candidates by counting comparisons against all N (no atomics, no
-// zeroing pass), and the finish reads the ranks from shared memory.
+// Small batches (N <= kFusedMax candidates): the ranks and the cut in one
+// block, everything in shared memory.  The cleaned survival values are
+// non-negative (zero as +0), so their bit patterns order like the values:
+// candidate e's rank counts the i < e with bits >= its own and the i > e with
+// bits > its own.  Each candidate's comparison range is split over
+// blockDim / N threads that add their counts with shared-memory atomics.
 constexpr int kFusedMax = 1024;
 
 __global__ void __launch_bounds__(kFinThreads) schedule_fused_kernel(
     int R, int gamma, int imax, int early_stop, const float* __restrict__ a,
-    const float* __restrict__ sps, long long* __restrict__ sfix, int32_t* __restrict__ rank_out,
-    int32_t* __restrict__ ell, int32_t* __restrict__ row_off, int32_t* __restrict__ B_out,
-    double* __restrict__ E_out, uint32_t* status) {
+    const float* __restrict__ sps, int32_t* __restrict__ rank_out, int32_t* __restrict__ ell,
+    int32_t* __restrict__ row_off, int32_t* __restrict__ B_out, double* __restrict__ E_out,
+    uint32_t* status) {
   __shared__ float as[kFusedMax];
+  __shared__ uint32_t ab[kFusedMax];
   __shared__ int32_t rk[kFusedMax];
+  __shared__ long long sf[kFusedMax];
   grid_dependency_wait();  // the survival values
-  const int N = R * gamma;
-  for (int e = threadIdx.x; e < N; e += blockDim.x) as[e] = clean_a(a[e], status);
-  __syncthreads();
-  for (int e = threadIdx.x; e < N; e += blockDim.x) {
-    const float ae = as[e];
-    int cnt = 0;
-    for (int i = 0; i < N; ++i) {
-      const float ai = as[i];
-      cnt += (ai > ae) | ((ai == ae) & (i < e));
-    }
-    rk[e] = cnt;
-    rank_out[e] = cnt;
+  const int N = R * gamma, nt = blockDim.x;
+  for (int e = threadIdx.x; e < N; e += nt) {
+    const float v = clean_a(a[e], status) + 0.0f;  // -0 -> +0
+    as[e] = v;
+    ab[e] = __float_as_uint(v);
+    rk[e] = 0;
   }
   __syncthreads();
-  schedule_finish(R, gamma, imax, early_stop, a, sps, rk, sfix, ell, row_off, B_out, E_out,
-                  status);
+  const int P = max(1, nt / N);  // threads per candidate
+  const int span = (N + P - 1) / P;
+  for (int t = threadIdx.x; t < N * P; t += nt) {
+    const int e = t % N, part = t / N;
+    const int i0 = part * span, i1 = min(N, i0 + span);
+    const uint32_t be = ab[e];
+    int cnt = 0;
+    const int im = min(max(e, i0), i1);
+#pragma unroll 8
+    for (int i = i0; i < im; ++i) cnt += ab[i] >= be ? 1 : 0;
+#pragma unroll 8
+    for (int i = max(im, e + 1); i < i1; ++i) cnt += ab[i] > be ? 1 : 0;
+    if (cnt) atomicAdd(&rk[e], cnt);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < N; e += nt) rank_out[e] = rk[e];
+  schedule_finish(R, gamma, imax, early_stop, as, sps, rk, sf, ell, row_off, B_out, E_out, status);
 }
 
 }  // namespace
@@ -352,8 +366,8 @@ cudaError_t launch_schedule(const SchedArgs& s, cudaStream_t st) {
   if (N <= kFusedMax) {
     DSPARK_LAUNCH(kKindSchedFinish, st,
                   launch_pdl(schedule_fused_kernel, dim3(1), dim3(kFinThreads), 0, st, s.R,
-                             s.gamma, imax0 < 0 ? 0 : imax0, s.early_stop, s.a, s.sps, s.sfix,
-                             s.rank, s.ell, s.row_off, s.B_out, s.E_out, s.status));
+                             s.gamma, imax0 < 0 ? 0 : imax0, s.early_stop, s.a, s.sps, s.rank,
+                             s.ell, s.row_off, s.B_out, s.E_out, s.status));
     return cudaGetLastError();
   }
   cudaError_t e = cudaMemsetAsync(s.rank, 0, sizeof(int32_t) * (size_t)N, st);
