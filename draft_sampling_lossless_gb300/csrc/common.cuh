@@ -25,6 +25,7 @@ constexpr uint32_t kFlagTokenRange = 0x1u;
 constexpr uint32_t kFlagNonFinite = 0x2u;
 constexpr uint32_t kFlagRowRange = 0x4u;
 constexpr uint32_t kFlagSpsRange = 0x8u;
+constexpr uint32_t kFlagWaitTimeout = 0x10u;  // a bounded on-chip wait gave up
 
 // log2(e) as a double-float pair (hi = fp32 rounding, lo = remainder) so that
 // y * log2(e) / T carries no shared fp32 rounding of the constant.

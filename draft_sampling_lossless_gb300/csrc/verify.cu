@@ -32,23 +32,6 @@ constexpr int kFinTile = 256;    // tokens per warp item of the final pass
 
 // ---------------------------------------------------------------- rows
 
-// Kahan-compensated fp32 running sum (the row normaliser scales every
-// residual weight of the final draw, so its error must stay far below the
-// per-element fp32 rounding).
-struct Kahan {
-  float s = 0.f, c = 0.f;
-  __device__ __forceinline__ void add(float x) {
-    const float y = x - c;
-    const float t = s + y;
-    c = (t - s) - y;
-    s = t;
-  }
-  // value in units of 2^-40
-  __device__ __forceinline__ long long fixed40() const {
-    return __float2ll_rn(s * 1099511627776.0f) - __float2ll_rn(c * 1099511627776.0f);
-  }
-};
-
 // load8 with an L2 evict-first cache policy: the row pass streams every
 // verified target row once, and should not push the draft's W (kept with an
 // evict-last policy for the final draw) out of L2.
@@ -87,66 +70,284 @@ __device__ __forceinline__ void load8_stream<float>(const float* p, int v0, int 
   }
 }
 
+// 1024 tokens of one row as raw 16-byte vectors: lane l holds tokens
+// i*256 + l*8 .. +7 of group i (bf16: one uint4 per group; fp32: two).
 template <typename T>
-__global__ void __launch_bounds__(256) verify_rows_kernel(
+struct RowRaw;
+template <>
+struct RowRaw<__nv_bfloat16> {
+  uint4 q[4];
+  __device__ __forceinline__ void load(const __nv_bfloat16* p, int lim, uint64_t pol) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int v0 = i * 256 + lane * 8;
+      if (v0 + 8 <= lim) {
+        asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                     : "=r"(q[i].x), "=r"(q[i].y), "=r"(q[i].z), "=r"(q[i].w)
+                     : "l"(p + v0), "l"(pol));
+      } else {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t lo = v0 + 2 * k < lim ? (uint32_t)__bfloat16_as_ushort(p[v0 + 2 * k]) : 0xff80u;
+          const uint32_t hi = v0 + 2 * k + 1 < lim ? (uint32_t)__bfloat16_as_ushort(p[v0 + 2 * k + 1]) : 0xff80u;
+          w[k] = lo | (hi << 16);  // 0xff80 = -inf
+        }
+        q[i] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+  }
+  __device__ __forceinline__ void get(int i, float (&o)[8]) const {
+    const uint32_t w[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      o[2 * k] = __uint_as_float(w[k] << 16);
+      o[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+    }
+  }
+};
+template <>
+struct RowRaw<float> {
+  float x[4][8];
+  __device__ __forceinline__ void load(const float* p, int lim, uint64_t pol) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) load8_stream<float>(p, i * 256 + lane * 8, lim, x[i], -INFINITY, pol);
+  }
+  __device__ __forceinline__ void get(int i, float (&o)[8]) const {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = x[i][e];
+  }
+};
+
+// One warp item: 1024 tokens of one verified row -> the exact fixed-point sum
+// of 2^(a - ref) over them as a double (greedy: the argmax pair).  Sums run
+// as fp32 trees over 8 tokens, each tree converted to 2^-40 units and added
+// as integers, so the result does not depend on the order of the adds.
+template <typename T>
+__device__ __forceinline__ void row_item(const RowRaw<T>& raw, int c, int V, ScalePair sc,
+                                         int greedy, double* out) {
+  const int lane = threadIdx.x & 31;
+  if (greedy) {
+    ArgMax am{-INFINITY, 0x7fffffff};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float x[8];
+      raw.get(i, x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int v = c * kRowChunk + i * 256 + lane * 8 + e;
+        if (v < V) am = better(am, ArgMax{x[e], v});
+      }
+    }
+    am = warp_argmax(am);
+    if (lane == 0) *reinterpret_cast<ArgMax*>(out) = am;
+    return;
+  }
+  // the scaled values' maximum is the scaled maximum (the scale is positive)
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float x[8];
+    raw.get(i, x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) m = fmaxf(m, x[e]);
+  }
+  m = scaled_clamped(warp_max(m), sc);
+  double S = 0.0;
+  if (m > -1.0e38f) {
+    const float ref = ceilf(m);
+    long long f = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float t[8];
+      raw.get(i, t);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) t[e] = ex2_fast(scaled_clamped(t[e], sc) - ref);
+#pragma unroll
+      for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+        for (int e = 0; e < w; ++e) t[e] += t[e + w];
+      f += __float2ll_rn(t[0] * 1099511627776.0f);  // 2^40
+    }
+    f = warp_sum(f);
+    S = fix_to_double(f, (int)ref - kFixRel);
+  }
+  if (lane == 0) *out = S;
+}
+
+// The verified-row list of the row pass, built by every block in shared
+// memory: s_r0 = row_off, s_pre = exclusive prefix of the rows per request
+// (1 + ell[n], 0 for an invalid ell -- the decide kernel reports it).
+__device__ __forceinline__ int build_row_list(int R, int gamma, const int32_t* __restrict__ ell,
+                                              const int32_t* __restrict__ row_off, int* s_r0,
+                                              int* s_pre, int* s_scan) {
+  int cnt[4], loc = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int n = threadIdx.x * 4 + q;
+    cnt[q] = 0;
+    if (n < R) {
+      const int L = ell[n];
+      s_r0[n] = row_off[n];
+      cnt[q] = (L >= 0 && L <= gamma) ? L + 1 : 0;
+    }
+    loc += cnt[q];
+  }
+  const int incl = block_inclusive_scan(loc, s_scan);
+  int run = incl - loc;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int n = threadIdx.x * 4 + q;
+    if (n < R) s_pre[n] = run;
+    run += cnt[q];
+  }
+  if (threadIdx.x == blockDim.x - 1) s_pre[R] = incl;
+  __syncthreads();
+  return s_pre[R];
+}
+
+constexpr int kRowsSmem = 1024;  // requests whose row list fits shared memory
+
+// The row pass for bf16 targets with V % 8 == 0 (16-byte aligned rows): each
+// warp streams its items' 2 KiB row chunks into a ring of kRowStages slots in
+// shared memory with bulk copies (L2 evict-first), so all of a warp's
+// upcoming chunks are in flight while it reduces the current one, at few
+// registers.  Every wait is bounded; a timeout sets the timeout flag.
+constexpr int kRowStages = 4;
+constexpr uint32_t kRowSlot = kRowChunk * 2;  // bytes of one bf16 chunk
+constexpr size_t kRowsTmaSmem = 8 * kRowStages * kRowSlot;
+
+__global__ void __launch_bounds__(256) verify_rows_tma_kernel(
+    int R, int gamma, int V, int n_chunks, long long n_rows,
+    const __nv_bfloat16* __restrict__ target, const int32_t* __restrict__ ell,
+    const int32_t* __restrict__ row_off, ScalePair sc, int greedy, double* __restrict__ row_part,
+    uint32_t* status) {
+  extern __shared__ __align__(16) uint8_t rows_ring[];
+  __shared__ int s_r0[kRowsSmem];
+  __shared__ int s_pre[kRowsSmem + 1];
+  __shared__ int s_scan[32];
+  __shared__ uint64_t bars[8][kRowStages];
+  __shared__ double* s_out[8][kRowStages];
+  __shared__ int s_c[8][kRowStages];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint64_t pol = sm100::policy_evict_first();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 8 * kRowStages; ++i) sm100::mbar_init(sm100::smem_u32(&bars[0][0] + i), 1);
+    sm100::fence_mbar_init();
+  }
+  grid_dependency_wait();  // ell, row_off
+  const int n_verified = build_row_list(R, gamma, ell, row_off, s_r0, s_pre, s_scan);
+  const uint32_t total = (uint32_t)n_verified * (uint32_t)n_chunks;
+  const uint32_t nwarps = gridDim.x * 8, w0 = blockIdx.x * 8 + warp;
+  uint8_t* ring = rows_ring + (size_t)warp * kRowStages * kRowSlot;
+  // lane 0: decode item `it` and start its copy into slot s
+  auto issue = [&](uint32_t it, int s) {
+    const int k = (int)(it / (uint32_t)n_chunks);
+    const int c = (int)(it - (uint32_t)k * (uint32_t)n_chunks);
+    int lo = 0, hi = R - 1;  // the request n with s_pre[n] <= k < s_pre[n + 1]
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_pre[mid] <= k) lo = mid;
+      else hi = mid - 1;
+    }
+    const int n = lo, j = k - s_pre[n];
+    const long long row = (long long)s_r0[n] + j;
+    const uint32_t bar = sm100::smem_u32(&bars[warp][s]);
+    s_c[warp][s] = c;
+    if (row < 0 || row >= n_rows) {  // reported by the decide kernel
+      s_out[warp][s] = nullptr;
+      sm100::mbar_arrive(bar);
+      return;
+    }
+    s_out[warp][s] = row_part + ((size_t)n * (gamma + 1) + j) * n_chunks + c;
+    const uint32_t bytes = (uint32_t)min(kRowChunk, V - c * kRowChunk) * 2u;
+    sm100::mbar_arrive_expect_tx(bar, bytes);
+    sm100::bulk_load_hint(sm100::smem_u32(ring + s * kRowSlot),
+                          target + (size_t)row * V + (size_t)c * kRowChunk, bytes, bar, pol);
+  };
+  if (lane == 0)
+    for (int s = 0; s < kRowStages; ++s) {
+      const uint32_t it = w0 + (uint32_t)s * nwarps;
+      if (it < total) issue(it, s);
+    }
+  __syncwarp();
+  for (uint32_t q = 0;; ++q) {
+    const uint32_t it = w0 + q * nwarps;
+    if (it >= total) break;
+    const int s = (int)(q % kRowStages);
+    const bool ok = sm100::mbar_wait(sm100::smem_u32(&bars[warp][s]), (q / kRowStages) & 1);
+    if (!__all_sync(0xffffffffu, ok)) {
+      // give up: flag it, then wait (bounded) for this warp's other copies
+      if (lane == 0) {
+        set_flag(status, kFlagWaitTimeout);
+        for (uint32_t r = q + 1; r < q + kRowStages; ++r)
+          if (w0 + r * nwarps < total)
+            sm100::mbar_wait(sm100::smem_u32(&bars[warp][r % kRowStages]), (r / kRowStages) & 1);
+      }
+      break;
+    }
+    double* out = s_out[warp][s];
+    const int c = s_c[warp][s];
+    if (out != nullptr) {
+      const int lim = V - c * kRowChunk;
+      RowRaw<__nv_bfloat16> x;
+      const uint8_t* slot = ring + s * kRowSlot;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int v0 = i * 256 + lane * 8;
+        if (v0 + 8 <= lim) {
+          x.q[i] = *reinterpret_cast<const uint4*>(slot + v0 * 2);
+        } else {
+          uint32_t w[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint16_t* h = reinterpret_cast<const uint16_t*>(slot) + v0 + 2 * k;
+            const uint32_t lo = v0 + 2 * k < lim ? h[0] : 0xff80u;  // -inf past V
+            const uint32_t hi = v0 + 2 * k + 1 < lim ? h[1] : 0xff80u;
+            w[k] = lo | (hi << 16);
+          }
+          x.q[i] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      row_item<__nv_bfloat16>(x, c, V, sc, greedy, out);
+    }
+    __syncwarp();
+    if (lane == 0) {
+      const uint32_t next = it + kRowStages * nwarps;
+      if (next < total) {
+        sm100::fence_proxy_async_smem();  // this slot's generic reads before the refill
+        issue(next, s);
+      }
+    }
+    __syncwarp();
+  }
+}
+
+// The same pass for R > kRowsSmem: items (n, j, c) over every request and
+// position, ell and row_off read from global memory, unverified j skipped.
+template <typename T>
+__global__ void __launch_bounds__(256) verify_rows_wide_kernel(
     int R, int gamma, int V, int n_chunks, long long n_rows, const T* __restrict__ target,
     const int32_t* __restrict__ ell, const int32_t* __restrict__ row_off, ScalePair sc,
     int greedy, double* __restrict__ row_part) {
-  const int lane = threadIdx.x & 31;
   const uint64_t pol = sm100::policy_evict_first();
   grid_dependency_wait();  // ell, row_off
   const long long total = (long long)R * (gamma + 1) * n_chunks;
   const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
   for (long long item = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
        item < total; item += nwarps) {
-    const int c = (int)(item % n_chunks);
     const long long nj = item / n_chunks;
-    const int j = (int)(nj % (gamma + 1));
-    const int n = (int)(nj / (gamma + 1));
+    const int c = (int)(item - nj * n_chunks);
+    const int n = (int)(nj / (gamma + 1)), j = (int)(nj - (long long)n * (gamma + 1));
     const int L = ell[n];
     if (j > L || L > gamma) continue;
     const long long row = (long long)row_off[n] + j;
     if (row < 0 || row >= n_rows) continue;  // reported by the decide kernel
-    const T* tr = target + (size_t)row * V;
-    double* out = row_part + ((size_t)n * (gamma + 1) + j) * n_chunks + c;
-    float x[4][8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      load8_stream<T>(tr, c * kRowChunk + i * 256 + lane * 8, V, x[i], -INFINITY, pol);
-    if (greedy) {
-      ArgMax am{-INFINITY, 0x7fffffff};
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int v = c * kRowChunk + i * 256 + lane * 8 + e;
-          if (v < V) am = better(am, ArgMax{x[i][e], v});
-        }
-      am = warp_argmax(am);
-      if (lane == 0) *reinterpret_cast<ArgMax*>(out) = am;
-      continue;
-    }
-    float m = -3.0e38f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        x[i][e] = scaled_clamped(x[i][e], sc);
-        m = fmaxf(m, x[i][e]);
-      }
-    m = warp_max(m);
-    double S = 0.0;
-    if (m > -1.0e38f) {
-      const float ref = ceilf(m);
-      Kahan k;
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) k.add(ex2_fast(x[i][e] - ref));
-      const long long f = warp_sum(k.fixed40());
-      S = fix_to_double(f, (int)ref - kFixRel);
-    }
-    if (lane == 0) *out = S;
+    RowRaw<T> x;
+    x.load(target + (size_t)row * V + (size_t)c * kRowChunk, V - c * kRowChunk, pol);
+    row_item<T>(x, c, V, sc, greedy, row_part + ((size_t)n * (gamma + 1) + j) * n_chunks + c);
   }
 }
 
@@ -617,9 +818,21 @@ __global__ void __launch_bounds__(256) final_pick_tc_kernel(
   if (tid == 0) out_tokens[(size_t)n * (gamma + 1) + st.n_acc] = hsel * 128 + isel;
 }
 
-int row_grid(long long items) {
+// The row pass's grid: as many blocks as fit on the GPU at once (every block
+// strides over the items), at most one warp per item.
+template <typename K>
+int row_grid(K kernel, long long items, size_t dyn_smem) {
+  int per_sm = 0, dev = 0, n_sm = 0;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1)
+    n_sm = 148;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, dyn_smem) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const long long resident = (long long)per_sm * n_sm;
   const long long blocks = (items + 7) / 8;
-  return (int)(blocks < 152 * 16 ? blocks : 152 * 16);
+  return (int)(blocks < resident ? (blocks < 1 ? 1 : blocks) : resident);
 }
 
 template <typename T>
@@ -631,10 +844,30 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t st) {
   const T* z = (const T*)a.z;
   const T* tg = (const T*)a.target;
   const long long items = (long long)a.R * (a.gamma + 1) * n_chunks;
-  DSPARK_LAUNCH(kKindVerifyRows, st,
-                launch_pdl(verify_rows_kernel<T>, dim3(row_grid(items)), dim3(256), 0, st, a.R,
-                           a.gamma, a.V, n_chunks, a.n_rows, tg, a.ell, a.row_off, sc,
-                           (int)greedy, a.row_part));
+  const bool staged = sizeof(T) == 2 && a.R <= kRowsSmem && a.V % 8 == 0 &&
+                      ((uintptr_t)a.target & 15) == 0;
+  if (staged) {
+    static int grid = 0;  // attribute and occupancy once per process
+    if (grid == 0) {
+      cudaError_t e = cudaFuncSetAttribute(verify_rows_tma_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)kRowsTmaSmem);
+      if (e != cudaSuccess) return e;
+      grid = row_grid(verify_rows_tma_kernel, 1ll << 40, kRowsTmaSmem);
+    }
+    const int g = (int)(grid < (items + 7) / 8 ? grid : (items + 7) / 8);
+    DSPARK_LAUNCH(kKindVerifyRows, st,
+                  launch_pdl(verify_rows_tma_kernel, dim3(g), dim3(256), kRowsTmaSmem, st, a.R,
+                             a.gamma, a.V, n_chunks, a.n_rows,
+                             reinterpret_cast<const __nv_bfloat16*>(tg), a.ell, a.row_off, sc,
+                             (int)greedy, a.row_part, a.status));
+  } else {
+    DSPARK_LAUNCH(kKindVerifyRows, st,
+                  launch_pdl(verify_rows_wide_kernel<T>,
+                             dim3(row_grid(verify_rows_wide_kernel<T>, items, 0)), dim3(256), 0,
+                             st, a.R, a.gamma, a.V, n_chunks, a.n_rows, tg, a.ell, a.row_off, sc,
+                             (int)greedy, a.row_part));
+  }
   DSPARK_LAUNCH(kKindVerifyDecide, st,
                 launch_pdl(verify_decide_kernel<T>, dim3(a.R), dim3(256), 0, st, a.gamma, a.V,
                            n_chunks, a.n_rows, tg, sc, (int)greedy, a.anchor, a.tokens, a.q_lse,
