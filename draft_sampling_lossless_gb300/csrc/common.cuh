@@ -13,7 +13,7 @@ namespace dspark {
 // Vocabulary tile of the draft / final-sampling partial sums, and chunk of
 // the verification row pass.
 constexpr int kTileV = 256;
-constexpr int kChunkV = 1024;  // tokens per warp item of the verification row pass
+constexpr int kChunkV = 4096;  // tokens per warp item of the verification row pass
 // Fixed-point fraction bits: weights relative to a tile's power-of-two
 // reference (each <= 1) are summed exactly as integers in units of 2^-kFixRel;
 // normalised weights (p, residual) in units of 2^-kFixAbs.

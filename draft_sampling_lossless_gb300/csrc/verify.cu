@@ -27,7 +27,9 @@ namespace dspark {
 
 namespace {
 
-constexpr int kRowChunk = kChunkV;
+constexpr int kRowChunk = kChunkV;          // tokens per row-pass item
+constexpr int kRowSub = 1024;               // tokens per sub-chunk (one bulk copy)
+constexpr int kRowGroup = kRowChunk / kRowSub;  // sub-chunks per item
 constexpr int kFinTile = 256;    // tokens per warp item of the final pass
 
 // ---------------------------------------------------------------- rows
@@ -106,6 +108,17 @@ struct RowRaw<__nv_bfloat16> {
       o[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
     }
   }
+  // the largest of the 32 values (NaN ignored), on bf16 pairs
+  __device__ __forceinline__ float max() const {
+    __nv_bfloat162 m = *reinterpret_cast<const __nv_bfloat162*>(&q[0].x);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t w[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) m = __hmax2(m, *reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+    }
+    return fmaxf(__low2float(m), __high2float(m));
+  }
 };
 template <>
 struct RowRaw<float> {
@@ -119,63 +132,94 @@ struct RowRaw<float> {
 #pragma unroll
     for (int e = 0; e < 8; ++e) o[e] = x[i][e];
   }
+  __device__ __forceinline__ float max() const {
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m = fmaxf(m, x[i][e]);
+    return m;
+  }
 };
 
-// One warp item: 1024 tokens of one verified row -> the exact fixed-point sum
-// of 2^(a - ref) over them as a double (greedy: the argmax pair).  Sums run
-// as fp32 trees over 8 tokens, each tree converted to 2^-40 units and added
-// as integers, so the result does not depend on the order of the adds.
-template <typename T>
-__device__ __forceinline__ void row_item(const RowRaw<T>& raw, int c, int V, ScalePair sc,
-                                         int greedy, double* out) {
-  const int lane = threadIdx.x & 31;
-  if (greedy) {
-    ArgMax am{-INFINITY, 0x7fffffff};
+// Running state of one warp item (kRowChunk tokens of a verified row, taken
+// as kRowGroup sub-chunks of kRowSub tokens): per lane the fixed-point sum of
+// 2^(a - ref) in 2^-40 units against a warp-wide power-of-two reference
+// that only grows (the sum is shifted down when it does), or the greedy
+// argmax.  a = y * c with c = log2(e)/T rounded to fp32: the largest a is
+// the scaled largest y (c > 0), each exponent argument is one FMA (-inf
+// weighs 0).  Per sub-chunk a lane adds its 32 weights as an fp32 tree and
+// converts the tree once.  A NaN surfaces in a tree, +inf in a maximum:
+// both flag the row non-finite and weigh 0.
+struct RowState {
+  long long acc = 0;
+  int ref = INT_MIN;
+  bool bad = false;
+  ArgMax am{-INFINITY, 0x7fffffff};
+
+  template <typename T>
+  __device__ __forceinline__ void add(const RowRaw<T>& raw, int v0, int V, ScalePair sc,
+                                      int greedy) {
+    const int lane = threadIdx.x & 31;
+    if (greedy) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float x[8];
+        raw.get(i, x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int v = v0 + i * 256 + lane * 8 + e;
+          if (v < V) am = better(am, ArgMax{x[e], v});
+        }
+      }
+      return;
+    }
+    const float m = warp_max(raw.max()) * sc.hi;
+    if (!(m < 3.0e38f)) {  // +inf or NaN
+      bad = true;
+      return;
+    }
+    if (m <= -1.0e38f) return;  // no mass here
+    const int cref = (int)ceilf(m);
+    if (ref == INT_MIN) {
+      ref = cref;
+    } else if (cref > ref) {
+      const int d = cref - ref;
+      acc = d >= 63 ? 0 : (acc >> d);
+      ref = cref;
+    }
+    const float fref = (float)ref;
+    float t[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       float x[8];
       raw.get(i, x);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int v = c * kRowChunk + i * 256 + lane * 8 + e;
-        if (v < V) am = better(am, ArgMax{x[e], v});
-      }
-    }
-    am = warp_argmax(am);
-    if (lane == 0) *reinterpret_cast<ArgMax*>(out) = am;
-    return;
-  }
-  // the scaled values' maximum is the scaled maximum (the scale is positive)
-  float m = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float x[8];
-    raw.get(i, x);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) m = fmaxf(m, x[e]);
-  }
-  m = scaled_clamped(warp_max(m), sc);
-  double S = 0.0;
-  if (m > -1.0e38f) {
-    const float ref = ceilf(m);
-    long long f = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float t[8];
-      raw.get(i, t);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) t[e] = ex2_fast(scaled_clamped(t[e], sc) - ref);
+      for (int e = 0; e < 8; ++e) x[e] = ex2_fast(fmaf(x[e], sc.hi, -fref));
 #pragma unroll
       for (int w = 4; w > 0; w >>= 1)
 #pragma unroll
-        for (int e = 0; e < w; ++e) t[e] += t[e + w];
-      f += __float2ll_rn(t[0] * 1099511627776.0f);  // 2^40
+        for (int e = 0; e < w; ++e) x[e] += x[e + w];
+      t[i] = x[0];
     }
-    f = warp_sum(f);
-    S = fix_to_double(f, (int)ref - kFixRel);
+    const float sum = (t[0] + t[1]) + (t[2] + t[3]);
+    if (sum != sum) bad = true;
+    else acc += __float2ll_rn(sum * 1099511627776.0f);  // 2^40
   }
-  if (lane == 0) *out = S;
-}
+
+  // the item's partial (sampling: a double of the exact fixed-point total)
+  __device__ __forceinline__ void store(int greedy, double* out, uint32_t* status) {
+    const int lane = threadIdx.x & 31;
+    if (greedy) {
+      const ArgMax r = warp_argmax(am);
+      if (lane == 0) *reinterpret_cast<ArgMax*>(out) = r;
+      return;
+    }
+    const long long f = warp_sum(acc);
+    if (__any_sync(0xffffffffu, bad) && lane == 0) set_flag(status, kFlagNonFinite);
+    if (lane == 0) *out = (ref == INT_MIN || f <= 0) ? 0.0 : fix_to_double(f, ref - kFixRel);
+  }
+};
 
 // The verified-row list of the row pass, built by every block in shared
 // memory: s_r0 = row_off, s_pre = exclusive prefix of the rows per request
@@ -210,13 +254,16 @@ __device__ __forceinline__ int build_row_list(int R, int gamma, const int32_t* _
 
 constexpr int kRowsSmem = 1024;  // requests whose row list fits shared memory
 
-// The row pass for bf16 targets with V % 8 == 0 (16-byte aligned rows): each
-// warp streams its items' 2 KiB row chunks into a ring of kRowStages slots in
-// shared memory with bulk copies (L2 evict-first), so all of a warp's
-// upcoming chunks are in flight while it reduces the current one, at few
-// registers.  Every wait is bounded; a timeout sets the timeout flag.
+// The row pass for bf16 targets with V % 8 == 0 (16-byte aligned rows).
+// Item = (verified row, chunk of kRowChunk tokens), strided over the grid's
+// warps.  Each warp streams its items' sub-chunks (2 KiB each) in order
+// through a ring of kRowStages shared-memory slots with bulk copies (L2
+// evict-first): lane 0 keeps the copies kRowStages units ahead of the
+// reduction, so every warp has its next item's data in flight while it
+// reduces the current one, at few registers.  Every wait is bounded; a
+// timeout sets the timeout flag.
 constexpr int kRowStages = 4;
-constexpr uint32_t kRowSlot = kRowChunk * 2;  // bytes of one bf16 chunk
+constexpr uint32_t kRowSlot = kRowSub * 2;  // bytes of one bf16 sub-chunk
 constexpr size_t kRowsTmaSmem = 8 * kRowStages * kRowSlot;
 
 __global__ void __launch_bounds__(256) verify_rows_tma_kernel(
@@ -229,8 +276,7 @@ __global__ void __launch_bounds__(256) verify_rows_tma_kernel(
   __shared__ int s_pre[kRowsSmem + 1];
   __shared__ int s_scan[32];
   __shared__ uint64_t bars[8][kRowStages];
-  __shared__ double* s_out[8][kRowStages];
-  __shared__ int s_c[8][kRowStages];
+  __shared__ double* s_out[8][kRowStages];  // the unit's item output (null: row out of range)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint64_t pol = sm100::policy_evict_first();
   if (threadIdx.x == 0) {
@@ -239,13 +285,25 @@ __global__ void __launch_bounds__(256) verify_rows_tma_kernel(
   }
   grid_dependency_wait();  // ell, row_off
   const int n_verified = build_row_list(R, gamma, ell, row_off, s_r0, s_pre, s_scan);
+  const int n_subs = (V + kRowSub - 1) / kRowSub;
   const uint32_t total = (uint32_t)n_verified * (uint32_t)n_chunks;
   const uint32_t nwarps = gridDim.x * 8, w0 = blockIdx.x * 8 + warp;
   uint8_t* ring = rows_ring + (size_t)warp * kRowStages * kRowSlot;
-  // lane 0: decode item `it` and start its copy into slot s
-  auto issue = [&](uint32_t it, int s) {
-    const int k = (int)(it / (uint32_t)n_chunks);
-    const int c = (int)(it - (uint32_t)k * (uint32_t)n_chunks);
+  auto subs_of = [&](uint32_t item) -> int {
+    const int c = (int)(item % (uint32_t)n_chunks);
+    return min(kRowGroup, n_subs - c * kRowGroup);
+  };
+  // producer cursor (lane 0): the next unit to copy
+  uint32_t p_item = w0;
+  int p_sub = 0, p_nsub = 0;
+  const __nv_bfloat16* p_src = nullptr;  // sub-chunk 0 of p_item's chunk, null: nothing to copy
+  double* p_out = nullptr;
+  auto p_decode = [&]() {
+    p_sub = 0;
+    if (p_item >= total) return;
+    const int k = (int)(p_item / (uint32_t)n_chunks);
+    const int c = (int)(p_item - (uint32_t)k * (uint32_t)n_chunks);
+    p_nsub = min(kRowGroup, n_subs - c * kRowGroup);
     int lo = 0, hi = R - 1;  // the request n with s_pre[n] <= k < s_pre[n + 1]
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -254,84 +312,103 @@ __global__ void __launch_bounds__(256) verify_rows_tma_kernel(
     }
     const int n = lo, j = k - s_pre[n];
     const long long row = (long long)s_r0[n] + j;
-    const uint32_t bar = sm100::smem_u32(&bars[warp][s]);
-    s_c[warp][s] = c;
     if (row < 0 || row >= n_rows) {  // reported by the decide kernel
-      s_out[warp][s] = nullptr;
-      sm100::mbar_arrive(bar);
-      return;
+      p_src = nullptr;
+      p_out = nullptr;
+    } else {
+      p_src = target + (size_t)row * V + (size_t)c * kRowChunk;
+      p_out = row_part + ((size_t)n * (gamma + 1) + j) * n_chunks + c;
     }
-    s_out[warp][s] = row_part + ((size_t)n * (gamma + 1) + j) * n_chunks + c;
-    const uint32_t bytes = (uint32_t)min(kRowChunk, V - c * kRowChunk) * 2u;
-    sm100::mbar_arrive_expect_tx(bar, bytes);
-    sm100::bulk_load_hint(sm100::smem_u32(ring + s * kRowSlot),
-                          target + (size_t)row * V + (size_t)c * kRowChunk, bytes, bar, pol);
   };
-  if (lane == 0)
-    for (int s = 0; s < kRowStages; ++s) {
-      const uint32_t it = w0 + (uint32_t)s * nwarps;
-      if (it < total) issue(it, s);
+  auto p_issue = [&](int slot) {  // copy the producer's unit into `slot`, advance
+    if (p_item >= total) return;
+    const uint32_t bar = sm100::smem_u32(&bars[warp][slot]);
+    s_out[warp][slot] = p_out;
+    if (p_src == nullptr) {
+      sm100::mbar_arrive(bar);
+    } else {
+      const int v0 = (p_item % (uint32_t)n_chunks) * kRowChunk + p_sub * kRowSub;
+      const uint32_t bytes = (uint32_t)min(kRowSub, V - v0) * 2u;
+      sm100::mbar_arrive_expect_tx(bar, bytes);
+      sm100::bulk_load_hint(sm100::smem_u32(ring + slot * kRowSlot), p_src + p_sub * kRowSub,
+                            bytes, bar, pol);
     }
+    if (++p_sub == p_nsub) {
+      p_item += nwarps;
+      p_decode();
+    }
+  };
+  if (lane == 0) {
+    p_decode();
+    for (int sl = 0; sl < kRowStages; ++sl) p_issue(sl);
+  }
   __syncwarp();
-  for (uint32_t q = 0;; ++q) {
-    const uint32_t it = w0 + q * nwarps;
-    if (it >= total) break;
-    const int s = (int)(q % kRowStages);
-    const bool ok = sm100::mbar_wait(sm100::smem_u32(&bars[warp][s]), (q / kRowStages) & 1);
-    if (!__all_sync(0xffffffffu, ok)) {
-      // give up: flag it, then wait (bounded) for this warp's other copies
+  uint32_t u = 0;  // units consumed by this warp
+  for (uint32_t item = w0; item < total; item += nwarps) {
+    const int c = (int)(item % (uint32_t)n_chunks), nsub = subs_of(item);
+    RowState st;
+    double* out = nullptr;
+    bool failed = false;
+    for (int sb = 0; sb < nsub; ++sb, ++u) {
+      const int slot = (int)(u % kRowStages);
+      const bool ok = sm100::mbar_wait(sm100::smem_u32(&bars[warp][slot]), (u / kRowStages) & 1);
+      if (!__all_sync(0xffffffffu, ok)) {
+        failed = true;
+        break;
+      }
+      out = s_out[warp][slot];
+      if (out != nullptr) {
+        const int v0 = c * kRowChunk + sb * kRowSub, lim = V - v0;
+        RowRaw<__nv_bfloat16> x;
+        const uint8_t* sl = ring + slot * kRowSlot;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int e0 = i * 256 + lane * 8;
+          if (e0 + 8 <= lim) {
+            x.q[i] = *reinterpret_cast<const uint4*>(sl + e0 * 2);
+          } else {
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint16_t* h = reinterpret_cast<const uint16_t*>(sl) + e0 + 2 * k;
+              const uint32_t lo = e0 + 2 * k < lim ? h[0] : 0xff80u;  // -inf past V
+              const uint32_t hi = e0 + 2 * k + 1 < lim ? h[1] : 0xff80u;
+              w[k] = lo | (hi << 16);
+            }
+            x.q[i] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        st.add(x, v0, V, sc, greedy);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        sm100::fence_proxy_async_smem();  // this slot's generic reads before the refill
+        p_issue(slot);
+      }
+      __syncwarp();
+    }
+    if (failed) {
+      // give up: flag it, then wait (bounded) for this warp's copies in flight
       if (lane == 0) {
         set_flag(status, kFlagWaitTimeout);
-        for (uint32_t r = q + 1; r < q + kRowStages; ++r)
-          if (w0 + r * nwarps < total)
-            sm100::mbar_wait(sm100::smem_u32(&bars[warp][r % kRowStages]), (r / kRowStages) & 1);
+        for (uint32_t r = u + 1; r < u + kRowStages; ++r)
+          sm100::mbar_wait(sm100::smem_u32(&bars[warp][r % kRowStages]), (r / kRowStages) & 1);
       }
       break;
     }
-    double* out = s_out[warp][s];
-    const int c = s_c[warp][s];
-    if (out != nullptr) {
-      const int lim = V - c * kRowChunk;
-      RowRaw<__nv_bfloat16> x;
-      const uint8_t* slot = ring + s * kRowSlot;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int v0 = i * 256 + lane * 8;
-        if (v0 + 8 <= lim) {
-          x.q[i] = *reinterpret_cast<const uint4*>(slot + v0 * 2);
-        } else {
-          uint32_t w[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint16_t* h = reinterpret_cast<const uint16_t*>(slot) + v0 + 2 * k;
-            const uint32_t lo = v0 + 2 * k < lim ? h[0] : 0xff80u;  // -inf past V
-            const uint32_t hi = v0 + 2 * k + 1 < lim ? h[1] : 0xff80u;
-            w[k] = lo | (hi << 16);
-          }
-          x.q[i] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-      }
-      row_item<__nv_bfloat16>(x, c, V, sc, greedy, out);
-    }
-    __syncwarp();
-    if (lane == 0) {
-      const uint32_t next = it + kRowStages * nwarps;
-      if (next < total) {
-        sm100::fence_proxy_async_smem();  // this slot's generic reads before the refill
-        issue(next, s);
-      }
-    }
-    __syncwarp();
+    if (out != nullptr) st.store(greedy, out, status);
   }
 }
 
-// The same pass for R > kRowsSmem: items (n, j, c) over every request and
-// position, ell and row_off read from global memory, unverified j skipped.
+// The same pass for the other cases (R > kRowsSmem, fp32 targets, rows not
+// 16-byte aligned): items (n, j, c) over every request and position, ell
+// and row_off read from global memory, unverified j skipped, the sub-chunks
+// loaded with plain vector loads.
 template <typename T>
 __global__ void __launch_bounds__(256) verify_rows_wide_kernel(
     int R, int gamma, int V, int n_chunks, long long n_rows, const T* __restrict__ target,
     const int32_t* __restrict__ ell, const int32_t* __restrict__ row_off, ScalePair sc,
-    int greedy, double* __restrict__ row_part) {
+    int greedy, double* __restrict__ row_part, uint32_t* status) {
   const uint64_t pol = sm100::policy_evict_first();
   grid_dependency_wait();  // ell, row_off
   const long long total = (long long)R * (gamma + 1) * n_chunks;
@@ -345,9 +422,15 @@ __global__ void __launch_bounds__(256) verify_rows_wide_kernel(
     if (j > L || L > gamma) continue;
     const long long row = (long long)row_off[n] + j;
     if (row < 0 || row >= n_rows) continue;  // reported by the decide kernel
-    RowRaw<T> x;
-    x.load(target + (size_t)row * V + (size_t)c * kRowChunk, V - c * kRowChunk, pol);
-    row_item<T>(x, c, V, sc, greedy, row_part + ((size_t)n * (gamma + 1) + j) * n_chunks + c);
+    RowState st;
+    for (int sb = 0; sb < kRowGroup; ++sb) {
+      const int v0 = c * kRowChunk + sb * kRowSub;
+      if (v0 >= V) break;
+      RowRaw<T> x;
+      x.load(target + (size_t)row * V + v0, V - v0, pol);
+      st.add(x, v0, V, sc, greedy);
+    }
+    st.store(greedy, row_part + ((size_t)n * (gamma + 1) + j) * n_chunks + c, status);
   }
 }
 
@@ -866,7 +949,7 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t st) {
                   launch_pdl(verify_rows_wide_kernel<T>,
                              dim3(row_grid(verify_rows_wide_kernel<T>, items, 0)), dim3(256), 0,
                              st, a.R, a.gamma, a.V, n_chunks, a.n_rows, tg, a.ell, a.row_off, sc,
-                             (int)greedy, a.row_part));
+                             (int)greedy, a.row_part, a.status));
   }
   DSPARK_LAUNCH(kKindVerifyDecide, st,
                 launch_pdl(verify_decide_kernel<T>, dim3(a.R), dim3(256), 0, st, a.gamma, a.V,
