@@ -148,6 +148,28 @@ __device__ __forceinline__ void mma_chunk(uint32_t d_tmem, uint64_t da, uint64_t
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
+// Two fp32 values in one 64-bit register pair, and the packed two-wide fp32
+// add and FMA of the 5th-generation SM (one instruction for both lanes).
+__device__ __forceinline__ unsigned long long pack2(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unpack2(unsigned long long r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
 // Per-thread running state of one (request, half tile) partial.
 struct Part {
   long long acc;  // sum of 2^(a - ref) in units of 2^-40
@@ -175,23 +197,29 @@ __device__ __forceinline__ void epi_block(const uint32_t (&b0)[32], const uint32
                                           int lim, const TcParams& p, Part& s, float (&gs)[4]) {
 #pragma unroll
   for (int g = 0; g < 4; ++g) gs[g] = 0.f;
-  float y[64];
+  // y = z + bias on element pairs (packed two-wide fp32 adds)
+  unsigned long long y2[32];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const uint32_t w0[4] = {z0[q].x, z0[q].y, z0[q].z, z0[q].w};
     const uint32_t w1[4] = {z1[q].x, z1[q].y, z1[q].z, z1[q].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      y[q * 8 + 2 * e] = bf_lo(w0[e]) + __uint_as_float(b0[q * 8 + 2 * e]);
-      y[q * 8 + 2 * e + 1] = bf_hi(w0[e]) + __uint_as_float(b0[q * 8 + 2 * e + 1]);
-      y[32 + q * 8 + 2 * e] = bf_lo(w1[e]) + __uint_as_float(b1[q * 8 + 2 * e]);
-      y[32 + q * 8 + 2 * e + 1] = bf_hi(w1[e]) + __uint_as_float(b1[q * 8 + 2 * e + 1]);
+      y2[q * 4 + e] = add2(pack2(bf_lo(w0[e]), bf_hi(w0[e])),
+                           pack2(__uint_as_float(b0[q * 8 + 2 * e]), __uint_as_float(b0[q * 8 + 2 * e + 1])));
+      y2[16 + q * 4 + e] = add2(pack2(bf_lo(w1[e]), bf_hi(w1[e])),
+                                pack2(__uint_as_float(b1[q * 8 + 2 * e]), __uint_as_float(b1[q * 8 + 2 * e + 1])));
     }
   }
+  float y[64];
+#pragma unroll
+  for (int e = 0; e < 32; ++e) unpack2(y2[e], y[2 * e], y[2 * e + 1]);
   if (lim < 64) {
 #pragma unroll
     for (int e = 0; e < 64; ++e)
       if (e >= lim) y[e] = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) y2[e] = pack2(y[2 * e], y[2 * e + 1]);
   }
   if (p.greedy) {
     ArgMax t[32];
@@ -235,18 +263,26 @@ __device__ __forceinline__ void epi_block(const uint32_t (&b0)[32], const uint32
     s.ref = cref;
   }
   const float fref = static_cast<float>(s.ref);
+  const unsigned long long c2 = pack2(p.sc.hi, p.sc.hi), r2 = pack2(-fref, -fref);
   long long add = 0;
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
-    float t[16];
+    unsigned long long t2[8];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) t[e] = ex2_approx(fmaf(y[g * 16 + e], p.sc.hi, -fref));
+    for (int e = 0; e < 8; ++e) {
+      float a0, a1;
+      unpack2(fma2(y2[g * 8 + e], c2, r2), a0, a1);  // a - ref
+      t2[e] = pack2(ex2_approx(a0), ex2_approx(a1));
+    }
 #pragma unroll
-    for (int w = 8; w > 0; w >>= 1)
+    for (int w = 4; w > 0; w >>= 1)
 #pragma unroll
-      for (int e = 0; e < w; ++e) t[e] += t[e + w];
-    gs[g] = t[0];
-    add += __float2ll_rn(t[0] * 1099511627776.0f);  // 2^40
+      for (int e = 0; e < w; ++e) t2[e] = add2(t2[e], t2[e + w]);
+    float t0, t1;
+    unpack2(t2[0], t0, t1);
+    const float tg = t0 + t1;
+    gs[g] = tg;
+    add += __float2ll_rn(tg * 1099511627776.0f);  // 2^40
   }
   s.acc += add;
 }
