@@ -467,16 +467,19 @@ __device__ __forceinline__ float scale_pow2(float x, int k) {
   return x * __int_as_float((k1 + 127) << 23) * __int_as_float((k2 + 127) << 23);
 }
 
-// floor(u * F) exactly, for u in [0, 1) and 0 <= F < 2^62.
+// floor(u * F) exactly, for u in [0, 1) and 0 <= F < 2^62, from u's bits
+// (u = m * 2^(E - 150)) and a 128-bit integer product: no conversion
+// instructions (those between floats and 64-bit integers are slow here).
+// u >= 1 (outside the contract) clamps to F.
 __device__ __forceinline__ long long floor_mul(float u, long long F) {
   if (!(u > 0.0f)) return 0;
-  int e;
-  const float mf = frexpf(u, &e);  // u = mf * 2^e, mf in [0.5, 1)
-  const unsigned long long m = (unsigned long long)(mf * 16777216.0f);  // u = m * 2^(e-24)
+  if (!(u < 1.0f)) return F;
+  const uint32_t b = __float_as_uint(u);
+  const int E = (int)(b >> 23);  // u > 0: no sign bit
+  const unsigned long long m = E ? ((b & 0x7fffffu) | 0x800000u) : (b & 0x7fffffu);
+  const int sh = 150 - (E ? E : 1);  // u = m * 2^-sh, sh > 23 since u < 1
   const unsigned long long lo = m * (unsigned long long)F;
   const unsigned long long hi = __umul64hi(m, (unsigned long long)F);
-  const int sh = 24 - e;
-  if (sh <= 0) return F;  // u >= 1: outside the contract, clamp
   if (sh >= 128) return 0;
   if (sh >= 64) return (long long)(hi >> (sh - 64));
   return (long long)((lo >> sh) | (hi << (64 - sh)));

@@ -458,7 +458,8 @@ __device__ void finish_request(FinishScratch& s, int n, int V, int gamma, int k,
     const double total = fix_to_double(F, g);  // sum_v 2^a_v
     q_lse[out] = kDeferLog ? total : (double)fix_log(F, g);
     // q(x) = 2^a / total = w * 2^ref / (F * 2^g)
-    q_tok[out] = scale_pow2(w / (float)F, (int)ref - g);
+    const int fm = 63 - __clzll(F);
+    q_tok[out] = scale_pow2(w / fix_to_float(F, -fm), (int)ref - g - fm);
     s.tok = tsel * TW + isel;
   }
   S::sync();
@@ -523,32 +524,38 @@ __device__ __forceinline__ void finish_group(FinishScratch& s, int n, int V, int
   }
   S::sync();
   if (w == 0) {
+    // lanes 0-15: the group's tokens.  Weights 2^(a - ref) <= 1 in 32-bit
+    // fixed point (2^-27 units: 16 of them stay below 2^31) and their scan,
+    // all in 32-bit integer arithmetic.
     const bool ok = lane < 16 && vz < V;
     float y = ok ? zv + s.bias[lane] : -INFINITY;
     if (ok && (isnan(y) || y == INFINITY)) y = -INFINITY;
     const float a = scaled(y, sc);
     const float amax = warp_max(a);
     const float ref = ceilf(amax);
-    float wt = 0.f;
-    const long long f = (ok && a > -INFINITY && amax > -INFINITY) ? rel_fix(a, ref, &wt) : 0ll;
-    long long cum = f;
+    const float wt = (ok && a > -INFINITY && amax > -INFINITY) ? exp2f(a - ref) : 0.f;
+    const uint32_t f = __float2uint_rn(wt * 134217728.0f);  // 2^27
+    uint32_t cum = f;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long x = __shfl_up_sync(0xffffffffu, cum, o);
+    for (int o = 1; o < 16; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xffffffffu, cum, o);
       if (lane >= o) cum += x;
     }
-    const long long mass = __shfl_sync(0xffffffffu, cum, 31);
+    const uint32_t mass = __shfl_sync(0xffffffffu, cum, 15);
     // the draw is the first token whose running sum exceeds f2 * mass
-    const long long thr_g = f2 < 1.5f ? floor_mul(f2, mass) : LLONG_MAX;
-    const unsigned hit = __ballot_sync(0xffffffffu, f > 0 && cum > thr_g);
-    const unsigned has = __ballot_sync(0xffffffffu, f > 0);
+    const uint32_t thr_g =
+        f2 < 1.5f ? __umulhi(__float2uint_rz(f2 * 4294967040.0f), mass) : 0xffffffffu;
+    const unsigned hit = __ballot_sync(0xffffffffu, lane < 16 && f > 0 && cum > thr_g);
+    const unsigned has = __ballot_sync(0xffffffffu, lane < 16 && f > 0);
     const int isel = hit ? __ffs(hit) - 1 : (has ? 31 - __clz(has) : 0);
     if (lane == isel) {
       const int tok = gv0 + isel;
       tokens[out] = tok;
       const double total = fix_to_double(F, g);  // sum_v 2^a_v
       q_lse[out] = kDeferLog ? total : (double)fix_log(F, g);
-      q_tok[out] = scale_pow2(wt / (float)F, (int)ref - g);
+      // q(x) = 2^a / total = wt * 2^ref / (F * 2^g)
+      const int fm = 63 - __clzll(F);
+      q_tok[out] = scale_pow2(wt / fix_to_float(F, -fm), (int)ref - g - fm);
       s.tok = isel;
     }
   }
