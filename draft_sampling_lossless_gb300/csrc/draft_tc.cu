@@ -85,14 +85,16 @@ size_t tc_smem_bytes(int nK) {
 
 // Bounded wait that also gives up at once when another role of the CTA has
 // already timed out, so a broken pipeline ends the kernel quickly.
+// After the first tries the thread sleeps in the wait (woken by the phase
+// completion), so waiting roles leave the issue slots to working warps.
 __device__ __forceinline__ bool wait_abortable(uint32_t bar, uint32_t parity,
                                                volatile int* abort_flag, uint32_t* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
 #pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait_sleep(bar, parity, 2000)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > 1000000000ull) {
       *abort_flag = 1;
