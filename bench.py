@@ -318,9 +318,14 @@ def recorded_traffic(kind, wl):
     e = want.get((kind, wl.name))
     if e is None:
         return None
-    src = os.path.join(ROOT, "draft_sampling_lossless_gb300", "csrc", e["file"])
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    if h != e.get("sha"):
+    # the kernel's sources ('+'-separated), hashed in order
+    hs = hashlib.sha256()
+    for name in e["file"].split("+"):
+        src = os.path.join(ROOT, "draft_sampling_lossless_gb300", "csrc", name)
+        if not os.path.exists(src):
+            return None
+        hs.update(open(src, "rb").read())
+    if hs.hexdigest()[:16] != e.get("sha"):
         return None
     return float(e["bytes_per_launch"])
 
