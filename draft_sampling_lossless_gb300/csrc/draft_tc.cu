@@ -165,6 +165,16 @@ __device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigne
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
+__device__ __forceinline__ unsigned long long sub2(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
 __device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
                                                    unsigned long long c) {
   unsigned long long r;
@@ -266,7 +276,6 @@ __device__ __forceinline__ void epi_block(const uint32_t (&b0)[32], const uint32
   }
   const float fref = static_cast<float>(s.ref);
   const unsigned long long c2 = pack2(p.sc.hi, p.sc.hi), r2 = pack2(-fref, -fref);
-  long long add = 0;
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
     unsigned long long t2[8];
@@ -282,11 +291,11 @@ __device__ __forceinline__ void epi_block(const uint32_t (&b0)[32], const uint32
       for (int e = 0; e < w; ++e) t2[e] = add2(t2[e], t2[e + w]);
     float t0, t1;
     unpack2(t2[0], t0, t1);
-    const float tg = t0 + t1;
-    gs[g] = tg;
-    add += __float2ll_rn(tg * 1099511627776.0f);  // 2^40
+    gs[g] = t0 + t1;
   }
-  s.acc += add;
+  // one conversion to 2^-40 units per 64 tokens (64-bit conversions issue on
+  // the narrow FP64 pipe)
+  s.acc += __float2ll_rn(((gs[0] + gs[1]) + (gs[2] + gs[3])) * 1099511627776.0f);
 }
 
 // Stores the four 16-token group sums gs of block jj (0, 1) of a 128-token
@@ -973,10 +982,19 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
 // 32 consecutive tokens of one request's final row: p = 2^(a_p) / Sp from the
 // target logits and, for a residual draw, q = 2^(a_q) / Sq from the draft
 // logits z + bias; adds the fixed-point sums of max(0, p - q) (p itself for a
-// bonus draw) and of p.
+// bonus draw) and of p.  a = y * c with c = log2(e)/T rounded to fp32 (the
+// rounding the row normaliser Sp and the draft normaliser Sq were formed
+// with), each exponent argument one FMA against a power-of-two reference
+// from the block's largest y; the normalisations 2^ref / S stay (hi, lo)
+// pairs, so p - q keeps its precision where p and q nearly cancel.  Element
+// pairs use the packed two-wide fp32 instructions.  The block sums are added
+// to the caller's fp32 running sums (converted to fixed point once per
+// 128-token partial: conversions to 64-bit integers issue on the narrow FP64
+// pipe).  A NaN input makes its block contribute nothing (the row pass
+// reports non-finite target rows).
 __device__ __forceinline__ void fin_block(const uint32_t (&b)[32], const uint4 (&zq)[4],
                                           const uint4 (&tq)[4], int lim, bool resid, ScalePair sc,
-                                          InvPair ip, InvPair iq, long long& fr, long long& fp) {
+                                          InvPair ip, InvPair iq, float& fr, float& fp) {
   float ap[32], aq[32];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -987,15 +1005,15 @@ __device__ __forceinline__ void fin_block(const uint32_t (&b)[32], const uint4 (
       const int i = q * 8 + 2 * e;
       ap[i] = bf_lo(wt[e]);
       ap[i + 1] = bf_hi(wt[e]);
-      aq[i] = bf_lo(wz[e]) + __uint_as_float(b[i]);
-      aq[i + 1] = bf_hi(wz[e]) + __uint_as_float(b[i + 1]);
+      unpack2(add2(pack2(bf_lo(wz[e]), bf_hi(wz[e])),
+                   pack2(__uint_as_float(b[i]), __uint_as_float(b[i + 1]))),
+              aq[i], aq[i + 1]);
     }
   }
+  if (lim < 32) {
 #pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    const bool in = e < lim;
-    ap[e] = in ? scaled_clamped(ap[e], sc) : -3.0e38f;
-    aq[e] = in && resid ? scaled_clamped(aq[e], sc) : -3.0e38f;
+    for (int e = 0; e < 32; ++e)
+      if (e >= lim) ap[e] = aq[e] = -INFINITY;
   }
   float mp[16], mq[16];
 #pragma unroll
@@ -1010,41 +1028,53 @@ __device__ __forceinline__ void fin_block(const uint32_t (&b)[32], const uint4 (
       mp[e] = fmaxf(mp[e], mp[e + w]);
       mq[e] = fmaxf(mq[e], mq[e + w]);
     }
-  if (mp[0] <= -1.0e38f) return;  // no target mass here: both sums stay 0
-  const int refp = static_cast<int>(ceilf(mp[0]));
-  const int refq = mq[0] > -1.0e38f ? static_cast<int>(ceilf(mq[0])) : 0;
+  const float cp = mp[0] * sc.hi, cq = resid ? mq[0] * sc.hi : -INFINITY;
+  if (!(cp > -1.0e38f && cp < 3.0e38f)) return;  // no target mass here (or +inf): sums stay 0
+  const bool qlive = cq > -1.0e38f && cq < 3.0e38f;
+  const int refp = static_cast<int>(ceilf(cp));
+  const int refq = qlive ? static_cast<int>(ceilf(cq)) : 0;
   const ScalePair kp{scale_pow2(ip.hi, refp + ip.e), scale_pow2(ip.lo, refp + ip.e)};
-  const ScalePair kq = mq[0] > -1.0e38f
-                           ? ScalePair{scale_pow2(iq.hi, refq + iq.e), scale_pow2(iq.lo, refq + iq.e)}
-                           : ScalePair{0.f, 0.f};
-  const float fp_ref = static_cast<float>(refp), fq_ref = static_cast<float>(refq);
-  constexpr float k2_60 = 1152921504606846976.0f;  // 2^60
+  const ScalePair kq =
+      qlive ? ScalePair{scale_pow2(iq.hi, refq + iq.e), scale_pow2(iq.lo, refq + iq.e)}
+            : ScalePair{0.f, 0.f};
+  const unsigned long long c2 = pack2(sc.hi, sc.hi);
+  const unsigned long long rp2 = pack2(-(float)refp, -(float)refp);
+  const unsigned long long rq2 = pack2(-(float)refq, -(float)refq);
+  const unsigned long long kph = pack2(kp.hi, kp.hi), kpl = pack2(kp.lo, kp.lo);
+  const unsigned long long kqh = pack2(kq.hi, kq.hi), kql = pack2(kq.lo, kq.lo);
+  unsigned long long sp2[16], sr2[16];
 #pragma unroll
-  for (int g = 0; g < 2; ++g) {
-    float sp[16], sr[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const float wp = ex2_fast(ap[g * 16 + e] - fp_ref);
-      const float pv = fmaf(wp, kp.hi, wp * kp.lo);
-      float rho = pv;
-      if (resid) {
-        const float wq = ex2_fast(aq[g * 16 + e] - fq_ref);
-        rho = fmaxf(0.0f, pv - fmaf(wq, kq.hi, wq * kq.lo));
-      }
-      sp[e] = pv;
-      sr[e] = rho;
+  for (int i = 0; i < 16; ++i) {
+    float a0, a1;
+    unpack2(fma2(pack2(ap[2 * i], ap[2 * i + 1]), c2, rp2), a0, a1);
+    const unsigned long long wp = pack2(ex2_fast(a0), ex2_fast(a1));
+    const unsigned long long pv = fma2(wp, kph, mul2(wp, kpl));
+    sp2[i] = pv;
+    if (resid && qlive) {
+      unpack2(fma2(pack2(aq[2 * i], aq[2 * i + 1]), c2, rq2), a0, a1);
+      const unsigned long long wq = pack2(ex2_fast(a0), ex2_fast(a1));
+      float r0, r1;
+      unpack2(sub2(pv, fma2(wq, kqh, mul2(wq, kql))), r0, r1);
+      sr2[i] = pack2(fmaxf(0.0f, r0), fmaxf(0.0f, r1));
+    } else {
+      sr2[i] = pv;
     }
-#pragma unroll
-    for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-      for (int e = 0; e < w; ++e) {
-        sp[e] += sp[e + w];
-        sr[e] += sr[e + w];
-      }
-    fp += __float2ll_rn(sp[0] * k2_60);
-    fr += __float2ll_rn(sr[0] * k2_60);
   }
+#pragma unroll
+  for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      sp2[i] = add2(sp2[i], sp2[i + w]);
+      sr2[i] = add2(sr2[i], sr2[i + w]);
+    }
+  float p0, p1, r0, r1;
+  unpack2(sp2[0], p0, p1);
+  unpack2(sr2[0], r0, r1);
+  const float spv = p0 + p1, srv = r0 + r1;
+  if (spv == spv) fp += spv;
+  if (srv == srv) fr += srv;
 }
+
 
 __global__ void __launch_bounds__(kThreads, 1)
     final_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const FinalParams p) {
@@ -1254,7 +1284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = live && t < p.n_vt;
       wait_abortable(b_accFull + 8 * a, aph, &s_abort, p.status);
       tc_fence_after();
-      long long fr = 0, fp = 0;
+      float fr = 0.f, fp = 0.f;
 #pragma unroll 1
       for (int jj = 0; jj < kFinSteps / 2; ++jj) {
         const int j = half * (kFinSteps / 2) + jj;
@@ -1288,8 +1318,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(b_accEmpty + 8 * a);
       if (n < p.R && t < p.n_vt && t * 2 + half < p.n_halves) {
         long long* o = p.fin_part + ((size_t)n * p.n_halves + t * 2 + half) * 2;
-        o[0] = fr;
-        o[1] = fp;
+        o[0] = __float2ll_rn(fr * 1152921504606846976.0f);  // 2^60
+        o[1] = __float2ll_rn(fp * 1152921504606846976.0f);
       }
     }
   }

@@ -869,24 +869,27 @@ __global__ void __launch_bounds__(256) final_pick_tc_kernel(
     tile_bias_recompute<128, BlockSync>(b, V, hsel * 128, s.erow, s.bias);
     bv = tid < 128 ? s.bias[tid] : 0.f;
   }
-  const float ap = ok ? scaled_clamped(tv, sc) : -3.0e38f;
-  const float aq = ok && resid ? scaled_clamped(zv + bv, sc) : -3.0e38f;
-  const float mp = g_max_f<BlockSync>(ap, s.shf);
-  const float mq = g_max_f<BlockSync>(aq, s.shf);
+  // the same arithmetic as the final pass's blocks: a = y * c (c rounded to
+  // fp32), one FMA per exponent argument, (hi, lo) normalisations
+  const float yp = ok ? tv : -INFINITY;
+  const float yq = ok && resid ? zv + bv : -INFINITY;
+  const float mp = g_max_f<BlockSync>(yp, s.shf) * sc.hi;
+  const float mq = g_max_f<BlockSync>(yq, s.shf) * sc.hi;
   long long f = 0;
-  if (ok && mp > -1.0e38f) {
+  if (ok && mp > -1.0e38f && mp < 3.0e38f) {
     const int refp = (int)ceilf(mp);
-    const float wp = ex2_fast(ap - (float)refp);
+    const float wp = ex2_fast(fmaf(yp, sc.hi, -(float)refp));
     const float pv = fmaf(wp, scale_pow2(st.ip.hi, refp + st.ip.e),
                           wp * scale_pow2(st.ip.lo, refp + st.ip.e));
     float rho = pv;
-    if (resid && mq > -1.0e38f) {
+    if (resid && mq > -1.0e38f && mq < 3.0e38f) {
       const int refq = (int)ceilf(mq);
-      const float wq = ex2_fast(aq - (float)refq);
+      const float wq = ex2_fast(fmaf(yq, sc.hi, -(float)refq));
       rho = fmaxf(0.0f, pv - fmaf(wq, scale_pow2(st.iq.hi, refq + st.iq.e),
                                   wq * scale_pow2(st.iq.lo, refq + st.iq.e)));
     }
-    f = __float2ll_rn((col == 0 ? rho : pv) * 1152921504606846976.0f);  // 2^60
+    const float val = col == 0 ? rho : pv;
+    if (val == val) f = __float2ll_rn(val * 1152921504606846976.0f);  // 2^60
   }
   long long mass;
   const long long cum = g_scan_ll<BlockSync>(f, s.shl, &mass);
