@@ -500,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_32x32b_x32(tmem + lane_base + a * BN + col + 32, b1);
         const int v0 = t * BN + col;
         if (kBiasOut) {
-          tmem_wait_ld();
+          tmem_wait_ld_regs(b0, b1);
           if (valid) {
             float* dst = p.bias_out + (size_t)n * p.V;
 #pragma unroll
@@ -526,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(b_emptyZ + 8 * (half * 4 + zs));
-        tmem_wait_ld();
+        tmem_wait_ld_regs(b0, b1);
         float gs[4] = {0.f, 0.f, 0.f, 0.f};
         if (valid) epi_block(b0, b1, z0, z1, v0, min(64, p.V - v0), p, s, gs);
         if (own && !p.greedy) store_groups(p.sub + o * 8, jj, gs, s.ref, ref0);
@@ -880,7 +880,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(b_emptyZ + 8 * (half * 4 + zs));
-          tmem_wait_ld();
+          tmem_wait_ld_regs(b0, b1);
           float gs[4] = {0.f, 0.f, 0.f, 0.f};
           if (valid) epi_block(b0, b1, z0, z1, v0, min(64, p.V - v0), p, s, gs);
           if (own && !p.greedy) store_groups(p.sub + o * 8, jj, gs, s.ref, ref0);
@@ -981,83 +981,58 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
 
 // 32 consecutive tokens of one request's final row: p = 2^(a_p) / Sp from the
 // target logits and, for a residual draw, q = 2^(a_q) / Sq from the draft
-// logits z + bias; adds the fixed-point sums of max(0, p - q) (p itself for a
-// bonus draw) and of p.  a = y * c with c = log2(e)/T rounded to fp32 (the
-// rounding the row normaliser Sp and the draft normaliser Sq were formed
-// with), each exponent argument one FMA against a power-of-two reference
-// from the block's largest y; the normalisations 2^ref / S stay (hi, lo)
-// pairs, so p - q keeps its precision where p and q nearly cancel.  Element
-// pairs use the packed two-wide fp32 instructions.  The block sums are added
-// to the caller's fp32 running sums (converted to fixed point once per
-// 128-token partial: conversions to 64-bit integers issue on the narrow FP64
-// pipe).  A NaN input makes its block contribute nothing (the row pass
+// logits z + bias; adds the sums of max(0, p - q) (p itself for a bonus
+// draw) and of p to the caller's fp32 running sums (converted to fixed point
+// once per 128-token partial).  a = y * c with c = log2(e)/T rounded to fp32
+// (the rounding Sp and Sq were formed with).  With 1/S = (hi + lo) * 2^e,
+// hi in [0.5, 1), every token has 2^a <= S < 2^(1 - e), so
+//   p = 2^(a + e) * (hi + lo),  a + e <= 1:
+// one FMA for the exponent argument, one ex2, and the (hi, lo) product --
+// no block maximum, reference or rescaling.  p - q keeps its precision where
+// p and q nearly cancel.  Element pairs use the packed two-wide fp32
+// instructions; a NaN input makes its block contribute nothing (the row pass
 // reports non-finite target rows).
 __device__ __forceinline__ void fin_block(const uint32_t (&b)[32], const uint4 (&zq)[4],
                                           const uint4 (&tq)[4], int lim, bool resid, ScalePair sc,
                                           InvPair ip, InvPair iq, float& fr, float& fp) {
-  float ap[32], aq[32];
+  if (ip.hi == 0.f) return;  // no target normaliser: no mass
+  const bool qlive = resid && iq.hi != 0.f;
+  const unsigned long long c2 = pack2(sc.hi, sc.hi);
+  const unsigned long long ep2 = pack2((float)ip.e, (float)ip.e);
+  const unsigned long long eq2 = pack2((float)iq.e, (float)iq.e);
+  const unsigned long long kph = pack2(ip.hi, ip.hi), kpl = pack2(ip.lo, ip.lo);
+  const unsigned long long kqh = pack2(iq.hi, iq.hi), kql = pack2(iq.lo, iq.lo);
+  unsigned long long sp2[16], sr2[16];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const uint32_t wt[4] = {tq[q].x, tq[q].y, tq[q].z, tq[q].w};
     const uint32_t wz[4] = {zq[q].x, zq[q].y, zq[q].z, zq[q].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int i = q * 8 + 2 * e;
-      ap[i] = bf_lo(wt[e]);
-      ap[i + 1] = bf_hi(wt[e]);
-      unpack2(add2(pack2(bf_lo(wz[e]), bf_hi(wz[e])),
-                   pack2(__uint_as_float(b[i]), __uint_as_float(b[i + 1]))),
-              aq[i], aq[i + 1]);
-    }
-  }
-  if (lim < 32) {
-#pragma unroll
-    for (int e = 0; e < 32; ++e)
-      if (e >= lim) ap[e] = aq[e] = -INFINITY;
-  }
-  float mp[16], mq[16];
-#pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    mp[e] = fmaxf(ap[e], ap[e + 16]);
-    mq[e] = fmaxf(aq[e], aq[e + 16]);
-  }
-#pragma unroll
-  for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-    for (int e = 0; e < w; ++e) {
-      mp[e] = fmaxf(mp[e], mp[e + w]);
-      mq[e] = fmaxf(mq[e], mq[e + w]);
-    }
-  const float cp = mp[0] * sc.hi, cq = resid ? mq[0] * sc.hi : -INFINITY;
-  if (!(cp > -1.0e38f && cp < 3.0e38f)) return;  // no target mass here (or +inf): sums stay 0
-  const bool qlive = cq > -1.0e38f && cq < 3.0e38f;
-  const int refp = static_cast<int>(ceilf(cp));
-  const int refq = qlive ? static_cast<int>(ceilf(cq)) : 0;
-  const ScalePair kp{scale_pow2(ip.hi, refp + ip.e), scale_pow2(ip.lo, refp + ip.e)};
-  const ScalePair kq =
-      qlive ? ScalePair{scale_pow2(iq.hi, refq + iq.e), scale_pow2(iq.lo, refq + iq.e)}
-            : ScalePair{0.f, 0.f};
-  const unsigned long long c2 = pack2(sc.hi, sc.hi);
-  const unsigned long long rp2 = pack2(-(float)refp, -(float)refp);
-  const unsigned long long rq2 = pack2(-(float)refq, -(float)refq);
-  const unsigned long long kph = pack2(kp.hi, kp.hi), kpl = pack2(kp.lo, kp.lo);
-  const unsigned long long kqh = pack2(kq.hi, kq.hi), kql = pack2(kq.lo, kq.lo);
-  unsigned long long sp2[16], sr2[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    float a0, a1;
-    unpack2(fma2(pack2(ap[2 * i], ap[2 * i + 1]), c2, rp2), a0, a1);
-    const unsigned long long wp = pack2(ex2_fast(a0), ex2_fast(a1));
-    const unsigned long long pv = fma2(wp, kph, mul2(wp, kpl));
-    sp2[i] = pv;
-    if (resid && qlive) {
-      unpack2(fma2(pack2(aq[2 * i], aq[2 * i + 1]), c2, rq2), a0, a1);
-      const unsigned long long wq = pack2(ex2_fast(a0), ex2_fast(a1));
-      float r0, r1;
-      unpack2(sub2(pv, fma2(wq, kqh, mul2(wq, kql))), r0, r1);
-      sr2[i] = pack2(fmaxf(0.0f, r0), fmaxf(0.0f, r1));
-    } else {
-      sr2[i] = pv;
+      const int i = q * 4 + e;  // pair index: tokens 2i, 2i + 1
+      float yp0 = bf_lo(wt[e]), yp1 = bf_hi(wt[e]);
+      if (2 * i >= lim) yp0 = -INFINITY;
+      if (2 * i + 1 >= lim) yp1 = -INFINITY;
+      float a0, a1;
+      unpack2(fma2(pack2(yp0, yp1), c2, ep2), a0, a1);
+      const unsigned long long wp = pack2(ex2_fast(a0), ex2_fast(a1));
+      const unsigned long long pv = fma2(wp, kph, mul2(wp, kpl));
+      sp2[i] = pv;
+      if (qlive) {
+        float yq0, yq1;
+        unpack2(add2(pack2(bf_lo(wz[e]), bf_hi(wz[e])),
+                     pack2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1]))),
+                yq0, yq1);
+        if (2 * i >= lim) yq0 = -INFINITY;
+        if (2 * i + 1 >= lim) yq1 = -INFINITY;
+        unpack2(fma2(pack2(yq0, yq1), c2, eq2), a0, a1);
+        const unsigned long long wq = pack2(ex2_fast(a0), ex2_fast(a1));
+        float r0, r1;
+        unpack2(sub2(pv, fma2(wq, kqh, mul2(wq, kql))), r0, r1);
+        sr2[i] = pack2(fmaxf(0.0f, r0), fmaxf(0.0f, r1));
+      } else {
+        sr2[i] = pv;
+      }
     }
   }
 #pragma unroll
@@ -1310,7 +1285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(b_emptyZ + 8 * (half * 4 + zs));
-        tmem_wait_ld();
+        tmem_wait_ld_regs(b);
         if (valid) fin_block(b, zq, tq, min(32, p.V - v0), resid, p.sc, st.ip, st.iq, fr, fp);
       }
       tc_fence_before();

@@ -224,6 +224,25 @@ __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// The wait, with the registers the loads wrote tied to it: each is an in-out
+// operand of an empty volatile statement issued after the wait, so no use of
+// them can be scheduled before the data has arrived.
+template <int N>
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&v)[N]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(v[i]));
+}
+template <int N>
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&v)[N], uint32_t (&w)[N]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    asm volatile("" : "+r"(v[i]));
+    asm volatile("" : "+r"(w[i]));
+  }
+}
+
 // Shared-memory matrix descriptor for a K-major operand stored in the
 // 128-byte swizzled layout (rows of 64 bf16 = 128 bytes, 8-row groups of
 // 1024 bytes, base 1024-byte aligned): start address, leading byte offset

@@ -870,23 +870,17 @@ __global__ void __launch_bounds__(256) final_pick_tc_kernel(
     bv = tid < 128 ? s.bias[tid] : 0.f;
   }
   // the same arithmetic as the final pass's blocks: a = y * c (c rounded to
-  // fp32), one FMA per exponent argument, (hi, lo) normalisations
+  // fp32), p = 2^(a + e) * (hi + lo) with 1/Sp = (hi + lo) * 2^e, q alike
   const float yp = ok ? tv : -INFINITY;
   const float yq = ok && resid ? zv + bv : -INFINITY;
-  const float mp = g_max_f<BlockSync>(yp, s.shf) * sc.hi;
-  const float mq = g_max_f<BlockSync>(yq, s.shf) * sc.hi;
   long long f = 0;
-  if (ok && mp > -1.0e38f && mp < 3.0e38f) {
-    const int refp = (int)ceilf(mp);
-    const float wp = ex2_fast(fmaf(yp, sc.hi, -(float)refp));
-    const float pv = fmaf(wp, scale_pow2(st.ip.hi, refp + st.ip.e),
-                          wp * scale_pow2(st.ip.lo, refp + st.ip.e));
+  if (ok && st.ip.hi != 0.f) {
+    const float wp = ex2_fast(fmaf(yp, sc.hi, (float)st.ip.e));
+    const float pv = fmaf(wp, st.ip.hi, wp * st.ip.lo);
     float rho = pv;
-    if (resid && mq > -1.0e38f && mq < 3.0e38f) {
-      const int refq = (int)ceilf(mq);
-      const float wq = ex2_fast(fmaf(yq, sc.hi, -(float)refq));
-      rho = fmaxf(0.0f, pv - fmaf(wq, scale_pow2(st.iq.hi, refq + st.iq.e),
-                                  wq * scale_pow2(st.iq.lo, refq + st.iq.e)));
+    if (resid && st.iq.hi != 0.f) {
+      const float wq = ex2_fast(fmaf(yq, sc.hi, (float)st.iq.e));
+      rho = fmaxf(0.0f, pv - fmaf(wq, st.iq.hi, wq * st.iq.lo));
     }
     const float val = col == 0 ? rho : pv;
     if (val == val) f = __float2ll_rn(val * 1152921504606846976.0f);  // 2^60
