@@ -997,57 +997,66 @@ __device__ __forceinline__ void fin_block(const uint32_t (&b)[32], const uint4 (
                                           InvPair ip, InvPair iq, float& fr, float& fp) {
   if (ip.hi == 0.f) return;  // no target normaliser: no mass
   const bool qlive = resid && iq.hi != 0.f;
-  const unsigned long long c2 = pack2(sc.hi, sc.hi);
-  const unsigned long long ep2 = pack2((float)ip.e, (float)ip.e);
-  const unsigned long long eq2 = pack2((float)iq.e, (float)iq.e);
-  const unsigned long long kph = pack2(ip.hi, ip.hi), kpl = pack2(ip.lo, ip.lo);
-  const unsigned long long kqh = pack2(iq.hi, iq.hi), kql = pack2(iq.lo, iq.lo);
-  unsigned long long sp2[16], sr2[16];
+  // stage-major: each step over all 32 tokens before the next, so that the
+  // independent operations of one step issue back to back
+  float x[32];  // exponent arguments of p, then weights, then p
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const uint32_t wt[4] = {tq[q].x, tq[q].y, tq[q].z, tq[q].w};
-    const uint32_t wz[4] = {zq[q].x, zq[q].y, zq[q].z, zq[q].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int i = q * 4 + e;  // pair index: tokens 2i, 2i + 1
-      float yp0 = bf_lo(wt[e]), yp1 = bf_hi(wt[e]);
-      if (2 * i >= lim) yp0 = -INFINITY;
-      if (2 * i + 1 >= lim) yp1 = -INFINITY;
-      float a0, a1;
-      unpack2(fma2(pack2(yp0, yp1), c2, ep2), a0, a1);
-      const unsigned long long wp = pack2(ex2_fast(a0), ex2_fast(a1));
-      const unsigned long long pv = fma2(wp, kph, mul2(wp, kpl));
-      sp2[i] = pv;
-      if (qlive) {
-        float yq0, yq1;
-        unpack2(add2(pack2(bf_lo(wz[e]), bf_hi(wz[e])),
-                     pack2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1]))),
-                yq0, yq1);
-        if (2 * i >= lim) yq0 = -INFINITY;
-        if (2 * i + 1 >= lim) yq1 = -INFINITY;
-        unpack2(fma2(pack2(yq0, yq1), c2, eq2), a0, a1);
-        const unsigned long long wq = pack2(ex2_fast(a0), ex2_fast(a1));
-        float r0, r1;
-        unpack2(sub2(pv, fma2(wq, kqh, mul2(wq, kql))), r0, r1);
-        sr2[i] = pack2(fmaxf(0.0f, r0), fmaxf(0.0f, r1));
-      } else {
-        sr2[i] = pv;
-      }
+      x[q * 8 + 2 * e] = bf_lo(wt[e]);
+      x[q * 8 + 2 * e + 1] = bf_hi(wt[e]);
     }
   }
+  if (lim < 32) {
 #pragma unroll
-  for (int w = 8; w > 0; w >>= 1)
+    for (int i = 0; i < 32; ++i)
+      if (i >= lim) x[i] = -INFINITY;
+  }
+  const float ep = (float)ip.e;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) x[i] = fmaf(x[i], sc.hi, ep);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) x[i] = ex2_fast(x[i]);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) x[i] = fmaf(x[i], ip.hi, x[i] * ip.lo);  // p
+  float r[32];
+  if (qlive) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t wz[4] = {zq[q].x, zq[q].y, zq[q].z, zq[q].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        r[q * 8 + 2 * e] = bf_lo(wz[e]) + __uint_as_float(b[q * 8 + 2 * e]);
+        r[q * 8 + 2 * e + 1] = bf_hi(wz[e]) + __uint_as_float(b[q * 8 + 2 * e + 1]);
+      }
+    }
+    if (lim < 32) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i >= lim) r[i] = -INFINITY;
+    }
+    const float eq = (float)iq.e;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = fmaf(r[i], sc.hi, eq);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = ex2_fast(r[i]);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = fmaxf(0.0f, x[i] - fmaf(r[i], iq.hi, r[i] * iq.lo));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = x[i];
+  }
+#pragma unroll
+  for (int w = 16; w > 0; w >>= 1)
 #pragma unroll
     for (int i = 0; i < w; ++i) {
-      sp2[i] = add2(sp2[i], sp2[i + w]);
-      sr2[i] = add2(sr2[i], sr2[i + w]);
+      x[i] += x[i + w];
+      r[i] += r[i + w];
     }
-  float p0, p1, r0, r1;
-  unpack2(sp2[0], p0, p1);
-  unpack2(sr2[0], r0, r1);
-  const float spv = p0 + p1, srv = r0 + r1;
-  if (spv == spv) fp += spv;
-  if (srv == srv) fr += srv;
+  if (x[0] == x[0]) fp += x[0];
+  if (r[0] == r[0]) fr += r[0];
 }
 
 
