@@ -276,21 +276,24 @@ __device__ __forceinline__ void epi_block(const uint32_t (&b0)[32], const uint32
   }
   const float fref = static_cast<float>(s.ref);
   const unsigned long long c2 = pack2(p.sc.hi, p.sc.hi), r2 = pack2(-fref, -fref);
+  // stage-major: all 64 exponent arguments, then all 64 ex2, then the four
+  // 16-token trees, so that independent operations issue back to back
+#pragma unroll
+  for (int e = 0; e < 32; ++e) unpack2(fma2(y2[e], c2, r2), y[2 * e], y[2 * e + 1]);  // a - ref
+#pragma unroll
+  for (int e = 0; e < 64; ++e) y[e] = ex2_approx(y[e]);
+#pragma unroll
+  for (int e = 0; e < 32; ++e) y2[e] = pack2(y[2 * e], y[2 * e + 1]);
+#pragma unroll
+  for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+#pragma unroll
+      for (int e = 0; e < w; ++e) y2[g * 8 + e] = add2(y2[g * 8 + e], y2[g * 8 + e + w]);
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
-    unsigned long long t2[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      float a0, a1;
-      unpack2(fma2(y2[g * 8 + e], c2, r2), a0, a1);  // a - ref
-      t2[e] = pack2(ex2_approx(a0), ex2_approx(a1));
-    }
-#pragma unroll
-    for (int w = 4; w > 0; w >>= 1)
-#pragma unroll
-      for (int e = 0; e < w; ++e) t2[e] = add2(t2[e], t2[e + w]);
     float t0, t1;
-    unpack2(t2[0], t0, t1);
+    unpack2(y2[g * 8], t0, t1);
     gs[g] = t0 + t1;
   }
   // one conversion to 2^-40 units per 64 tokens (64-bit conversions issue on
