@@ -33,6 +33,14 @@ SMALL = {
     # more than 64 requests on one 128-row tile (the unpaired tensor-core layout)
     "rows_100": W["qwen3_4b"].scaled(name="rows_100", R=100, gamma=3, V=4000, r=128, d=32,
                                      n_sps=0),
+    # bf16 with a rank above the tensor-core path's 256: the CUDA-core draft
+    # and final draw
+    "big_rank_bf16": W["qwen3_4b"].scaled(name="big_rank_bf16", R=5, gamma=3, V=2000, r=320,
+                                          d=24, n_sps=0),
+    # more requests than the row pass lists in shared memory (plain-load row
+    # pass over every (request, position)), several 128-row tiles in the draft
+    "many_requests": W["qwen3_4b"].scaled(name="many_requests", R=1100, gamma=2, V=512, r=16,
+                                          d=8, n_sps=0),
 }
 
 pytestmark = pytest.mark.gpu
@@ -60,6 +68,30 @@ def test_all_stages_match_oracle(name):
 @pytest.mark.parametrize("seed", [11, 12, 13])
 def test_mid_bf16_more_seeds(seed):
     st = _full("mid_bf16", seed=seed)
+    assert st.unexplained == [], st.unexplained
+
+
+def test_extreme_uniforms():
+    """u = 0 and u = 1 - 2^-24 for the draft draws and the final draws: the
+    ends of the inverse-CDF searches (first partial, tile, group and token
+    with mass; the last ones).  Mismatches there can only be near-ties, since
+    both ends sit where the tiniest probabilities decide; each must be one."""
+    c = Case(SMALL["mid_bf16"], seed=7)
+    R, G = c.wl.R, c.wl.gamma
+    top = np.float32(1.0 - 2.0 ** -24)
+    ud = np.zeros((R, G), dtype=np.float32)
+    ud[::2] = top
+    ud[:, 1::2] = top - ud[:, 1::2]  # alternate the ends along each row too
+    uf = np.where(np.arange(R) % 2 == 0, top, np.float32(0.0)).astype(np.float32)
+    c.u_draft = ud.astype(np.float64)
+    c.g["u_draft"] = torch.from_numpy(ud).cuda()
+    c.u_fin = uf.astype(np.float64)
+    c.g["u_fin"] = torch.from_numpy(uf).cuda()
+    st = Stats()
+    c.draft(st)
+    c.confidence(st)
+    o = c.schedule(st, c.a_o.astype(np.float32), early_stop=True)
+    c.verify(st, o["ell"])
     assert st.unexplained == [], st.unexplained
 
 
