@@ -599,25 +599,28 @@ size_t persist_smem_bytes(int nK, int pair) {
 }
 
 // Grid-wide barrier among the 256 epilogue threads of every CTA (bounded:
-// gives up after about two seconds, setting the timeout flag).
+// gives up after about two seconds, setting the timeout flag).  The CTA
+// barrier orders every thread's writes before thread 0's release-add, and
+// thread 0's acquire-load of the full count orders the other CTAs' writes
+// before everything after the second CTA barrier, so no full fence is needed.
 __device__ __forceinline__ void grid_sync(unsigned* ctr, unsigned target, volatile int* abort_flag,
                                           uint32_t* status) {
   NamedSync<2, 256>::sync();
   if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(ctr, 1u);
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
     if (!*abort_flag) {
       const uint64_t t0 = globaltimer_ns();
-      while (*reinterpret_cast<volatile unsigned*>(ctr) < target) {
-        if (globaltimer_ns() - t0 > 2000000000ull) {
+      for (int spin = 1;; ++spin) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if (v >= target) break;
+        if ((spin & 63) == 0 && globaltimer_ns() - t0 > 2000000000ull) {
           *abort_flag = 1;
           set_flag(status, kFlagTimeout);
           break;
         }
-        __nanosleep(64);
       }
     }
-    __threadfence();
   }
   NamedSync<2, 256>::sync();
 }
