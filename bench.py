@@ -172,9 +172,9 @@ def run_ours(args, wl, world, rank, local):
     step = DSparkStep(wl.R, wl.gamma, wl.V, wl.r, wl.n_sps_eff, device=dev)
 
     def front():
-        step.draft(g["z"], g["E"], g["Wt"], g["anchor"], g["ud"], wl.T)
-        step.confidence(g["h"], g["w"], g["E"], g["anchor"], g["sts"], c_in=g["c_in"])
-        step.schedule(g["sps"], True, 0)
+        # draft + confidence head + scheduler: one call (one launch here)
+        step.draft_schedule(g["z"], g["E"], g["Wt"], g["anchor"], g["ud"], wl.T, g["h"], g["w"],
+                            g["E"], g["sts"], g["sps"], c_in=g["c_in"])
 
     # pass 0: the scheduled batch and the target logits the target model would
     # produce for it (a harness input, packed in the scheduler's row order)
@@ -332,8 +332,9 @@ def recorded_traffic(kind, wl):
 
 def run_e2e(args, wl, inp, g, step, target, dev, Bd):
     """Per step: pinned host -> device copies of the step's inputs (base
-    logits, hidden states, anchors, uniforms, target logits), the four calls,
-    and device -> host copies of the result (emitted tokens, n_acc, B)."""
+    logits, hidden states, anchors, uniforms, target logits), the library
+    calls (draft + confidence + schedule in one, then verify), and device ->
+    host copies of the result (emitted tokens, n_acc, B)."""
     pin = lambda t: (t.cpu().pin_memory() if t is not None else None)
     host = dict(z=pin(inp.z), h=pin(inp.h), anchor=pin(inp.anchor), ud=pin(inp.u_draft),
                 ua=pin(inp.u_acc), uf=pin(inp.u_fin), c_in=pin(inp.c_in), target=pin(target))
@@ -348,9 +349,8 @@ def run_e2e(args, wl, inp, g, step, target, dev, Bd):
         for k, v in host.items():
             if v is not None:
                 dbuf[k].copy_(v, non_blocking=True)
-        step.draft(dbuf["z"], g["E"], g["Wt"], dbuf["anchor"], dbuf["ud"], wl.T)
-        step.confidence(dbuf["h"], g["w"], g["E"], dbuf["anchor"], g["sts"], c_in=dbuf["c_in"])
-        step.schedule(g["sps"], True, 0)
+        step.draft_schedule(dbuf["z"], g["E"], g["Wt"], dbuf["anchor"], dbuf["ud"], wl.T,
+                            dbuf["h"], g["w"], g["E"], g["sts"], g["sps"], c_in=dbuf["c_in"])
         step.verify(dbuf["z"], g["E"], g["Wt"], dbuf["anchor"], dbuf["target"], dbuf["ua"],
                     dbuf["uf"], wl.T)
         out_h["out"].copy_(step.out_tokens, non_blocking=True)

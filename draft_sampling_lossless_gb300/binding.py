@@ -37,6 +37,7 @@ SYMBOLS = (
     "dspark_trace_kinds",
     "dspark_trace_get",
     "dspark_schedule_noalloc",
+    "dspark_draft_schedule",
 )
 
 
@@ -82,6 +83,11 @@ def lib() -> ctypes.CDLL:
         L.dspark_schedule_noalloc.restype = c_int
         L.dspark_schedule_noalloc.argtypes = [c_int, c_int, vp, vp, c_int, c_int, c_int, vp, vp,
                                               vp, vp, vp, vp]
+        L.dspark_draft_schedule.restype = c_int
+        L.dspark_draft_schedule.argtypes = [c_int, c_int, c_int, c_int, c_float, vp, vp, vp, c_int,
+                                            vp, vp, c_int, vp, vp, vp, vp, vp, vp, c_int, c_int,
+                                            c_int, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, c_size,
+                                            vp]
         L.dspark_launch_count.restype = ctypes.c_longlong
         L.dspark_launch_count.argtypes = []
         for f in ("dspark_trace_start", "dspark_trace_stop", "dspark_trace_collect",
@@ -207,6 +213,19 @@ def dspark_schedule(a, sps, early_stop, max_B, ell, row_off, B_out, E_out, ws, s
     _check("dspark_schedule", lib().dspark_schedule(
         R, G, _p(a), _p(sps), sps.numel(), int(early_stop), int(max_B), _p(ell), _p(row_off),
         _p(B_out), _p(E_out), _p(ws), ws.numel(), _stream(stream)))
+
+
+def dspark_draft_schedule(z, E, Wt, anchor, u_draft, temperature, hidden, w, E1, sts_t, c_in,
+                          sps, early_stop, max_B, tokens, q_lse, q_tok, c_out, a_out, ell,
+                          row_off, B_out, E_out, ws, stream=None):
+    R, G, V = z.shape
+    r = E.shape[1]
+    d = hidden.shape[2] if hidden is not None else 0
+    _check("dspark_draft_schedule", lib().dspark_draft_schedule(
+        R, G, V, r, float(temperature), _p(z), _p(E), _p(Wt), _dt(z), _p(anchor), _p(u_draft),
+        d, _p(hidden), _p(w), _p(E1), _p(sts_t), _p(c_in), _p(sps), sps.numel(),
+        int(early_stop), int(max_B), _p(tokens), _p(q_lse), _p(q_tok), _p(c_out), _p(a_out),
+        _p(ell), _p(row_off), _p(B_out), _p(E_out), _p(ws), ws.numel(), _stream(stream)))
 
 
 def dspark_verify(z, E, Wt, anchor, tokens, q_lse, q_tok, ell, row_off, target, u_acc, u_fin,

@@ -30,7 +30,7 @@ int cuda_fail(cudaError_t e, const char* where) {
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-  size_t status, bias, part, sub, row_part, vstate, fin_part, prev, stage, rank, sfix, total;
+  size_t status, bias, part, sub, row_part, vstate, fin_part, prev, stage, rank, sfix, hpart, total;
 };
 
 bool sizes_ok(int R, int gamma, int V, int r) {
@@ -66,6 +66,9 @@ Layout layout(int R, int gamma, int V, int r) {
   off += align_up(N * sizeof(int32_t));
   L.sfix = off;
   off += align_up(N * sizeof(long long));
+  L.hpart = off;  // lane partials of the confidence head when the draft runs it
+  off += align_up((N < (size_t)kFuseMaxCandidates ? N : (size_t)kFuseMaxCandidates) * 32 *
+                  sizeof(float));
   L.total = off;
   return L;
 }
@@ -136,10 +139,15 @@ int dspark_device_status(void* ws, int clear, uint32_t* flags, void* stream) {
   return DSPARK_OK;
 }
 
-int dspark_draft_sample(int R, int gamma, int V, int r, float temperature, const void* z,
-                        const void* E, const void* Wt, int dt, const int32_t* anchor,
-                        const float* u_draft, int32_t* tokens, double* q_lse, float* q_tok,
-                        void* ws, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Validates dspark_draft_sample's arguments and fills its launch arguments.
+int draft_args(int R, int gamma, int V, int r, float temperature, const void* z, const void* E,
+               const void* Wt, int dt, const int32_t* anchor, const float* u_draft,
+               int32_t* tokens, double* q_lse, float* q_tok, void* ws, size_t ws_bytes,
+               DraftArgs& a) {
   int s = check_common(R, gamma, V, r, dt);
   if (s) return s;
   if (!isfinite(temperature) || temperature < 0.0f)
@@ -154,7 +162,6 @@ int dspark_draft_sample(int R, int gamma, int V, int r, float temperature, const
   if (temperature > 0.0f) REQUIRE(u_draft);
   const Layout L = layout(R, gamma, V, r);
   if ((s = check_ws(ws, ws_bytes, L))) return s;
-  DraftArgs a;
   a.R = R;
   a.gamma = gamma;
   a.V = V;
@@ -175,15 +182,14 @@ int dspark_draft_sample(int R, int gamma, int V, int r, float temperature, const
   a.sub = at<float>(ws, L.sub);
   a.grid_counter = at<unsigned>(ws, L.status + 64);
   a.stage = at<void>(ws, L.stage);
-  cudaError_t e = launch_draft(a, (cudaStream_t)stream);
-  if (e != cudaSuccess) return cuda_fail(e, "dspark_draft_sample");
   return DSPARK_OK;
 }
 
-int dspark_confidence(int R, int gamma, int d, int r, int V, const void* hidden, const float* w,
-                      const void* E1, int dt, const int32_t* anchor, const int32_t* tokens,
-                      const float* sts_t, const float* c_in, float* c_out, float* a_out,
-                      void* ws, size_t ws_bytes, void* stream) {
+// Validates dspark_confidence's arguments and fills its launch arguments.
+int conf_args(int R, int gamma, int d, int r, int V, const void* hidden, const float* w,
+              const void* E1, int dt, const int32_t* anchor, const int32_t* tokens,
+              const float* sts_t, const float* c_in, float* c_out, float* a_out, void* ws,
+              size_t ws_bytes, ConfArgs& a) {
   if (R < 1 || gamma < 1 || gamma > kMaxGamma || (long long)R * gamma > (1 << 20))
     return fail(DSPARK_ERR_INVALID_ARG, "sizes out of range (R=%d gamma=%d)", R, gamma);
   REQUIRE(c_out);
@@ -201,7 +207,6 @@ int dspark_confidence(int R, int gamma, int d, int r, int V, const void* hidden,
   }
   if (ws == nullptr) return fail(DSPARK_ERR_INVALID_ARG, "workspace is NULL");
   if (ws_bytes < 256) return fail(DSPARK_ERR_WORKSPACE, "workspace has %zu bytes, needs 256", ws_bytes);
-  ConfArgs a;
   a.R = R;
   a.gamma = gamma;
   a.d = d;
@@ -218,14 +223,13 @@ int dspark_confidence(int R, int gamma, int d, int r, int V, const void* hidden,
   a.c_out = c_out;
   a.a_out = a_out;
   a.status = at<uint32_t>(ws, 0);
-  cudaError_t e = launch_confidence(a, (cudaStream_t)stream);
-  if (e != cudaSuccess) return cuda_fail(e, "dspark_confidence");
   return DSPARK_OK;
 }
 
-int dspark_schedule(int R, int gamma, const float* a, const float* sps, int n_sps, int early_stop,
-                    int max_B, int32_t* ell, int32_t* row_off, int32_t* B_out, double* E_out,
-                    void* ws, size_t ws_bytes, void* stream) {
+// Validates dspark_schedule's arguments and fills its launch arguments.
+int sched_args(int R, int gamma, const float* a, const float* sps, int n_sps, int early_stop,
+               int max_B, int32_t* ell, int32_t* row_off, int32_t* B_out, double* E_out,
+               void* ws, size_t ws_bytes, SchedArgs& s) {
   if (R < 1 || gamma < 1 || gamma > kMaxGamma || (long long)R * gamma > (1 << 20))
     return fail(DSPARK_ERR_INVALID_ARG, "sizes out of range (R=%d gamma=%d)", R, gamma);
   REQUIRE(a);
@@ -243,7 +247,6 @@ int dspark_schedule(int R, int gamma, const float* a, const float* sps, int n_sp
                 n_sps, R + imax);
   if (ws == nullptr) return fail(DSPARK_ERR_INVALID_ARG, "workspace is NULL");
   if (((uintptr_t)ws & 255) != 0) return fail(DSPARK_ERR_INVALID_ARG, "workspace not 256-byte aligned");
-  SchedArgs s;
   s.R = R;
   s.gamma = gamma;
   s.n_sps = n_sps;
@@ -264,8 +267,103 @@ int dspark_schedule(int R, int gamma, const float* a, const float* sps, int n_sp
   s.sfix = at<long long>(ws, off);
   off += align_up((size_t)N * sizeof(long long));
   if (ws_bytes < off) return fail(DSPARK_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, off);
+  s.imax = imax;
+  return DSPARK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dspark_draft_sample(int R, int gamma, int V, int r, float temperature, const void* z,
+                        const void* E, const void* Wt, int dt, const int32_t* anchor,
+                        const float* u_draft, int32_t* tokens, double* q_lse, float* q_tok,
+                        void* ws, size_t ws_bytes, void* stream) {
+  DraftArgs a;
+  int s = draft_args(R, gamma, V, r, temperature, z, E, Wt, dt, anchor, u_draft, tokens, q_lse,
+                     q_tok, ws, ws_bytes, a);
+  if (s) return s;
+  cudaError_t e = launch_draft(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dspark_draft_sample");
+  return DSPARK_OK;
+}
+
+int dspark_confidence(int R, int gamma, int d, int r, int V, const void* hidden, const float* w,
+                      const void* E1, int dt, const int32_t* anchor, const int32_t* tokens,
+                      const float* sts_t, const float* c_in, float* c_out, float* a_out,
+                      void* ws, size_t ws_bytes, void* stream) {
+  ConfArgs a;
+  int s = conf_args(R, gamma, d, r, V, hidden, w, E1, dt, anchor, tokens, sts_t, c_in, c_out,
+                    a_out, ws, ws_bytes, a);
+  if (s) return s;
+  cudaError_t e = launch_confidence(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dspark_confidence");
+  return DSPARK_OK;
+}
+
+int dspark_schedule(int R, int gamma, const float* a, const float* sps, int n_sps, int early_stop,
+                    int max_B, int32_t* ell, int32_t* row_off, int32_t* B_out, double* E_out,
+                    void* ws, size_t ws_bytes, void* stream) {
+  SchedArgs s;
+  int st = sched_args(R, gamma, a, sps, n_sps, early_stop, max_B, ell, row_off, B_out, E_out, ws,
+                      ws_bytes, s);
+  if (st) return st;
   cudaError_t e = launch_schedule(s, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "dspark_schedule");
+  return DSPARK_OK;
+}
+
+int dspark_draft_schedule(int R, int gamma, int V, int r, float temperature, const void* z,
+                          const void* E, const void* Wt, int dt, const int32_t* anchor,
+                          const float* u_draft, int d, const void* hidden, const float* w,
+                          const void* E1, const float* sts_t, const float* c_in,
+                          const float* sps, int n_sps, int early_stop, int max_B,
+                          int32_t* tokens, double* q_lse, float* q_tok, float* c_out,
+                          float* a_out, int32_t* ell, int32_t* row_off, int32_t* B_out,
+                          double* E_out, void* ws, size_t ws_bytes, void* stream) {
+  DraftArgs da;
+  ConfArgs ca;
+  SchedArgs sa;
+  int s = draft_args(R, gamma, V, r, temperature, z, E, Wt, dt, anchor, u_draft, tokens, q_lse,
+                     q_tok, ws, ws_bytes, da);
+  if (s) return s;
+  if ((s = conf_args(R, gamma, d, r, V, hidden, w, E1, dt, anchor, tokens, sts_t, c_in, c_out,
+                     a_out, ws, ws_bytes, ca)))
+    return s;
+  if ((s = sched_args(R, gamma, a_out, sps, n_sps, early_stop, max_B, ell, row_off, B_out, E_out,
+                      ws, ws_bytes, sa)))
+    return s;
+  const Layout L = layout(R, gamma, V, r);
+  DraftFuse f;
+  f.d = d;
+  f.h = hidden;
+  f.w = w;
+  f.E1 = E1;
+  f.sts = sts_t;
+  f.c_in = c_in;
+  f.c_out = c_out;
+  f.a_out = a_out;
+  f.hpart = at<float>(ws, L.hpart);
+  f.early_stop = early_stop;
+  f.imax = sa.imax < 0 ? 0 : sa.imax;
+  f.sps = sps;
+  f.rank = at<int32_t>(ws, L.rank);
+  f.ell = ell;
+  f.row_off = row_off;
+  f.B_out = B_out;
+  f.E_out = E_out;
+  int fused = 0;
+  da.fuse = &f;
+  da.fused = &fused;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = launch_draft(da, st);
+  if (e != cudaSuccess) return cuda_fail(e, "dspark_draft_schedule (draft)");
+  if (!fused) {
+    e = launch_confidence(ca, st);
+    if (e != cudaSuccess) return cuda_fail(e, "dspark_draft_schedule (confidence)");
+    e = launch_schedule(sa, st);
+    if (e != cudaSuccess) return cuda_fail(e, "dspark_draft_schedule (schedule)");
+  }
   return DSPARK_OK;
 }
 

@@ -246,6 +246,31 @@ void trace_end(int kind, cudaStream_t st);
 // ---------------------------------------------------------------- launchers
 // (defined in the kernel translation units; all enqueue on `st`)
 
+// The confidence head and the prefix scheduler, evaluated by the persistent
+// draft kernel after its last position when the caller asks for the three
+// stages in one call (dspark_draft_schedule) and the shapes allow it (see
+// draft_fuse_supported).  Same arithmetic as the confidence and scheduler
+// kernels, so the results are bit-identical to the separate calls.
+struct DraftFuse {
+  int d;
+  const void* h;      // [R][gamma][d] bf16, NULL when c_in is given
+  const float* w;     // [d + r]
+  const void* E1;     // [V][r] bf16
+  const float* sts;   // [gamma]
+  const float* c_in;  // [R][gamma] or NULL
+  float* c_out;       // [R][gamma]
+  float* a_out;       // [R][gamma]
+  float* hpart;       // [R * gamma][32] scratch: lane partials of w_h . h
+  int early_stop, imax;
+  const float* sps;
+  int32_t* rank;      // [R * gamma] scratch
+  int32_t* ell;
+  int32_t* row_off;
+  int32_t* B_out;
+  double* E_out;
+};
+constexpr int kFuseMaxCandidates = 8192;
+
 struct DraftArgs {
   int R, gamma, V, r, dt;
   float T;
@@ -263,8 +288,13 @@ struct DraftArgs {
   float* sub;       // [R][n_tiles][8] 16-token group sums of 128-token partials
   unsigned* grid_counter;  // grid-barrier counter of the persistent draft kernel
   void* stage;             // [R][r] bf16: E rows of the latest drafted tokens
+  const DraftFuse* fuse = nullptr;  // confidence + scheduler in the same launch, if possible
+  int* fused = nullptr;             // out: 1 when the launch included them
 };
 cudaError_t launch_draft(const DraftArgs& a, cudaStream_t st);
+// Whether the persistent draft can also evaluate the confidence head and the
+// scheduler for these arguments (host-side shape and alignment checks).
+bool draft_fuse_supported(const DraftArgs& a, const DraftFuse& f);
 cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st);
 
 // Tensor-core path of the draft (bf16, r % 8 == 0, r <= 256, 16-byte aligned
@@ -295,6 +325,7 @@ cudaError_t launch_confidence(const ConfArgs& a, cudaStream_t st);
 
 struct SchedArgs {
   int R, gamma, n_sps, early_stop, max_B;
+  int imax;  // last admissible candidate count (R * gamma, or max_B - R)
   const float* a;
   const float* sps;
   int32_t* ell;

@@ -11,10 +11,13 @@
 // applies sigma(s / t_k); thread 0 then forms the running product along the
 // block.  HBM-bound: R * gamma * (d + r) elements.
 #include "common.cuh"
+#include "confidence.cuh"
 
 namespace dspark {
 
 namespace {
+
+using namespace conf;
 
 // sum_i w[i] * x[i] over n elements, the warp's lanes taking eight at a time
 // (x 16-byte aligned and n a multiple of 8 for the vector path).  The vector
@@ -69,28 +72,6 @@ __device__ __forceinline__ float warp_dot(const float* __restrict__ w, const T* 
   return s;
 }
 
-// One warp per (request, position): c = sigmoid((w_h . h + w_e . E1[prev]) / sts).
-// bf16 with vector loads (the common case): the lane's whole share of h
-// (up to kHLoads 16-byte loads) and the previous token are requested
-// together, then the E1 row once the token is known, so a dot product costs
-// about two memory round trips; w (shared by every warp) is read through L1.
-constexpr int kHLoads = 16;  // d <= 32 * 8 * kHLoads = 4096 on the one-pass path
-
-__device__ __forceinline__ float dot8_bf16(const uint4 q, const float* __restrict__ w) {
-  const float4 w0 = __ldg(reinterpret_cast<const float4*>(w));
-  const float4 w1 = __ldg(reinterpret_cast<const float4*>(w + 4));
-  float s = 0.f;
-  s = fmaf(w0.x, __uint_as_float(q.x << 16), s);
-  s = fmaf(w0.y, __uint_as_float(q.x & 0xffff0000u), s);
-  s = fmaf(w0.z, __uint_as_float(q.y << 16), s);
-  s = fmaf(w0.w, __uint_as_float(q.y & 0xffff0000u), s);
-  s = fmaf(w1.x, __uint_as_float(q.z << 16), s);
-  s = fmaf(w1.y, __uint_as_float(q.z & 0xffff0000u), s);
-  s = fmaf(w1.z, __uint_as_float(q.w << 16), s);
-  s = fmaf(w1.w, __uint_as_float(q.w & 0xffff0000u), s);
-  return s;
-}
-
 template <typename T>
 __global__ void confidence_kernel(int gamma, int d, int r, int V, int vec,
                                   const T* __restrict__ h, const float* __restrict__ w,
@@ -107,12 +88,7 @@ __global__ void confidence_kernel(int gamma, int d, int r, int V, int vec,
   uint4 hq[kHLoads];
   if (one_pass && k < gamma && c_in == nullptr) {
     // h does not depend on the draft: request it before waiting for the tokens
-    const __nv_bfloat16* hp = reinterpret_cast<const __nv_bfloat16*>(h) + idx * d;
-#pragma unroll
-    for (int i = 0; i < kHLoads; ++i) {
-      const int j = (i * 32 + lane) * 8;
-      hq[i] = j < d ? __ldcs(reinterpret_cast<const uint4*>(hp + j)) : make_uint4(0, 0, 0, 0);
-    }
+    conf_load_h(reinterpret_cast<const __nv_bfloat16*>(h) + idx * d, d, hq);
   }
   grid_dependency_wait();  // the drafted tokens
   if (k < gamma) {
@@ -125,25 +101,15 @@ __global__ void confidence_kernel(int gamma, int d, int r, int V, int vec,
         if (lane == 0) set_flag(status, kFlagTokenRange);
         prev = -1;
       }
-      float s = 0.f;
       if (one_pass) {
-        uint4 eq = make_uint4(0, 0, 0, 0);
-        const int je = lane * 8;
-        if (prev >= 0 && je < r)
-          eq = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(E1) +
-                                               (size_t)prev * r + je);
-#pragma unroll
-        for (int i = 0; i < kHLoads; ++i) {
-          const int j = (i * 32 + lane) * 8;
-          if (j < d) s += dot8_bf16(hq[i], w + j);
-        }
-        if (prev >= 0 && je < r) s += dot8_bf16(eq, w + d + je);
+        const uint4 eq = conf_load_e1(reinterpret_cast<const __nv_bfloat16*>(E1), prev, r);
+        c = conf_sigma(conf_h_lane(hq, w, d), eq, prev, r, w + d, sts[k]);
       } else {
-        s = warp_dot<T>(w, h + idx * d, d, vec);
+        float s = warp_dot<T>(w, h + idx * d, d, vec);
         if (prev >= 0) s += warp_dot<T>(w + d, E1 + (size_t)prev * r, r, vec);
+        s = warp_sum(s);
+        c = 1.0f / (1.0f + expf(-s / sts[k]));
       }
-      s = warp_sum(s);
-      c = 1.0f / (1.0f + expf(-s / sts[k]));
     }
     if (lane == 0) {
       if (!isfinite(c)) set_flag(status, kFlagNonFinite);

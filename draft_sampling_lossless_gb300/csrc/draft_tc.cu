@@ -36,7 +36,9 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "confidence.cuh"
 #include "finish.cuh"
+#include "schedule.cuh"
 #include "sm100.cuh"
 
 namespace dspark {
@@ -562,6 +564,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   barrier.  The Wt and z producers run ahead across positions through
 //   their rings (neither operand depends on the drafted tokens), so their
 //   loads overlap the finish and the barriers.  TMEM is allocated once.
+// With `fuse` the launch also evaluates the confidence head and the
+// scheduler, off the per-position path where it can: the hidden-state terms
+// at position 0 while its first accumulator is computed, the head itself
+// (c_k needs x_{k-1} only) at the last position while its first accumulator
+// is computed, the candidates' ranks by the CTAs without a finish during the
+// last finish, and the one-block cut by CTA 0 after the loop.
 struct PersistParams {
   TcParams p;
   const __nv_bfloat16* z;
@@ -574,6 +582,8 @@ struct PersistParams {
   unsigned* grid_counter;  // zeroed before the launch
   int pair;                // R <= 64: two vocabulary tiles per accumulator
   __nv_bfloat16* stage;    // [R][r]: E rows of the tokens drawn at the last position
+  int fuse;                // also the confidence head and the scheduler (f)
+  DraftFuse f;
 };
 
 // Paired layout (R <= 64).  A 128-row accumulator holds two vocabulary tiles:
@@ -603,26 +613,117 @@ size_t persist_smem_bytes(int nK, int pair) {
 // barrier orders every thread's writes before thread 0's release-add, and
 // thread 0's acquire-load of the full count orders the other CTAs' writes
 // before everything after the second CTA barrier, so no full fence is needed.
+__device__ __forceinline__ void grid_arrive_wait(unsigned* ctr, unsigned target,
+                                                 volatile int* abort_flag, uint32_t* status) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
+  if (*abort_flag) return;
+  const uint64_t t0 = globaltimer_ns();
+  for (int spin = 1;; ++spin) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= target) break;
+    if ((spin & 63) == 0 && globaltimer_ns() - t0 > 2000000000ull) {
+      *abort_flag = 1;
+      set_flag(status, kFlagTimeout);
+      break;
+    }
+  }
+}
+
 __device__ __forceinline__ void grid_sync(unsigned* ctr, unsigned target, volatile int* abort_flag,
                                           uint32_t* status) {
   NamedSync<2, 256>::sync();
-  if (threadIdx.x == 0) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
-    if (!*abort_flag) {
-      const uint64_t t0 = globaltimer_ns();
-      for (int spin = 1;; ++spin) {
-        unsigned v;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
-        if (v >= target) break;
-        if ((spin & 63) == 0 && globaltimer_ns() - t0 > 2000000000ull) {
-          *abort_flag = 1;
-          set_flag(status, kFlagTimeout);
-          break;
+  if (threadIdx.x == 0) grid_arrive_wait(ctr, target, abort_flag, status);
+  NamedSync<2, 256>::sync();
+}
+
+// Confidence head after the last draft position, for the CTA's own requests
+// (epilogue warps; the lane partials of w_h . h were stored at position 0 by
+// the same threads).  Same per-warp arithmetic as the confidence kernel.
+__device__ __noinline__ void fused_confidence(const PersistParams& pp, int cta, int n_ctas,
+                                              float* s_conf) {
+  const TcParams& p = pp.p;
+  const DraftFuse& f = pp.f;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int nn = cta; nn < p.R; nn += n_ctas) {
+    for (int kk = warp; kk < p.gamma; kk += 8) {
+      const size_t idx = (size_t)nn * p.gamma + kk;
+      float c;
+      if (f.c_in != nullptr) {
+        c = f.c_in[idx];
+      } else {
+        int prev = kk == 0 ? pp.anchor[nn] : pp.tokens[idx - 1];
+        if (prev >= p.V || prev < -1) {
+          if (lane == 0) set_flag(p.status, kFlagTokenRange);
+          prev = -1;
         }
+        const uint4 eq = conf::conf_load_e1(static_cast<const __nv_bfloat16*>(f.E1), prev, p.r);
+        c = conf::conf_sigma(f.hpart[idx * 32 + lane], eq, prev, p.r, f.w + f.d, f.sts[kk]);
+      }
+      if (lane == 0) {
+        if (!isfinite(c)) set_flag(p.status, kFlagNonFinite);
+        s_conf[kk] = c;
+        f.c_out[idx] = c;
       }
     }
+    NamedSync<3, 256>::sync();
+    if ((int)threadIdx.x < p.gamma) {
+      // a_j = prod_{i <= j} c_i, each thread its own prefix
+      float run = 1.0f;
+      for (int j = 0; j <= (int)threadIdx.x; ++j) run = run * s_conf[j];
+      f.a_out[(size_t)nn * p.gamma + threadIdx.x] = run;
+    }
+    NamedSync<3, 256>::sync();
   }
-  NamedSync<2, 256>::sync();
+}
+
+// Ranks of the scheduler's candidates, by the epilogue warps of the CTAs
+// without a finish at the last draft position (every CTA when each has one),
+// between that position's two grid barriers: the survival values were written
+// before the first.  Each candidate's rank counts the i < e whose value is >=
+// its own and the i > e whose value is above it (the cleaned values are >= +0,
+// so their bits order like the values); a warp per candidate.  `buf` is the
+// Wt ring, idle after the last MMA.
+__device__ __noinline__ void fused_rank(const PersistParams& pp, int cta, int n_ctas,
+                                        uint32_t* ab) {
+  const TcParams& p = pp.p;
+  const DraftFuse& f = pp.f;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = p.R * p.gamma;
+  const int w0 = p.R < n_ctas ? p.R : 0, nwk = n_ctas - w0;  // worker CTAs
+  if (cta < w0) return;
+  for (int e = threadIdx.x; e < N; e += 256)
+    ab[e] = __float_as_uint(sched::clean_a(__ldcg(f.a_out + e), p.status) + 0.0f);
+  NamedSync<3, 256>::sync();
+  for (int e = (cta - w0) + warp * nwk; e < N; e += 8 * nwk) {
+    const uint32_t be = ab[e];
+    int cnt = 0;
+    for (int i = lane; i < N; i += 32) {
+      const uint32_t x = ab[i];
+      cnt += i < e ? (x >= be ? 1 : 0) : (i > e && x > be ? 1 : 0);
+    }
+    cnt = warp_sum(cnt);
+    if (lane == 0) f.rank[e] = cnt;
+  }
+}
+
+// The scheduler's one-block cut, by CTA 0 after the last grid barrier (every
+// rank written), every thread of the CTA; `buf` is the dynamic shared memory,
+// idle by then.
+__device__ __noinline__ void fused_cut(const PersistParams& pp, uint8_t* buf) {
+  const TcParams& p = pp.p;
+  const DraftFuse& f = pp.f;
+  const int N = p.R * p.gamma;
+  float* as = reinterpret_cast<float*>(buf);
+  int32_t* rk = reinterpret_cast<int32_t*>(buf + (size_t)N * 4);
+  long long* sfix = reinterpret_cast<long long*>(buf + (size_t)N * 8);
+  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+    as[e] = __ldcg(f.a_out + e);
+    rk[e] = __ldcg(f.rank + e);
+  }
+  __syncthreads();
+  sched::schedule_finish(p.R, p.gamma, f.imax, f.early_stop, as, f.sps, rk, sfix, f.ell,
+                         f.row_off, f.B_out, f.E_out, p.status);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -634,6 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_abort;
   __shared__ int s_tok[BM];
+  __shared__ float s_conf[kMaxGamma];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
@@ -855,6 +957,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       NamedSync<1, 288>::sync();  // release the MMA warp
+      if (k == 0 && pp.fuse && pp.f.c_in == nullptr) {
+        // the confidence head's hidden-state term does not depend on the
+        // draft: its lane partials while the first accumulator is computed
+        for (int nn = cta; nn < p.R; nn += n_ctas)
+          for (int kk = warp; kk < p.gamma; kk += 8) {
+            const size_t idx = (size_t)nn * p.gamma + kk;
+            uint4 hq[conf::kHLoads];
+            conf::conf_load_h(static_cast<const __nv_bfloat16*>(pp.f.h) + idx * pp.f.d, pp.f.d,
+                              hq);
+            pp.f.hpart[idx * 32 + lane] = conf::conf_h_lane(hq, pp.f.w, pp.f.d);
+          }
+      }
+      // c_k depends on x_{k-1} only: every confidence is known once the
+      // last position's A is; evaluate the head while its first accumulator
+      // is computed (written before this position's first grid barrier)
+      if (k == p.gamma - 1 && pp.fuse) fused_confidence(pp, cta, (int)n_ctas, s_conf);
       // partial pass over this CTA's units
       for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++acc_it, zit += kZBoxes) {
         const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
@@ -911,6 +1029,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         finish_request<__nv_bfloat16, kHalf, NamedSync<3, 256>, true>(
             fs, nn, p.V, p.gamma, k, p.n_parts, pp.z, b, p.sc, p.greedy, p.part, pp.u, pp.tokens,
             pp.q_lse, pp.q_tok, p.status, k + 1 < p.gamma ? pp.stage : nullptr, p.sub);
+      if (k == p.gamma - 1 && pp.fuse && !s_abort)
+        fused_rank(pp, cta, (int)n_ctas, reinterpret_cast<uint32_t*>(sB));
       // the finish scratch (generic) is overwritten by the next A's TMA
       fence_proxy_async_smem();
       grid_sync(pp.grid_counter, (++epoch) * n_ctas, &s_abort, p.status);
@@ -931,6 +1051,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
+  if (pp.fuse && cta == 0 && !s_abort) fused_cut(pp, smem);
 }
 
 // ---------------------------------------------------------------- final draw
@@ -1488,6 +1609,13 @@ cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st) {
   pp.grid_counter = a.grid_counter;
   pp.pair = pair;
   pp.stage = static_cast<__nv_bfloat16*>(a.stage);
+  pp.fuse = a.fuse != nullptr && draft_fuse_supported(a, *a.fuse) ? 1 : 0;
+  // the scheduler's values, ranks and fixed-point sums (16 bytes a candidate)
+  // go below the mbarriers in the dynamic shared memory
+  if (16ull * a.R * a.gamma > persist_a_bytes(p.nK, pair) + (size_t)kStagesB * kBBytes +
+                                  (size_t)persist_z_slots(pair) * kZBytes)
+    pp.fuse = 0;
+  if (pp.fuse) pp.f = *a.fuse;
   static bool attr_set = false;
   if (!attr_set) {
     e = cudaFuncSetAttribute(draft_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1520,7 +1648,24 @@ cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st) {
   DSPARK_LAUNCH(kKindDraftPersistent, st,
                 e = cudaLaunchKernelEx(&cfg, draft_persistent_kernel, tm_w, tm_z, tm_a, pp));
   if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e == cudaSuccess && a.fused != nullptr) *a.fused = pp.fuse;
+  return e;
+}
+
+// The persistent draft can also run the confidence head and the scheduler
+// when the head takes the confidence kernel's one-pass path (bf16 hidden
+// states and embedding, d <= 4096 and a multiple of 8, 16-byte aligned rows
+// and weights) or the confidences are given, and the candidates' values,
+// ranks and fixed-point sums fit the kernel's shared memory.
+bool draft_fuse_supported(const DraftArgs& a, const DraftFuse& f) {
+  const long long N = (long long)a.R * a.gamma;
+  if (N > kFuseMaxCandidates || a.dt != 0) return false;
+  if (f.c_in != nullptr) return true;
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(f.h) | reinterpret_cast<uintptr_t>(f.E1) |
+                        reinterpret_cast<uintptr_t>(f.w);
+  return f.h != nullptr && f.E1 != nullptr && (mis & 15) == 0 && f.d >= 1 &&
+         f.d <= 32 * 8 * conf::kHLoads && f.d % 8 == 0 && a.r % 8 == 0 && a.r <= 256;
 }
 
 // bias[n][v] = E[prev[n * prev_stride]] . Wt[v] on the tensor cores (rows of

@@ -1,5 +1,6 @@
-"""One DSpark speculative step on the GPU: output buffers plus the four
-libdspark calls, enqueued on one stream.  Marshalling only -- every stage
+"""One DSpark speculative step on the GPU: output buffers plus the
+libdspark calls (the four stages, or draft + confidence + schedule fused
+and verify), enqueued on one stream.  Marshalling only -- every stage
 runs in the CUDA library."""
 
 from __future__ import annotations
@@ -44,6 +45,14 @@ class DSparkStep:
     def schedule(self, sps, early_stop=True, max_B=0, a=None, stream=None):
         B.dspark_schedule(self.a if a is None else a, sps, early_stop, max_B, self.ell,
                           self.row_off, self.B, self.E, self.ws, stream)
+
+    def draft_schedule(self, z, E, Wt, anchor, u_draft, T, hidden, w, E1, sts_t, sps,
+                       c_in=None, early_stop=True, max_B=0, stream=None):
+        """draft + confidence + schedule in one call (one launch when the
+        shapes allow it); the same results as the three calls."""
+        B.dspark_draft_schedule(z, E, Wt, anchor, u_draft, T, hidden, w, E1, sts_t, c_in, sps,
+                                early_stop, max_B, self.tokens, self.q_lse, self.q_tok, self.c,
+                                self.a, self.ell, self.row_off, self.B, self.E, self.ws, stream)
 
     def verify(self, z, E, Wt, anchor, target, u_acc, u_fin, T, tokens=None, q_lse=None,
                q_tok=None, ell=None, row_off=None, stream=None):

@@ -179,6 +179,37 @@ int dspark_schedule(int R, int gamma, const float* a, const float* sps, int n_sp
                     void* stream);
 
 /*
+ * dspark_draft_schedule -- dspark_draft_sample, dspark_confidence and
+ * dspark_schedule in one call.
+ *
+ * The three stages of the news article's figure 1 pipeline (draft, confidence
+ * head with STS, hardware-aware scheduler; innovation 1 and sections 2.1 and
+ * 2.2) with the arguments of the three calls, in that order: the draft's,
+ * then the head's (d, hidden, w, E1, sts_t, c_in; r, V and dt are the
+ * draft's), then the scheduler's (sps, n_sps, early_stop, max_B), then every
+ * output.  The confidence head reads the tokens just drafted; the scheduler
+ * reads a_out.  Results are bit-identical to the three calls in sequence.
+ *
+ * When the draft runs as one persistent launch and the head takes its bf16
+ * one-pass form (d <= 4096 and a multiple of 8, 16-byte aligned rows and
+ * weights) or c_in is given, and R * gamma <= 8192, the head and the
+ * scheduler run inside that launch after the last draft position (the hidden
+ * states' term at the first position, while its bias is computed); otherwise
+ * the three stages are launched one after another.  Errors: those of the
+ * three calls.
+ */
+int dspark_draft_schedule(int R, int gamma, int V, int r, float temperature,
+                          const void* z, const void* E, const void* Wt, int dt,
+                          const int32_t* anchor, const float* u_draft,
+                          int d, const void* hidden, const float* w, const void* E1,
+                          const float* sts_t, const float* c_in,
+                          const float* sps, int n_sps, int early_stop, int max_B,
+                          int32_t* tokens, double* q_lse, float* q_tok,
+                          float* c_out, float* a_out,
+                          int32_t* ell, int32_t* row_off, int32_t* B_out, double* E_out,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/*
  * dspark_verify -- lossless rejection-sampling or greedy verification.
  *
  * Forum post "为什么DSpark 可以加速推理？以及DSpark会不会导致降智？", lossless

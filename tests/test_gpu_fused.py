@@ -1,0 +1,102 @@
+"""dspark_draft_schedule (draft + confidence head + scheduler in one call)
+against the three separate calls on the same inputs: every output must be
+bit-identical.  The separate calls are each held to the oracle by
+test_gpu_parity.py, so this carries their parity over to the fused call.
+Covers the fused persistent launch (bf16 tensor-core draft with the head's
+one-pass form, or given confidences) and the shapes that fall back to three
+launches (fp32, a Markov rank above 256)."""
+
+import numpy as np
+import pytest
+import torch
+
+from draft_sampling_lossless_gb300 import synth
+from draft_sampling_lossless_gb300.pipeline import DSparkStep
+
+from test_gpu_parity import SMALL
+
+pytestmark = pytest.mark.gpu
+
+W = synth.WORKLOADS
+
+CASES = {
+    **{k: SMALL[k] for k in ("tiny", "tiny_ragged_f32", "mid_bf16", "mid_t07", "mid_greedy",
+                             "stress_small", "one_request", "odd_tiles", "rows_100",
+                             "big_rank_bf16", "many_requests")},
+    # the bench's shape, smaller vocabulary
+    "qwen_shape": W["qwen3_4b"].scaled(name="qwen_shape", V=20000, n_sps=0),
+}
+
+OUTPUTS = ("tokens", "q_lse", "q_tok", "c", "a", "ell", "row_off", "B", "E")
+
+
+def _inputs(wl, seed=None):
+    inp = synth.make_inputs(wl, device="cuda", seed=seed)
+    g = dict(z=inp.z, E=inp.E, Wt=inp.Wt(), anchor=inp.anchor, ud=inp.u_draft, h=inp.h,
+             w=inp.w_conf, sts=inp.sts_t, c_in=inp.c_in, sps=inp.sps)
+    return g
+
+
+def _separate(wl, g, early_stop, max_B):
+    s = DSparkStep(wl.R, wl.gamma, wl.V, wl.r, wl.n_sps_eff)
+    s.draft(g["z"], g["E"], g["Wt"], g["anchor"], g["ud"], wl.T)
+    s.confidence(g["h"], g["w"], g["E"], g["anchor"], g["sts"], c_in=g["c_in"])
+    s.schedule(g["sps"], early_stop, max_B)
+    torch.cuda.synchronize()
+    assert s.status() == 0, f"device status {s.status():#x}"
+    return s
+
+
+def _fused(wl, g, early_stop, max_B):
+    s = DSparkStep(wl.R, wl.gamma, wl.V, wl.r, wl.n_sps_eff)
+    s.draft_schedule(g["z"], g["E"], g["Wt"], g["anchor"], g["ud"], wl.T, g["h"], g["w"],
+                     g["E"], g["sts"], g["sps"], c_in=g["c_in"], early_stop=early_stop,
+                     max_B=max_B)
+    torch.cuda.synchronize()
+    assert s.status() == 0, f"device status {s.status():#x}"
+    return s
+
+
+def _same(a: DSparkStep, b: DSparkStep):
+    for name in OUTPUTS:
+        x, y = getattr(a, name).cpu(), getattr(b, name).cpu()
+        assert torch.equal(x.view(torch.uint8) if x.dtype.is_floating_point else x,
+                           y.view(torch.uint8) if y.dtype.is_floating_point else y), name
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+@pytest.mark.parametrize("early_stop", [True, False])
+def test_fused_equals_separate_calls(name, early_stop):
+    wl = CASES[name]
+    g = _inputs(wl)
+    _same(_separate(wl, g, early_stop, 0), _fused(wl, g, early_stop, 0))
+
+
+def test_fused_with_batch_cap():
+    wl = CASES["mid_bf16"]
+    g = _inputs(wl, seed=5)
+    cap = wl.R + 7
+    a, b = _separate(wl, g, True, cap), _fused(wl, g, True, cap)
+    _same(a, b)
+    assert int(b.B.item()) <= cap
+
+
+def test_fused_full_size_workload():
+    """The bench's workload (Qwen3-4B shape) at full size."""
+    wl = W["qwen3_4b"]
+    g = _inputs(wl)
+    _same(_separate(wl, g, True, 0), _fused(wl, g, True, 0))
+
+
+def test_fused_repeated_calls_reuse_workspace():
+    """Two fused steps on one workspace (the grid-barrier counter and the
+    scratch are re-initialised per call)."""
+    wl = CASES["mid_t07"]
+    g1, g2 = _inputs(wl, seed=11), _inputs(wl, seed=12)
+    s = DSparkStep(wl.R, wl.gamma, wl.V, wl.r, wl.n_sps_eff)
+    for g in (g1, g2):
+        s.draft_schedule(g["z"], g["E"], g["Wt"], g["anchor"], g["ud"], wl.T, g["h"], g["w"],
+                         g["E"], g["sts"], g["sps"], c_in=g["c_in"])
+    torch.cuda.synchronize()
+    assert s.status() == 0
+    _same(_separate(wl, g2, True, 0), s)
