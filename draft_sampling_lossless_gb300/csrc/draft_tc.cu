@@ -569,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // at position 0 while its first accumulator is computed, the head itself
 // (c_k needs x_{k-1} only) at the last position while its first accumulator
 // is computed, the candidates' ranks by the CTAs without a finish during the
-// last finish, and the one-block cut by CTA 0 after the loop.
+// last finish, and the one-block cut by one CTA after the loop.
 struct PersistParams {
   TcParams p;
   const __nv_bfloat16* z;
@@ -707,9 +707,9 @@ __device__ __noinline__ void fused_rank(const PersistParams& pp, int cta, int n_
   }
 }
 
-// The scheduler's one-block cut, by CTA 0 after the last grid barrier (every
-// rank written), every thread of the CTA; `buf` is the dynamic shared memory,
-// idle by then.
+// The scheduler's one-block cut, by one CTA after the last grid barrier
+// (every rank written), every thread of the CTA; `buf` is the dynamic shared
+// memory, idle by then.
 __device__ __noinline__ void fused_cut(const PersistParams& pp, uint8_t* buf) {
   const TcParams& p = pp.p;
   const DraftFuse& f = pp.f;
@@ -1051,7 +1051,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
-  if (pp.fuse && cta == 0 && !s_abort) fused_cut(pp, smem);
+  // the cut on a CTA without requests when there is one (no logarithm pass)
+  if (pp.fuse && cta == (p.R < (int)n_ctas ? (int)n_ctas - 1 : 0) && !s_abort) fused_cut(pp, smem);
 }
 
 // ---------------------------------------------------------------- final draw

@@ -144,13 +144,16 @@ struct RowRaw<float> {
 
 // Running state of one warp item (kRowChunk tokens of a verified row, taken
 // as kRowGroup sub-chunks of kRowSub tokens): per lane the fixed-point sum of
-// 2^(a - ref) in 2^-40 units against a warp-wide power-of-two reference
+// 2^(a - ref) in 2^-40 units against the lane's own power-of-two reference
 // that only grows (the sum is shifted down when it does), or the greedy
 // argmax.  a = y * c with c = log2(e)/T rounded to fp32: the largest a is
 // the scaled largest y (c > 0), each exponent argument is one FMA (-inf
 // weighs 0).  Per sub-chunk a lane adds its 32 weights as an fp32 tree and
-// converts the tree once.  A NaN surfaces in a tree, +inf in a maximum:
-// both flag the row non-finite and weigh 0.
+// converts the tree once; no warp-wide step until the item's partial, where
+// the lanes' sums are brought to the largest reference (shifted down, so
+// each lane loses less than one 2^-40 unit of it) and added exactly.  A NaN
+// surfaces in a tree, +inf in a maximum: both flag the row non-finite and
+// weigh 0.
 struct RowState {
   long long acc = 0;
   int ref = INT_MIN;
@@ -174,12 +177,12 @@ struct RowState {
       }
       return;
     }
-    const float m = warp_max(raw.max()) * sc.hi;
+    const float m = raw.max() * sc.hi;
     if (!(m < 3.0e38f)) {  // +inf or NaN
       bad = true;
       return;
     }
-    if (m <= -1.0e38f) return;  // no mass here
+    if (m <= -1.0e38f) return;  // no mass in this lane's values
     const int cref = (int)ceilf(m);
     if (ref == INT_MIN) {
       ref = cref;
@@ -215,9 +218,13 @@ struct RowState {
       if (lane == 0) *reinterpret_cast<ArgMax*>(out) = r;
       return;
     }
-    const long long f = warp_sum(acc);
+    int rmax = ref;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) rmax = max(rmax, __shfl_xor_sync(0xffffffffu, rmax, o));
+    const int d = ref == INT_MIN ? 64 : rmax - ref;
+    const long long f = warp_sum(d >= 63 ? 0ll : (acc >> d));
     if (__any_sync(0xffffffffu, bad) && lane == 0) set_flag(status, kFlagNonFinite);
-    if (lane == 0) *out = (ref == INT_MIN || f <= 0) ? 0.0 : fix_to_double(f, ref - kFixRel);
+    if (lane == 0) *out = (rmax == INT_MIN || f <= 0) ? 0.0 : fix_to_double(f, rmax - kFixRel);
   }
 };
 
