@@ -1236,16 +1236,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (warp == kWarpW && lane == 0) tma_prefetch(&tm_w);
+  if (pair && threadIdx.x < 256) {
+    // the zero blocks of the paired A operand depend on nothing: before the wait
+    for (int c = 0; c <= p.nK; ++c) {
+      uint4* blk = reinterpret_cast<uint4*>(sA + (size_t)(2 * c) * kPairBlk);
+      for (int i = threadIdx.x; i < (int)(kPairBlk / 16); i += 256) blk[i] = make_uint4(0, 0, 0, 0);
+    }
+  }
   grid_dependency_wait();  // the verification state and previous tokens
   // A operand: E rows of the token before each request's rejected position
   {
     const int rows = pair ? 64 : BM;
-    if (pair && threadIdx.x < 256) {
-      for (int c = 0; c <= p.nK; ++c) {
-        uint4* blk = reinterpret_cast<uint4*>(sA + (size_t)(2 * c) * kPairBlk);
-        for (int i = threadIdx.x; i < (int)(kPairBlk / 16); i += 256) blk[i] = make_uint4(0, 0, 0, 0);
-      }
-    }
     if (threadIdx.x < rows) {
       const int n = r0 + threadIdx.x;
       int tok = -1;

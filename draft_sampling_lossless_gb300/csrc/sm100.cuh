@@ -70,13 +70,15 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 // Waits for the phase with the given parity to complete; gives up after
 // about one second (returns false) so that no kernel can wait forever.
+// After the first test the thread sleeps in try_wait (woken when the phase
+// completes), so waiting warps do not take issue slots from working ones.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
 #pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait_sleep(bar, parity, 2000)) return true;
     if (globaltimer_ns() - t0 > 1000000000ull) return false;
   }
 }

@@ -267,11 +267,17 @@ constexpr int kRowsSmem = 1024;  // requests whose row list fits shared memory
 // through a ring of kRowStages shared-memory slots with bulk copies (L2
 // evict-first): lane 0 keeps the copies kRowStages units ahead of the
 // reduction, so every warp has its next item's data in flight while it
-// reduces the current one, at few registers.  Every wait is bounded; a
-// timeout sets the timeout flag.
-constexpr int kRowStages = 4;
+// reduces the current one, at few registers.  Three slots a warp and the
+// request list sized by R (after the rings) let four blocks share an SM, so
+// the grid's warps outnumber the items of a typical verify batch and each
+// warp streams about one item.  Every wait is bounded; a timeout sets the
+// timeout flag.
+constexpr int kRowStages = 3;
 constexpr uint32_t kRowSlot = kRowSub * 2;  // bytes of one bf16 sub-chunk
-constexpr size_t kRowsTmaSmem = 8 * kRowStages * kRowSlot;
+constexpr size_t kRowsTmaSmem = 8 * kRowStages * kRowSlot;  // the rings; the lists follow
+__host__ __device__ constexpr size_t rows_tma_smem(int R) {
+  return kRowsTmaSmem + (size_t)(2 * R + 1) * sizeof(int);
+}
 
 __global__ void __launch_bounds__(256) verify_rows_tma_kernel(
     int R, int gamma, int V, int n_chunks, long long n_rows,
@@ -279,8 +285,8 @@ __global__ void __launch_bounds__(256) verify_rows_tma_kernel(
     const int32_t* __restrict__ row_off, ScalePair sc, int greedy, double* __restrict__ row_part,
     uint32_t* status) {
   extern __shared__ __align__(16) uint8_t rows_ring[];
-  __shared__ int s_r0[kRowsSmem];
-  __shared__ int s_pre[kRowsSmem + 1];
+  int* s_r0 = reinterpret_cast<int*>(rows_ring + kRowsTmaSmem);  // [R]
+  int* s_pre = s_r0 + R;                                          // [R + 1]
   __shared__ int s_scan[32];
   __shared__ uint64_t bars[8][kRowStages];
   __shared__ double* s_out[8][kRowStages];  // the unit's item output (null: row out of range)
@@ -520,10 +526,26 @@ __global__ void __launch_bounds__(256) verify_decide_kernel(
   __shared__ int Spg[kMaxGamma + 1];
   __shared__ ArgMax am_s[kMaxGamma + 1];
   __shared__ int bad_s;
-  grid_dependency_wait();  // the row partials
   const int n = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  // The schedule, the drafted tokens and the target logits were complete
+  // before the row pass (the kernel this one waits for) could finish: the
+  // accept test's operands are requested before the wait, so their memory
+  // latency overlaps it; only the row partials come after.
   const int L = ell[n];
   const long long r0 = row_off[n];
+  int x_pre = -1;
+  float tx_pre = 0.f, qx_pre = 1.f, u_pre = 1.f;
+  if (wid == 0 && lane < L && L <= gamma && r0 >= 0 && r0 + L < n_rows) {
+    x_pre = tokens[(size_t)n * gamma + lane];
+    if (x_pre >= 0 && x_pre < V) {
+      tx_pre = to_f32<T>(target[(size_t)(r0 + lane) * V + x_pre]);
+      if (!greedy) {
+        qx_pre = q_tok[(size_t)n * gamma + lane];
+        u_pre = u_acc[(size_t)n * gamma + lane];
+      }
+    }
+  }
+  grid_dependency_wait();  // the row partials
   if (tid == 0) {
     bad_s = (L < 0 || L > gamma || r0 < 0 || r0 + L >= n_rows);
     if (bad_s) set_flag(status, kFlagRowRange);
@@ -571,15 +593,14 @@ __global__ void __launch_bounds__(256) verify_decide_kernel(
   // n_acc = the first rejection
   bool acc = true;
   if (lane < L) {
-    const int x = tokens[(size_t)n * gamma + lane];
+    const int x = x_pre;
     if (x < 0 || x >= V) {
       set_flag(status, kFlagTokenRange);
       acc = false;
     } else if (greedy) {
       acc = (x == am_s[lane].i);
     } else {
-      acc = accept_test(to_f32<T>(target[(size_t)(r0 + lane) * V + x]), sc, SpF[lane], Spg[lane],
-                        q_tok[(size_t)n * gamma + lane], u_acc[(size_t)n * gamma + lane]);
+      acc = accept_test(tx_pre, sc, SpF[lane], Spg[lane], qx_pre, u_pre);
     }
   }
   const unsigned live = L >= 32 ? 0xffffffffu : ((1u << L) - 1u);
@@ -809,8 +830,10 @@ __global__ void __launch_bounds__(256) final_pick_tc_kernel(
     const long long* __restrict__ fin_part, const float* __restrict__ u_fin,
     int32_t* __restrict__ out_tokens, uint32_t* status) {
   __shared__ FinishScratch s;
-  grid_dependency_wait();  // the final partials
   const int n = blockIdx.x, tid = threadIdx.x;
+  // The verification state was complete before the final pass (the kernel
+  // this one waits for) could finish: it, the uniform and the previous
+  // token's E row are read before the wait; the partials after it.
   const VerifyState st = vstate[n];
   if (st.mode < 0) return;
   const bool resid = st.mode == 1;
@@ -818,6 +841,8 @@ __global__ void __launch_bounds__(256) final_pick_tc_kernel(
     for (int i = tid; i < r; i += 256)
       s.erow[i] = st.prev >= 0 ? __bfloat162float(E[(size_t)st.prev * r + i]) : 0.f;
   }
+  const float u = u_fin[n];
+  grid_dependency_wait();  // the final partials
   const long long* P = fin_part + (size_t)n * n_halves * 2;
   const int seg = (n_halves + 255) / 256;
   const int t0 = min(n_halves, tid * seg), t1 = min(n_halves, t0 + seg);
@@ -840,7 +865,7 @@ __global__ void __launch_bounds__(256) final_pick_tc_kernel(
     }
     return;
   }
-  const long long thr = floor_mul(u_fin[n], F);  // C > u*F  <=>  C > floor(u*F)
+  const long long thr = floor_mul(u, F);  // C > u*F  <=>  C > floor(u*F)
   int cand = 0x7fffffff;
   long long base = 0, ssel = 0;
   {
@@ -934,17 +959,26 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t st) {
   const bool staged = sizeof(T) == 2 && a.R <= kRowsSmem && a.V % 8 == 0 &&
                       ((uintptr_t)a.target & 15) == 0;
   if (staged) {
-    static int grid = 0;  // attribute and occupancy once per process
-    if (grid == 0) {
+    // the attribute once per process (for the largest list); the resident
+    // grid whenever the list size changes
+    static bool attr = false;
+    static size_t grid_dyn = 0;
+    static int grid = 0;
+    const size_t dyn = rows_tma_smem(a.R);
+    if (!attr) {
       cudaError_t e = cudaFuncSetAttribute(verify_rows_tma_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)kRowsTmaSmem);
+                                           (int)rows_tma_smem(kRowsSmem));
       if (e != cudaSuccess) return e;
-      grid = row_grid(verify_rows_tma_kernel, 1ll << 40, kRowsTmaSmem);
+      attr = true;
+    }
+    if (grid_dyn != dyn) {
+      grid = row_grid(verify_rows_tma_kernel, 1ll << 40, dyn);
+      grid_dyn = dyn;
     }
     const int g = (int)(grid < (items + 7) / 8 ? grid : (items + 7) / 8);
     DSPARK_LAUNCH(kKindVerifyRows, st,
-                  launch_pdl(verify_rows_tma_kernel, dim3(g), dim3(256), kRowsTmaSmem, st, a.R,
+                  launch_pdl(verify_rows_tma_kernel, dim3(g), dim3(256), dyn, st, a.R,
                              a.gamma, a.V, n_chunks, a.n_rows,
                              reinterpret_cast<const __nv_bfloat16*>(tg), a.ell, a.row_off, sc,
                              (int)greedy, a.row_part, a.status));
