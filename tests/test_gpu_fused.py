@@ -4,7 +4,8 @@ bit-identical.  The separate calls are each held to the oracle by
 test_gpu_parity.py, so this carries their parity over to the fused call.
 Covers the fused persistent launch (bf16 tensor-core draft with the head's
 one-pass form, or given confidences) and the shapes that fall back to three
-launches (fp32, a Markov rank above 256)."""
+launches (fp32, a Markov rank above 256, more than 8192 candidates, a hidden
+size above 4096)."""
 
 import numpy as np
 import pytest
@@ -25,6 +26,12 @@ CASES = {
                              "big_rank_bf16", "many_requests")},
     # the bench's shape, smaller vocabulary
     "qwen_shape": W["qwen3_4b"].scaled(name="qwen_shape", V=20000, n_sps=0),
+    # more candidates than the fused launch takes (R * gamma > 8192): three launches
+    "many_candidates": W["stress"].scaled(name="many_candidates", R=520, gamma=16, V=512, r=16,
+                                          n_sps=0),
+    # a hidden size past the head's one-pass form (d > 4096): three launches
+    "wide_hidden": W["qwen3_4b"].scaled(name="wide_hidden", R=4, gamma=3, V=1024, r=64, d=4104,
+                                        n_sps=0),
 }
 
 OUTPUTS = ("tokens", "q_lse", "q_tok", "c", "a", "ell", "row_off", "B", "E")
