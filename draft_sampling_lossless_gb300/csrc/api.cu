@@ -30,7 +30,8 @@ int cuda_fail(cudaError_t e, const char* where) {
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-  size_t status, bias, part, sub, row_part, vstate, fin_part, prev, stage, rank, sfix, hpart, total;
+  size_t status, bias, part, sub, row_part, vstate, fin_part, prev, stage, rank, sfix, hpart, vcnt,
+      total;
 };
 
 bool sizes_ok(int R, int gamma, int V, int r) {
@@ -69,6 +70,8 @@ Layout layout(int R, int gamma, int V, int r) {
   L.hpart = off;  // lane partials of the confidence head when the draft runs it
   off += align_up((N < (size_t)kFuseMaxCandidates ? N : (size_t)kFuseMaxCandidates) * 32 *
                   sizeof(float));
+  L.vcnt = off;  // the row pass's per-request item counters (zero between calls)
+  off += align_up((size_t)R * sizeof(int));
   L.total = off;
   return L;
 }
@@ -428,6 +431,7 @@ int dspark_verify(int R, int gamma, int V, int r, float temperature, const void*
   a.bias = at<float>(ws, L.bias);
   a.fin_part = at<long long>(ws, L.fin_part);
   a.prev = at<int32_t>(ws, L.prev);
+  a.vcnt = at<int>(ws, L.vcnt);
   cudaError_t e = launch_verify(a, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "dspark_verify");
   return DSPARK_OK;

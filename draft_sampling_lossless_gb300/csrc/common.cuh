@@ -436,6 +436,7 @@ struct VerifyArgs {
   float* bias;           // [R][V]
   long long* fin_part;   // [R][n_tiles][2]
   int32_t* prev;         // [R]
+  int* vcnt;             // [R] row-pass items counted per request, zero between calls
 };
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t st);
 // Final-draw partial sums on the tensor cores: fin_part[R][ceil(V / 128)][2]

@@ -261,6 +261,35 @@ __device__ __forceinline__ int build_row_list(int R, int gamma, const int32_t* _
 
 constexpr int kRowsSmem = 1024;  // requests whose row list fits shared memory
 
+template <typename T>
+__device__ __noinline__ void decide_request(
+    int n, int gamma, int V, int n_chunks, long long n_rows, const T* __restrict__ target,
+    ScalePair sc, int greedy, const int32_t* __restrict__ anchor,
+    const int32_t* __restrict__ tokens, const double* __restrict__ q_lse,
+    const float* __restrict__ q_tok, const int32_t* __restrict__ ell,
+    const int32_t* __restrict__ row_off, const float* __restrict__ u_acc,
+    const double* __restrict__ row_part, double* __restrict__ p_lse,
+    int32_t* __restrict__ n_acc_out, int32_t* __restrict__ out_tokens,
+    VerifyState* __restrict__ vstate, int32_t* __restrict__ prev_out, uint32_t* status);
+
+// What the row pass needs to run each request's decide itself: the block that
+// completes a request's last item runs it (per-request item counters in the
+// workspace, returned to zero by that block).
+struct DecideOut {
+  int on;
+  const int32_t* anchor;
+  const int32_t* tokens;
+  const double* q_lse;
+  const float* q_tok;
+  const float* u_acc;
+  double* p_lse;
+  int32_t* n_acc;
+  int32_t* out_tokens;
+  VerifyState* vstate;
+  int32_t* prev;
+  int* cnt;  // [R] items counted so far, zero between calls
+};
+
 // The row pass for bf16 targets with V % 8 == 0 (16-byte aligned rows).
 // Item = (verified row, chunk of kRowChunk tokens), strided over the grid's
 // warps.  Each warp streams its items' sub-chunks (2 KiB each) in order
@@ -276,17 +305,21 @@ constexpr int kRowStages = 3;
 constexpr uint32_t kRowSlot = kRowSub * 2;  // bytes of one bf16 sub-chunk
 constexpr size_t kRowsTmaSmem = 8 * kRowStages * kRowSlot;  // the rings; the lists follow
 __host__ __device__ constexpr size_t rows_tma_smem(int R) {
-  return kRowsTmaSmem + (size_t)(2 * R + 1) * sizeof(int);
+  return kRowsTmaSmem + (size_t)(4 * R + 1) * sizeof(int);  // rings; r0, pre, items, winners
 }
 
-__global__ void __launch_bounds__(256) verify_rows_tma_kernel(
+__global__ void __launch_bounds__(256, 4) verify_rows_tma_kernel(
     int R, int gamma, int V, int n_chunks, long long n_rows,
     const __nv_bfloat16* __restrict__ target, const int32_t* __restrict__ ell,
     const int32_t* __restrict__ row_off, ScalePair sc, int greedy, double* __restrict__ row_part,
-    uint32_t* status) {
+    uint32_t* status, const DecideOut dec) {
   extern __shared__ __align__(16) uint8_t rows_ring[];
   int* s_r0 = reinterpret_cast<int*>(rows_ring + kRowsTmaSmem);  // [R]
   int* s_pre = s_r0 + R;                                          // [R + 1]
+  int* s_cnt = s_pre + R + 1;                                     // [R] items done here
+  int* s_win = s_cnt + R;                                         // [R] requests decided here
+  __shared__ int s_req[8][kRowStages];
+  __shared__ int s_nwin;
   __shared__ int s_scan[32];
   __shared__ uint64_t bars[8][kRowStages];
   __shared__ double* s_out[8][kRowStages];  // the unit's item output (null: row out of range)
@@ -296,6 +329,7 @@ __global__ void __launch_bounds__(256) verify_rows_tma_kernel(
     for (int i = 0; i < 8 * kRowStages; ++i) sm100::mbar_init(sm100::smem_u32(&bars[0][0] + i), 1);
     sm100::fence_mbar_init();
   }
+  for (int i = threadIdx.x; i < R; i += blockDim.x) s_cnt[i] = 0;
   grid_dependency_wait();  // ell, row_off
   const int n_verified = build_row_list(R, gamma, ell, row_off, s_r0, s_pre, s_scan);
   const int n_subs = (V + kRowSub - 1) / kRowSub;
@@ -311,6 +345,7 @@ __global__ void __launch_bounds__(256) verify_rows_tma_kernel(
   int p_sub = 0, p_nsub = 0;
   const __nv_bfloat16* p_src = nullptr;  // sub-chunk 0 of p_item's chunk, null: nothing to copy
   double* p_out = nullptr;
+  int p_req = 0;
   auto p_decode = [&]() {
     p_sub = 0;
     if (p_item >= total) return;
@@ -324,6 +359,7 @@ __global__ void __launch_bounds__(256) verify_rows_tma_kernel(
       else hi = mid - 1;
     }
     const int n = lo, j = k - s_pre[n];
+    p_req = n;
     const long long row = (long long)s_r0[n] + j;
     if (row < 0 || row >= n_rows) {  // reported by the decide kernel
       p_src = nullptr;
@@ -337,6 +373,7 @@ __global__ void __launch_bounds__(256) verify_rows_tma_kernel(
     if (p_item >= total) return;
     const uint32_t bar = sm100::smem_u32(&bars[warp][slot]);
     s_out[warp][slot] = p_out;
+    s_req[warp][slot] = p_req;
     if (p_src == nullptr) {
       sm100::mbar_arrive(bar);
     } else {
@@ -361,6 +398,7 @@ __global__ void __launch_bounds__(256) verify_rows_tma_kernel(
     const int c = (int)(item % (uint32_t)n_chunks), nsub = subs_of(item);
     RowState st;
     double* out = nullptr;
+    int req = 0;
     bool failed = false;
     for (int sb = 0; sb < nsub; ++sb, ++u) {
       const int slot = (int)(u % kRowStages);
@@ -370,6 +408,7 @@ __global__ void __launch_bounds__(256) verify_rows_tma_kernel(
         break;
       }
       out = s_out[warp][slot];
+      req = s_req[warp][slot];
       if (out != nullptr) {
         const int v0 = c * kRowChunk + sb * kRowSub, lim = V - v0;
         RowRaw<__nv_bfloat16> x;
@@ -410,6 +449,44 @@ __global__ void __launch_bounds__(256) verify_rows_tma_kernel(
       break;
     }
     if (out != nullptr) st.store(greedy, out, status);
+    if (dec.on && lane == 0) atomicAdd(s_cnt + req, 1);
+  }
+  if (!dec.on) return;
+  // Each request's decide, by the block that completes its last item: the
+  // block publishes its item counts (its partials ordered before them by the
+  // block barrier and the fence); the one whose count completes a request
+  // (1 + l rows of n_chunks items) runs the decide and zeroes the counter.
+  // A request with no verified rows (an invalid l) is decided by block
+  // n mod gridDim.x.
+  __syncthreads();
+  if (threadIdx.x == 0) s_nwin = 0;
+  __syncthreads();
+  for (int n = threadIdx.x; n < R; n += blockDim.x) {
+    const int items = (s_pre[n + 1] - s_pre[n]) * n_chunks;
+    const int c = s_cnt[n];
+    bool win = false;
+    if (items == 0) {
+      win = n % (int)gridDim.x == (int)blockIdx.x;
+    } else if (c > 0) {
+      __threadfence();
+      const int old = atomicAdd(dec.cnt + n, c);
+      if (old + c == items) {
+        win = true;
+        dec.cnt[n] = 0;
+      }
+    }
+    if (win) s_win[atomicAdd(&s_nwin, 1)] = n;
+  }
+  __syncthreads();
+  const int nw = s_nwin;
+  if (nw == 0) return;
+  __threadfence();  // the other blocks' partials, published before their counts
+  for (int i = 0; i < nw; ++i) {
+    decide_request<__nv_bfloat16>(s_win[i], gamma, V, n_chunks, n_rows, target, sc, greedy,
+                                  dec.anchor, dec.tokens, dec.q_lse, dec.q_tok, ell, row_off,
+                                  dec.u_acc, row_part, dec.p_lse, dec.n_acc, dec.out_tokens,
+                                  dec.vstate, dec.prev, status);
+    __syncthreads();
   }
 }
 
@@ -487,11 +564,12 @@ __device__ __forceinline__ long long warp_fix_total(const double* __restrict__ p
 #pragma unroll
     for (int i = 0; i < kReg; ++i) {
       const int c = lane + 32 * i;
-      pv[i] = c < n_chunks ? clean(pj[c]) : 0.0;
+      pv[i] = c < n_chunks ? clean(__ldcg(pj + c)) : 0.0;
       emax = max(emax, double_exponent(pv[i]));
     }
   } else {
-    for (int c = lane; c < n_chunks; c += 32) emax = max(emax, double_exponent(clean(pj[c])));
+    for (int c = lane; c < n_chunks; c += 32)
+      emax = max(emax, double_exponent(clean(__ldcg(pj + c))));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
@@ -505,16 +583,21 @@ __device__ __forceinline__ long long warp_fix_total(const double* __restrict__ p
 #pragma unroll
     for (int i = 0; i < kReg; ++i) loc += double_to_fix(pv[i], g);
   } else {
-    for (int c = lane; c < n_chunks; c += 32) loc += double_to_fix(clean(pj[c]), g);
+    for (int c = lane; c < n_chunks; c += 32) loc += double_to_fix(clean(__ldcg(pj + c)), g);
   }
   *g_out = g;
   return warp_sum(loc);
 }
 
 
+// The accept tests and the final-draw state of request n, by one block of 256
+// threads (every thread must call it; it returns with warps at different
+// points, so a caller's next block barrier orders what follows).  Used by the
+// decide kernel and by the row pass's block that completes request n's last
+// item (row partials written by other blocks of that kernel: L2 loads).
 template <typename T>
-__global__ void __launch_bounds__(256) verify_decide_kernel(
-    int gamma, int V, int n_chunks, long long n_rows, const T* __restrict__ target,
+__device__ __noinline__ void decide_request(
+    int n, int gamma, int V, int n_chunks, long long n_rows, const T* __restrict__ target,
     ScalePair sc, int greedy, const int32_t* __restrict__ anchor,
     const int32_t* __restrict__ tokens, const double* __restrict__ q_lse,
     const float* __restrict__ q_tok, const int32_t* __restrict__ ell,
@@ -526,11 +609,7 @@ __global__ void __launch_bounds__(256) verify_decide_kernel(
   __shared__ int Spg[kMaxGamma + 1];
   __shared__ ArgMax am_s[kMaxGamma + 1];
   __shared__ int bad_s;
-  const int n = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  // The schedule, the drafted tokens and the target logits were complete
-  // before the row pass (the kernel this one waits for) could finish: the
-  // accept test's operands are requested before the wait, so their memory
-  // latency overlaps it; only the row partials come after.
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int L = ell[n];
   const long long r0 = row_off[n];
   int x_pre = -1;
@@ -545,7 +624,6 @@ __global__ void __launch_bounds__(256) verify_decide_kernel(
       }
     }
   }
-  grid_dependency_wait();  // the row partials
   if (tid == 0) {
     bad_s = (L < 0 || L > gamma || r0 < 0 || r0 + L >= n_rows);
     if (bad_s) set_flag(status, kFlagRowRange);
@@ -567,8 +645,10 @@ __global__ void __launch_bounds__(256) verify_decide_kernel(
     const double* pj = part + (size_t)j * n_chunks;
     if (greedy) {
       ArgMax am{-INFINITY, 0x7fffffff};
-      for (int c = lane; c < n_chunks; c += 32)
-        am = better(am, reinterpret_cast<const ArgMax*>(pj)[c]);
+      for (int c = lane; c < n_chunks; c += 32) {
+        const long long raw = __ldcg(reinterpret_cast<const long long*>(pj) + c);
+        am = better(am, ArgMax{__int_as_float((int)(raw & 0xffffffffll)), (int)(raw >> 32)});
+      }
       am = warp_argmax(am);
       if (lane == 0) {
         am_s[j] = am;
@@ -627,6 +707,22 @@ __global__ void __launch_bounds__(256) verify_decide_kernel(
   }
   vstate[n] = st;
   prev_out[n] = st.prev;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) verify_decide_kernel(
+    int gamma, int V, int n_chunks, long long n_rows, const T* __restrict__ target,
+    ScalePair sc, int greedy, const int32_t* __restrict__ anchor,
+    const int32_t* __restrict__ tokens, const double* __restrict__ q_lse,
+    const float* __restrict__ q_tok, const int32_t* __restrict__ ell,
+    const int32_t* __restrict__ row_off, const float* __restrict__ u_acc,
+    const double* __restrict__ row_part, double* __restrict__ p_lse,
+    int32_t* __restrict__ n_acc_out, int32_t* __restrict__ out_tokens,
+    VerifyState* __restrict__ vstate, int32_t* __restrict__ prev_out, uint32_t* status) {
+  grid_dependency_wait();  // the row partials
+  decide_request<T>(blockIdx.x, gamma, V, n_chunks, n_rows, target, sc, greedy, anchor, tokens,
+                    q_lse, q_tok, ell, row_off, u_acc, row_part, p_lse, n_acc_out, out_tokens,
+                    vstate, prev_out, status);
 }
 
 // ---------------------------------------------------------------- final draw
@@ -958,6 +1054,9 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t st) {
   const long long items = (long long)a.R * (a.gamma + 1) * n_chunks;
   const bool staged = sizeof(T) == 2 && a.R <= kRowsSmem && a.V % 8 == 0 &&
                       ((uintptr_t)a.target & 15) == 0;
+  // the staged row pass runs every request's decide itself
+  const DecideOut dec{staged && a.vcnt != nullptr ? 1 : 0, a.anchor, a.tokens, a.q_lse, a.q_tok,
+                      a.u_acc, a.p_lse, a.n_acc, a.out_tokens, a.vstate, a.prev, a.vcnt};
   if (staged) {
     // the attribute once per process (for the largest list); the resident
     // grid whenever the list size changes
@@ -981,7 +1080,7 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t st) {
                   launch_pdl(verify_rows_tma_kernel, dim3(g), dim3(256), dyn, st, a.R,
                              a.gamma, a.V, n_chunks, a.n_rows,
                              reinterpret_cast<const __nv_bfloat16*>(tg), a.ell, a.row_off, sc,
-                             (int)greedy, a.row_part, a.status));
+                             (int)greedy, a.row_part, a.status, dec));
   } else {
     DSPARK_LAUNCH(kKindVerifyRows, st,
                   launch_pdl(verify_rows_wide_kernel<T>,
@@ -989,11 +1088,13 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t st) {
                              st, a.R, a.gamma, a.V, n_chunks, a.n_rows, tg, a.ell, a.row_off, sc,
                              (int)greedy, a.row_part, a.status));
   }
-  DSPARK_LAUNCH(kKindVerifyDecide, st,
-                launch_pdl(verify_decide_kernel<T>, dim3(a.R), dim3(256), 0, st, a.gamma, a.V,
-                           n_chunks, a.n_rows, tg, sc, (int)greedy, a.anchor, a.tokens, a.q_lse,
-                           a.q_tok, a.ell, a.row_off, a.u_acc, (const double*)a.row_part, a.p_lse,
-                           a.n_acc, a.out_tokens, a.vstate, a.prev, a.status));
+  if (!dec.on)
+    DSPARK_LAUNCH(kKindVerifyDecide, st,
+                  launch_pdl(verify_decide_kernel<T>, dim3(a.R), dim3(256), 0, st, a.gamma, a.V,
+                             n_chunks, a.n_rows, tg, sc, (int)greedy, a.anchor, a.tokens,
+                             a.q_lse, a.q_tok, a.ell, a.row_off, a.u_acc,
+                             (const double*)a.row_part, a.p_lse, a.n_acc, a.out_tokens, a.vstate,
+                             a.prev, a.status));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || greedy) return e;
   if (tc_shape_supported(a.dt, a.V, a.r, a.z, a.E, a.Wt) &&

@@ -22,8 +22,11 @@
  *   bytes, at least dspark_workspace_bytes(...) for the same sizes, 256-byte
  *   aligned.  Its first 4 bytes are a device status word: kernels OR the
  *   DSPARK_DEVFLAG_* bits into it when they meet bad data they can only see
- *   on the device (a token id out of range, a non-finite value).  Zero it once
- *   after allocating the workspace; read it with dspark_device_status().
+ *   on the device (a token id out of range, a non-finite value).  Zero the
+ *   whole workspace once after allocating it; read the word with
+ *   dspark_device_status().  Calls leave the workspace's counters at zero
+ *   when they complete; after a call that set DSPARK_DEVFLAG_TIMEOUT, zero
+ *   the workspace again before reusing it.
  *   Two calls in flight at the same time need two workspaces.
  * - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
  *   call only enqueues work on it and returns; nothing is synchronised.
