@@ -138,28 +138,20 @@ __device__ inline ArgMax block_argmax(ArgMax a, ArgMax* sh) {
 
 __device__ inline int block_min_int(int v, int* sh) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  v = __reduce_min_sync(0xffffffffu, v);
   __syncthreads();
   if (lane == 0) sh[wid] = v;
   __syncthreads();
-  int t = lane < nw ? sh[lane] : 0x7fffffff;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) t = min(t, __shfl_xor_sync(0xffffffffu, t, o));
-  return t;
+  return __reduce_min_sync(0xffffffffu, lane < nw ? sh[lane] : 0x7fffffff);
 }
 
 __device__ inline int block_max_int(int v, int* sh) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  v = __reduce_max_sync(0xffffffffu, v);
   __syncthreads();
   if (lane == 0) sh[wid] = v;
   __syncthreads();
-  int t = lane < nw ? sh[lane] : -0x7fffffff;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) t = max(t, __shfl_xor_sync(0xffffffffu, t, o));
-  return t;
+  return __reduce_max_sync(0xffffffffu, lane < nw ? sh[lane] : -0x7fffffff);
 }
 
 // Inclusive block scan (Hillis-Steele over warps); `sh` holds 32 elements.

@@ -702,7 +702,7 @@ __device__ __noinline__ void fused_rank(const PersistParams& pp, int cta, int n_
       const uint32_t x = ab[i];
       cnt += i < e ? (x >= be ? 1 : 0) : (i > e && x > be ? 1 : 0);
     }
-    cnt = warp_sum(cnt);
+    cnt = __reduce_add_sync(0xffffffffu, cnt);
     if (lane == 0) f.rank[e] = cnt;
   }
 }

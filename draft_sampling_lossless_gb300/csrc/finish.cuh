@@ -53,6 +53,16 @@ struct FinishScratch {
 
 // ---- reductions over 256 threads (8 warps), every thread gets the result
 
+// Warp maximum of floats that are never NaN (-inf allowed), as one integer
+// reduction instruction on an order-preserving image of the bits (a negative
+// float's magnitude bits flipped), instead of five dependent shuffles.
+__device__ __forceinline__ float warp_max_nonan(float a) {
+  int k = __float_as_int(a);
+  k = k >= 0 ? k : (k ^ 0x7fffffff);
+  k = __reduce_max_sync(0xffffffffu, k);
+  return __int_as_float(k >= 0 ? k : (k ^ 0x7fffffff));
+}
+
 // Inclusive scan over the 256 threads; *total receives the sum of all.
 template <class S>
 __device__ __forceinline__ long long g_scan_ll(long long v, long long* sh, long long* total) {
@@ -79,8 +89,7 @@ __device__ __forceinline__ long long g_scan_ll(long long v, long long* sh, long 
 template <class S>
 __device__ __forceinline__ int g_min_i(int v, int* sh) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  v = __reduce_min_sync(0xffffffffu, v);  // one warp-wide reduction instruction
   S::sync();
   if (lane == 0) sh[wid] = v;
   S::sync();
@@ -93,8 +102,7 @@ __device__ __forceinline__ int g_min_i(int v, int* sh) {
 template <class S>
 __device__ __forceinline__ int g_max_i(int v, int* sh) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  v = __reduce_max_sync(0xffffffffu, v);
   S::sync();
   if (lane == 0) sh[wid] = v;
   S::sync();
@@ -104,10 +112,11 @@ __device__ __forceinline__ int g_max_i(int v, int* sh) {
   return r;
 }
 
+// (v never NaN)
 template <class S>
 __device__ __forceinline__ float g_max_f(float v, float* sh) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  v = warp_max(v);
+  v = warp_max_nonan(v);
   S::sync();
   if (lane == 0) sh[wid] = v;
   S::sync();
@@ -531,7 +540,7 @@ __device__ __forceinline__ void finish_group(FinishScratch& s, int n, int V, int
     float y = ok ? zv + s.bias[lane] : -INFINITY;
     if (ok && (isnan(y) || y == INFINITY)) y = -INFINITY;
     const float a = scaled(y, sc);
-    const float amax = warp_max(a);
+    const float amax = warp_max_nonan(a);  // y was cleaned: no NaN
     const float ref = ceilf(amax);
     const float wt = (ok && a > -INFINITY && amax > -INFINITY) ? exp2f(a - ref) : 0.f;
     const uint32_t f = __float2uint_rn(wt * 134217728.0f);  // 2^27

@@ -218,9 +218,7 @@ struct RowState {
       if (lane == 0) *reinterpret_cast<ArgMax*>(out) = r;
       return;
     }
-    int rmax = ref;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) rmax = max(rmax, __shfl_xor_sync(0xffffffffu, rmax, o));
+    const int rmax = __reduce_max_sync(0xffffffffu, ref);
     const int d = ref == INT_MIN ? 64 : rmax - ref;
     const long long f = warp_sum(d >= 63 ? 0ll : (acc >> d));
     if (__any_sync(0xffffffffu, bad) && lane == 0) set_flag(status, kFlagNonFinite);
@@ -571,8 +569,7 @@ __device__ __forceinline__ long long warp_fix_total(const double* __restrict__ p
     for (int c = lane; c < n_chunks; c += 32)
       emax = max(emax, double_exponent(clean(__ldcg(pj + c))));
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
+  emax = __reduce_max_sync(0xffffffffu, emax);
   if (emax == INT_MIN) {
     *g_out = 0;
     return 0;
@@ -902,11 +899,8 @@ __global__ void __launch_bounds__(256) final_pick_kernel(
     if (w[e] > 0) last = tid * 8 + e;
     if (pick == 0x7fffffff && w[e] > 0 && run > thr) pick = tid * 8 + e;
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    pick = min(pick, __shfl_xor_sync(0xffffffffu, pick, o));
-    last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-  }
+  pick = __reduce_min_sync(0xffffffffu, pick);
+  last = __reduce_max_sync(0xffffffffu, last);
   if (tid == 0) {
     const int idx = pick != 0x7fffffff ? pick : (last >= 0 ? last : 0);
     out_tokens[(size_t)n * (gamma + 1) + st.n_acc] = tsel_s * kFinTile + idx;
