@@ -397,6 +397,16 @@ __device__ __forceinline__ void load8<float>(const float* p, int v0, int V, floa
   }
 }
 
+// Exact warp sum of non-negative 64-bit values whose total is below 2^63:
+// three 21-bit limbs, each summed by one reduction instruction.
+__device__ __forceinline__ long long warp_sum_nonneg_ll(long long v) {
+  const unsigned long long u = (unsigned long long)v;
+  const unsigned long long a = __reduce_add_sync(0xffffffffu, (unsigned)(u >> 42));
+  const unsigned long long b = __reduce_add_sync(0xffffffffu, (unsigned)(u >> 21) & 0x1fffffu);
+  const unsigned long long c = __reduce_add_sync(0xffffffffu, (unsigned)u & 0x1fffffu);
+  return (long long)((a << 42) + (b << 21) + c);
+}
+
 __device__ __forceinline__ long long warp_sum_ll(long long v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

@@ -38,6 +38,7 @@ struct BiasSrc {
 // Shared-memory scratch of one finish (about 8 KiB).
 struct FinishScratch {
   long long shl[8];
+  long long shl2[8];
   float shf[8];
   int shi[8];
   ArgMax sha[8];
@@ -84,6 +85,43 @@ __device__ __forceinline__ long long g_scan_ll(long long v, long long* sh, long 
   }
   *total = tot;
   return v + off;
+}
+
+// Two inclusive scans at once (the same latency as one); *ta, *tb the totals.
+template <class S>
+__device__ __forceinline__ void g_scan_ll2(long long& a, long long& b, long long* sha,
+                                           long long* shb, long long* ta, long long* tb) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long na = __shfl_up_sync(0xffffffffu, a, o);
+    const long long nb = __shfl_up_sync(0xffffffffu, b, o);
+    if (lane >= o) {
+      a += na;
+      b += nb;
+    }
+  }
+  S::sync();
+  if (lane == 31) {
+    sha[wid] = a;
+    shb[wid] = b;
+  }
+  S::sync();
+  long long oa = 0, ob = 0, sa = 0, sb = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const long long xa = sha[w], xb = shb[w];
+    if (w < wid) {
+      oa += xa;
+      ob += xb;
+    }
+    sa += xa;
+    sb += xb;
+  }
+  a += oa;
+  b += ob;
+  *ta = sa;
+  *tb = sb;
 }
 
 template <class S>

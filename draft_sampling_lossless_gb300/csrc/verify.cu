@@ -220,7 +220,7 @@ struct RowState {
     }
     const int rmax = __reduce_max_sync(0xffffffffu, ref);
     const int d = ref == INT_MIN ? 64 : rmax - ref;
-    const long long f = warp_sum(d >= 63 ? 0ll : (acc >> d));
+    const long long f = warp_sum_nonneg_ll(d >= 63 ? 0ll : (acc >> d));
     if (__any_sync(0xffffffffu, bad) && lane == 0) set_flag(status, kFlagNonFinite);
     if (lane == 0) *out = (rmax == INT_MIN || f <= 0) ? 0.0 : fix_to_double(f, rmax - kFixRel);
   }
@@ -583,7 +583,7 @@ __device__ __forceinline__ long long warp_fix_total(const double* __restrict__ p
     for (int c = lane; c < n_chunks; c += 32) loc += double_to_fix(clean(__ldcg(pj + c)), g);
   }
   *g_out = g;
-  return warp_sum(loc);
+  return warp_sum_nonneg_ll(loc);
 }
 
 
@@ -941,13 +941,14 @@ __global__ void __launch_bounds__(256) final_pick_tc_kernel(
     lr += P[2 * t];
     lp += P[2 * t + 1];
   }
-  long long Fr;
-  g_scan_ll<BlockSync>(lr, s.shl, &Fr);
-  // the residual column, unless p and q agree everywhere (then p itself)
+  // both columns' scans at once; the residual column unless p and q agree
+  // everywhere (then p itself)
+  long long ir = lr, ip = lp, Fr, Fp;
+  g_scan_ll2<BlockSync>(ir, ip, s.shl, s.shl2, &Fr, &Fp);
   const int col = (resid && Fr > 0) ? 0 : 1;
   const long long loc = col == 0 ? lr : lp;
-  long long F;
-  const long long incl = g_scan_ll<BlockSync>(loc, s.shl, &F);
+  const long long F = col == 0 ? Fr : Fp;
+  const long long incl = col == 0 ? ir : ip;
   if (F <= 0) {
     if (tid == 0) {
       set_flag(status, kFlagNonFinite);
