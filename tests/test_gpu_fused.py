@@ -107,3 +107,52 @@ def test_fused_repeated_calls_reuse_workspace():
     torch.cuda.synchronize()
     assert s.status() == 0
     _same(_separate(wl, g2, True, 0), s)
+
+
+def _verify_with(wl, g, step_src, ell, row_off, target, ws_step=None):
+    """dspark_verify on a fresh (or the given) step with explicit lengths."""
+    s = ws_step or DSparkStep(wl.R, wl.gamma, wl.V, wl.r, wl.n_sps_eff, max_rows=target.shape[0])
+    s.verify(g["z"], g["E"], g["Wt"], g["anchor"], target, g["ua"], g["uf"], wl.T,
+             tokens=step_src.tokens, q_lse=step_src.q_lse, q_tok=step_src.q_tok, ell=ell,
+             row_off=row_off)
+    torch.cuda.synchronize()
+    return s
+
+
+def test_row_pass_decide_flags_bad_length_and_leaves_counters_zero():
+    """A request whose verify length is out of range gets no rows in the row
+    pass; its decide still runs (flags the row-range bit, emits -1s, n_acc 0),
+    the other requests are unaffected, and the per-request counters the row
+    pass uses are back at zero for the next call on the same workspace."""
+    wl = CASES["mid_bf16"]
+    inp = synth.make_inputs(wl, device="cuda", seed=21)
+    g = dict(z=inp.z, E=inp.E, Wt=inp.Wt(), anchor=inp.anchor, ud=inp.u_draft, h=inp.h,
+             w=inp.w_conf, sts=inp.sts_t, c_in=inp.c_in, sps=inp.sps, ua=inp.u_acc, uf=inp.u_fin)
+    src = _fused(wl, g, True, 0)
+    R, G = wl.R, wl.gamma
+    ell_ok = src.ell.clone()
+    bad = 3
+    ell_ok[bad] = 0
+    counts = (1 + ell_ok).to(torch.int64)
+    row_off = torch.zeros(R + 1, dtype=torch.int32, device="cuda")
+    row_off[1:] = torch.cumsum(counts, 0).to(torch.int32)
+    dense = synth.make_target(inp, tokens=src.tokens).reshape(R, G + 1, wl.V)
+    rows = torch.cat([r * (G + 1) + torch.arange(int(counts[r]), device="cuda") for r in range(R)])
+    target = dense.reshape(-1, wl.V)[rows].contiguous()
+    ref = _verify_with(wl, g, src, ell_ok, row_off, target)
+    assert ref.status() == 0
+    ell_bad = ell_ok.clone()
+    ell_bad[bad] = G + 3
+    s = _verify_with(wl, g, src, ell_bad, row_off, target)
+    assert s.status() & 0x4, f"row-range flag not set: {s.status():#x}"
+    out, ref_out = s.out_tokens.cpu(), ref.out_tokens.cpu()
+    assert torch.all(out[bad] == -1) and int(s.n_acc[bad].item()) == 0
+    keep = torch.arange(R) != bad
+    assert torch.equal(out[keep], ref_out[keep])
+    assert torch.equal(s.n_acc.cpu()[keep], ref.n_acc.cpu()[keep])
+    # the same workspace again, valid lengths: the same results as a fresh one
+    s.status(clear=True)
+    again = _verify_with(wl, g, src, ell_ok, row_off, target, ws_step=s)
+    assert again.status() == 0
+    assert torch.equal(again.out_tokens.cpu(), ref_out)
+    assert torch.equal(again.n_acc.cpu(), ref.n_acc.cpu())
