@@ -21,6 +21,7 @@
 //              recomputing it with the same warp routine, compared with u*total
 //              in exact integer arithmetic
 #include "common.cuh"
+#include "f32x2.cuh"
 #include "finish.cuh"
 
 namespace dspark {
@@ -192,18 +193,27 @@ struct RowState {
       ref = cref;
     }
     const float fref = (float)ref;
+    // pairs of tokens through the packed fp32 FMA and adds: the same
+    // roundings, in the same tree, as one token at a time
+    const unsigned long long c2 = pack2(sc.hi, sc.hi), r2 = pack2(-fref, -fref);
     float t[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       float x[8];
       raw.get(i, x);
+      unsigned long long p2[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = ex2_fast(fmaf(x[e], sc.hi, -fref));
-#pragma unroll
-      for (int w = 4; w > 0; w >>= 1)
-#pragma unroll
-        for (int e = 0; e < w; ++e) x[e] += x[e + w];
-      t[i] = x[0];
+      for (int e = 0; e < 4; ++e) {
+        float a, b;
+        unpack2(fma2(pack2(x[2 * e], x[2 * e + 1]), c2, r2), a, b);
+        p2[e] = pack2(ex2_fast(a), ex2_fast(b));
+      }
+      p2[0] = add2(p2[0], p2[2]);  // tokens e and e + 4
+      p2[1] = add2(p2[1], p2[3]);
+      p2[0] = add2(p2[0], p2[1]);  // e and e + 2
+      float a, b;
+      unpack2(p2[0], a, b);
+      t[i] = a + b;
     }
     const float sum = (t[0] + t[1]) + (t[2] + t[3]);
     if (sum != sum) bad = true;
@@ -343,12 +353,13 @@ __global__ void __launch_bounds__(256, 4) verify_rows_tma_kernel(
   int p_sub = 0, p_nsub = 0;
   const __nv_bfloat16* p_src = nullptr;  // sub-chunk 0 of p_item's chunk, null: nothing to copy
   double* p_out = nullptr;
-  int p_req = 0;
+  int p_req = 0, p_c = 0;
   auto p_decode = [&]() {
     p_sub = 0;
     if (p_item >= total) return;
     const int k = (int)(p_item / (uint32_t)n_chunks);
     const int c = (int)(p_item - (uint32_t)k * (uint32_t)n_chunks);
+    p_c = c;
     p_nsub = min(kRowGroup, n_subs - c * kRowGroup);
     int lo = 0, hi = R - 1;  // the request n with s_pre[n] <= k < s_pre[n + 1]
     while (lo < hi) {
@@ -375,7 +386,7 @@ __global__ void __launch_bounds__(256, 4) verify_rows_tma_kernel(
     if (p_src == nullptr) {
       sm100::mbar_arrive(bar);
     } else {
-      const int v0 = (p_item % (uint32_t)n_chunks) * kRowChunk + p_sub * kRowSub;
+      const int v0 = p_c * kRowChunk + p_sub * kRowSub;
       const uint32_t bytes = (uint32_t)min(kRowSub, V - v0) * 2u;
       sm100::mbar_arrive_expect_tx(bar, bytes);
       sm100::bulk_load_hint(sm100::smem_u32(ring + slot * kRowSlot), p_src + p_sub * kRowSub,
