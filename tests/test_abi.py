@@ -109,3 +109,27 @@ def test_confidence_and_verify_reject_bad_arguments(lib):
                            n, f, 1 << 30, n) == 1  # n_target_rows = 0
     assert L.dspark_verify(4, 4, 1024, 16, 1.0, f, f, f, 1, f, f, f, f, f, f, f, 20, n, f, f, f,
                            n, f, 1 << 30, n) == 1  # u_acc NULL with T > 0
+
+
+def test_draft_schedule_rejects_bad_arguments_without_launching(lib):
+    """The fused call validates the draft's, the head's and the scheduler's
+    arguments before it launches anything (every case below fails one)."""
+    L = lib.lib()
+    f, n = _fake(), _null()
+    ws_n = 1 << 30
+
+    def call(R=4, G=4, V=1024, r=16, T=1.0, dt=0, d=64, hidden=f, c_in=n, n_sps=100,
+             max_B=0, sps=f, ws_bytes=ws_n):
+        return L.dspark_draft_schedule(R, G, V, r, T, f, f, f, dt, f, f, d, hidden, f, f, f, c_in,
+                                       sps, n_sps, 1, max_B, f, f, f, f, f, f, f, f, f, f,
+                                       ws_bytes, n)
+
+    assert call(R=0) == 1
+    assert call(T=-1.0) == 1
+    assert call(hidden=n) == 1  # the head needs hidden states when c_in is NULL
+    assert call(d=0) == 1
+    assert call(n_sps=20) == 1  # imax = R*G = 16: needs n_sps > 20
+    assert "SPS table" in _err(L)
+    assert call(max_B=3) == 1  # a cap below R
+    assert call(sps=n) == 1
+    assert call(ws_bytes=1024) == 4  # DSPARK_ERR_WORKSPACE
