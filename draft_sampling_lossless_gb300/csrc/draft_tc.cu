@@ -530,7 +530,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   epilogue warps gather A(k) (E rows of x_{k-1}), release the MMA warp,
 //   run the partial pass over the CTA's tiles, grid barrier, run the finish
 //   of the CTA's requests (scratch aliased on the A tile, idle by then), grid
-//   barrier.  The Wt and z producers run ahead across positions through
+//   barrier (none after the last position: nothing reads across CTAs after
+//   it).  The Wt and z producers run ahead across positions through
 //   their rings (neither operand depends on the drafted tokens), so their
 //   loads overlap the finish and the barriers.  TMEM is allocated once.
 // With `fuse` the launch also evaluates the confidence head and the
@@ -538,7 +539,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // at position 0 while its first accumulator is computed, the head itself
 // (c_k needs x_{k-1} only) at the last position while its first accumulator
 // is computed, the candidates' ranks by the CTAs without a finish during the
-// last finish, and the one-block cut by one CTA after the loop.
+// last finish, and the one-block cut by one CTA after the loop, once the
+// ranking CTAs have signalled it (the other CTAs do not wait).
 struct PersistParams {
   TcParams p;
   const __nv_bfloat16* z;
@@ -548,7 +550,7 @@ struct PersistParams {
   double* q_lse;
   float* q_tok;
   const float* u;
-  unsigned* grid_counter;  // zeroed before the launch
+  unsigned* grid_counter;  // [2], zeroed before the launch: grid barrier, ranking CTAs done
   int pair;                // R <= 64: two vocabulary tiles per accumulator
   __nv_bfloat16* stage;    // [R][r]: E rows of the tokens drawn at the last position
   int fuse;                // also the confidence head and the scheduler (f)
@@ -679,10 +681,29 @@ __device__ __noinline__ void fused_rank(const PersistParams& pp, int cta, int n_
 // The scheduler's one-block cut, by one CTA after the last grid barrier
 // (every rank written), every thread of the CTA; `buf` is the dynamic shared
 // memory, idle by then.
-__device__ __noinline__ void fused_cut(const PersistParams& pp, uint8_t* buf) {
+__device__ __noinline__ void fused_cut(const PersistParams& pp, uint8_t* buf, int n_ctas,
+                                       volatile int* s_abort) {
   const TcParams& p = pp.p;
   const DraftFuse& f = pp.f;
   const int N = p.R * p.gamma;
+  // every ranking CTA has published its ranks (bounded wait, about 2 s)
+  if (threadIdx.x == 0) {
+    const unsigned want = (unsigned)(n_ctas - (p.R < n_ctas ? p.R : 0));
+    const uint64_t t0 = globaltimer_ns();
+    for (int spin = 1;; ++spin) {
+      unsigned v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(pp.grid_counter + 1)
+                   : "memory");
+      if (v >= want) break;
+      if ((spin & 63) == 0 && globaltimer_ns() - t0 > 2000000000ull) {
+        *s_abort = 1;
+        set_flag(p.status, kFlagTimeout);
+        break;
+      }
+    }
+  }
+  __syncthreads();
+  if (*s_abort) return;
   float* as = reinterpret_cast<float*>(buf);
   int32_t* rk = reinterpret_cast<int32_t*>(buf + (size_t)N * 4);
   long long* sfix = reinterpret_cast<long long*>(buf + (size_t)N * 8);
@@ -998,11 +1019,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         finish_request<__nv_bfloat16, kHalf, NamedSync<3, 256>, true>(
             fs, nn, p.V, p.gamma, k, p.n_parts, pp.z, b, p.sc, p.greedy, p.part, pp.u, pp.tokens,
             pp.q_lse, pp.q_tok, p.status, k + 1 < p.gamma ? pp.stage : nullptr, p.sub);
-      if (k == p.gamma - 1 && pp.fuse && !s_abort)
+      if (k + 1 < p.gamma) {
+        // the finish scratch (generic) is overwritten by the next A's TMA;
+        // every CTA needs every staged row before it loads the next A
+        fence_proxy_async_smem();
+        grid_sync(pp.grid_counter, (++epoch) * n_ctas, &s_abort, p.status);
+      } else if (pp.fuse && !s_abort) {
+        // after the last position only the cut waits, for the ranks: the
+        // ranking CTAs signal it (release) and nobody waits for the finishes
         fused_rank(pp, cta, (int)n_ctas, reinterpret_cast<uint32_t*>(sB));
-      // the finish scratch (generic) is overwritten by the next A's TMA
-      fence_proxy_async_smem();
-      grid_sync(pp.grid_counter, (++epoch) * n_ctas, &s_abort, p.status);
+        NamedSync<3, 256>::sync();
+        if (threadIdx.x == 0 && cta >= (p.R < (int)n_ctas ? p.R : 0))
+          asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(pp.grid_counter + 1)
+                       : "memory");
+      }
     }
     // The finishes left each q_lse entry holding its normaliser; take the
     // logarithms here, off the per-position path (same CTA, same requests).
@@ -1021,7 +1051,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
   // the cut on a CTA without requests when there is one (no logarithm pass)
-  if (pp.fuse && cta == (p.R < (int)n_ctas ? (int)n_ctas - 1 : 0) && !s_abort) fused_cut(pp, smem);
+  if (pp.fuse && cta == (p.R < (int)n_ctas ? (int)n_ctas - 1 : 0) && !s_abort)
+    fused_cut(pp, smem, (int)n_ctas, &s_abort);
 }
 
 // ---------------------------------------------------------------- final draw
@@ -1604,7 +1635,7 @@ cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st) {
   int gx = sm_count() / n_rt;
   if (gx < 1) return cudaErrorNotSupported;
   if (gx > n_units) gx = n_units;
-  e = cudaMemsetAsync(a.grid_counter, 0, sizeof(unsigned), st);
+  e = cudaMemsetAsync(a.grid_counter, 0, 2 * sizeof(unsigned), st);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(gx, n_rt);
