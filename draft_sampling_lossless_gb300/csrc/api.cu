@@ -31,7 +31,7 @@ size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
   size_t status, bias, part, sub, row_part, vstate, fin_part, prev, stage, rank, sfix, hpart, vcnt,
-      total;
+      tkey, spre, total;
 };
 
 bool sizes_ok(int R, int gamma, int V, int r) {
@@ -72,6 +72,12 @@ Layout layout(int R, int gamma, int V, int r) {
                   sizeof(float));
   L.vcnt = off;  // the row pass's per-request item counters (zero between calls)
   off += align_up((size_t)R * sizeof(int));
+  // the fused scheduler's Theta keys and prefixes by rank
+  const size_t nf = (N < (size_t)kFuseMaxCandidates ? N : (size_t)kFuseMaxCandidates) + 1;
+  L.tkey = off;
+  off += align_up(nf * sizeof(unsigned long long));
+  L.spre = off;
+  off += align_up(nf * sizeof(long long));
   L.total = off;
   return L;
 }
@@ -351,6 +357,8 @@ int dspark_draft_schedule(int R, int gamma, int V, int r, float temperature, con
   f.imax = sa.imax < 0 ? 0 : sa.imax;
   f.sps = sps;
   f.rank = at<int32_t>(ws, L.rank);
+  f.tkey = at<unsigned long long>(ws, L.tkey);
+  f.spre = at<long long>(ws, L.spre);
   f.ell = ell;
   f.row_off = row_off;
   f.B_out = B_out;

@@ -256,6 +256,8 @@ struct DraftFuse {
   int early_stop, imax;
   const float* sps;
   int32_t* rank;      // [R * gamma] scratch
+  unsigned long long* tkey;  // [R * gamma + 1] scratch: Theta_i order keys by rank
+  long long* spre;           // [R * gamma + 1] scratch: exact prefixes S_i by rank
   int32_t* ell;
   int32_t* row_off;
   int32_t* B_out;

@@ -663,18 +663,37 @@ __device__ __noinline__ void fused_rank(const PersistParams& pp, int cta, int n_
   const int N = p.R * p.gamma;
   const int w0 = p.R < n_ctas ? p.R : 0, nwk = n_ctas - w0;  // worker CTAs
   if (cta < w0) return;
-  for (int e = threadIdx.x; e < N; e += 256)
-    ab[e] = __float_as_uint(sched::clean_a(__ldcg(f.a_out + e), p.status) + 0.0f);
+  long long* fx = reinterpret_cast<long long*>(ab + ((N + 1) & ~1));  // 8-byte aligned
+  for (int e = threadIdx.x; e < N; e += 256) {
+    const float v = sched::clean_a(__ldcg(f.a_out + e), p.status) + 0.0f;
+    ab[e] = __float_as_uint(v);
+    fx[e] = sched::to_fixed(v);
+  }
   NamedSync<3, 256>::sync();
+  // with its rank, each candidate's exact prefix S_rank (the sum of the
+  // values ranked before it) and Theta_rank's key; the last-ranked one also
+  // gives S_N and Theta_N
   for (int e = (cta - w0) + warp * nwk; e < N; e += 8 * nwk) {
     const uint32_t be = ab[e];
     int cnt = 0;
+    long long sacc = 0;
     for (int i = lane; i < N; i += 32) {
       const uint32_t x = ab[i];
-      cnt += i < e ? (x >= be ? 1 : 0) : (i > e && x > be ? 1 : 0);
+      const bool before = i < e ? (x >= be) : (i > e && x > be);
+      cnt += before ? 1 : 0;
+      sacc += before ? fx[i] : 0ll;
     }
     cnt = __reduce_add_sync(0xffffffffu, cnt);
-    if (lane == 0) f.rank[e] = cnt;
+    const long long S = warp_sum_nonneg_ll(sacc);
+    if (lane == 0) {
+      f.rank[e] = cnt;
+      f.spre[cnt] = S;
+      if (cnt <= f.imax) f.tkey[cnt] = sched::theta_key_of(p.R, cnt, S, f.sps, p.status);
+      if (cnt == N - 1) {
+        f.spre[N] = S + fx[e];
+        if (N <= f.imax) f.tkey[N] = sched::theta_key_of(p.R, N, S + fx[e], f.sps, p.status);
+      }
+    }
   }
 }
 
@@ -704,16 +723,11 @@ __device__ __noinline__ void fused_cut(const PersistParams& pp, uint8_t* buf, in
   }
   __syncthreads();
   if (*s_abort) return;
-  float* as = reinterpret_cast<float*>(buf);
-  int32_t* rk = reinterpret_cast<int32_t*>(buf + (size_t)N * 4);
-  long long* sfix = reinterpret_cast<long long*>(buf + (size_t)N * 8);
-  for (int e = threadIdx.x; e < N; e += blockDim.x) {
-    as[e] = __ldcg(f.a_out + e);
-    rk[e] = __ldcg(f.rank + e);
-  }
+  int32_t* rk = reinterpret_cast<int32_t*>(buf);
+  for (int e = threadIdx.x; e < N; e += blockDim.x) rk[e] = __ldcg(f.rank + e);
   __syncthreads();
-  sched::schedule_finish(p.R, p.gamma, f.imax, f.early_stop, as, f.sps, rk, sfix, f.ell,
-                         f.row_off, f.B_out, f.E_out, p.status);
+  sched::schedule_cut_keys(p.R, p.gamma, f.imax, f.early_stop, f.tkey, f.spre, rk, f.ell,
+                           f.row_off, f.B_out, f.E_out);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)

@@ -121,6 +121,94 @@ __device__ __forceinline__ unsigned long long dbl_key(unsigned long long b) {
   return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
 }
 
+// Theta_i's order key from the exact prefix S_i (units of 2^-40), in the
+// oracle's operation order ((double)S * 2^-40 + R) * SPS[R + i]: S rounded
+// to a double, the sum rounded, the product rounded; returned as an order
+// key of the double's bits.  A non-finite SPS entry counts as 0 (flagged).
+__device__ __forceinline__ unsigned long long theta_key_of(int R, int i, long long S,
+                                                           const float* __restrict__ sps,
+                                                           uint32_t* status) {
+  const unsigned long long e =
+      rne53(((unsigned long long)R << 40) + rne53((unsigned long long)S));  // (R + S 2^-40) 2^40
+  float sv = sps[R + i];
+  if (!isfinite(sv)) {
+    set_flag(status, kFlagNonFinite);
+    sv = 0.0f;
+  }
+  return dbl_key(dbl_mul_float(dbl_bits(e, -40), sv));
+}
+
+// The block's first argmax over (key, index) pairs: the largest key, the
+// lowest index among equal keys (index 0x7fffffff: no candidate).
+__device__ inline int block_first_argmax(unsigned long long v, int bi, unsigned long long* shk,
+                                         int* shidx, int* res) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ov > v || (ov == v && oi < bi)) {
+      v = ov;
+      bi = oi;
+    }
+  }
+  __syncthreads();
+  if (lane == 0) {
+    shk[wid] = v;
+    shidx[wid] = bi;
+  }
+  __syncthreads();
+  if (wid == 0) {
+    v = lane < nw ? shk[lane] : 0ull;
+    bi = lane < nw ? shidx[lane] : 0x7fffffff;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long ov = __shfl_xor_sync(0xffffffffu, v, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > v || (ov == v && oi < bi)) {
+        v = ov;
+        bi = oi;
+      }
+    }
+    if (lane == 0) *res = bi;
+  }
+  __syncthreads();
+  return *res;
+}
+
+// l_r = the number of request r's candidates ranked below i*, row_off (their
+// exclusive scan of 1 + l_r), by one whole block.
+__device__ inline void schedule_lengths(int R, int gamma, int istar, const int32_t* rank,
+                                        int32_t* __restrict__ ell,
+                                        int32_t* __restrict__ row_off, long long* shl) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int rseg = (R + nt - 1) / nt;
+  const int r0 = min(R, tid * rseg), r1 = min(R, r0 + rseg);
+  long long lsum = 0;
+  for (int r = r0; r < r1; ++r) {
+    int c = 0;
+    for (int j = 0; j < gamma; ++j) c += rank[(size_t)r * gamma + j] < istar;
+    ell[r] = c;
+    lsum += 1 + c;
+  }
+  long long rincl = block_inclusive_scan(lsum, shl);
+  long long run = rincl - lsum;
+  for (int r = r0; r < r1; ++r) {
+    row_off[r] = (int32_t)run;
+    run += 1 + ell[r];
+  }
+  if (tid == nt - 1) row_off[R] = (int32_t)rincl;
+}
+
+// E = R + S_{i*} as the oracle's double, B = R + i*.
+__device__ __forceinline__ void schedule_store_EB(int R, int istar, long long S,
+                                                  int32_t* __restrict__ B_out,
+                                                  double* __restrict__ E_out) {
+  const unsigned long long e = rne53(((unsigned long long)R << 40) + rne53((unsigned long long)S));
+  E_out[0] = __longlong_as_double((long long)dbl_bits(e, -40));
+  B_out[0] = R + istar;
+}
+
 // The cut and the per-request outputs, by one whole block (any multiple of
 // 32 threads; every thread of the block must call it), given every
 // candidate's rank.
@@ -157,14 +245,7 @@ __device__ inline void schedule_finish(
   // S rounded to a double, the sum rounded, the product rounded; returned as
   // an order key of the double's bits.
   auto theta_key = [&](int i, long long S) -> unsigned long long {
-    const unsigned long long e =
-        rne53(((unsigned long long)R << 40) + rne53((unsigned long long)S));  // (R + S 2^-40) 2^40
-    float s = sps[R + i];
-    if (!isfinite(s)) {
-      set_flag(status, kFlagNonFinite);
-      s = 0.0f;
-    }
-    return dbl_key(dbl_mul_float(dbl_bits(e, -40), s));
+    return theta_key_of(R, i, S, sps, status);
   };
   int my_stop = 0x7fffffff;
   unsigned long long best_v = 0;
@@ -195,68 +276,57 @@ __device__ inline void schedule_finish(
   } else {
     // first argmax: max value, then lowest index
     // (key 0 is below every double's key: a thread with no i never wins)
-    const int lane = tid & 31, wid = tid >> 5, nw = nt >> 5;
-    unsigned long long v = best_v;
-    int bi = best_i;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long ov = __shfl_xor_sync(0xffffffffu, v, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ov > v || (ov == v && oi < bi)) {
-        v = ov;
-        bi = oi;
-      }
-    }
-    __syncthreads();
-    if (lane == 0) {
-      shk[wid] = v;
-      shidx[wid] = bi;
-    }
-    __syncthreads();
-    if (wid == 0) {
-      v = lane < nw ? shk[lane] : 0ull;
-      bi = lane < nw ? shidx[lane] : 0x7fffffff;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long ov = __shfl_xor_sync(0xffffffffu, v, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > v || (ov == v && oi < bi)) {
-          v = ov;
-          bi = oi;
-        }
-      }
-      if (lane == 0) istar_s = bi;
-    }
-    __syncthreads();
-    istar = istar_s;
+    istar = block_first_argmax(best_v, best_i, shk, shidx, &istar_s);
     if (istar == 0x7fffffff) istar = 0;
   }
   // 3. E = R + S_{i*}
   if (istar >= i0 && istar < i1) {
     long long S = S0;
     for (int i = i0; i < istar; ++i) S += sfix[i];
-    const unsigned long long e =
-        rne53(((unsigned long long)R << 40) + rne53((unsigned long long)S));
-    E_out[0] = __longlong_as_double((long long)dbl_bits(e, -40));
-    B_out[0] = R + istar;
+    schedule_store_EB(R, istar, S, B_out, E_out);
   }
   // 4. l_r = number of request r's candidates ranked below i*, and row_off
-  const int rseg = (R + nt - 1) / nt;
-  const int r0 = min(R, tid * rseg), r1 = min(R, r0 + rseg);
-  long long lsum = 0;
-  for (int r = r0; r < r1; ++r) {
-    int c = 0;
-    for (int j = 0; j < gamma; ++j) c += rank[(size_t)r * gamma + j] < istar;
-    ell[r] = c;
-    lsum += 1 + c;
+  schedule_lengths(R, gamma, istar, rank, ell, row_off, shl);
+}
+
+// The same cut when every Theta_i key (i = 0..imax) and every prefix S_i
+// (i = 0..N) is already known (the persistent draft's ranking CTAs form them
+// with the ranks): the stop or the first argmax over the keys, E from
+// S_{i*}, then the lengths.  The same definitions as schedule_finish, so the
+// same results.  tkey and spre are read from L2 (written by other CTAs).
+__device__ inline void schedule_cut_keys(int R, int gamma, int imax, int early_stop,
+                                         const unsigned long long* tkey, const long long* spre,
+                                         const int32_t* rank, int32_t* __restrict__ ell,
+                                         int32_t* __restrict__ row_off,
+                                         int32_t* __restrict__ B_out,
+                                         double* __restrict__ E_out) {
+  __shared__ long long shl[32];
+  __shared__ int shi[32];
+  __shared__ unsigned long long shk[32];
+  __shared__ int shidx[32];
+  __shared__ int istar_s;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  int my_stop = 0x7fffffff;
+  unsigned long long best_v = 0;
+  int best_i = 0x7fffffff;
+  for (int i = tid; i <= imax; i += nt) {
+    const unsigned long long th = __ldcg(tkey + i);
+    if (i > 0 && !(th > __ldcg(tkey + i - 1))) my_stop = min(my_stop, i - 1);
+    if (best_i == 0x7fffffff || th > best_v) {  // i ascends within the thread
+      best_v = th;
+      best_i = i;
+    }
   }
-  long long rincl = block_inclusive_scan(lsum, shl);
-  long long run = rincl - lsum;
-  for (int r = r0; r < r1; ++r) {
-    row_off[r] = (int32_t)run;
-    run += 1 + ell[r];
+  int istar;
+  if (early_stop) {
+    const int st = block_min_int(my_stop, shi);
+    istar = st == 0x7fffffff ? imax : st;
+  } else {
+    istar = block_first_argmax(best_v, best_i, shk, shidx, &istar_s);
+    if (istar == 0x7fffffff) istar = 0;
   }
-  if (tid == nt - 1) row_off[R] = (int32_t)rincl;
+  if (tid == 0) schedule_store_EB(R, istar, __ldcg(spre + istar), B_out, E_out);
+  schedule_lengths(R, gamma, istar, rank, ell, row_off, shl);
 }
 
 }  // namespace sched
