@@ -1,36 +1,43 @@
-// Fused Markov-bias GEMM + draft-sampler partial pass on the 5th-generation
-// tensor cores (tcgen05, TMEM accumulators, TMA operand loads).
+// The tensor-core kernels of the draft and of the final draw (5th-generation
+// tensor cores: tcgen05 MMA into TMEM accumulators, TMA operand loads).
 //
 // "DSpark.让每一轮计算，多走几步" (explainer), Markov head panel, and the news
 // article "DSpark: Confidence-Scheduled Speculative Decoding with
 // Semi-Autoregressive Generation", innovation 1, second stage: at draft
 // position k every request's previous token selects a row of the low-rank
 // table E, and bias = E[x_{k-1}] . W is added to the backbone logits before
-// the draw.
-//
-// One launch per draft position k.  The bias is never written to memory: per
-// (128-request tile, 256-token tile) the MMA
+// the draw.  The bias is never written to memory: per vocabulary tile the MMA
 //     D[m][v] = sum_i E[x_{k-1}(m)][i] * Wt[v][i]          (M=128, N=256, K=r)
 // lands in tensor memory, and the epilogue turns each thread's row of D plus
 // the matching slice of z into y = z + bias, a = y * log2(e)/T and, per
 // 128-token half tile, the exact fixed-point sum of 2^(a - ref) (greedy: the
-// half tile's max and argmax).  The per-request finish kernel consumes these
-// partials.
+// half tile's max and argmax) with its 16-token group sums.
 //
-// Warp roles (352 threads, persistent over the CTA's vocabulary tiles):
-//   warps 0-7  epilogue: warp w reads TMEM lane quadrant w % 4 (requests
-//              32(w%4) .. +31 of the tile) and token half w / 4 of the tile
+// Kernels:
+//   draft_persistent_kernel  every draft position in one cooperative launch
+//       (the main path): partial pass, grid barrier, the per-request finish
+//       (finish.cuh) that draws x_k and stages E[x_k] for the next A operand,
+//       grid barrier; optionally also the confidence head and the scheduler
+//       (dspark_draft_schedule).
+//   draft_fused_tc_kernel    one draft position's partial pass (the fallback
+//       when a cooperative launch is not possible; the finish is a separate
+//       launch), or in bias-out mode the fp32 bias rows.
+//   final_tc_kernel          the verification's final draw: the rejected
+//       position's bias in TMEM and, per half tile, the fixed-point sums of
+//       the target's p and of max(0, p - q).
+//
+// Warp roles (352 threads, one CTA an SM):
+//   warps 0-7  epilogue: warp w reads TMEM lane quadrant w % 4 and token
+//              half w / 4 of the accumulator; also the gathers and finishes
 //   warp 8     TMA producer of Wt K-chunks [256 tokens x 64] (3-stage ring)
 //   warp 9     TMEM allocation and the single MMA-issuing thread
-//   warp 10    TMA producer of z boxes [128 requests x 64 tokens] (4-box ring)
-// The A operand (the 128 gathered E rows) is built once per CTA in the
-// 128-byte swizzled K-major layout.  Two 256-column accumulators alternate so
-// the MMA of tile t+1 overlaps the epilogue of tile t.  Every mbarrier wait is
-// bounded (about one second); a timeout sets DSPARK_DEVFLAG_TIMEOUT, makes the
-// other waits of the CTA give up at once, and the kernel runs to completion.
-//
-// The same kernel in bias-out mode (no z stream) writes the fp32 bias rows
-// instead of partial sums; verification uses it for its residual draws.
+//   warp 10    producer of z (TMA boxes) or of the final draw's rows
+// A operands are in the 128-byte swizzled K-major layout; with R <= 64 the
+// paired layout puts two vocabulary tiles in one accumulator.  Two 256-column
+// accumulators alternate so the MMA of one unit overlaps the epilogue of the
+// previous one.  Every wait is bounded (about one second on an mbarrier, two
+// on a grid barrier); a timeout sets DSPARK_DEVFLAG_TIMEOUT, makes the other
+// waits of the CTA give up at once, and the kernel runs to completion.
 #include <climits>
 
 #include <cudaTypedefs.h>
@@ -608,9 +615,11 @@ __device__ __forceinline__ void grid_sync(unsigned* ctr, unsigned target, volati
   NamedSync<2, 256>::sync();
 }
 
-// Confidence head after the last draft position, for the CTA's own requests
-// (epilogue warps; the lane partials of w_h . h were stored at position 0 by
-// the same threads).  Same per-warp arithmetic as the confidence kernel.
+// Confidence head at the last draft position (c_k needs x_{k-1} only, and
+// every such token is drawn by then), for the CTA's own requests, by the
+// epilogue warps while the position's first accumulator is computed; the
+// lane partials of w_h . h were stored at position 0 by the same threads.
+// Same per-warp arithmetic as the confidence kernel.
 __device__ __noinline__ void fused_confidence(const PersistParams& pp, int cta, int n_ctas,
                                               float* s_conf) {
   const TcParams& p = pp.p;
@@ -650,11 +659,12 @@ __device__ __noinline__ void fused_confidence(const PersistParams& pp, int cta, 
 
 // Ranks of the scheduler's candidates, by the epilogue warps of the CTAs
 // without a finish at the last draft position (every CTA when each has one),
-// between that position's two grid barriers: the survival values were written
-// before the first.  Each candidate's rank counts the i < e whose value is >=
-// its own and the i > e whose value is above it (the cleaned values are >= +0,
-// so their bits order like the values); a warp per candidate.  `buf` is the
-// Wt ring, idle after the last MMA.
+// after that position's grid barrier (the survival values were written
+// before it); the cut waits for their signal, nobody else does.  Each
+// candidate's rank counts the i < e whose value is >= its own and the i > e
+// whose value is above it (the cleaned values are >= +0, so their bits order
+// like the values); a warp per candidate.  `ab` points into the Wt ring,
+// idle after the last MMA: the values' bits, then their fixed-point images.
 __device__ __noinline__ void fused_rank(const PersistParams& pp, int cta, int n_ctas,
                                         uint32_t* ab) {
   const TcParams& p = pp.p;
