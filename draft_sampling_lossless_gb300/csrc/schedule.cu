@@ -8,7 +8,8 @@
 // stop.  Explainer "DSpark.让每一轮计算，多走几步", survival panel:
 // E = R + sum a, rate = E / T(B), candidates added in sorted order.
 //
-// Two launches:
+// For R * gamma <= 1024 one block does both steps below (schedule_fused_
+// kernel); larger batches take two launches:
 //   rank   -- the position of every candidate in the total order
 //             (a descending, then flat index n*gamma + j ascending), counted by
 //             comparisons against all others; ranks are a permutation because
@@ -18,6 +19,9 @@
 //             the 2^-40 fixed-point survival values, Theta_i rounded exactly as
 //             the oracle's double arithmetic rounds it, the early-stop or
 //             argmax cut, then l_r, row_off, B and E.
+// The persistent draft kernel can run the same steps after its last position
+// (dspark_draft_schedule): its idle CTAs rank the candidates and form the
+// prefixes and Theta keys, one CTA finds the cut (schedule.cuh).
 // No floating-point double instruction runs here: the double roundings are
 // reproduced with integer arithmetic (round to nearest, ties to even), which
 // gives the same bits and avoids the narrow FP64 pipe.

@@ -7,19 +7,23 @@
 // one more (bonus) token comes from the next target distribution.  CSDN
 // tutorial, section 五: the first rejection ends the block.
 //
-// Launches (stochastic; greedy needs only the first two):
-//   rows    -- every verified target row streamed once: a warp per 1024-token
-//              chunk, 16-byte loads, the chunk's exact sum of
-//              2^(t*log2e/T - ref) (greedy: the chunk's argmax)
-//   decide  -- per request: row normalisers, p_lse, the sequential accept test
-//              u < p(x)/q(x), n_acc, the accepted tokens and the final-draw setup
-//   bias    -- Markov bias of each rejected position (tensor cores when the
-//              shapes allow, else CUDA cores)
-//   final   -- a warp per (request, 256-token tile): exact fixed-point sums of
-//              the residual max(0, p - q) and of p, both normalised
-//   pick    -- per request: inverse CDF over the tiles, then inside the tile by
-//              recomputing it with the same warp routine, compared with u*total
-//              in exact integer arithmetic
+// Launches on the bf16 tensor-core path (the common case):
+//   rows   -- verify_rows_tma_kernel: every verified target row streamed once
+//             (4096-token items, 2 KiB bulk copies through a per-warp ring),
+//             each item's exact fixed-point sum of 2^(t*log2e/T - ref) (greedy:
+//             its argmax); the block that completes a request's last item then
+//             runs that request's decide: row normalisers, p_lse, the accept
+//             tests u < p(x)/q(x) in order, n_acc, the accepted tokens and the
+//             final draw's state
+//   final  -- final_tc_kernel (draft_tc.cu): the rejected position's bias on
+//             the tensor cores and, per 128-token half tile, the exact sums of
+//             p and of max(0, p - q), both normalised
+//   pick   -- per request: inverse CDF over the half tiles, then inside the
+//             chosen one by recomputing it with the same arithmetic, compared
+//             with u*total in exact integer arithmetic
+// Other shapes (fp32, R > 1024, unaligned rows) use plain-load rows, a
+// separate decide kernel and the CUDA-core bias / final / pick kernels.
+// Greedy verification needs only the rows and the decide.
 #include "common.cuh"
 #include "f32x2.cuh"
 #include "finish.cuh"
