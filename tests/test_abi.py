@@ -47,6 +47,18 @@ def test_workspace_bytes(lib):
     assert lib.workspace_bytes(4, 4, 1024, 0) == 0
 
 
+def test_workspace_grows_with_the_batch_and_caps_the_fused_scratch(lib):
+    """The fused head and scheduler keep 32 lane partials, a Theta key and a
+    prefix per candidate for at most 8192 candidates (larger batches take the
+    separate launches): doubling gamma below the cap adds that scratch, above
+    it only the per-candidate arrays every path needs."""
+    R, V, r = 512, 4096, 64
+    w8, w16, w32 = (lib.workspace_bytes(R, g, V, r) for g in (8, 16, 32))
+    fused_scratch = 4096 * (32 * 4 + 16)  # the 4096 candidates gamma 8 -> 16 adds
+    assert w16 - w8 > fused_scratch
+    assert w32 - w16 < fused_scratch  # 8192 -> 16384 candidates: capped
+
+
 def _null():
     return ctypes.c_void_p(None)
 
