@@ -313,7 +313,7 @@ int dspark_confidence(int R, int gamma, int d, int r, int V, const void* hidden,
 int dspark_schedule(int R, int gamma, const float* a, const float* sps, int n_sps, int early_stop,
                     int max_B, int32_t* ell, int32_t* row_off, int32_t* B_out, double* E_out,
                     void* ws, size_t ws_bytes, void* stream) {
-  SchedArgs s;
+  SchedArgs s{};
   int st = sched_args(R, gamma, a, sps, n_sps, early_stop, max_B, ell, row_off, B_out, E_out, ws,
                       ws_bytes, s);
   if (st) return st;
@@ -332,7 +332,7 @@ int dspark_draft_schedule(int R, int gamma, int V, int r, float temperature, con
                           double* E_out, void* ws, size_t ws_bytes, void* stream) {
   DraftArgs da;
   ConfArgs ca;
-  SchedArgs sa;
+  SchedArgs sa{};
   int s = draft_args(R, gamma, V, r, temperature, z, E, Wt, dt, anchor, u_draft, tokens, q_lse,
                      q_tok, ws, ws_bytes, da);
   if (s) return s;

@@ -227,6 +227,19 @@ void trace_begin(int kind, cudaStream_t st);
 void set_error_text(const char* msg);  // the text dspark_last_error() returns
 void trace_end(int kind, cudaStream_t st);
 
+// Launch set-up that belongs to a device, not to the process (launch_state.cu).
+// Each is resolved on the calling thread's current device, once per device,
+// under a lock, so a process that drives several GPUs or calls from several
+// host threads sets every device up itself.
+int sm_count();  // multiprocessors of the current device
+// Raises `func`'s dynamic shared-memory limit on the current device to at
+// least `bytes` (cudaFuncSetAttribute is per device).
+cudaError_t ensure_smem_attr(const void* func, int bytes);
+// Resident blocks of `func` per multiprocessor of the current device at
+// `threads` threads and `dyn_smem` bytes of dynamic shared memory, cached per
+// (device, func, threads, dyn_smem); 0 if the query fails.
+int blocks_per_sm(const void* func, int threads, size_t dyn_smem);
+
 // Every kernel launch: counted, and bracketed by trace events when tracing.
 #define DSPARK_LAUNCH(kind, st, ...)   \
   do {                                 \

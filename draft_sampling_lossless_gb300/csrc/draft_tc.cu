@@ -1467,26 +1467,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
 }
 
+// The driver's tensor-map encoder (a process-wide entry point, the same for
+// every device); resolved once, thread-safely, by the static's initialiser.
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() {
     void* f = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    return (PFN_cuTensorMapEncodeTiled_v12000) nullptr;
+  }();
   return fn;
-}
-
-int sm_count() {
-  static int n[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return 148;
-  if (n[dev] == 0) cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev);
-  return n[dev] > 0 ? n[dev] : 148;
 }
 
 cudaError_t encode_w(CUtensorMap* m, const void* Wt, int V, int r) {
@@ -1533,14 +1526,9 @@ cudaError_t encode_stage(CUtensorMap* m, const void* stage, int R, int r, int bo
 template <bool kBiasOut>
 cudaError_t launch_tc(const CUtensorMap& tm_w, const CUtensorMap& tm_z, const TcParams& p,
                       cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(draft_fused_tc_kernel<kBiasOut>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)tc_smem_bytes(4));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = ensure_smem_attr((const void*)draft_fused_tc_kernel<kBiasOut>,
+                                   (int)tc_smem_bytes(4));
+  if (e != cudaSuccess) return e;
   const int n_rt = (p.R + BM - 1) / BM;
   int gx = sm_count() / n_rt;
   if (gx < 1) gx = 1;
@@ -1642,18 +1630,11 @@ cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st) {
                                   (size_t)persist_z_slots(pair) * kZBytes)
     pp.fuse = 0;
   if (pp.fuse) pp.f = *a.fuse;
-  static bool attr_set = false;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(draft_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)tc_smem_bytes(4));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  e = ensure_smem_attr((const void*)draft_persistent_kernel, (int)tc_smem_bytes(4));
+  if (e != cudaSuccess) return e;
   const size_t smem = persist_smem_bytes(p.nK, pair);
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, draft_persistent_kernel, kThreads,
-                                                    smem);
-  if (e != cudaSuccess || per_sm < 1) return cudaErrorNotSupported;
+  if (blocks_per_sm((const void*)draft_persistent_kernel, kThreads, smem) < 1)
+    return cudaErrorNotSupported;
   const int n_rt = (a.R + BM - 1) / BM;
   const int n_units = pair ? (p.n_vt + 1) / 2 : p.n_vt;
   int gx = sm_count() / n_rt;
@@ -1748,13 +1729,8 @@ cudaError_t launch_final_tc(const VerifyArgs& a, const VerifyState* vstate, long
   p.fin_part = fin_part;
   p.status = a.status;
   p.pair = a.R <= 64 ? 1 : 0;
-  static bool attr_set = false;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(final_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)final_smem_bytes(4, 1));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  e = ensure_smem_attr((const void*)final_tc_kernel, (int)final_smem_bytes(4, 1));
+  if (e != cudaSuccess) return e;
   const int n_rt = (a.R + BM - 1) / BM;
   const int n_units = p.pair ? (p.n_vt + 1) / 2 : p.n_vt;
   int gx = sm_count() / n_rt;

@@ -113,7 +113,7 @@ int dspark_schedule_noalloc(int R, int gamma, const float* a, const float* sps, 
     set_error_text(g_msg);
     return DSPARK_ERR_CUDA;
   }
-  SchedArgs s;
+  SchedArgs s{};
   s.R = R;
   s.gamma = gamma;
   s.n_sps = n_sps;

@@ -1040,15 +1040,9 @@ __global__ void __launch_bounds__(256) final_pick_tc_kernel(
 // strides over the items), at most one warp per item.
 template <typename K>
 int row_grid(K kernel, long long items, size_t dyn_smem) {
-  int per_sm = 0, dev = 0, n_sm = 0;
-  cudaGetDevice(&dev);
-  if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1)
-    n_sm = 148;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, dyn_smem) !=
-          cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
-  const long long resident = (long long)per_sm * n_sm;
+  int per_sm = blocks_per_sm((const void*)kernel, 256, dyn_smem);
+  if (per_sm < 1) per_sm = 1;
+  const long long resident = (long long)per_sm * sm_count();
   const long long blocks = (items + 7) / 8;
   return (int)(blocks < resident ? (blocks < 1 ? 1 : blocks) : resident);
 }
@@ -1068,23 +1062,13 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t st) {
   const DecideOut dec{staged && a.vcnt != nullptr ? 1 : 0, a.anchor, a.tokens, a.q_lse, a.q_tok,
                       a.u_acc, a.p_lse, a.n_acc, a.out_tokens, a.vstate, a.prev, a.vcnt};
   if (staged) {
-    // the attribute once per process (for the largest list); the resident
-    // grid whenever the list size changes
-    static bool attr = false;
-    static size_t grid_dyn = 0;
-    static int grid = 0;
+    // the opt-in for the largest list, once per device; the resident grid
+    // for this list size (cached per device and size)
     const size_t dyn = rows_tma_smem(a.R);
-    if (!attr) {
-      cudaError_t e = cudaFuncSetAttribute(verify_rows_tma_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)rows_tma_smem(kRowsSmem));
-      if (e != cudaSuccess) return e;
-      attr = true;
-    }
-    if (grid_dyn != dyn) {
-      grid = row_grid(verify_rows_tma_kernel, 1ll << 40, dyn);
-      grid_dyn = dyn;
-    }
+    cudaError_t ea = ensure_smem_attr((const void*)verify_rows_tma_kernel,
+                                      (int)rows_tma_smem(kRowsSmem));
+    if (ea != cudaSuccess) return ea;
+    const int grid = row_grid(verify_rows_tma_kernel, 1ll << 40, dyn);
     const int g = (int)(grid < (items + 7) / 8 ? grid : (items + 7) / 8);
     DSPARK_LAUNCH(kKindVerifyRows, st,
                   launch_pdl(verify_rows_tma_kernel, dim3(g), dim3(256), dyn, st, a.R,
