@@ -32,14 +32,14 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from draft_sampling_lossless_gb300 import synth  # noqa: E402
+from draft_sampling_lossless_gb300 import synth, target_model  # noqa: E402
 
 METRIC = "draft+verify positions/s"
 UNIT = "positions/s"
 L2_FLUSH_BYTES = 512 << 20
 
-# Algorithmic bytes per launch of each kernel (what the method must move; see
-# the design notes), as functions of the workload and the scheduled batch B.
+# Algorithmic bytes per launch of each kernel (what the method must move), as
+# functions of the workload and the scheduled batch B.
 def algorithmic_bytes(kind, wl, B, n_rej):
     e = 2 if wl.dtype == "bf16" else 4
     R, V, r = wl.R, wl.V, wl.r
@@ -182,7 +182,7 @@ def run_ours(args, wl, world, rank, local):
     torch.cuda.synchronize()
     Bn = int(step.B.item())
     ell = step.ell.cpu().numpy()
-    dense = synth.make_target(inp, tokens=step.tokens)
+    dense = target_model.target_logits(inp, step.tokens)
     rows = np.concatenate([r * (wl.gamma + 1) + np.arange(ell[r] + 1) for r in range(wl.R)])
     target = dense.reshape(-1, wl.V)[torch.from_numpy(rows).to(dev)].contiguous()
     del dense
@@ -439,7 +439,7 @@ def oracle_step(wl, inp, reqs):
 def cpu_inputs(wl):
     inp = synth.make_inputs(wl, device="cpu")
     tok = torch.zeros((wl.R, wl.gamma), dtype=torch.int32)
-    inp.extra["target"] = synth.make_target(inp, tokens=tok)
+    inp.extra["target"] = target_model.target_logits(inp, tok)
     return inp
 
 

@@ -7,16 +7,13 @@ oracle consume what it produces, and random numbers the method itself draws
 (the draft, acceptance and final uniforms) are produced here and passed in as
 inputs.
 
-Readings of the workload descriptions (all stated again in the design notes):
+Readings of the workload descriptions:
 
 * ``N(mu, s)`` is a normal with standard deviation ``s``.
-* Target logits are correlated with the *base* draft logits ``z`` of the same
-  position (``alpha * z + N(0, noise)``); the Markov bias is left out of the
-  target recipe so that this generator needs no part of the method.  The bonus
-  row (the position after the last draft token) uses a fresh ``z'``.
-* Greedy workload: the target row is a copy of ``z`` in which one token is
-  raised to ``rowmax + 1``; with probability 0.8 that token is the drafted one,
-  otherwise a uniformly chosen other token.
+* The target logits themselves are formed by the target-model stand-in
+  (``target_model.py``) from the draws made here (``target_draws``): the
+  correlation ``alpha``, the noise, the fresh bonus-row logits ``z'`` and,
+  for the greedy workload, which token each row plants.
 * Uniforms are 24-bit: ``k * 2**-24`` with ``k`` uniform in ``[0, 2**24)``.
 * Hidden states are ``N(0, 1)``; confidence weights ``N(0, 0.05)`` for every
   workload (the tiny workload's stated value carried to the others).
@@ -191,58 +188,51 @@ def make_inputs(wl: Workload, device="cpu", seed: int | None = None) -> Inputs:
                   sts_temperatures(wl).to(device), c_in, sps_table(wl).to(device))
 
 
-def make_target(inp: Inputs, tokens: torch.Tensor | None = None, seed: int | None = None,
-                rows=None) -> torch.Tensor:
-    """Dense target logits [R, gamma+1, V]: row j is the target distribution for
-    draft position j+1 (row gamma is the bonus row).
+@dataclass
+class TargetDraws:
+    """Random draws of the target-model stand-in (no arithmetic of the
+    method): per-request correlation alpha and noise scale, the fresh bonus
+    row z', and for the greedy workload which token each row plants."""
+    alpha: torch.Tensor  # [R] f32
+    noise_std: torch.Tensor  # [R] f32
+    z_bonus: torch.Tensor  # [R, 1, V] in the workload's dtype
+    keep: torch.Tensor | None  # [R, gamma] bool: plant the drafted token (greedy)
+    other: torch.Tensor | None  # [R, gamma] int64 in [0, V-1): offset of the other token
+    seed: int
+    chunk: int = 16
 
-    ``tokens`` ([R, gamma] int32, the drafted tokens) is needed only by the
-    greedy workload, whose planted argmax follows the drafted token with
-    probability 0.8.
-    """
+    def noise_chunks(self, wl: Workload, device):
+        """N(0, 1) fp32 noise [r1 - r0, gamma + 1, V] for consecutive chunks
+        of requests, always drawn in the same order from one stream."""
+        g = _gen(self.seed, "tnoise", device)
+        for r0 in range(0, wl.R, self.chunk):
+            r1 = min(wl.R, r0 + self.chunk)
+            yield r0, r1, torch.randn((r1 - r0, wl.gamma + 1, wl.V), generator=g, device=device,
+                                      dtype=torch.float32)
+
+
+def target_draws(inp: Inputs, seed: int | None = None) -> TargetDraws:
     wl = inp.wl
     s = wl.seed if seed is None else seed
     dev = inp.z.device
     R, G, V = wl.R, wl.gamma, wl.V
-    dt = wl.torch_dtype
-    zb = _normal((R, 1, V), wl.z_std, dt, s, "zbonus", dev)
-    if wl.target == "mix":
-        if isinstance(wl.alpha, tuple):
-            ga = _gen(s, "alpha", dev)
-            lo, hi = wl.alpha
-            alpha = lo + (hi - lo) * torch.rand((R,), generator=ga, device=dev, dtype=torch.float32)
-        else:
-            alpha = torch.full((R,), float(wl.alpha), device=dev, dtype=torch.float32)
-        out = torch.empty((R, G + 1, V), dtype=dt, device=dev)
-        g = _gen(s, "tnoise", dev)
-        for r0 in range(0, R, 16):
-            r1 = min(R, r0 + 16)
-            a = alpha[r0:r1].view(-1, 1, 1)
-            if wl.noise_std is None:
-                nstd = torch.sqrt(1.0 - a * a) * wl.z_std
-            else:
-                nstd = torch.full_like(a, float(wl.noise_std))
-            base = torch.cat([inp.z[r0:r1].float(), zb[r0:r1].float()], dim=1)
-            noise = torch.randn(base.shape, generator=g, device=dev, dtype=torch.float32)
-            out[r0:r1] = (a * base + nstd * noise).to(dt)
-        return out
+    zb = _normal((R, 1, V), wl.z_std, wl.torch_dtype, s, "zbonus", dev)
+    if isinstance(wl.alpha, tuple):
+        lo, hi = wl.alpha
+        alpha = lo + (hi - lo) * torch.rand((R,), generator=_gen(s, "alpha", dev), device=dev,
+                                            dtype=torch.float32)
+    else:
+        alpha = torch.full((R,), float(wl.alpha), device=dev, dtype=torch.float32)
+    if wl.noise_std is None:
+        nstd = torch.sqrt(1.0 - alpha * alpha) * wl.z_std
+    else:
+        nstd = torch.full_like(alpha, float(wl.noise_std))
+    keep = other = None
     if wl.target == "greedy":
-        if tokens is None:
-            raise ValueError("greedy target needs the drafted tokens")
-        out = torch.cat([inp.z, zb], dim=1).clone()
-        gp = _gen(s, "gpick", dev)
-        go = _gen(s, "gother", dev)
-        keep = torch.rand((R, G), generator=gp, device=dev) < 0.8
-        other = torch.randint(0, V - 1, (R, G), generator=go, device=dev, dtype=torch.int64)
-        tok = tokens.to(dev).long()
-        other = (tok + 1 + other) % V
-        pick = torch.where(keep, tok, other)
-        rowmax = out[:, :G, :].float().amax(dim=-1)
-        ridx = torch.arange(R, device=dev).view(-1, 1).expand(R, G)
-        jidx = torch.arange(G, device=dev).view(1, -1).expand(R, G)
-        out[ridx, jidx, pick] = (rowmax + 1.0).to(dt)
-        return out
-    raise ValueError(wl.target)
+        keep = torch.rand((R, G), generator=_gen(s, "gpick", dev), device=dev) < 0.8
+        other = torch.randint(0, V - 1, (R, G), generator=_gen(s, "gother", dev), device=dev,
+                              dtype=torch.int64)
+    return TargetDraws(alpha, nstd, zb, keep, other, s)
 
 
 def to_f64(t: torch.Tensor | None) -> np.ndarray | None:

@@ -23,7 +23,7 @@ import numpy as np
 import torch
 
 import oracle
-from draft_sampling_lossless_gb300 import synth
+from draft_sampling_lossless_gb300 import synth, target_model
 from draft_sampling_lossless_gb300.pipeline import DSparkStep
 
 REL = 1e-5
@@ -192,8 +192,7 @@ class Case:
         wl, g = self.wl, self.g
         R, G, V = wl.R, wl.gamma, wl.V
         tok_full = self.oracle_tokens_full()
-        dense = synth.make_target(self.inp, tokens=torch.from_numpy(tok_full).to(torch.int32),
-                                  seed=self.seed)
+        dense = target_model.target_logits(self.inp, torch.from_numpy(tok_full), seed=self.seed)
         ell = np.zeros(R, dtype=np.int64)
         ell[self.sample] = ell_s
         row_off = np.concatenate([[0], np.cumsum(1 + ell)])

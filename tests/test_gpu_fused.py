@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 import torch
 
-from draft_sampling_lossless_gb300 import synth
+from draft_sampling_lossless_gb300 import synth, target_model
 from draft_sampling_lossless_gb300.pipeline import DSparkStep
 
 from test_gpu_parity import SMALL
@@ -136,7 +136,7 @@ def test_row_pass_decide_flags_bad_length_and_leaves_counters_zero():
     counts = (1 + ell_ok).to(torch.int64)
     row_off = torch.zeros(R + 1, dtype=torch.int32, device="cuda")
     row_off[1:] = torch.cumsum(counts, 0).to(torch.int32)
-    dense = synth.make_target(inp, tokens=src.tokens).reshape(R, G + 1, wl.V)
+    dense = target_model.target_logits(inp, src.tokens).reshape(R, G + 1, wl.V)
     rows = torch.cat([r * (G + 1) + torch.arange(int(counts[r]), device="cuda") for r in range(R)])
     target = dense.reshape(-1, wl.V)[rows].contiguous()
     ref = _verify_with(wl, g, src, ell_ok, row_off, target)

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from draft_sampling_lossless_gb300 import synth
+from draft_sampling_lossless_gb300 import synth, target_model
 from parity import Case, Stats
 
 W = synth.WORKLOADS
@@ -164,7 +164,7 @@ def test_chained_pipeline_tiny_matches_oracle_chain():
     Bn = int(s.B.item())
     tok = s.tokens.clone()
     # target built from the GPU's own tokens (a harness input, not an oracle input)
-    dense = synth.make_target(c.inp, tokens=tok.cpu())
+    dense = target_model.target_logits(c.inp, tok.cpu())
     ell = s.ell.cpu().numpy()
     rows = np.concatenate([r * (wl.gamma + 1) + np.arange(ell[r] + 1) for r in range(wl.R)])
     packed = dense.reshape(-1, wl.V)[torch.from_numpy(rows)].contiguous().cuda()
@@ -179,7 +179,7 @@ def test_chained_pipeline_tiny_matches_oracle_chain():
     assert np.allclose(s.a.cpu().numpy(), a_o, rtol=1e-5, atol=0)
     sched = oracle.schedule(a_o.astype(np.float32).astype(np.float64), c.sps64, True)
     assert np.array_equal(sched["ell"], ell)
-    dense_o = synth.make_target(c.inp, tokens=torch.from_numpy(t_o).to(torch.int32))
+    dense_o = target_model.target_logits(c.inp, torch.from_numpy(t_o))
     tgt = synth.to_f64(dense_o.reshape(-1, wl.V)[torch.from_numpy(rows)])
     o = oracle.verify(c.z64, c.E64, c.W64, c.anchor, t_o, wl.T, sched["ell"], sched["row_off"],
                       tgt, c.u_acc, c.u_fin)
