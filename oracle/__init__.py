@@ -1,5 +1,8 @@
-"""CPU oracle (test infrastructure only; see dspark_oracle.py)."""
+"""CPU oracles (TEST INFRASTRUCTURE ONLY): the numpy restatement in
+dspark_oracle.py (its functions are re-exported here) and the plain C++ one
+in dspark_oracle.cpp behind the same API in ``oracle.native``."""
 
+from . import native  # noqa: F401
 from .dspark_oracle import (  # noqa: F401
     confidence,
     draft_distribution,
@@ -9,6 +12,7 @@ from .dspark_oracle import (  # noqa: F401
     inverse_cdf,
     markov_bias,
     schedule,
+    schedule_capacity,
     softmax_rows,
     to_fixed,
     verify,

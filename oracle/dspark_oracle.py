@@ -28,7 +28,7 @@ Sources (page title, then section):
   probability sum_x min(p, q), failure mass sum_x max(0, p - q), and the
   emitted marginal equal to p.
 
-Readings where the pages are silent (each repeated in the design notes):
+Readings where the pages are silent:
 
 * x_0 is the anchor token, so the Markov bias is applied from the first
   draft position on; an anchor of -1 switches the first-position bias off.
@@ -45,6 +45,10 @@ Readings where the pages are silent (each repeated in the design notes):
   of 2^-40 and summed as an integer so that the sum does not depend on the
   order of additions.  Early stop adds candidate i+1 only while
   Theta_{i+1} > Theta_i; global mode takes the first argmax.
+* Capacity scheduling: a capacity K fixed before the step (the batch the
+  global search chose on the survival values two steps earlier) is filled
+  with the first min(max(K - R, 0), R * gamma) candidates of the current
+  order.
 * Verification: accept draft position j iff u_acc < p_j(x_j) / q_j(x_j)
   (strict); on the first rejection sample max(0, p - q) normalised with the
   request's final uniform, or p itself if that mass is zero; if every
@@ -228,6 +232,26 @@ def schedule(a, sps, early_stop=True, max_B=0):
     E = float(R) + float(S[i_star]) * 2.0 ** -FIX_SHIFT
     return dict(ell=ell, row_off=row_off, B=int(R + i_star), E=E, i_star=int(i_star),
                 theta=theta, order=order)
+
+
+def schedule_capacity(a, K):
+    """Capacity scheduling (news article, challenge 2): the verification
+    capacity K (a batch size fixed before this step, e.g. the batch the global
+    search chose on the survival values two steps earlier) is filled with the
+    current candidates in the current order, so the batch is exactly the first
+    i = min(max(K - R, 0), R * gamma) candidates.  Returns dict(ell, row_off,
+    B, E, i_star)."""
+    a = np.asarray(a, dtype=np.float64)
+    R, G = a.shape
+    N = R * G
+    rr, jj = np.meshgrid(np.arange(R), np.arange(G), indexing="ij")
+    order = np.lexsort((jj.ravel(), rr.ravel(), -a.ravel()))
+    i = int(max(0, min(N, int(K) - R)))
+    S = int(np.sum(to_fixed(a.ravel()[order[:i]])))
+    ell = np.bincount(rr.ravel()[order[:i]], minlength=R).astype(np.int64)
+    row_off = np.concatenate([[0], np.cumsum(1 + ell)]).astype(np.int64)
+    E = float(R) + float(S) * 2.0 ** -FIX_SHIFT
+    return dict(ell=ell, row_off=row_off, B=int(R + i), E=E, i_star=i)
 
 
 # --------------------------------------------------------------------------

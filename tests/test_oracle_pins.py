@@ -11,9 +11,20 @@ import os
 import numpy as np
 import pytest
 
-import oracle
+import oracle  # noqa: F401
+import oracle.dspark_oracle as numpy_oracle
+from oracle import native as cpp_oracle
 
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(params=["numpy", "cpp"], scope="module")
+def orc(request):
+    """Both oracles: the numpy restatement and the plain C++ one."""
+    if request.param == "cpp":
+        cpp_oracle.build()
+        return cpp_oracle
+    return numpy_oracle
 
 
 def gold(name):
@@ -27,35 +38,35 @@ def uni24(rng, shape):
 
 # ---------------------------------------------------------------- Markov head
 
-def test_markov_two_token_toy():
+def test_markov_two_token_toy(orc):
     g = gold("markov_two_token.json")
     # V = 2, rank 1: E[A] = 1, W = (ln 9, 0): the previous token A adds ln 9 to A.
     E = np.array([[1.0], [0.0]])
     W = np.array([[math.log(9.0), 0.0]])
     z = np.array(g["base_logits"]).reshape(1, 1, 2)
-    q = oracle.draft_distribution(z[:, 0, :], E, W, np.array([0]), 1.0)[0]
+    q = orc.draft_distribution(z[:, 0, :], E, W, np.array([0]), 1.0)[0]
     assert np.allclose(q, g["q_after"], atol=1e-12, rtol=0)
-    q0 = oracle.draft_distribution(z[:, 0, :], E, W, np.array([-1]), 1.0)[0]
+    q0 = orc.draft_distribution(z[:, 0, :], E, W, np.array([-1]), 1.0)[0]
     assert np.allclose(q0, g["q_before"], atol=1e-15, rtol=0)
     # The sampled token, its probability and the normaliser: closed forms.
     for u, want in [(0.0, 0), (0.8999, 0), (0.9, 1), (0.99, 1)]:
-        tok, lse, qt = oracle.draft_sample(z, E, W, np.array([0]), np.array([[u]]), 1.0)
+        tok, lse, qt = orc.draft_sample(z, E, W, np.array([0]), np.array([[u]]), 1.0)
         assert tok[0, 0] == want
         assert abs(lse[0, 0] - math.log(10.0)) < 1e-12  # ln(e^{ln 9} + e^0)
         assert abs(qt[0, 0] - (0.9 if want == 0 else 0.1)) < 1e-12
 
 
-def test_temperature_scales_logit_plus_bias():
+def test_temperature_scales_logit_plus_bias(orc):
     E = np.array([[1.0], [0.0]])
     W = np.array([[math.log(9.0), 0.0]])
     z = np.zeros((1, 2))
     for T in (0.5, 0.7, 2.0):
-        q = oracle.draft_distribution(z, E, W, np.array([0]), T)[0]
+        q = orc.draft_distribution(z, E, W, np.array([0]), T)[0]
         k = 9.0 ** (1.0 / T)
         assert abs(q[0] - k / (k + 1.0)) < 1e-12
 
 
-def test_draft_feeds_previous_token_left_to_right():
+def test_draft_feeds_previous_token_left_to_right(orc):
     # One-hot embedding (non-symmetric permutation) and a transition that
     # strongly favours perm[prev]; base logits zero.  The draft must follow
     # the chain anchor -> perm[anchor] -> perm[perm[anchor]] ...
@@ -69,7 +80,7 @@ def test_draft_feeds_previous_token_left_to_right():
     G = 5
     z = np.zeros((2, G, V))
     u = np.full((2, G), 0.5)
-    tok, _, qt = oracle.draft_sample(z, E, W, np.array([1, 4]), u, 1.0)
+    tok, _, qt = orc.draft_sample(z, E, W, np.array([1, 4]), u, 1.0)
     for r, a0 in enumerate([1, 4]):
         x = a0
         for k in range(G):
@@ -78,40 +89,40 @@ def test_draft_feeds_previous_token_left_to_right():
     assert np.all(qt > 1 - 1e-12)
 
 
-def test_anchor_minus_one_disables_first_bias():
+def test_anchor_minus_one_disables_first_bias(orc):
     E = np.array([[1.0], [0.0]])
     W = np.array([[-50.0, 0.0]])
     z = np.array([[[2.0, 0.0]]])
     # with the anchor bias token 0 would be all but impossible
-    tok_b, _, _ = oracle.draft_sample(z, E, W, np.array([0]), np.array([[0.5]]), 1.0)
-    tok_n, _, _ = oracle.draft_sample(z, E, W, np.array([-1]), np.array([[0.5]]), 1.0)
+    tok_b, _, _ = orc.draft_sample(z, E, W, np.array([0]), np.array([[0.5]]), 1.0)
+    tok_n, _, _ = orc.draft_sample(z, E, W, np.array([-1]), np.array([[0.5]]), 1.0)
     assert tok_b[0, 0] == 1 and tok_n[0, 0] == 0
 
 
-def test_greedy_draft_lowest_index_on_ties():
+def test_greedy_draft_lowest_index_on_ties(orc):
     z = np.array([[[1.0, 3.0, 3.0, 2.0], [5.0, 5.0, 0.0, 5.0]]])
     E = np.zeros((4, 1))
     W = np.zeros((1, 4))
-    tok, lse, qt = oracle.draft_sample(z, E, W, np.array([0]), np.zeros((1, 2)), 0.0)
+    tok, lse, qt = orc.draft_sample(z, E, W, np.array([0]), np.zeros((1, 2)), 0.0)
     assert tok.tolist() == [[1, 0]]
     assert lse.tolist() == [[3.0, 5.0]] and qt.tolist() == [[1.0, 1.0]]
 
 
 # ---------------------------------------------------------------- inverse CDF
 
-def test_inverse_cdf_boundary_reading():
+def test_inverse_cdf_boundary_reading(orc):
     w = np.array([[1.0, 1.0, 1.0, 1.0]])
     # smallest v with C_v > u * S: at u*S exactly on a boundary, the next token
-    assert oracle.inverse_cdf(w, np.array([0.25]))[0] == 1
-    assert oracle.inverse_cdf(w, np.array([0.25 - 2 ** -24]))[0] == 0
-    assert oracle.inverse_cdf(w, np.array([0.0]))[0] == 0
+    assert orc.inverse_cdf(w, np.array([0.25]))[0] == 1
+    assert orc.inverse_cdf(w, np.array([0.25 - 2 ** -24]))[0] == 0
+    assert orc.inverse_cdf(w, np.array([0.0]))[0] == 0
     # zero-weight tokens are never drawn
     w2 = np.array([[0.0, 2.0, 0.0, 0.0, 2.0, 0.0]])
-    got = [oracle.inverse_cdf(w2, np.array([u]))[0] for u in (0.0, 0.49, 0.5, 0.99)]
+    got = [orc.inverse_cdf(w2, np.array([u]))[0] for u in (0.0, 0.49, 0.5, 0.99)]
     assert got == [1, 1, 4, 4]
 
 
-def test_inverse_cdf_brute_force_small_vocab():
+def test_inverse_cdf_brute_force_small_vocab(orc):
     rng = np.random.default_rng(7)
     for V in range(1, 9):
         for _ in range(20):
@@ -128,14 +139,14 @@ def test_inverse_cdf_brute_force_small_vocab():
                     if cum > u * S:
                         want = v
                         break
-                assert oracle.inverse_cdf(w[None, :], np.array([u]))[0] == want
+                assert orc.inverse_cdf(w[None, :], np.array([u]))[0] == want
 
 
-def test_softmax_two_token_closed_form():
+def test_softmax_two_token_closed_form(orc):
     rng = np.random.default_rng(3)
     for _ in range(50):
         a, b = rng.normal(0, 5, size=2)
-        e, lse = oracle.softmax_rows(np.array([[a, b]]))
+        e, lse = orc.softmax_rows(np.array([[a, b]]))
         want_lse = max(a, b) + math.log1p(math.exp(-abs(a - b)))
         assert abs(lse[0] - want_lse) < 1e-12
         p0 = math.exp(a - lse[0])
@@ -144,7 +155,7 @@ def test_softmax_two_token_closed_form():
 
 # ---------------------------------------------------------------- confidence
 
-def test_confidence_closed_forms_and_indexing():
+def test_confidence_closed_forms_and_indexing(orc):
     # d = 1, rank 1.  Feature vector [h_k ; E1[x_{k-1}]].
     R, G, d, V = 1, 3, 1, 4
     h = np.array([[[1.0], [0.0], [0.0]]])
@@ -153,31 +164,31 @@ def test_confidence_closed_forms_and_indexing():
     anchor = np.array([0])  # E1[0] = 0
     tokens = np.array([[1, 3, 2]])  # x_1 = 1 (E1 = 1), x_2 = 3 (E1 = 2)
     t = np.array([1.0, 1.0, 2.0])
-    c, a = oracle.confidence(h, w, E1, anchor, tokens, t)
+    c, a = orc.confidence(h, w, E1, anchor, tokens, t)
     # k=1: s = ln3 -> 0.75 ; k=2: s = -ln3 (E1[x_1]=1) -> 0.25 ;
     # k=3: s = -2 ln3 (E1[x_2]=2), t=2 -> sigmoid(-ln3) = 0.25
     assert np.allclose(c[0], [0.75, 0.25, 0.25], atol=1e-15)
     assert np.allclose(a[0], [0.75, 0.1875, 0.046875], atol=1e-15)
 
 
-def test_survival_chain_page_values():
+def test_survival_chain_page_values(orc):
     g = gold("survival_chain.json")
     for case in g["cases"]:
         c = np.array([[case["c1"]] + g["conditionals_after_first"]])
-        _, a = oracle.confidence(None, None, None, None, None, None, c_in=c)
+        _, a = orc.confidence(None, None, None, None, None, None, c_in=c)
         assert np.allclose(a[0], case["a"], rtol=1e-14, atol=0)
     g = gold("tutorial_worked_example.json")
-    _, a = oracle.confidence(None, None, None, None, None, None,
+    _, a = orc.confidence(None, None, None, None, None, None,
                              c_in=np.array([g["confidences"]]))
     assert np.allclose(a[0], g["survival_products"], rtol=1e-14, atol=0)
 
 
-def test_survival_never_increases():
+def test_survival_never_increases(orc):
     rng = np.random.default_rng(11)
     c = rng.uniform(0, 1, size=(64, 16))
     c[:, 3] = 1.0  # c rounding to one
     c[5, :] = 1.0
-    _, a = oracle.confidence(None, None, None, None, None, None, c_in=c)
+    _, a = orc.confidence(None, None, None, None, None, None, c_in=c)
     assert np.all(np.diff(a, axis=1) <= 0)
     assert np.all(a[5] == 1.0)
 
@@ -196,7 +207,7 @@ def brute_force_best(a, sps):
     Theta(l) = (R + sum of the first l_r survival values of each request)
     * SPS[R + sum l].  Sums in the same 2^-40 integer units."""
     R, G = a.shape
-    fx = oracle.to_fixed(a)
+    fx = np.rint(np.asarray(a) * 2.0 ** 40).astype(np.int64)
     best, arg = None, []
     for ell in itertools.product(range(G + 1), repeat=R):
         s = sum(int(fx[r, :l].sum()) for r, l in enumerate(ell))
@@ -219,7 +230,7 @@ def unimodal(theta):
 
 
 @pytest.mark.parametrize("R,G", [(1, 4), (2, 3), (3, 2), (2, 4), (3, 3)])
-def test_scheduler_brute_force(R, G):
+def test_scheduler_brute_force(orc, R, G):
     rng = np.random.default_rng(100 * R + G)
     n_uni = 0
     for trial in range(40):
@@ -229,11 +240,11 @@ def test_scheduler_brute_force(R, G):
         else:
             sps = rng.uniform(1.0, 100.0, size=R * (G + 1) + 1)
         best, args = brute_force_best(a, sps)
-        glob = oracle.schedule(a, sps, early_stop=False)
+        glob = orc.schedule(a, sps, early_stop=False)
         assert glob["theta"][glob["i_star"]] == best
         if len(args) == 1:
             assert tuple(glob["ell"].tolist()) == args[0]
-        es = oracle.schedule(a, sps, early_stop=True)
+        es = orc.schedule(a, sps, early_stop=True)
         if unimodal(es["theta"]):
             n_uni += 1
             assert es["theta"][es["i_star"]] == best
@@ -247,72 +258,72 @@ def test_scheduler_brute_force(R, G):
     assert n_uni > 0
 
 
-def test_scheduler_early_stop_differs_on_sawtooth():
+def test_scheduler_early_stop_differs_on_sawtooth(orc):
     # One request, four candidates of 0.9.  SPS dips at B = 2 then recovers:
     # early stop keeps nothing, global search keeps all four.
     a = np.array([[0.9, 0.81, 0.729, 0.6561]], dtype=np.float32).astype(np.float64)
     sps = np.array([0.0, 100.0, 40.0, 60.0, 70.0, 80.0])
-    es = oracle.schedule(a, sps, early_stop=True)
-    gl = oracle.schedule(a, sps, early_stop=False)
+    es = orc.schedule(a, sps, early_stop=True)
+    gl = orc.schedule(a, sps, early_stop=False)
     assert es["ell"].tolist() == [0] and es["B"] == 1 and es["E"] == 1.0
     assert gl["ell"].tolist() == [4] and gl["B"] == 5
     assert abs(gl["E"] - (1.0 + a.sum())) < 1e-9
 
 
-def test_scheduler_plateau_stops():
+def test_scheduler_plateau_stops(orc):
     # Throughput that stays flat is not rising: stop (strict comparison).
     a = np.zeros((1, 3))
     sps = np.full(5, 10.0)
-    es = oracle.schedule(a, sps, early_stop=True)
+    es = orc.schedule(a, sps, early_stop=True)
     assert es["i_star"] == 0 and es["ell"].tolist() == [0]
 
 
-def test_scheduler_tie_order_request_then_position():
+def test_scheduler_tie_order_request_then_position(orc):
     a = np.full((3, 2), 0.5)
     sps = 1000.0 / (1.0 + 0.0 * np.arange(10))  # constant rate: only E matters
     for i_cap, want in [(1, [1, 0, 0]), (2, [2, 0, 0]), (3, [2, 1, 0]), (5, [2, 2, 1])]:
-        out = oracle.schedule(a, sps, early_stop=False, max_B=3 + i_cap)
+        out = orc.schedule(a, sps, early_stop=False, max_B=3 + i_cap)
         assert out["ell"].tolist() == want
         assert out["row_off"].tolist() == [0, 1 + want[0], 2 + want[0] + want[1],
                                             3 + sum(want)]
 
 
-def test_scheduler_sps_too_short_is_an_error():
+def test_scheduler_sps_too_short_is_an_error(orc):
     with pytest.raises(ValueError):
-        oracle.schedule(np.full((2, 2), 0.5), np.ones(6), early_stop=True)
+        orc.schedule(np.full((2, 2), 0.5), np.ones(6), early_stop=True)
 
 
-def test_fixed_point_rounds_half_to_even():
+def test_fixed_point_rounds_half_to_even(orc):
     u = 2.0 ** -40
-    assert oracle.to_fixed(np.array([0.5 * u, 1.5 * u, 2.5 * u, 1.0])).tolist() == \
+    assert orc.to_fixed(np.array([0.5 * u, 1.5 * u, 2.5 * u, 1.0])).tolist() == \
         [0, 2, 2, 1 << 40]
 
 
 # ---------------------------------------------------------------- verification
 
-def _two_token_step(q, p, n, rng):
+def _two_token_step(orc, q, p, n, rng):
     """n independent one-position steps with draft q and target p (V = 2)."""
     z = np.log(np.array(q)).reshape(1, 1, 2).repeat(n, axis=0)
     E = np.zeros((2, 1))
     W = np.zeros((1, 2))
     anchor = np.zeros(n, dtype=np.int64)
-    tok, _, _ = oracle.draft_sample(z, E, W, anchor, uni24(rng, (n, 1)), 1.0)
+    tok, _, _ = orc.draft_sample(z, E, W, anchor, uni24(rng, (n, 1)), 1.0)
     target = np.tile(np.log(np.array(p)), (2 * n, 1))  # row 0: position 1, row 1: bonus
     ell = np.ones(n, dtype=np.int64)
     row_off = np.arange(n + 1, dtype=np.int64) * 2
-    out = oracle.verify(z, E, W, anchor, tok, 1.0, ell, row_off, target,
+    out = orc.verify(z, E, W, anchor, tok, 1.0, ell, row_off, target,
                         uni24(rng, (n, 1)), uni24(rng, (n,)))
     return tok, out
 
 
 @pytest.mark.parametrize("qi", [0, 1, 2, 3])
-def test_lossless_marginal_chi_square(qi):
+def test_lossless_marginal_chi_square(orc, qi):
     g = gold("lossless_two_token.json")
     p = np.array(g["p"])
     q = np.array(g["q_cases"][qi])
     n = g["trials"]
     rng = np.random.default_rng(2024 + qi)
-    tok, out = _two_token_step(q, p, n, rng)
+    tok, out = _two_token_step(orc, q, p, n, rng)
     first = out["out_tokens"][:, 0]
     counts = np.bincount(first, minlength=2).astype(np.float64)
     expect = n * p
@@ -329,34 +340,34 @@ def test_lossless_marginal_chi_square(qi):
     assert np.all((out["out_tokens"][:, 1] >= 0) == (out["n_acc"] == 1))
 
 
-def test_identity_q_equals_p_accepts_everything():
+def test_identity_q_equals_p_accepts_everything(orc):
     rng = np.random.default_rng(5)
     R, G, V = 8, 4, 16
     z = rng.normal(0, 2, size=(R, G, V))
     E = rng.normal(0, 0.3, size=(V, 3))
     W = rng.normal(0, 0.3, size=(3, V))
     anchor = rng.integers(0, V, size=R)
-    tok, _, _ = oracle.draft_sample(z, E, W, anchor, uni24(rng, (R, G)), 1.0)
+    tok, _, _ = orc.draft_sample(z, E, W, anchor, uni24(rng, (R, G)), 1.0)
     # target row j = exactly the draft's logits for position j+1
     target = np.zeros((R * (G + 1), V))
     prev = anchor.copy()
     for j in range(G):
-        target[np.arange(R) * (G + 1) + j] = z[:, j, :] + oracle.markov_bias(E, W, prev)
+        target[np.arange(R) * (G + 1) + j] = z[:, j, :] + orc.markov_bias(E, W, prev)
         prev = tok[:, j]
     target[np.arange(R) * (G + 1) + G] = rng.normal(0, 2, size=(R, V))
     ell = np.full(R, G)
     row_off = np.arange(R + 1) * (G + 1)
-    out = oracle.verify(z, E, W, anchor, tok, 1.0, ell, row_off, target,
+    out = orc.verify(z, E, W, anchor, tok, 1.0, ell, row_off, target,
                         uni24(rng, (R, G)), uni24(rng, (R,)))
     assert out["n_acc"].tolist() == [G] * R
     assert np.all(out["out_tokens"][:, :G] == tok)
     assert np.all(out["final_kind"] == 0)
     # sum_x min(p, q) = 1 when q = p
-    q = oracle.draft_distribution(z[:, 0, :], E, W, anchor, 1.0)
+    q = orc.draft_distribution(z[:, 0, :], E, W, anchor, 1.0)
     assert np.allclose(np.minimum(q, q).sum(axis=1), 1.0, atol=1e-12)
 
 
-def test_greedy_verify_argmax_match():
+def test_greedy_verify_argmax_match(orc):
     V, G = 5, 3
     z = np.zeros((3, G, V))
     E = np.zeros((V, 1))
@@ -377,19 +388,195 @@ def test_greedy_verify_argmax_match():
     target = np.array(rows)
     ell = np.array([3, 3, 2])
     row_off = np.array([0, 4, 8, 11])
-    out = oracle.verify(z, E, W, anchor, tokens, 0.0, ell, row_off, target,
+    out = orc.verify(z, E, W, anchor, tokens, 0.0, ell, row_off, target,
                         np.zeros((3, G)), np.zeros(3))
     assert out["n_acc"].tolist() == [2, 3, 1]
     assert out["out_tokens"].tolist() == [[1, 2, 0, -1], [1, 2, 3, 0], [4, 1, -1, -1]]
 
 
-def test_verify_rejection_never_accepts_zero_target_mass():
+def test_verify_rejection_never_accepts_zero_target_mass(orc):
     # p(x) = 0 for the drafted token: strict u < p/q never accepts, even u = 0
     z = np.array([[[0.0, 0.0]]])
     E = np.zeros((2, 1))
     W = np.zeros((1, 2))
     target = np.array([[0.0, -np.inf], [0.0, 0.0]])
-    out = oracle.verify(z, E, W, np.array([0]), np.array([[1]]), 1.0, np.array([1]),
+    out = orc.verify(z, E, W, np.array([0]), np.array([[1]]), 1.0, np.array([1]),
                         np.array([0, 2]), target, np.array([[0.0]]), np.array([0.7]))
     assert out["n_acc"].tolist() == [0]
     assert out["out_tokens"][0].tolist() == [0, -1]
+
+
+# ------------------------------------------- verification branches, closed forms
+
+def _chi2_two(counts, p):
+    n = counts.sum()
+    expect = n * np.asarray(p)
+    return float(np.sum((counts - expect) ** 2 / expect))
+
+
+def test_verify_at_temperature_half_two_token(orc):
+    """T = 0.5 on V = 2 (forum post, lossless proof; explainer, lossless panel;
+    the temperature reading): the target row t = (0, ln 4) gives
+    p = softmax(t / T) = (1/17, 16/17) (p = (0.2, 0.8) if the row were not
+    divided by T), the draft q = (1/2, 1/2).  Acceptance = sum min(p, q) =
+    1/17 + 1/2, the emitted marginal is p, the bonus token after an
+    acceptance follows the bonus row's p, and the row's normaliser is
+    ln(1 + 16)."""
+    T, n = 0.5, 400_000
+    rng = np.random.default_rng(99)
+    p = np.array([1.0, 16.0]) / 17.0
+    z = np.zeros((n, 1, 2))
+    E, W = np.zeros((2, 1)), np.zeros((1, 2))
+    anchor = np.zeros(n, dtype=np.int64)
+    tok = rng.integers(0, 2, size=(n, 1))  # x_1 ~ q = (1/2, 1/2)
+    target = np.tile(np.array([0.0, math.log(4.0)]), (2 * n, 1))  # position 1, bonus
+    out = orc.verify(z, E, W, anchor, tok, T, np.ones(n, dtype=np.int64),
+                     np.arange(n + 1, dtype=np.int64) * 2, target, uni24(rng, (n, 1)),
+                     uni24(rng, (n,)))
+    acc = float(np.mean(out["n_acc"] == 1))
+    a_true = float(np.minimum(p, 0.5).sum())
+    assert abs(acc - a_true) <= 4 * math.sqrt(a_true * (1 - a_true) / n)
+    first = out["out_tokens"][:, 0]
+    assert _chi2_two(np.bincount(first, minlength=2).astype(np.float64), p) < 10.828
+    # after an acceptance the bonus token is drawn from the bonus row's p
+    bonus = out["out_tokens"][out["n_acc"] == 1, 1]
+    assert _chi2_two(np.bincount(bonus, minlength=2).astype(np.float64), p) < 10.828
+    for row in (0, 1, 2 * n - 1):
+        assert abs(out["p_lse"][row] - math.log(17.0)) < 1e-12
+
+
+def test_rejection_at_second_position_uses_the_previous_token(orc):
+    """gamma = 2; position 1 is always accepted (draft and target rows equal),
+    position 2's draft depends on x_1 through the Markov bias: E = (1, -1),
+    W = (-ln3/2, ln3/2), so q_2 = (1/4, 3/4) after x_1 = 0 and (3/4, 1/4) after
+    x_1 = 1 -- in both cases the over-drafted token (the one rejections hit) is
+    not x_1.  With p_2 = (0.6, 0.4) the residual max(0, p_2 - q_2) is a point
+    mass on x_1, and the token emitted at position 2 must follow p_2 after
+    either x_1 (the residual built from q_2 at x_2's bias instead would emit
+    the other token).  Acceptance at position 2: sum min(p_2, q_2) = 0.65."""
+    n = 300_000
+    rng = np.random.default_rng(2025)
+    p2 = np.array([0.6, 0.4])
+    E = np.array([[1.0], [-1.0]])
+    W = np.array([[-math.log(3.0) / 2, math.log(3.0) / 2]])
+    z = np.zeros((n, 2, 2))
+    anchor = np.full(n, -1, dtype=np.int64)  # no bias at position 1
+    x1 = rng.integers(0, 2, size=n)
+    q2_after = {0: np.array([0.25, 0.75]), 1: np.array([0.75, 0.25])}
+    u = rng.random(n)
+    x2 = np.where(x1 == 0, (u >= 0.25).astype(np.int64), (u >= 0.75).astype(np.int64))
+    tok = np.stack([x1, x2], axis=1)
+    rows = np.zeros((n, 3, 2))
+    rows[:, 1, :] = np.log(p2)
+    out = orc.verify(z, E, W, anchor, tok, 1.0, np.full(n, 2, dtype=np.int64),
+                     np.arange(n + 1, dtype=np.int64) * 3, rows.reshape(3 * n, 2),
+                     uni24(rng, (n, 2)), uni24(rng, (n,)))
+    assert np.all(out["n_acc"] >= 1)  # position 1: p = q, so u < 1 always accepts
+    second = out["out_tokens"][:, 1]
+    for v in (0, 1):
+        sel = x1 == v
+        acc = float(np.mean(out["n_acc"][sel] == 2))
+        a_true = float(np.minimum(p2, q2_after[v]).sum())
+        assert abs(acc - a_true) <= 4 * math.sqrt(a_true * (1 - a_true) / sel.sum())
+        counts = np.bincount(second[sel], minlength=2).astype(np.float64)
+        assert _chi2_two(counts, p2) < 10.828
+        rej = sel & (out["n_acc"] == 1)
+        assert np.all(second[rej] == v) and np.all(out["final_kind"][rej] == 1)
+
+
+def test_residual_with_zero_mass_draws_from_p(orc):
+    """A rejection whose residual max(0, p - q) is zero everywhere (the
+    reading for this case: draw from p).  Target row (0, -inf): p = (1, 0).
+    Draft logits (0, -744): q = (1, e^-744), a subnormal.  The drafted token
+    1 has p = 0, so it is rejected even at u = 0; p - q is (0, -e^-744), so
+    the residual mass is 0 and the final token is drawn from p: token 0."""
+    z = np.array([[[0.0, -744.0]]])
+    E, W = np.zeros((2, 1)), np.zeros((1, 2))
+    target = np.array([[0.0, -np.inf], [0.0, 0.0]])
+    for uf in (0.0, 0.5, 1.0 - 2.0 ** -24):
+        out = orc.verify(z, E, W, np.array([-1]), np.array([[1]]), 1.0, np.array([1]),
+                         np.array([0, 2]), target, np.array([[0.0]]), np.array([uf]))
+        assert out["n_acc"].tolist() == [0]
+        assert out["out_tokens"][0].tolist() == [0, -1]
+        assert out["final_kind"].tolist() == [2]
+
+
+def test_final_weights_closed_forms(orc):
+    """The distribution the final token is drawn from: the residual at the
+    rejected position (with that position's previous token), the bonus row's
+    p when all were accepted, p when the residual mass is zero."""
+    E = np.array([[1.0], [-1.0]])
+    W = np.array([[-math.log(3.0) / 2, math.log(3.0) / 2]])
+    z = np.zeros((1, 2, 2))
+    tokens = np.array([[0, 1]])
+    row = np.log(np.array([0.6, 0.4]))
+    # rejected at position 2 (j = 1): q_2 after x_1 = 0 is (1/4, 3/4)
+    w = orc.final_weights(z, E, W, np.array([-1]), tokens, 1.0, row, 1, 0, True)
+    assert np.allclose(w, [0.35, 0.0], atol=1e-12, rtol=0)
+    # rejected at position 1 (j = 0) after anchor 1: q_1 = (3/4, 1/4)
+    w = orc.final_weights(z, E, W, np.array([1]), tokens, 1.0, row, 0, 0, True)
+    assert np.allclose(w, [0.0, 0.15], atol=1e-12, rtol=0)
+    # all accepted: the bonus row's p, at the temperature
+    w = orc.final_weights(z, E, W, np.array([-1]), tokens, 0.5, np.array([0.0, math.log(4.0)]),
+                          2, 0, False)
+    assert np.allclose(w, [1 / 17, 16 / 17], atol=1e-12, rtol=0)
+    # zero residual mass: p
+    z0 = np.array([[[0.0, -744.0]]])
+    w = orc.final_weights(z0, np.zeros((2, 1)), np.zeros((1, 2)), np.array([-1]), np.array([[1]]),
+                          1.0, np.array([0.0, -np.inf]), 0, 0, True)
+    assert w.tolist() == [1.0, 0.0]
+
+
+# ------------------------------------------------ capacity (asynchronous) scheduling
+
+@pytest.mark.parametrize("R,G", [(1, 4), (2, 3), (3, 2), (3, 4)])
+def test_capacity_schedule_brute_force(orc, R, G):
+    """News article, challenge 2: the capacity K is fixed before the step; the
+    current candidates fill it in the current order.  For a fixed batch
+    B = K the top-(K - R) prefix maximises E over every allocation with
+    sum l = K - R (brute force over {0..gamma}^R); K outside [R, R(1+gamma)]
+    is clamped."""
+    rng = np.random.default_rng(7 * R + G)
+    for _ in range(25):
+        a = random_survival(rng, R, G)
+        fx = np.rint(a * 2.0 ** 40).astype(np.int64)
+        for K in range(R - 1, R * (G + 1) + 2):
+            out = orc.schedule_capacity(a, K)
+            i = max(0, min(R * G, K - R))
+            assert out["B"] == R + i and out["i_star"] == i
+            assert out["row_off"][-1] == out["B"]
+            best, arg = None, []
+            for ell in itertools.product(range(G + 1), repeat=R):
+                if sum(ell) != i:
+                    continue
+                s = sum(int(fx[r, :l].sum()) for r, l in enumerate(ell))
+                if best is None or s > best:
+                    best, arg = s, [ell]
+                elif s == best:
+                    arg.append(ell)
+            assert out["E"] == float(R) + float(best) * 2.0 ** -40
+            if len(arg) == 1:
+                assert tuple(out["ell"].tolist()) == arg[0]
+
+
+def test_capacity_from_two_steps_earlier_is_the_global_batch(orc):
+    """The capacity predicted from step t-2's survival values is the batch
+    the global search picks on them; with those same values now, the
+    capacity schedule reproduces the global search's lengths."""
+    rng = np.random.default_rng(31)
+    for _ in range(20):
+        R, G = 3, 4
+        a_old = random_survival(rng, R, G)
+        sps = rng.uniform(1.0, 100.0, size=R * (G + 1) + 1)
+        best, args = brute_force_best(a_old, sps)
+        K = orc.schedule(a_old, sps, early_stop=False)["B"]
+        assert R + sum(args[0]) == K
+        glob = orc.schedule(a_old, sps, early_stop=False)
+        cap = orc.schedule_capacity(a_old, K)
+        assert cap["ell"].tolist() == glob["ell"].tolist() and cap["E"] == glob["E"]
+
+
+def test_capacity_tie_order_request_then_position(orc):
+    a = np.full((3, 2), 0.5)
+    for K, want in [(4, [1, 0, 0]), (5, [2, 0, 0]), (6, [2, 1, 0]), (8, [2, 2, 1])]:
+        assert orc.schedule_capacity(a, K)["ell"].tolist() == want
