@@ -38,6 +38,8 @@ SYMBOLS = (
     "dspark_trace_get",
     "dspark_schedule_noalloc",
     "dspark_draft_schedule",
+    "dspark_check_wait_timeout",
+    "dspark_schedule_async",
 )
 
 
@@ -88,6 +90,10 @@ def lib() -> ctypes.CDLL:
                                             vp, vp, c_int, vp, vp, vp, vp, vp, vp, c_int, c_int,
                                             c_int, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, c_size,
                                             vp]
+        L.dspark_schedule_async.restype = c_int
+        L.dspark_schedule_async.argtypes = [c_int, c_int, vp, vp, vp, vp, vp, vp, vp, c_size, vp]
+        L.dspark_check_wait_timeout.restype = c_int
+        L.dspark_check_wait_timeout.argtypes = [c_int, vp, c_size, vp]
         L.dspark_launch_count.restype = ctypes.c_longlong
         L.dspark_launch_count.argtypes = []
         for f in ("dspark_trace_start", "dspark_trace_stop", "dspark_trace_collect",
@@ -215,6 +221,14 @@ def dspark_schedule(a, sps, early_stop, max_B, ell, row_off, B_out, E_out, ws, s
         _p(B_out), _p(E_out), _p(ws), ws.numel(), _stream(stream)))
 
 
+def dspark_schedule_async(a, capacity, ell, row_off, B_out, E_out, ws, stream=None):
+    """Capacity scheduling: capacity is a one-element int32 device tensor."""
+    R, G = a.shape
+    _check("dspark_schedule_async", lib().dspark_schedule_async(
+        R, G, _p(a), _p(capacity), _p(ell), _p(row_off), _p(B_out), _p(E_out), _p(ws), ws.numel(),
+        _stream(stream)))
+
+
 def dspark_draft_schedule(z, E, Wt, anchor, u_draft, temperature, hidden, w, E1, sts_t, c_in,
                           sps, early_stop, max_B, tokens, q_lse, q_tok, c_out, a_out, ell,
                           row_off, B_out, E_out, ws, stream=None):
@@ -247,3 +261,10 @@ def dspark_schedule_noalloc(a, sps, early_stop, max_B, ell, row_off, B_out, E_ou
     _check("dspark_schedule_noalloc", lib().dspark_schedule_noalloc(
         R, G, _p(a), _p(sps), sps.numel(), int(early_stop), int(max_B), _p(ell), _p(row_off),
         _p(B_out), _p(E_out), _p(dev_status), _stream(stream)))
+
+
+def dspark_check_wait_timeout(limit_us, ws, stream=None):
+    """Runs the library's bounded waits against barriers nothing completes
+    (diagnostic); afterwards the workspace's status word has the timeout bit."""
+    _check("dspark_check_wait_timeout",
+           lib().dspark_check_wait_timeout(int(limit_us), _p(ws), ws.numel(), _stream(stream)))

@@ -30,7 +30,7 @@ int cuda_fail(cudaError_t e, const char* where) {
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-  size_t status, bias, part, sub, row_part, vstate, fin_part, prev, stage, rank, sfix, hpart, vcnt,
+  size_t status, bias, part, sub, row_part, vstate, fin_part, prev, stage, rank, skeys, hpart, vcnt,
       tkey, spre, total;
 };
 
@@ -65,8 +65,8 @@ Layout layout(int R, int gamma, int V, int r) {
   off += align_up((size_t)R * r * 2);
   L.rank = off;
   off += align_up(N * sizeof(int32_t));
-  L.sfix = off;
-  off += align_up(N * sizeof(long long));
+  L.skeys = off;  // the scheduler's sort keys, two buffers
+  off += align_up(N * 2 * sizeof(unsigned long long));
   L.hpart = off;  // lane partials of the confidence head when the draft runs it
   off += align_up((N < (size_t)kFuseMaxCandidates ? N : (size_t)kFuseMaxCandidates) * 32 *
                   sizeof(float));
@@ -270,12 +270,10 @@ int sched_args(int R, int gamma, const float* a, const float* sps, int n_sps, in
   s.status = at<uint32_t>(ws, 0);
   // the scheduler's arrays follow the status word; any workspace sized by
   // dspark_workspace_bytes for these R and gamma covers them
-  size_t off = 256;
-  s.rank = at<int32_t>(ws, off);
-  off += align_up((size_t)N * sizeof(int32_t));
-  s.sfix = at<long long>(ws, off);
-  off += align_up((size_t)N * sizeof(long long));
-  if (ws_bytes < off) return fail(DSPARK_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, off);
+  s.rank = at<int32_t>(ws, 256);
+  s.keys = at<unsigned long long>(ws, 256 + align_up((size_t)N * sizeof(int32_t)));
+  const size_t need = 256 + sched_scratch_bytes((size_t)N);
+  if (ws_bytes < need) return fail(DSPARK_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, need);
   s.imax = imax;
   return DSPARK_OK;
 }
@@ -319,6 +317,39 @@ int dspark_schedule(int R, int gamma, const float* a, const float* sps, int n_sp
   if (st) return st;
   cudaError_t e = launch_schedule(s, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "dspark_schedule");
+  return DSPARK_OK;
+}
+
+int dspark_schedule_async(int R, int gamma, const float* a, const int32_t* capacity,
+                          int32_t* ell, int32_t* row_off, int32_t* B_out, double* E_out,
+                          void* ws, size_t ws_bytes, void* stream) {
+  if (R < 1 || gamma < 1 || gamma > kMaxGamma || (long long)R * gamma > (1 << 20))
+    return fail(DSPARK_ERR_INVALID_ARG, "sizes out of range (R=%d gamma=%d)", R, gamma);
+  REQUIRE(a);
+  REQUIRE(capacity);
+  REQUIRE(ell);
+  REQUIRE(row_off);
+  REQUIRE(B_out);
+  REQUIRE(E_out);
+  if (ws == nullptr) return fail(DSPARK_ERR_INVALID_ARG, "workspace is NULL");
+  if (((uintptr_t)ws & 255) != 0) return fail(DSPARK_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  const size_t N = (size_t)R * gamma;
+  const size_t need = 256 + sched_scratch_bytes(N);
+  if (ws_bytes < need) return fail(DSPARK_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+  SchedArgs sa{};
+  sa.R = R;
+  sa.gamma = gamma;
+  sa.a = a;
+  sa.ell = ell;
+  sa.row_off = row_off;
+  sa.B_out = B_out;
+  sa.E_out = E_out;
+  sa.status = at<uint32_t>(ws, 0);
+  sa.rank = at<int32_t>(ws, 256);
+  sa.keys = at<unsigned long long>(ws, 256 + align_up(N * sizeof(int32_t)));
+  sa.imax = (int)N;
+  cudaError_t e = launch_schedule_async(sa, capacity, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dspark_schedule_async");
   return DSPARK_OK;
 }
 
@@ -442,6 +473,23 @@ int dspark_verify(int R, int gamma, int V, int r, float temperature, const void*
   a.vcnt = at<int>(ws, L.vcnt);
   cudaError_t e = launch_verify(a, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "dspark_verify");
+  return DSPARK_OK;
+}
+
+int dspark_check_wait_timeout(int limit_us, void* ws, size_t ws_bytes, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000)
+    return fail(DSPARK_ERR_INVALID_ARG, "limit_us must be in [1, 1000000] (got %d)", limit_us);
+  REQUIRE(ws);
+  if (((uintptr_t)ws & 255) != 0) return fail(DSPARK_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  if (ws_bytes < 256) return fail(DSPARK_ERR_WORKSPACE, "workspace has %zu bytes, needs 256", ws_bytes);
+  cudaStream_t st = (cudaStream_t)stream;
+  // the same header words the persistent draft uses: status, grid counter
+  unsigned* ctr = at<unsigned>(ws, 64);
+  int* out = at<int>(ws, 128);
+  cudaError_t e = cudaMemsetAsync(ctr, 0, sizeof(unsigned), st);
+  if (e == cudaSuccess)
+    e = launch_wait_check((uint64_t)limit_us * 1000ull, ctr, at<uint32_t>(ws, 0), out, st);
+  if (e != cudaSuccess) return cuda_fail(e, "dspark_check_wait_timeout");
   return DSPARK_OK;
 }
 

@@ -187,8 +187,7 @@ enum KernelKind {
   kKindDraftPartial,
   kKindDraftFinish,
   kKindConfidence,
-  kKindRank,
-  kKindSchedFinish,
+  kKindSchedule,
   kKindVerifyRows,
   kKindVerifyDecide,
   kKindFinalPartial,
@@ -196,6 +195,7 @@ enum KernelKind {
   kKindDraftFusedTc,
   kKindDraftPersistent,
   kKindFinalTc,
+  kKindWaitCheck,
   kKindCount
 };
 
@@ -340,11 +340,24 @@ struct SchedArgs {
   int32_t* B_out;
   double* E_out;
   uint32_t* status;
-  int32_t* rank;      // [N] scratch
-  long long* sfix;    // [N] scratch: fixed-point value at sorted position
-  int32_t* sreq;      // [N] scratch: request id at sorted position
+  int32_t* rank;             // [N] scratch: each candidate's position in the order
+  unsigned long long* keys;  // [2N] scratch: the radix sort's ping-pong buffers
 };
+
+// Scheduler scratch for N candidates: rank (4N) then keys (16N), each rounded
+// up to 256 bytes.
+constexpr size_t sched_scratch_bytes(size_t N) {
+  return ((N * 4 + 255) & ~(size_t)255) + ((N * 16 + 255) & ~(size_t)255);
+}
 cudaError_t launch_schedule(const SchedArgs& a, cudaStream_t st);
+// Capacity (asynchronous) scheduling: the batch is the first
+// min(max(capacity[0] - R, 0), R*gamma) candidates; capacity is device memory.
+cudaError_t launch_schedule_async(const SchedArgs& a, const int32_t* capacity, cudaStream_t st);
+
+// The bounded-wait diagnostic (draft_tc.cu): waits that nothing completes,
+// each giving up after limit_ns.
+cudaError_t launch_wait_check(uint64_t limit_ns, unsigned* ctr, uint32_t* status, int* out,
+                              cudaStream_t st);
 
 // 1/S for a row normaliser S, as (hi + lo) * 2^e with hi in [0.5, 1): the
 // final pass scales it by a tile's power-of-two reference with exponent

@@ -97,8 +97,13 @@ size_t tc_smem_bytes(int nK) {
 // already timed out, so a broken pipeline ends the kernel quickly.
 // After the first tries the thread sleeps in the wait (woken by the phase
 // completion), so waiting roles leave the issue slots to working warps.
+// limit_ns: how long to wait before giving up (the kernels use about 1 s).
+constexpr uint64_t kMbarLimitNs = 1000000000ull;
+constexpr uint64_t kGridLimitNs = 2000000000ull;
+
 __device__ __forceinline__ bool wait_abortable(uint32_t bar, uint32_t parity,
-                                               volatile int* abort_flag, uint32_t* status) {
+                                               volatile int* abort_flag, uint32_t* status,
+                                               uint64_t limit_ns = kMbarLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
@@ -106,7 +111,7 @@ __device__ __forceinline__ bool wait_abortable(uint32_t bar, uint32_t parity,
     for (int i = 0; i < 16; ++i)
       if (mbar_try_wait_sleep(bar, parity, 2000)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > 1000000000ull) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       set_flag(status, kFlagTimeout);
       return false;
@@ -592,7 +597,8 @@ size_t persist_smem_bytes(int nK, int pair) {
 // thread 0's acquire-load of the full count orders the other CTAs' writes
 // before everything after the second CTA barrier, so no full fence is needed.
 __device__ __forceinline__ void grid_arrive_wait(unsigned* ctr, unsigned target,
-                                                 volatile int* abort_flag, uint32_t* status) {
+                                                 volatile int* abort_flag, uint32_t* status,
+                                                 uint64_t limit_ns = kGridLimitNs) {
   asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
   if (*abort_flag) return;
   const uint64_t t0 = globaltimer_ns();
@@ -600,7 +606,7 @@ __device__ __forceinline__ void grid_arrive_wait(unsigned* ctr, unsigned target,
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
     if (v >= target) break;
-    if ((spin & 63) == 0 && globaltimer_ns() - t0 > 2000000000ull) {
+    if ((spin & 63) == 0 && globaltimer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       set_flag(status, kFlagTimeout);
       break;
@@ -613,6 +619,31 @@ __device__ __forceinline__ void grid_sync(unsigned* ctr, unsigned target, volati
   NamedSync<2, 256>::sync();
   if (threadIdx.x == 0) grid_arrive_wait(ctr, target, abort_flag, status);
   NamedSync<2, 256>::sync();
+}
+
+// Diagnostic of the bounded waits above: one CTA waits on an mbarrier that
+// nothing arrives on, then on a grid-barrier target that only it counts
+// towards, each with a short limit.  Both waits must give up, set the
+// timeout bit and let the kernel return; the counter is put back to zero.
+// out[0] = 1 if the mbarrier wait reported success (it must not),
+// out[1] = the abort flag after the grid wait (it must be set).
+__global__ void wait_check_kernel(uint64_t limit_ns, unsigned* ctr, uint32_t* status, int* out) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+    abort_flag = 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const bool ok = wait_abortable(smem_u32(&bar), 0, &abort_flag, status, limit_ns);
+    abort_flag = 0;
+    grid_arrive_wait(ctr, 2u, &abort_flag, status, limit_ns);
+    out[0] = ok ? 1 : 0;
+    out[1] = abort_flag;
+    atomicExch(ctr, 0u);
+  }
 }
 
 // Confidence head at the last draft position (c_k needs x_{k-1} only, and
@@ -1740,6 +1771,13 @@ cudaError_t launch_final_tc(const VerifyArgs& a, const VerifyState* vstate, long
                 e = launch_pdl(final_tc_kernel, dim3(gx, n_rt), dim3(kThreads),
                                final_smem_bytes(p.nK, p.pair), st, tm_w, p));
   if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_check(uint64_t limit_ns, unsigned* ctr, uint32_t* status, int* out,
+                              cudaStream_t st) {
+  DSPARK_LAUNCH(kKindWaitCheck, st,
+                wait_check_kernel<<<1, 32, 0, st>>>(limit_ns, ctr, status, out));
   return cudaGetLastError();
 }
 

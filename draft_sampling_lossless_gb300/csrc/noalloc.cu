@@ -5,15 +5,15 @@
 // is reserved once at start-up, and an allocation in the decode loop would
 // break the plan or the graph capture that replays it), or a plugin running
 // inside a host framework that owns the device heap.  For them this file
-// provides dspark_schedule_noalloc: the same scheduler kernels as
-// dspark_schedule, with their scratch (candidate ranks, sorted fixed-point
-// survival values, a status word) in a file-scope device array instead of a
-// caller workspace.
+// provides dspark_schedule_noalloc: the same scheduler kernel as
+// dspark_schedule, with its scratch (candidate ranks, the sort's two key
+// buffers, a status word) in a file-scope device array instead of a caller
+// workspace.
 //
 // Limits and rules:
 // * at most kNoAllocMaxCandidates (= 32768) candidates, R * gamma; larger
 //   problems are rejected with DSPARK_ERR_INVALID_ARG;
-// * the array (32768 * 12 + 256 bytes, about 384 KiB) lives on every GPU that
+// * the array (32768 * 20 + 256 bytes, about 640 KiB) lives on every GPU that
 //   loads the library, until the process exits;
 // * every call shares it: calls that overlap on the GPU (two streams, or two
 //   host threads) race on it and must be serialised by the caller;
@@ -33,11 +33,13 @@ namespace {
 
 constexpr int kNoAllocMaxCandidates = 32768;
 constexpr size_t kRankBytes = (size_t)kNoAllocMaxCandidates * sizeof(int32_t);
-constexpr size_t kFixBytes = (size_t)kNoAllocMaxCandidates * sizeof(long long);
-constexpr size_t kScratchBytes = 256 + kRankBytes + kFixBytes;
+constexpr size_t kKeyBytes = (size_t)kNoAllocMaxCandidates * 2 * sizeof(unsigned long long);
+constexpr size_t kScratchBytes = 256 + kRankBytes + kKeyBytes;
+static_assert(kRankBytes + kKeyBytes == sched_scratch_bytes(kNoAllocMaxCandidates),
+              "the scheduler's scratch layout");
 
-// Layout: [0, 4) status word, [256, 256 + kRankBytes) ranks, then the
-// fixed-point values (8-byte aligned).
+// Layout: [0, 4) status word, [256, 256 + kRankBytes) ranks, then the two
+// sort-key buffers (8-byte words).
 static __device__ __align__(256) unsigned char g_sched_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
@@ -126,8 +128,9 @@ int dspark_schedule_noalloc(int R, int gamma, const float* a, const float* sps, 
   s.B_out = B_out;
   s.E_out = E_out;
   s.status = dev_status ? dev_status : reinterpret_cast<uint32_t*>(base);
-  s.rank = reinterpret_cast<int32_t*>(base + 256);  // zeroed by launch_schedule
-  s.sfix = reinterpret_cast<long long*>(base + 256 + kRankBytes);  // fully overwritten
+  s.imax = imax;
+  s.rank = reinterpret_cast<int32_t*>(base + 256);  // fully overwritten by each call
+  s.keys = reinterpret_cast<unsigned long long*>(base + 256 + kRankBytes);  // likewise
   e = launch_schedule(s, (cudaStream_t)stream);
   if (e != cudaSuccess) {
     snprintf(g_msg, sizeof(g_msg), "dspark_schedule_noalloc: %s", cudaGetErrorString(e));

@@ -1,7 +1,8 @@
-// Device-side pieces of the prefix scheduler shared by its own kernels and
-// by the persistent draft kernel, which can run the scheduler after its last
+// Device-side pieces of the prefix scheduler shared by its own kernel and by
+// the persistent draft kernel, which can run the scheduler after its last
 // draft position: survival-value cleaning, the exact 2^-40 fixed point, the
-// integer emulation of the double roundings of Theta, and the one-block cut.
+// integer emulation of the double roundings of Theta, E and B, and the
+// one-block cut over precomputed Theta keys.
 //
 // News article "DSpark: Confidence-Scheduled Speculative Decoding with
 // Semi-Autoregressive Generation", section 2.2 (objective, greedy order,
@@ -209,91 +210,11 @@ __device__ __forceinline__ void schedule_store_EB(int R, int istar, long long S,
   B_out[0] = R + istar;
 }
 
-// The cut and the per-request outputs, by one whole block (any multiple of
-// 32 threads; every thread of the block must call it), given every
-// candidate's rank.
-// a, rank and sfix may point to shared or global memory.
-__device__ inline void schedule_finish(
-    int R, int gamma, int imax, int early_stop, const float* a,
-    const float* __restrict__ sps, const int32_t* rank, long long* sfix,
-    int32_t* __restrict__ ell, int32_t* __restrict__ row_off, int32_t* __restrict__ B_out,
-    double* __restrict__ E_out, uint32_t* status) {
-  __shared__ long long shl[32];
-  __shared__ int shi[32];
-  __shared__ unsigned long long shk[32];
-  __shared__ int shidx[32];
-  __shared__ int istar_s;
-  const int N = R * gamma;
-  const int tid = threadIdx.x, nt = blockDim.x;
-  // 1. scatter the fixed-point survival values to their sorted positions
-  for (int e = tid; e < N; e += nt) {
-    float v = a[e];
-    v = (!(v >= 0.0f) || v == INFINITY) ? 0.0f : v;
-    sfix[rank[e]] = to_fixed(v);
-  }
-  __syncthreads();
-  // 2. Theta_i for i in [0, imax]; thread chunk [i0, i1) over i
-  const int n_i = imax + 1;
-  const int seg = (n_i + nt - 1) / nt;
-  const int i0 = min(n_i, tid * seg), i1 = min(n_i, i0 + seg);
-  long long loc = 0;
-  for (int i = i0; i < i1; ++i)
-    if (i < N) loc += sfix[i];
-  long long incl = block_inclusive_scan(loc, shl);
-  const long long S0 = incl - loc;  // exact: integers
-  // Theta in the oracle's operation order, ((double)S * 2^-40 + R) * SPS:
-  // S rounded to a double, the sum rounded, the product rounded; returned as
-  // an order key of the double's bits.
-  auto theta_key = [&](int i, long long S) -> unsigned long long {
-    return theta_key_of(R, i, S, sps, status);
-  };
-  int my_stop = 0x7fffffff;
-  unsigned long long best_v = 0;
-  int best_i = 0x7fffffff;
-  {
-    long long S = S0;
-    unsigned long long prev_th = 0;
-    for (int i = i0; i < i1; ++i) {
-      const unsigned long long th = theta_key(i, S);
-      if (i > i0 && !(th > prev_th) && my_stop == 0x7fffffff) my_stop = i - 1;
-      if (best_i == 0x7fffffff || th > best_v) {
-        best_v = th;
-        best_i = i;
-      }
-      prev_th = th;
-      if (i < N) S += sfix[i];
-    }
-    // the pair that straddles the chunk boundary (i1 - 1, i1)
-    if (i1 > i0 && i1 < n_i && my_stop == 0x7fffffff) {
-      const unsigned long long th = theta_key(i1, S);
-      if (!(th > prev_th)) my_stop = i1 - 1;
-    }
-  }
-  int istar;
-  if (early_stop) {
-    int s = block_min_int(my_stop, shi);
-    istar = s == 0x7fffffff ? imax : s;
-  } else {
-    // first argmax: max value, then lowest index
-    // (key 0 is below every double's key: a thread with no i never wins)
-    istar = block_first_argmax(best_v, best_i, shk, shidx, &istar_s);
-    if (istar == 0x7fffffff) istar = 0;
-  }
-  // 3. E = R + S_{i*}
-  if (istar >= i0 && istar < i1) {
-    long long S = S0;
-    for (int i = i0; i < istar; ++i) S += sfix[i];
-    schedule_store_EB(R, istar, S, B_out, E_out);
-  }
-  // 4. l_r = number of request r's candidates ranked below i*, and row_off
-  schedule_lengths(R, gamma, istar, rank, ell, row_off, shl);
-}
-
-// The same cut when every Theta_i key (i = 0..imax) and every prefix S_i
+// The cut when every Theta_i key (i = 0..imax) and every prefix S_i
 // (i = 0..N) is already known (the persistent draft's ranking CTAs form them
 // with the ranks): the stop or the first argmax over the keys, E from
-// S_{i*}, then the lengths.  The same definitions as schedule_finish, so the
-// same results.  tkey and spre are read from L2 (written by other CTAs).
+// S_{i*}, then the lengths.  The same definitions as the scheduler kernel's
+// cut (schedule.cu), so the same results.  tkey and spre are read from L2 (written by other CTAs).
 __device__ inline void schedule_cut_keys(int R, int gamma, int imax, int early_stop,
                                          const unsigned long long* tkey, const long long* spre,
                                          const int32_t* rank, int32_t* __restrict__ ell,

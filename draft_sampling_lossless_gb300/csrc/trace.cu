@@ -20,9 +20,9 @@ namespace {
 constexpr int kPairs = 8192;
 
 const char* const kNames[kKindCount] = {
-    "markov_bias",       "draft_partial",  "draft_finish", "confidence",  "schedule_rank",
-    "schedule_finish",   "verify_rows",    "verify_decide", "final_partial", "final_pick",
-    "draft_fused_tc",    "draft_persistent_tc", "final_tc",
+    "markov_bias",       "draft_partial",  "draft_finish", "confidence",  "schedule",
+    "verify_rows",    "verify_decide", "final_partial", "final_pick",
+    "draft_fused_tc",    "draft_persistent_tc", "final_tc", "wait_check",
 };
 
 std::mutex g_mu;

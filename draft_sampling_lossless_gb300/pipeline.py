@@ -46,6 +46,14 @@ class DSparkStep:
         B.dspark_schedule(self.a if a is None else a, sps, early_stop, max_B, self.ell,
                           self.row_off, self.B, self.E, self.ws, stream)
 
+    def schedule_async(self, capacity, a=None, stream=None):
+        """Capacity (asynchronous) scheduling: the batch holds exactly the
+        first capacity - R candidates (clamped); capacity is a one-element
+        int32 device tensor, e.g. the B of a global-search schedule of the
+        survival values two steps earlier."""
+        B.dspark_schedule_async(self.a if a is None else a, capacity, self.ell, self.row_off,
+                                self.B, self.E, self.ws, stream)
+
     def draft_schedule(self, z, E, Wt, anchor, u_draft, T, hidden, w, E1, sts_t, sps,
                        c_in=None, early_stop=True, max_B=0, stream=None):
         """draft + confidence + schedule in one call (one launch when the

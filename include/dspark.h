@@ -17,7 +17,11 @@
  * --------------------------------
  * - Every array argument is a DEVICE pointer owned by the caller, row-major,
  *   densely packed, with the layout given beside it.  The library never
- *   allocates, frees or retains memory and keeps no state between calls.
+ *   allocates, frees or retains the caller's memory.  Its only state that
+ *   outlives a call: per-device launch set-up (shared-memory opt-ins,
+ *   occupancy and SM counts, made once per device under a lock), launch
+ *   counters and trace events, and the static device scratch of
+ *   dspark_schedule_noalloc (shared by every call of that entry point).
  * - Scratch memory comes from the caller's workspace `ws` of `ws_bytes`
  *   bytes, at least dspark_workspace_bytes(...) for the same sizes, 256-byte
  *   aligned.  Its first 4 bytes are a device status word: kernels OR the
@@ -160,7 +164,8 @@ int dspark_confidence(int R, int gamma, int d, int r, int V,
  * panel (E = R + sum_r sum_{j<=l_r} a_{r,j}, rate = E / T(B)).
  *
  * Candidates (n, j) are ordered by a[n][j] descending, then n, then j
- * ascending.  With S_i the sum of the first i (each a rounded to a multiple
+ * ascending (a stable radix sort of the survival values over one cluster of
+ * thread blocks).  With S_i the sum of the first i (each a rounded to a multiple
  * of 2^-40 and summed exactly as an integer):
  *   Theta_i = (R + S_i) * SPS[R + i]                       (double)
  *   early_stop != 0: i* = first i with Theta_{i+1} <= Theta_i (else the last)
@@ -180,6 +185,37 @@ int dspark_schedule(int R, int gamma, const float* a, const float* sps, int n_sp
                     int early_stop, int max_B, int32_t* ell, int32_t* row_off,
                     int32_t* B_out, double* E_out, void* ws, size_t ws_bytes,
                     void* stream);
+
+/*
+ * dspark_schedule_async -- asynchronous scheduling with a capacity fixed
+ * before the step.
+ *
+ * News article, challenge 2: zero-overhead scheduling needs the next step's
+ * verification batch size before the current step finishes, and the
+ * profiled SPS curve is not smooth, so the verification capacity is taken
+ * from the confidences of two steps earlier while the candidates that fill it
+ * are still chosen by the current confidences; because the capacity does not
+ * depend on the current step's draft, a global search (no early stop) stays
+ * lossless.  Explainer, survival panel (production sets the capacity from
+ * earlier steps' predictions).
+ *
+ * With K = capacity[0], read on the device (so a capacity produced by an
+ * earlier call -- e.g. the B_out of a global-search dspark_schedule on the
+ * survival values of two steps earlier -- never needs a host read):
+ *   i*  = min(max(K - R, 0), R * gamma)
+ *   l_n = number of request n's candidates among the first i* of the order
+ *         (a descending, then n, then j ascending), as in dspark_schedule
+ *   B_out = R + i*,  E_out = R + S_{i*}  (S as in dspark_schedule)
+ *
+ *   a         [R][gamma] f32   current survival values (finite, >= 0)
+ *   capacity  [1] int32        device: the batch capacity K
+ *   ell, row_off, B_out, E_out as in dspark_schedule
+ * Uses the scheduler's part of `ws` (a workspace sized by
+ * dspark_workspace_bytes for R and gamma).
+ */
+int dspark_schedule_async(int R, int gamma, const float* a, const int32_t* capacity,
+                          int32_t* ell, int32_t* row_off, int32_t* B_out, double* E_out,
+                          void* ws, size_t ws_bytes, void* stream);
 
 /*
  * dspark_draft_schedule -- dspark_draft_sample, dspark_confidence and
@@ -280,6 +316,26 @@ int dspark_verify(int R, int gamma, int V, int r, float temperature,
 int dspark_schedule_noalloc(int R, int gamma, const float* a, const float* sps, int n_sps,
                             int early_stop, int max_B, int32_t* ell, int32_t* row_off,
                             int32_t* B_out, double* E_out, uint32_t* dev_status, void* stream);
+
+/*
+ * dspark_check_wait_timeout -- diagnostic of the library's bounded waits.
+ * The pages have no counterpart: this exercises the failure handling.
+ *
+ * Every on-chip wait in the library's kernels (an mbarrier phase, the
+ * persistent draft's grid barrier) gives up after a time limit, ORs
+ * DSPARK_DEVFLAG_TIMEOUT into the status word and lets the kernel return, so
+ * a stalled pipeline never leaves the GPU hung.  This call runs those same
+ * two waits in a one-block kernel against barriers that nothing completes,
+ * each with a limit of limit_us microseconds (1 .. 10^6).  Once the stream
+ * reaches it, the status word has DSPARK_DEVFLAG_TIMEOUT set and the device
+ * stays usable.  It uses the first 256 bytes of `ws` (at least 256 bytes,
+ * 256-byte aligned): the status word at byte 0, a counter at byte 64 that it
+ * leaves at zero, and at byte 128 two int32 results (1 if the mbarrier wait
+ * claimed success -- it must not -- and 1 if the grid wait gave up).
+ * Errors: DSPARK_ERR_INVALID_ARG (limit out of range, NULL or misaligned
+ * ws), DSPARK_ERR_WORKSPACE, DSPARK_ERR_CUDA.
+ */
+int dspark_check_wait_timeout(int limit_us, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Launch counting and kernel tracing (measurement support; no counterpart on

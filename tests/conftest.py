@@ -8,6 +8,18 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+# Lines that tests add (decision and near-tie counts, measured rates); printed
+# after the run so that they appear at the end of the log.
+SUMMARY = []
+
+
+def pytest_terminal_summary(terminalreporter):
+    if SUMMARY:
+        terminalreporter.write_sep("-", "measured counts")
+        for line in SUMMARY:
+            terminalreporter.write_line(line)
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
 

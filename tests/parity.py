@@ -22,7 +22,7 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-import oracle
+from oracle import native as oracle  # the plain C++ CPU oracle
 from draft_sampling_lossless_gb300 import synth, target_model
 from draft_sampling_lossless_gb300.pipeline import DSparkStep
 
@@ -37,6 +37,11 @@ class Stats:
     unexplained: list = field(default_factory=list)
     value_checks: int = 0
     worst_rel: dict = field(default_factory=dict)
+    tie_kinds: dict = field(default_factory=dict)  # near-ties by decision kind
+
+    def tie(self, kind):
+        self.near_ties += 1
+        self.tie_kinds[kind] = self.tie_kinds.get(kind, 0) + 1
 
     def rel(self, name, got, want, tol=REL):
         got = np.asarray(got, dtype=np.float64)
@@ -53,6 +58,8 @@ class Stats:
         self.near_ties += o.near_ties
         self.unexplained += o.unexplained
         self.value_checks += o.value_checks
+        for k, v in o.tie_kinds.items():
+            self.tie_kinds[k] = self.tie_kinds.get(k, 0) + v
         for k, v in o.worst_rel.items():
             self.worst_rel[k] = max(self.worst_rel.get(k, 0.0), v)
 
@@ -135,7 +142,7 @@ class Case:
                     tie = cdf_near_tie(np.exp(yy - yy.max()), self.u_draft[i, k],
                                        int(tok_g[i, k]), int(tok_o[i, k]))
                 if tie:
-                    st.near_ties += 1
+                    st.tie("draft")
                 else:
                     st.unexplained.append(("draft", int(self.sample[i]), k, int(tok_g[i, k]),
                                            int(tok_o[i, k])))
@@ -230,7 +237,7 @@ class Case:
                 j = min(na_o, na_g)  # the first differing acceptance test
                 tie = self._accept_tie(i, j, ro_s, tgt64)
                 if tie:
-                    st.near_ties += 1
+                    st.tie("accept")
                 else:
                     st.unexplained.append(("accept", int(self.sample[i]), j, na_g, na_o))
                 continue
@@ -247,7 +254,7 @@ class Case:
                                          wl.T, trow, na_o, i, na_o < ell_s[i])
                 tie = cdf_near_tie(w, self.u_fin[i], fg, fo)
             if tie:
-                st.near_ties += 1
+                st.tie("final")
             else:
                 st.unexplained.append(("final", int(self.sample[i]), na_o, fg, fo))
         return o

@@ -145,3 +145,26 @@ def test_draft_schedule_rejects_bad_arguments_without_launching(lib):
     assert call(max_B=3) == 1  # a cap below R
     assert call(sps=n) == 1
     assert call(ws_bytes=1024) == 4  # DSPARK_ERR_WORKSPACE
+
+
+def test_wait_check_rejects_bad_arguments_without_launching(lib):
+    L = lib.lib()
+    f, n = _fake(), _null()
+    assert L.dspark_check_wait_timeout(0, f, 1024, n) == 1
+    assert L.dspark_check_wait_timeout(1000001, f, 1024, n) == 1
+    assert L.dspark_check_wait_timeout(1000, n, 1024, n) == 1
+    assert L.dspark_check_wait_timeout(1000, ctypes.c_void_p(0x1010), 1024, n) == 1
+    assert L.dspark_check_wait_timeout(1000, f, 128, n) == 4
+
+
+def test_schedule_async_rejects_bad_arguments_without_launching(lib):
+    L = lib.lib()
+    f, n = _fake(), _null()
+    args = lambda R=4, G=4, a=f, cap=f, ws=f, nb=1 << 20: (R, G, a, cap, f, f, f, f, ws, nb, n)
+    assert L.dspark_schedule_async(*args(R=0)) == 1
+    assert L.dspark_schedule_async(*args(G=33)) == 1
+    assert L.dspark_schedule_async(*args(a=n)) == 1
+    assert L.dspark_schedule_async(*args(cap=n)) == 1
+    assert "capacity is NULL" in _err(L)
+    assert L.dspark_schedule_async(*args(ws=n)) == 1
+    assert L.dspark_schedule_async(*args(nb=256)) == 4

@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 import torch
 
-import oracle
+from oracle import native as oracle  # the plain C++ CPU oracle
 from draft_sampling_lossless_gb300 import synth, target_model
 from parity import Case, Stats
 

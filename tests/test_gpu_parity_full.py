@@ -1,13 +1,22 @@
 """GPU parity at the full sizes of the five workloads, in the launch
-configuration the benchmark times: the library runs every request, the oracle
-recomputes a sample of requests one by one (requests are independent in the
+configuration the benchmark times: the library runs every request, the
+oracle recomputes a sample of requests (requests are independent in the
 draft, confidence and verify stages); the scheduler is compared on all
-candidates."""
+candidates.
+
+The near-tie budget is measured where it can be: the Qwen3-4B shape over
+every request and 30 input seeds (more than 10^4 draft, acceptance and final
+decisions), and the DeepSeek-scale and greedy workloads over 8 seeds each.
+A near-tie is a decision where the two sides differ and the oracle's
+boundary between their choices lies within 1e-6 of the uniform (normalised);
+the count must stay at or below 1e-4 of the decisions.  The counts are
+printed at the end of the run."""
 
 import numpy as np
 import pytest
 import torch
 
+import conftest
 from draft_sampling_lossless_gb300 import synth
 from parity import Case, Stats
 
@@ -20,24 +29,54 @@ def _sample(R):
     return np.unique(np.array([0, 1, R // 2, R - 1]))
 
 
-@pytest.mark.parametrize("name", ["tiny", "qwen3_4b", "deepseek", "greedy", "stress"])
-def test_full_size_sampled_parity(name):
-    wl = W[name]
-    st = Stats()
-    c = Case(wl, gen_device="cuda", sample=_sample(wl.R))
+def _step(c: Case, st: Stats):
+    """Draft, confidence, both scheduler modes on all candidates, then
+    verification of the sampled requests with the scheduled lengths and with
+    full blocks (bonus draws)."""
+    wl = c.wl
     c.draft(st)
     c.confidence(st)
     # scheduler on all candidates: survival of the sampled requests from the
-    # oracle, the rest from the same seeded Beta draw (any valid survival set)
-    rng = np.random.default_rng(wl.seed)
+    # oracle, the rest from a seeded Beta draw (any valid survival set)
+    rng = np.random.default_rng(wl.seed if c.seed is None else c.seed)
     a_all = np.cumprod(rng.beta(8, 2, size=(wl.R, wl.gamma)), axis=1)
     a_all[c.sample] = c.a_o
     a32 = a_all.astype(np.float32)
     o = c.schedule(st, a32, early_stop=True)
     c.schedule(st, a32, early_stop=False)
     c.verify(st, o["ell"][c.sample])
-    # every sampled request also with a full block (bonus draws)
     c.verify(st, np.full(len(c.sample), wl.gamma))
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3_4b", "deepseek", "greedy", "stress"])
+def test_full_size_sampled_parity(name):
+    wl = W[name]
+    st = Stats()
+    _step(Case(wl, gen_device="cuda", sample=_sample(wl.R)), st)
     assert st.unexplained == [], st.unexplained
-    print(f"{name}: decisions={st.decisions} near_ties={st.near_ties} "
-          f"worst_rel={ {k: f'{v:.2e}' for k, v in st.worst_rel.items()} }")
+    conftest.SUMMARY.append(f"full-size parity {name}: decisions={st.decisions} "
+                            f"near_ties={st.near_ties} worst_rel="
+                            f"{ {k: f'{v:.2e}' for k, v in st.worst_rel.items()} }")
+
+
+# workload -> (seeds, requests compared per seed; None = all)
+NEAR_TIE = {"qwen3_4b": (30, None), "deepseek": (8, 32), "greedy": (8, 64)}
+
+
+@pytest.mark.parametrize("name", sorted(NEAR_TIE))
+def test_near_tie_rate_at_full_size(name):
+    wl = W[name]
+    seeds, n_s = NEAR_TIE[name]
+    sample = None if n_s is None else np.linspace(0, wl.R - 1, n_s).round().astype(np.int64)
+    st = Stats()
+    for s in range(seeds):
+        c = Case(wl, seed=7000 + 97 * s, gen_device="cuda", sample=sample)
+        _step(c, st)
+        del c
+        torch.cuda.empty_cache()
+    conftest.SUMMARY.append(
+        f"near-tie rate {name}: {seeds} seeds x {wl.R if n_s is None else n_s} requests, "
+        f"decisions={st.decisions} near_ties={st.near_ties} {st.tie_kinds} "
+        f"(budget {1e-4 * st.decisions:.2f}) unexplained={len(st.unexplained)}")
+    assert st.unexplained == [], st.unexplained[:10]
+    assert st.near_ties <= 1e-4 * st.decisions, (st.near_ties, st.decisions)
