@@ -3,6 +3,12 @@
 hidden 2560, bf16), through the libdspark C ABI.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload tiny|qwen3_4b|deepseek|greedy|stress] [--early-stop 0|1]
+                  [--verify-only]
+
+The other workloads are measured with --workload; --early-stop 0 runs the
+scheduler's global search; --verify-only times the verification alone on
+the scheduler's ragged batch (metric: verified rows/s).
 
 Prints ONE JSON line on rank 0.  `value` is draft+verify positions/s
 (R * gamma per step) over the device-timed steps (CUDA events on the launching
@@ -174,7 +180,8 @@ def run_ours(args, wl, world, rank, local):
     def front():
         # draft + confidence head + scheduler: one call (one launch here)
         step.draft_schedule(g["z"], g["E"], g["Wt"], g["anchor"], g["ud"], wl.T, g["h"], g["w"],
-                            g["E"], g["sts"], g["sps"], c_in=g["c_in"])
+                            g["E"], g["sts"], g["sps"], c_in=g["c_in"],
+                            early_stop=bool(args.early_stop))
 
     # pass 0: the scheduled batch and the target logits the target model would
     # produce for it (a harness input, packed in the scheduler's row order)
@@ -188,11 +195,16 @@ def run_ours(args, wl, world, rank, local):
     del dense
     step.p_lse = torch.zeros((Bn,), dtype=torch.float64, device=dev)
 
-    def one_step():
-        front()
+    def verify():
         step.verify(g["z"], g["E"], g["Wt"], g["anchor"], target, g["ua"], g["uf"], wl.T)
 
-    one_step()
+    def full_step():
+        front()
+        verify()
+
+    # --verify-only times the verification alone on the scheduler's batch
+    one_step = verify if args.verify_only else full_step
+    full_step()
     torch.cuda.synchronize()
     assert step.status() == 0, f"device status {step.status():#x}"
     assert int(step.B.item()) == Bn
@@ -238,7 +250,8 @@ def run_ours(args, wl, world, rank, local):
     clk = clocks.stop()
     ms = [a.elapsed_time(b) for a, b in ev]
     ms_local = sum(ms) / len(ms)
-    value, t_max = aggregate(wl.R * wl.gamma, ms_local / 1e3, world)
+    units = Bn if args.verify_only else wl.R * wl.gamma
+    value, t_max = aggregate(units, ms_local / 1e3, world)
     assert step.status() == 0, f"device status {step.status():#x}"
 
     # per-kernel device times: the same step captured with tracing on
@@ -256,7 +269,7 @@ def run_ours(args, wl, world, rank, local):
     del tgraph
 
     # end to end through the public calls with pinned host buffers
-    e2e = run_e2e(args, wl, inp, g, step, target, dev, Bd)
+    e2e = None if args.verify_only else run_e2e(args, wl, inp, g, step, target, dev, Bd)
 
     peaks, psrc = read_peaks()
     kernels = {k: {"launches_per_step": v[0] / args.steps, "avg_us": 1e3 * v[1] / v[0],
@@ -266,11 +279,14 @@ def run_ours(args, wl, world, rank, local):
     roof = roofline_entry(dom, totals[dom], wl, Bn, n_rej, peaks, psrc)
 
     out = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": "verify rows/s" if args.verify_only else METRIC, "value": value,
+        "unit": "rows/s" if args.verify_only else UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_max * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "config": {"workload": f"{wl.name}: R={wl.R} gamma={wl.gamma} V={wl.V} r={wl.r} "
                                f"d={wl.d} T={wl.T}", "B": Bn, "mean_n_acc": mean_acc,
+                   "early_stop": bool(args.early_stop),
+                   "timed": "verification only" if args.verify_only else "the whole step",
                    "l2": "flushed between timed steps (512 MiB write)", "cuda_graph": True,
                    "parallelism": f"replicas x{world}"},
         "e2e": e2e,
@@ -279,7 +295,7 @@ def run_ours(args, wl, world, rank, local):
         "roofline": roof,
         "kernels": kernels,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.verify_only:
         out["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
     return out
 
@@ -376,7 +392,8 @@ def run_e2e(args, wl, inp, g, step, target, dev, Bd):
         cur = torch.cuda.current_stream()
         cur.wait_event(drafted_in[s])
         step.draft_schedule(b["z"], g["E"], g["Wt"], b["anchor"], b["ud"], wl.T, b["h"], g["w"],
-                            g["E"], g["sts"], g["sps"], c_in=b["c_in"])
+                            g["E"], g["sts"], g["sps"], c_in=b["c_in"],
+                            early_stop=bool(args.early_stop))
         cur.wait_event(verified_in[s])
         step.verify(b["z"], g["E"], g["Wt"], b["anchor"], b["target"], b["ua"], b["uf"], wl.T)
         computed[s] = ev()
@@ -411,81 +428,114 @@ def run_e2e(args, wl, inp, g, step, target, dev, Bd):
 
 # --------------------------------------------------------------------- CPU
 
-def oracle_step(wl, inp, reqs):
-    """The CPU oracle over a sub-batch of requests (its own batch of size
-    len(reqs)): draft, confidence, schedule, verify."""
-    import oracle
+def oracle_step(wl, inp, reqs, cache):
+    """The plain C++ CPU oracle over a sub-batch of requests (scheduled as its
+    own batch): draft, confidence, schedule and verify are timed; the target
+    model's stand-in (building the target rows from the oracle's draft) is not.
+    Returns the seconds spent in the four stages."""
+    from oracle import native as oracle
 
     f = synth.to_f64
     idx = torch.as_tensor(reqs, dtype=torch.long)
+    if "E" not in cache:
+        cache["E"], cache["W"] = f(inp.E), f(inp.W)
+    E, W = cache["E"], cache["W"]
     z = f(inp.z[idx])
-    E = inp.extra.setdefault("E64", f(inp.E))
-    W = inp.extra.setdefault("W64", f(inp.W))
     anchor = inp.anchor[idx].numpy().astype(np.int64)
-    tok, ql, qt = oracle.draft_sample(z, E, W, anchor, f(inp.u_draft[idx]), wl.T)
+    t0 = time.perf_counter()
+    tok, _, _ = oracle.draft_sample(z, E, W, anchor, f(inp.u_draft[idx]), wl.T)
     c_in = f(inp.c_in[idx]) if inp.c_in is not None else None
     h = f(inp.h[idx]) if inp.h is not None else None
     _, a = oracle.confidence(h, f(inp.w_conf) if inp.w_conf is not None else None, E, anchor,
                              tok, f(inp.sts_t), c_in=c_in)
     sch = oracle.schedule(a.astype(np.float32).astype(np.float64), f(inp.sps), True)
-    tgt_dense = inp.extra["target"][idx]
+    t1 = time.perf_counter()
+    # the target model's forward pass is outside the path: its stand-in builds
+    # the sub-batch's target rows for the drafted tokens (not timed)
+    sub = synth.Inputs(wl.scaled(R=len(reqs)), inp.z[idx], inp.E, inp.W, inp.anchor[idx],
+                       inp.u_draft[idx], inp.u_acc[idx], inp.u_fin[idx], None, None,
+                       inp.sts_t, None, inp.sps)
+    dense = target_model.target_logits(sub, torch.from_numpy(tok))
     G = wl.gamma
     rows = np.concatenate([r * (G + 1) + np.arange(sch["ell"][r] + 1) for r in range(len(reqs))])
-    tgt = f(tgt_dense.reshape(-1, wl.V)[torch.from_numpy(rows)])
+    tgt = f(dense.reshape(-1, wl.V)[torch.from_numpy(rows)])
+    t2 = time.perf_counter()
     oracle.verify(z, E, W, anchor, tok, wl.T, sch["ell"], sch["row_off"], tgt,
                   f(inp.u_acc[idx]), f(inp.u_fin[idx]))
+    return (t1 - t0) + (time.perf_counter() - t2)
 
 
 def cpu_inputs(wl):
-    inp = synth.make_inputs(wl, device="cpu")
-    tok = torch.zeros((wl.R, wl.gamma), dtype=torch.int32)
-    inp.extra["target"] = target_model.target_logits(inp, tok)
-    return inp
+    return synth.make_inputs(wl, device="cpu")
+
+
+def _timed_oracle(wl, inp, n_req, threads, budget_s, cache):
+    """Sub-batches of n_req consecutive requests through the oracle on
+    `threads` OpenMP threads until about budget_s seconds of stage time."""
+    from oracle import native as oracle
+
+    n0 = oracle.threads()
+    oracle.set_threads(threads)
+    try:
+        done, spent, k = 0, 0.0, 0
+        while spent < budget_s or done == 0:
+            reqs = [(k + i) % wl.R for i in range(n_req)]
+            spent += oracle_step(wl, inp, reqs, cache)
+            done += n_req
+            k += n_req
+    finally:
+        oracle.set_threads(n0)
+    return done, spent
 
 
 def cpu_baseline(wl, budget_s=15.0, inp=None):
-    """The oracle, as it stands, on sub-batches of requests until about
-    budget_s seconds of CPU work."""
+    """The plain C++ oracle, as it stands, on the host cores: one thread on
+    single requests, and every core (OpenMP over requests) on sub-batches of
+    one request per core; bounded to about budget_s seconds in all."""
     inp = inp or cpu_inputs(wl)
-    done, t0 = 0, time.perf_counter()
-    k = 0
-    while True:
-        oracle_step(wl, inp, [k % wl.R])
-        done += 1
-        k += 1
-        if time.perf_counter() - t0 > budget_s:
-            break
-    t = time.perf_counter() - t0
     cores = len(os.sched_getaffinity(0))
-    return {"value": done * wl.gamma / t, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{done} single-request sub-batches of {wl.name} (all four stages, "
-                      f"gamma={wl.gamma}, V={wl.V}), numpy float64, {t:.1f} s"}
+    n_req = min(cores, wl.R)  # distinct requests, one a core
+    cache = {}
+    d1, t1 = _timed_oracle(wl, inp, 1, 1, budget_s / 3, cache)
+    dn, tn = _timed_oracle(wl, inp, n_req, cores, 2 * budget_s / 3, cache)
+    return {"value": dn * wl.gamma / tn, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{dn} requests of {wl.name} in sub-batches of {n_req} (one a core), all "
+                      f"four stages of the plain C++ oracle (double), {tn:.1f} s of stage time; "
+                      f"the target stand-in untimed",
+            "single_thread": {"value": d1 * wl.gamma / t1, "unit": UNIT, "cores": 1,
+                              "sample": f"{d1} single requests, {t1:.1f} s"}}
 
 
 def run_reference(args, wl):
+    """The reference arm: the plain C++ CPU oracle (there is no reference
+    implementation to install), every host core, each step one sub-batch of
+    one request per core."""
     inp = cpu_inputs(wl)
+    cores = len(os.sched_getaffinity(0))
+    cache = {}
+    from oracle import native as oracle
+
+    oracle.set_threads(cores)
+    n_req = min(cores, wl.R)  # distinct requests, one a core
     for i in range(args.warmup):
-        oracle_step(wl, inp, [i % wl.R])
+        oracle_step(wl, inp, [(i * n_req + j) % wl.R for j in range(n_req)], cache)
     times = []
-    budget = 180.0
+    budget = 150.0
     t_all = time.perf_counter()
     for i in range(args.steps):
-        t0 = time.perf_counter()
-        oracle_step(wl, inp, [i % wl.R])
-        times.append(time.perf_counter() - t0)
+        times.append(oracle_step(wl, inp, [(i * n_req + j) % wl.R for j in range(n_req)], cache))
         if time.perf_counter() - t_all > budget and len(times) >= 3:
             break
     t = sum(times) / len(times)
-    value = wl.gamma / t
-    cores = len(os.sched_getaffinity(0))
-    sample = (f"{len(times)} timed steps, each one request of {wl.name} as its own batch "
-              f"(all four stages), numpy float64")
+    value = n_req * wl.gamma / t
+    sample = (f"{len(times)} timed steps, each a sub-batch of {n_req} requests of {wl.name} "
+              f"(one a core) through all four stages of the plain C++ oracle")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
             "steps": len(times), "warmup": args.warmup, "ms_per_step": t * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": {"workload": f"{wl.name}: R={wl.R} gamma={wl.gamma} V={wl.V} r={wl.r} "
-                                   f"d={wl.d} T={wl.T}", "sample_requests_per_step": 1},
+                                   f"d={wl.d} T={wl.T}", "sample_requests_per_step": n_req},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -499,6 +549,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3_4b", choices=list(synth.WORKLOADS))
+    ap.add_argument("--early-stop", type=int, default=1, choices=[0, 1],
+                    help="scheduler stop rule: 1 early stop, 0 global search")
+    ap.add_argument("--verify-only", action="store_true",
+                    help="time the verification alone on the scheduled batch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     args = ap.parse_args()

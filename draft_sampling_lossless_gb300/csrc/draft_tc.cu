@@ -79,6 +79,7 @@ struct TcParams {
   int R, gamma, V, r, k, nK, n_vt, n_parts;
   int greedy;
   ScalePair sc;
+  float c12, crest;  // log2(e)/T = c12 + crest, c12 with 12 significant bits
   const __nv_bfloat16* E;
   const int32_t* prev;
   int prev_stride;
@@ -180,67 +181,164 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
   return r;
 }
 
-// 64 consecutive tokens of one request row (two 32-column accumulator loads
-// and their z values): y = z + bias, then the greedy argmax or the
-// fixed-point sum of 2^(a - ref) with a = y*log2(e)/T.  `lim` = number of the
-// 64 tokens that lie below V.  gs receives the sums of the four 16-token
-// groups in units of 2^ref (s.ref on return; 0 where a group has no mass).
-// The maxima and sums are trees, so a warp has independent work to issue
-// while MUFU and FMA results come back.
-__device__ __forceinline__ void epi_block(const uint32_t (&b0)[32], const uint32_t (&b1)[32],
-                                          const uint4 (&z0)[4], const uint4 (&z1)[4], int v0,
-                                          int lim, const TcParams& p, Part& s, float (&gs)[4]) {
+// TwoSum (Knuth): s = RN(a + b) and the exact error a + b - s, for any
+// order of magnitudes; the packed form does two pairs at once.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& err) {
+  s = a + b;
+  const float bb = s - a;
+  err = (a - (s - bb)) + (b - bb);
+}
+__device__ __forceinline__ void two_sum2(unsigned long long a, unsigned long long b,
+                                         unsigned long long& s, unsigned long long& err) {
+  const unsigned long long t = add2(a, b);
+  const unsigned long long bb = sub2(t, a);
+  err = add2(sub2(a, sub2(t, bb)), sub2(b, bb));
+  s = t;
+}
+
+// round(x * 2^40) for 0 <= x < 2^22, from the float's bits (no conversion
+// instruction): exact once x * 2^40 >= 2^23, where the float holds an
+// integer; below, the bits under 2^-40 are dropped (less than one unit).
+__device__ __forceinline__ long long fix40(float x) {
+  const uint32_t b = __float_as_uint(x);
+  const int e = (int)(b >> 23);  // x >= 0: the biased exponent
+  const unsigned long long m = (b & 0x7fffffu) | (e ? 0x800000u : 0u);
+  const int sh = e - 110;  // x * 2^40 = m * 2^(e - 150 + 40)
+  return (long long)(sh >= 0 ? m << sh : (sh > -24 ? m >> -sh : 0ull));
+}
+
+// Greedy: the arg-max of y = z + b over 32 consecutive tokens of one
+// request row (one 32-column accumulator load b and the z words zq), half h
+// (tokens v0 + 32h ..) of a 64-token block; `lim` = number of the block's
+// tokens below V.  NaN and +inf set s.bad.
+__device__ __forceinline__ void epi_half_greedy(const uint32_t (&b)[32], const uint4 (&zq)[4],
+                                                int h, int v0, int lim, Part& s) {
+  const int t0 = h * 32;
+  ArgMax t[16];
+  float chk = -INFINITY;
 #pragma unroll
-  for (int g = 0; g < 4; ++g) gs[g] = 0.f;
-  // y = z + bias on element pairs (packed two-wide fp32 adds)
-  unsigned long long y2[32];
+  for (int k = 0; k < 16; ++k) {
+    const uint32_t zw = (&zq[0].x)[k];
+    float ya, yb;
+    unpack2(add2(pack2(bf_lo(zw), bf_hi(zw)),
+                 pack2(__uint_as_float(b[2 * k]), __uint_as_float(b[2 * k + 1]))),
+            ya, yb);
+    if (t0 + 2 * k >= lim) ya = -INFINITY;
+    if (t0 + 2 * k + 1 >= lim) yb = -INFINITY;
+    t[k] = better(ArgMax{ya, v0 + t0 + 2 * k}, ArgMax{yb, v0 + t0 + 2 * k + 1});
+    chk = fmax_nan(chk, fmax_nan(ya, yb));
+  }
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint32_t w0[4] = {z0[q].x, z0[q].y, z0[q].z, z0[q].w};
-    const uint32_t w1[4] = {z1[q].x, z1[q].y, z1[q].z, z1[q].w};
+  for (int w = 8; w > 0; w >>= 1)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      y2[q * 4 + e] = add2(pack2(bf_lo(w0[e]), bf_hi(w0[e])),
-                           pack2(__uint_as_float(b0[q * 8 + 2 * e]), __uint_as_float(b0[q * 8 + 2 * e + 1])));
-      y2[16 + q * 4 + e] = add2(pack2(bf_lo(w1[e]), bf_hi(w1[e])),
-                                pack2(__uint_as_float(b1[q * 8 + 2 * e]), __uint_as_float(b1[q * 8 + 2 * e + 1])));
+    for (int e = 0; e < w; ++e) t[e] = better(t[e], t[e + w]);
+  s.best = better(s.best, t[0]);
+  if (!(chk < INFINITY)) s.bad = 1;
+}
+
+// One weight 2^(x c + e) for two tokens at once, with the exponent split as
+// in the draft epilogue: x c = P + x' (P = x_hi c12 exact for a bf16 x_hi;
+// x' the rest), n = rint(P + bq c12 + e) clamped at -125, the fraction
+// f = (P - rint(P + bq c12)) + bq c12 + (x_hi + bq) crest in [-1/2, 1/2]
+// to ex2, 2^n from the magic number's bits.  xx: the bf16 values (z, or the
+// target logits with bb = 0); bb: the Markov bias (or zero).
+__device__ __forceinline__ unsigned long long pow2_split2(unsigned long long xx,
+                                                          unsigned long long bb,
+                                                          unsigned long long c12,
+                                                          unsigned long long cr2,
+                                                          unsigned long long k2, float klo) {
+  const unsigned long long P = mul2(xx, c12);
+  float qa, qb;
+  unpack2(add2(fma2(bb, c12, P), k2), qa, qb);  // 1.5 * 2^23 + n
+  qa = fmaxf(qa, klo);
+  qb = fmaxf(qb, klo);
+  const unsigned long long M = sub2(pack2(qa, qb), k2);
+  unsigned long long F = fma2(bb, c12, sub2(P, M));
+  F = fma2(xx, cr2, fma2(bb, cr2, F));
+  float fa, fb;
+  unpack2(F, fa, fb);
+  const float sa = __uint_as_float(__float_as_uint(qa) * 8388608u + 0x3f800000u);  // 2^n
+  const float sb = __uint_as_float(__float_as_uint(qb) * 8388608u + 0x3f800000u);
+  return pack2(ex2_approx(fa) * sa, ex2_approx(fb) * sb);
+}
+
+// (h, l) += (x, y) for double-float pairs: TwoSum of the high parts, the low
+// parts added (their rounding is 2^-24 of a 2^-24 term).
+__device__ __forceinline__ void add_pair(float& h, float& l, float x, float y) {
+  float t, e;
+  two_sum(h, x, t, e);
+  h = t;
+  l += e + y;
+}
+
+// TwoSum tree over 8 packed pairs (16 values): the sum as (hi, lo).
+// Plain packed adds form the four-value partial sums (each a rounding near
+// 2^-25 of a partial, about the size of one weight's own fp32 rounding);
+// TwoSum the two levels above, so no rounding of a 16-token or larger sum
+// reaches the fixed-point totals.
+__device__ __forceinline__ void sum16(unsigned long long (&v)[8], float& hi, float& lo) {
+#pragma unroll
+  for (int e = 0; e < 4; ++e) v[e] = add2(v[e], v[e + 4]);
+#pragma unroll
+  for (int e = 0; e < 2; ++e) v[e] = add2(v[e], v[e + 2]);
+  unsigned long long s2, e2;
+  two_sum2(v[0], v[1], s2, e2);
+  float ha, hb, la, lb, er;
+  unpack2(s2, ha, hb);
+  unpack2(e2, la, lb);
+  two_sum(ha, hb, hi, er);
+  lo = er + (la + lb);
+}
+
+// Sampling: 32 consecutive tokens of one request row (one 32-column
+// accumulator load b = the Markov bias, and the z words zq), half h (tokens
+// 32h .. 32h + 31) of a 64-token block; `lim` = number of the block's tokens
+// below V.  Adds the fixed-point sum of 2^t, t = (z + b) log2(e)/T - ref, to
+// s.acc (units of 2^(s.ref - 40)), the sums of the half's two 16-token groups
+// to gs[2h], gs[2h + 1] (units of 2^s.ref), and the low parts of their
+// compensated sums to lo (converted once per block by the caller).  When the
+// half raises the lane's reference, s.acc, lo and the groups already summed
+// are rescaled exactly.
+//
+// The reference: ref = ceil(max y * c) from fp32 y = z + b (rounded
+// monotone in y, c = log2(e)/T > 0); NaN and +inf surface in that maximum
+// and drop the half (flagged); -inf (a masked token) weighs 0.
+// Each weight is formed without rounding y or t at the magnitude of the
+// logits (an fp32 y or t near 8 is off by up to 5e-7, which would shift
+// every CDF boundary after it):
+//   c = c12 + crest, c12 with 12 significant bits, so P = z c12 is exact
+//   (z is bf16); Q = P + b c12 (rounded) only picks the integer M = rint(Q)
+//   (a magic-number round) and n = M - ref (clamped at -125 so 2^n stays
+//   normal); P - M is exact; the fraction f = (P - M) + b c12 + (z + b) crest
+//   lies in [-1/2, 1/2] and is rounded twice at that magnitude (about 2e-8);
+//   2^f comes from ex2 (5.5e-8 RMS relative error on [-1/2, 1/2], measured on
+//   this GPU); 2^n scales it exactly, built from the magic number's bits.
+// The sums are compensated: plain packed adds form four-token partials,
+// TwoSum the levels above; a group's high part is converted to 2^-40 units
+// exactly with integer operations.
+__device__ __forceinline__ void epi_half(const uint32_t (&b)[32], const uint4 (&zq)[4], int h,
+                                         int lim, const TcParams& p, Part& s, float (&gs)[4],
+                                         float& lo) {
+  const int t0 = h * 32;
+  const bool ragged = lim < t0 + 32;  // warp-uniform: only the vocabulary's last block
+  float mx[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const uint32_t zw = (&zq[0].x)[k];
+    float ya, yb;
+    unpack2(add2(pack2(bf_lo(zw), bf_hi(zw)),
+                 pack2(__uint_as_float(b[2 * k]), __uint_as_float(b[2 * k + 1]))),
+            ya, yb);
+    if (ragged) {
+      if (t0 + 2 * k >= lim) ya = -INFINITY;
+      if (t0 + 2 * k + 1 >= lim) yb = -INFINITY;
     }
+    mx[k & 7] = fmax_nan(mx[k & 7], fmax_nan(ya, yb));
   }
-  float y[64];
 #pragma unroll
-  for (int e = 0; e < 32; ++e) unpack2(y2[e], y[2 * e], y[2 * e + 1]);
-  if (lim < 64) {
-#pragma unroll
-    for (int e = 0; e < 64; ++e)
-      if (e >= lim) y[e] = -INFINITY;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) y2[e] = pack2(y[2 * e], y[2 * e + 1]);
-  }
-  if (p.greedy) {
-    ArgMax t[32];
-    float chk = -INFINITY;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      t[e] = better(ArgMax{y[e], v0 + e}, ArgMax{y[e + 32], v0 + e + 32});
-      chk = fmax_nan(chk, fmax_nan(y[e], y[e + 32]));
-    }
-#pragma unroll
-    for (int w = 16; w > 0; w >>= 1)
-#pragma unroll
-      for (int e = 0; e < w; ++e) t[e] = better(t[e], t[e + w]);
-    s.best = better(s.best, t[0]);
-    if (!(chk < INFINITY)) s.bad = 1;
-    return;
-  }
-  // a = y * c with c = log2(e)/T rounded to fp32.  The block maximum is taken
-  // on y: the rounded product is monotone in y (c > 0), so the largest a is
-  // the product of the largest y.  NaN and +inf surface in that maximum;
-  // -inf (a masked token) stays -inf through the product and weighs 0.
-  float mx[32];
-#pragma unroll
-  for (int e = 0; e < 32; ++e) mx[e] = fmax_nan(y[e], y[e + 32]);
-#pragma unroll
-  for (int w = 16; w > 0; w >>= 1)
+  for (int w = 4; w > 0; w >>= 1)
 #pragma unroll
     for (int e = 0; e < w; ++e) mx[e] = fmax_nan(mx[e], mx[e + w]);
   const float cmax = mx[0] * p.sc.hi;
@@ -255,33 +353,68 @@ __device__ __forceinline__ void epi_block(const uint32_t (&b0)[32], const uint32
   } else if (cref > s.ref) {
     const int d = cref - s.ref;
     s.acc = d >= 63 ? 0 : (s.acc >> d);
+    const float sc = __int_as_float((127 - min(d, 126)) << 23);  // 2^-d, exact
+    lo *= sc;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) gs[g] *= sc;
     s.ref = cref;
   }
-  const float fref = static_cast<float>(s.ref);
-  const unsigned long long c2 = pack2(p.sc.hi, p.sc.hi), r2 = pack2(-fref, -fref);
-  // stage-major: all 64 exponent arguments, then all 64 ex2, then the four
-  // 16-token trees, so that independent operations issue back to back
+  const float kmag = 12582912.0f - static_cast<float>(s.ref);  // 1.5 * 2^23 - ref, exact
+  const float klo = 12582912.0f - 125.0f;
+  const unsigned long long c12 = pack2(p.c12, p.c12), cr2 = pack2(p.crest, p.crest);
+  const unsigned long long k2 = pack2(kmag, kmag);
 #pragma unroll
-  for (int e = 0; e < 32; ++e) unpack2(fma2(y2[e], c2, r2), y[2 * e], y[2 * e + 1]);  // a - ref
+  for (int gg = 0; gg < 2; ++gg) {
+    unsigned long long w2[8];
 #pragma unroll
-  for (int e = 0; e < 64; ++e) y[e] = ex2_approx(y[e]);
-#pragma unroll
-  for (int e = 0; e < 32; ++e) y2[e] = pack2(y[2 * e], y[2 * e + 1]);
-#pragma unroll
-  for (int w = 4; w > 0; w >>= 1)
-#pragma unroll
-    for (int g = 0; g < 4; ++g)
-#pragma unroll
-      for (int e = 0; e < w; ++e) y2[g * 8 + e] = add2(y2[g * 8 + e], y2[g * 8 + e + w]);
-#pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    float t0, t1;
-    unpack2(y2[g * 8], t0, t1);
-    gs[g] = t0 + t1;
+    for (int e = 0; e < 8; ++e) {
+      const int k = gg * 8 + e;  // the token pair (t0 + 2k, t0 + 2k + 1)
+      const uint32_t zw = (&zq[0].x)[k];
+      w2[e] = pow2_split2(pack2(bf_lo(zw), bf_hi(zw)),
+                          pack2(__uint_as_float(b[2 * k]), __uint_as_float(b[2 * k + 1])), c12,
+                          cr2, k2, klo);
+      if (ragged) {
+        float wa, wb;
+        unpack2(w2[e], wa, wb);
+        w2[e] = pack2(t0 + 2 * k < lim ? wa : 0.f, t0 + 2 * k + 1 < lim ? wb : 0.f);
+      }
+    }
+    float hi, glo;
+    sum16(w2, hi, glo);
+    gs[h * 2 + gg] = hi + glo;
+    s.acc += fix40(hi);
+    lo += glo;
   }
-  // one conversion to 2^-40 units per 64 tokens (64-bit conversions issue on
-  // the narrow FP64 pipe)
-  s.acc += __float2ll_rn(((gs[0] + gs[1]) + (gs[2] + gs[3])) * 1099511627776.0f);
+}
+
+// One 64-token block of a request row: its two 32-column halves one after
+// the other, the second loaded once the first is done (fewer live registers).
+// b0 must hold the first half's load, already issued at column tcol.  Every
+// lane of the warp calls this (the loads are warp-collective); `valid`
+// lanes compute.
+__device__ __forceinline__ void epi_block(uint32_t (&b0)[32], uint32_t (&b1)[32], uint32_t tcol,
+                                          const uint4 (&z0)[4], const uint4 (&z1)[4], int v0,
+                                          int lim, bool valid, const TcParams& p, Part& s,
+                                          float (&gs)[4]) {
+  float lo = 0.f;
+  tmem_wait_ld_regs(b0);
+  if (valid) {
+    if (p.greedy)
+      epi_half_greedy(b0, z0, 0, v0, lim, s);
+    else
+      epi_half(b0, z0, 0, lim, p, s, gs, lo);
+  }
+  __syncwarp();
+  tmem_ld_32x32b_x32(tcol + 32, b1);
+  tmem_wait_ld_regs(b1);
+  if (valid) {
+    if (p.greedy) {
+      epi_half_greedy(b1, z1, 1, v0, lim, s);
+    } else {
+      epi_half(b1, z1, 1, lim, p, s, gs, lo);
+      s.acc += __float2ll_rn(lo * 1099511627776.0f);  // one 64-bit conversion a block
+    }
+  }
 }
 
 // Stores the four 16-token group sums gs of block jj (0, 1) of a 128-token
@@ -480,12 +613,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int jj = 0; jj < 2; ++jj) {
         const int j = half * 2 + jj;  // z box (64 tokens) of this warp
         const int col = j * 64;
-        uint32_t b0[32], b1[32];
-        __syncwarp();  // tcgen05.ld is warp-collective: reconverge first
-        tmem_ld_32x32b_x32(tmem + lane_base + a * BN + col, b0);
-        tmem_ld_32x32b_x32(tmem + lane_base + a * BN + col + 32, b1);
+        const uint32_t tcol = tmem + lane_base + a * BN + col;
         const int v0 = t * BN + col;
         if (kBiasOut) {
+          uint32_t b0[32], b1[32];
+          __syncwarp();  // tcgen05.ld is warp-collective: reconverge first
+          tmem_ld_32x32b_x32(tcol, b0);
+          tmem_ld_32x32b_x32(tcol + 32, b1);
           tmem_wait_ld_regs(b0, b1);
           if (valid) {
             float* dst = p.bias_out + (size_t)n * p.V;
@@ -500,6 +634,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           continue;
         }
+        uint32_t b0[32], b1[32];
+        __syncwarp();  // tcgen05.ld is warp-collective: reconverge first
+        tmem_ld_32x32b_x32(tcol, b0);  // the first half, while the z box is awaited
         const uint32_t zs = (zit0 + j) % kZBoxes;
         wait_abortable(b_fullZ + 8 * (half * 4 + zs), (cpar >> zs) & 1u, &s_abort, p.status);
         cpar ^= 1u << zs;
@@ -512,9 +649,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(b_emptyZ + 8 * (half * 4 + zs));
-        tmem_wait_ld_regs(b0, b1);
         float gs[4] = {0.f, 0.f, 0.f, 0.f};
-        if (valid) epi_block(b0, b1, z0, z1, v0, min(64, p.V - v0), p, s, gs);
+        epi_block(b0, b1, tcol, z0, z1, v0, min(64, p.V - v0), valid, p, s, gs);
         if (own && !p.greedy) store_groups(p.sub + o * 8, jj, gs, s.ref, ref0);
       }
       tc_fence_before();
@@ -1032,10 +1168,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int jj = 0; jj < 2; ++jj) {
           const int j = half * 2 + jj;
           const int col = j * 64;
+          const uint32_t tcol = tmem + lane_base + a * BN + col;
           uint32_t b0[32], b1[32];
           __syncwarp();
-          tmem_ld_32x32b_x32(tmem + lane_base + a * BN + col, b0);
-          tmem_ld_32x32b_x32(tmem + lane_base + a * BN + col + 32, b1);
+          tmem_ld_32x32b_x32(tcol, b0);  // the first half, while the z box is awaited
           const int v0 = t * BN + col;
           const uint32_t zs = (zit + j) % nzs;
           wait_abortable(b_fullZ + 8 * (half * 4 + zs), (cpar >> zs) & 1u, &s_abort, p.status);
@@ -1049,9 +1185,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(b_emptyZ + 8 * (half * 4 + zs));
-          tmem_wait_ld_regs(b0, b1);
           float gs[4] = {0.f, 0.f, 0.f, 0.f};
-          if (valid) epi_block(b0, b1, z0, z1, v0, min(64, p.V - v0), p, s, gs);
+          epi_block(b0, b1, tcol, z0, z1, v0, min(64, p.V - v0), valid, p, s, gs);
           if (own && !p.greedy) store_groups(p.sub + o * 8, jj, gs, s.ref, ref0);
         }
         tc_fence_before();
@@ -1128,6 +1263,7 @@ struct FinalParams {
   int R, V, r, nK, n_vt, n_halves, gamma, pair;
   long long n_rows;
   ScalePair sc;
+  float c12, crest;  // log2(e)/T = c12 + crest, c12 with 12 significant bits
   const __nv_bfloat16* E;
   const __nv_bfloat16* z;       // [R][gamma][V]
   const __nv_bfloat16* target;  // [n_rows][V]
@@ -1162,84 +1298,69 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// 32 consecutive tokens of one request's final row: p = 2^(a_p) / Sp from the
-// target logits and, for a residual draw, q = 2^(a_q) / Sq from the draft
-// logits z + bias; adds the sums of max(0, p - q) (p itself for a bonus
-// draw) and of p to the caller's fp32 running sums (converted to fixed point
-// once per 128-token partial).  a = y * c with c = log2(e)/T rounded to fp32
-// (the rounding Sp and Sq were formed with).  With 1/S = (hi + lo) * 2^e,
-// hi in [0.5, 1), every token has 2^a <= S < 2^(1 - e), so
-//   p = 2^(a + e) * (hi + lo),  a + e <= 1:
-// one FMA for the exponent argument, one ex2, and the (hi, lo) product --
-// no block maximum, reference or rescaling.  p - q keeps its precision where
-// p and q nearly cancel.  Element pairs use the packed two-wide fp32
-// instructions; a NaN input makes its block contribute nothing (the row pass
-// reports non-finite target rows).
+// The final draw's weights for 32 tokens of one request row (accumulator
+// load b = the Markov bias of the rejected position, z and target words):
+// p = 2^(t c + ep) (hi + lo) with 1/Sp = (hi + lo) 2^ep (so p <= 2), and the
+// residual max(0, p - q), q = 2^((z + b) c + eq) (iq.hi + iq.lo), or p itself
+// for a bonus draw.  The exponents are split as in the draft epilogue (no
+// fp32 rounding of t c or of z + b at the magnitude of the logits) and the
+// 16-token sums are TwoSum trees; acc holds (residual hi, lo, p hi, lo).
+// A NaN group is left out (the pick's recompute flags it).
 __device__ __forceinline__ void fin_block(const uint32_t (&b)[32], const uint4 (&zq)[4],
-                                          const uint4 (&tq)[4], int lim, bool resid, ScalePair sc,
-                                          InvPair ip, InvPair iq, float& fr, float& fp) {
+                                          const uint4 (&tq)[4], int lim, bool resid, float c12,
+                                          float crest, InvPair ip, InvPair iq, float (&acc)[4]) {
   if (ip.hi == 0.f) return;  // no target normaliser: no mass
   const bool qlive = resid && iq.hi != 0.f;
-  // stage-major: each step over all 32 tokens before the next, so that the
-  // independent operations of one step issue back to back
-  float x[32];  // exponent arguments of p, then weights, then p
+  const unsigned long long c2 = pack2(c12, c12), cr2 = pack2(crest, crest);
+  const float kp = 12582912.0f + (float)ip.e, kq = 12582912.0f + (float)iq.e;
+  const unsigned long long kp2 = pack2(kp, kp), kq2 = pack2(kq, kq);
+  const float klo = 12582912.0f - 125.0f;
+  const unsigned long long iph = pack2(ip.hi, ip.hi), ipl = pack2(ip.lo, ip.lo);
+  const unsigned long long iqh = pack2(iq.hi, iq.hi), iql = pack2(iq.lo, iq.lo);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint32_t wt[4] = {tq[q].x, tq[q].y, tq[q].z, tq[q].w};
+  for (int gg = 0; gg < 2; ++gg) {
+    unsigned long long p2[8], r2[8];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      x[q * 8 + 2 * e] = bf_lo(wt[e]);
-      x[q * 8 + 2 * e + 1] = bf_hi(wt[e]);
-    }
-  }
-  if (lim < 32) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (i >= lim) x[i] = -INFINITY;
-  }
-  const float ep = (float)ip.e;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) x[i] = fmaf(x[i], sc.hi, ep);
-#pragma unroll
-  for (int i = 0; i < 32; ++i) x[i] = ex2_fast(x[i]);
-#pragma unroll
-  for (int i = 0; i < 32; ++i) x[i] = fmaf(x[i], ip.hi, x[i] * ip.lo);  // p
-  float r[32];
-  if (qlive) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t wz[4] = {zq[q].x, zq[q].y, zq[q].z, zq[q].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        r[q * 8 + 2 * e] = bf_lo(wz[e]) + __uint_as_float(b[q * 8 + 2 * e]);
-        r[q * 8 + 2 * e + 1] = bf_hi(wz[e]) + __uint_as_float(b[q * 8 + 2 * e + 1]);
+    for (int e = 0; e < 8; ++e) {
+      const int k = gg * 8 + e;  // the token pair (2k, 2k + 1)
+      const uint32_t tw = (&tq[0].x)[k];
+      const unsigned long long wp =
+          pow2_split2(pack2(bf_lo(tw), bf_hi(tw)), 0ull, c2, cr2, kp2, klo);
+      unsigned long long pp = fma2(wp, iph, mul2(wp, ipl));
+      float pa, pb;
+      unpack2(pp, pa, pb);
+      if (2 * k >= lim) pa = 0.f;
+      if (2 * k + 1 >= lim) pb = 0.f;
+      p2[e] = pack2(pa, pb);
+      if (qlive) {
+        const uint32_t zw = (&zq[0].x)[k];
+        const unsigned long long wq =
+            pow2_split2(pack2(bf_lo(zw), bf_hi(zw)),
+                        pack2(__uint_as_float(b[2 * k]), __uint_as_float(b[2 * k + 1])), c2, cr2,
+                        kq2, klo);
+        float qa, qb;
+        unpack2(fma2(wq, iqh, mul2(wq, iql)), qa, qb);
+        r2[e] = pack2(fmaxf(0.0f, pa - qa), fmaxf(0.0f, pb - qb));
+      } else {
+        r2[e] = p2[e];
       }
     }
-    if (lim < 32) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i >= lim) r[i] = -INFINITY;
-    }
-    const float eq = (float)iq.e;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) r[i] = fmaf(r[i], sc.hi, eq);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) r[i] = ex2_fast(r[i]);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) r[i] = fmaxf(0.0f, x[i] - fmaf(r[i], iq.hi, r[i] * iq.lo));
-  } else {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) r[i] = x[i];
+    float ph, pl, rh, rl;
+    sum16(p2, ph, pl);
+    sum16(r2, rh, rl);
+    if (ph == ph) add_pair(acc[2], acc[3], ph, pl);
+    if (rh == rh) add_pair(acc[0], acc[1], rh, rl);
   }
-#pragma unroll
-  for (int w = 16; w > 0; w >>= 1)
-#pragma unroll
-    for (int i = 0; i < w; ++i) {
-      x[i] += x[i + w];
-      r[i] += r[i + w];
-    }
-  if (x[0] == x[0]) fp += x[0];
-  if (r[0] == r[0]) fr += r[0];
+}
+
+// round(x * 2^60) for 0 <= x < 8, from the float's bits (exact once
+// x * 2^60 >= 2^23; below, the bits under 2^-60 are dropped).
+__device__ __forceinline__ long long fix60(float x) {
+  const uint32_t b = __float_as_uint(x);
+  const int e = (int)(b >> 23);
+  const unsigned long long m = (b & 0x7fffffu) | (e ? 0x800000u : 0u);
+  const int sh = e - 90;  // x * 2^60 = m * 2^(e - 150 + 60)
+  return (long long)(sh >= 0 ? m << sh : (sh > -24 ? m >> -sh : 0ull));
 }
 
 
@@ -1452,7 +1573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = live && t < p.n_vt;
       wait_abortable(b_accFull + 8 * a, aph, &s_abort, p.status);
       tc_fence_after();
-      float fr = 0.f, fp = 0.f;
+      float facc[4] = {0.f, 0.f, 0.f, 0.f};  // residual (hi, lo), p (hi, lo)
 #pragma unroll 1
       for (int jj = 0; jj < kFinSteps / 2; ++jj) {
         const int j = half * (kFinSteps / 2) + jj;
@@ -1479,15 +1600,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(b_emptyZ + 8 * (half * 4 + zs));
         tmem_wait_ld_regs(b);
-        if (valid) fin_block(b, zq, tq, min(32, p.V - v0), resid, p.sc, st.ip, st.iq, fr, fp);
+        if (valid)
+          fin_block(b, zq, tq, min(32, p.V - v0), resid, p.c12, p.crest, st.ip, st.iq, facc);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_accEmpty + 8 * a);
       if (n < p.R && t < p.n_vt && t * 2 + half < p.n_halves) {
         long long* o = p.fin_part + ((size_t)n * p.n_halves + t * 2 + half) * 2;
-        o[0] = __float2ll_rn(fr * 1152921504606846976.0f);  // 2^60
-        o[1] = __float2ll_rn(fp * 1152921504606846976.0f);
+        // 2^-60 units: the high parts from their bits, one conversion a low part
+        o[0] = fix60(facc[0]) + __float2ll_rn(facc[1] * 1152921504606846976.0f);
+        o[1] = fix60(facc[2]) + __float2ll_rn(facc[3] * 1152921504606846976.0f);
       }
     }
   }
@@ -1496,6 +1619,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
+}
+
+// c = c12 + crest with c12 = c rounded to 12 significant bits (a bf16 times
+// c12 is exact in fp32) and crest the fp32 rounding of the remainder.
+void split12(double c, float* c12, float* crest) {
+  int e = 0;
+  const double m = frexp(c, &e);  // c = m 2^e, m in [1/2, 1)
+  const double h = ldexp(nearbyint(ldexp(m, 12)), e - 12);
+  *c12 = (float)h;
+  *crest = (float)(c - h);
 }
 
 // The driver's tensor-map encoder (a process-wide entry point, the same for
@@ -1603,6 +1736,7 @@ cudaError_t launch_draft_partial_tc(const DraftArgs& a, int k, const int32_t* pr
   p.n_parts = (a.V + kHalf - 1) / kHalf;
   p.greedy = a.T == 0.0f;
   p.sc = make_scale(p.greedy ? 1.0 : 1.4426950408889634 / (double)a.T);
+  split12(p.greedy ? 1.0 : 1.4426950408889634 / (double)a.T, &p.c12, &p.crest);
   p.E = static_cast<const __nv_bfloat16*>(a.E);
   p.prev = prev;
   p.prev_stride = prev_stride;
@@ -1637,6 +1771,7 @@ cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st) {
   p.n_parts = (a.V + kHalf - 1) / kHalf;
   p.greedy = a.T == 0.0f;
   p.sc = make_scale(p.greedy ? 1.0 : 1.4426950408889634 / (double)a.T);
+  split12(p.greedy ? 1.0 : 1.4426950408889634 / (double)a.T, &p.c12, &p.crest);
   p.E = static_cast<const __nv_bfloat16*>(a.E);
   p.prev = nullptr;
   p.prev_stride = 0;
@@ -1752,6 +1887,7 @@ cudaError_t launch_final_tc(const VerifyArgs& a, const VerifyState* vstate, long
   p.gamma = a.gamma;
   p.n_rows = a.n_rows;
   p.sc = make_scale(1.4426950408889634 / (double)a.T);
+  split12(1.4426950408889634 / (double)a.T, &p.c12, &p.crest);
   p.E = static_cast<const __nv_bfloat16*>(a.E);
   p.z = static_cast<const __nv_bfloat16*>(a.z);
   p.target = static_cast<const __nv_bfloat16*>(a.target);

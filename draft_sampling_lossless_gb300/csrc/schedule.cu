@@ -11,7 +11,8 @@
 // survival panel: E = R + sum a, rate = E / T(B).
 //
 // The kernel (schedule_radix_kernel) runs on a cluster of C <= 8 CTAs of 512
-// threads; CTA c owns a contiguous chunk of the candidates and of the
+// threads (one CTA per 1024 candidates, so a mid-size batch still has several
+// CTAs' loads in flight); CTA c owns a contiguous chunk of the candidates and of the
 // requests.  Candidates are 64-bit words (key << 32 | flat index n*gamma + j)
 // with key = 0xffffffff - bits(a): for a >= 0 the float's bits order like its
 // value, so ascending keys are descending a.
@@ -59,7 +60,7 @@ constexpr int kSortThreads = 512;
 constexpr int kSortWarps = kSortThreads / 32;
 constexpr int kBins = 256;
 constexpr int kMaxClusterCtas = 8;
-constexpr int kPerCta = 4096;  // candidates a CTA owns before the cluster grows
+constexpr int kPerCta = 1024;  // candidates a CTA owns before the cluster grows
 
 enum { kModeEarly = 0, kModeGlobal = 1, kModeCapacity = 2 };
 
@@ -145,15 +146,23 @@ __global__ void __launch_bounds__(kSortThreads) schedule_radix_kernel(
     const int sh = 32 + 8 * pass;
     for (int i = tid; i < kSortWarps * kBins; i += kSortThreads) (&wcnt[0][0])[i] = 0;
     __syncthreads();
-    for (int base = w0; base < w1; base += 32) {
-      const int e = base + lane;
-      const bool ok = e < w1;
-      const unsigned m = __ballot_sync(0xffffffffu, ok);
-      if (ok) {
-        const unsigned long long x = pass == 0 ? candidate(a, e, status) : src[e];
-        const unsigned d = (unsigned)(x >> sh) & 255u;
-        const unsigned peers = __match_any_sync(m, d);
-        if (lane == __ffs(peers) - 1) wcnt[wid][d] += __popc(peers);
+    // four rounds of 32 at a time: their loads are in flight together
+    for (int base = w0; base < w1; base += 128) {
+      unsigned long long xs[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int e = base + q * 32 + lane;
+        xs[q] = e < w1 ? (pass == 0 ? candidate(a, e, status) : src[e]) : 0ull;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const bool ok = base + q * 32 + lane < w1;
+        const unsigned m = __ballot_sync(0xffffffffu, ok);
+        if (ok) {
+          const unsigned d = (unsigned)(xs[q] >> sh) & 255u;
+          const unsigned peers = __match_any_sync(m, d);
+          if (lane == __ffs(peers) - 1) wcnt[wid][d] += __popc(peers);
+        }
       }
     }
     __syncthreads();
@@ -185,23 +194,29 @@ __global__ void __launch_bounds__(kSortThreads) schedule_radix_kernel(
         for (int w = 0; w < kSortWarps; ++w) wcnt[w][tid] += base;
       }
       __syncthreads();
-      for (int base = w0; base < w1; base += 32) {
-        const int e = base + lane;
-        const bool ok = e < w1;
-        const unsigned m = __ballot_sync(0xffffffffu, ok);
-        unsigned long long x = 0;
-        unsigned d = 0, peers = 0;
-        int pos = 0;
-        if (ok) {
-          x = pass == 0 ? candidate(a, e, status) : src[e];
-          d = (unsigned)(x >> sh) & 255u;
-          peers = __match_any_sync(m, d);
-          pos = wcnt[wid][d] + __popc(peers & lt_mask);
+      for (int base = w0; base < w1; base += 128) {
+        unsigned long long xs[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int e = base + q * 32 + lane;
+          xs[q] = e < w1 ? (pass == 0 ? candidate(a, e, status) : src[e]) : 0ull;
         }
-        __syncwarp();
-        if (ok && lane == __ffs(peers) - 1) wcnt[wid][d] += __popc(peers);
-        __syncwarp();
-        if (ok) dst[pos] = x;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // in order: the scatter is stable
+          const bool ok = base + q * 32 + lane < w1;
+          const unsigned m = __ballot_sync(0xffffffffu, ok);
+          unsigned d = 0, peers = 0;
+          int pos = 0;
+          if (ok) {
+            d = (unsigned)(xs[q] >> sh) & 255u;
+            peers = __match_any_sync(m, d);
+            pos = wcnt[wid][d] + __popc(peers & lt_mask);
+          }
+          __syncwarp();
+          if (ok && lane == __ffs(peers) - 1) wcnt[wid][d] += __popc(peers);
+          __syncwarp();
+          if (ok) dst[pos] = xs[q];
+        }
       }
       cl.sync();  // the pass's output is complete and visible to the cluster
       src = dst;
@@ -297,6 +312,7 @@ __global__ void __launch_bounds__(kSortThreads) schedule_radix_kernel(
   long long lsum = 0;
   for (int r = q0; r < q1; ++r) {
     int cnt = 0;
+#pragma unroll 8
     for (int j = 0; j < gamma; ++j) cnt += __ldcg(rank + (size_t)r * gamma + j) < istar;
     ell[r] = cnt;
     lsum += 1 + cnt;
@@ -327,14 +343,14 @@ cudaError_t launch_radix(const SchedArgs& s, int mode, const int32_t* capacity, 
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = C;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = C > 1 ? 2 : 1;  // one CTA: a plain launch (an implicit cluster of one)
   cudaError_t e = cudaSuccess;
   DSPARK_LAUNCH(kKindSchedule, st,
                 e = cudaLaunchKernelEx(&cfg, schedule_radix_kernel, s.R, s.gamma, imax, mode,
