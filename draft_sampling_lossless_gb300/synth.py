@@ -17,6 +17,9 @@ Readings of the workload descriptions:
 * Uniforms are 24-bit: ``k * 2**-24`` with ``k`` uniform in ``[0, 2**24)``.
 * Hidden states are ``N(0, 1)``; confidence weights ``N(0, 0.05)`` for every
   workload (the tiny workload's stated value carried to the others).
+* The RNN head's recurrence matrix U (``rnn_recurrence``) is ``N(0,
+  0.5 / sqrt(r))`` in the workload's dtype: a spectral radius near 0.5, so
+  the state is a decaying sum over the prefix.
 """
 
 from __future__ import annotations
@@ -88,7 +91,7 @@ WORKLOADS = {
 
 # Tensor ids: one generator stream per tensor.
 _TID = dict(z=1, E=2, W=3, anchor=4, u_draft=5, u_acc=6, u_fin=7, h=8, w=9, c=10,
-            tnoise=11, zbonus=12, alpha=13, gpick=14, gother=15)
+            tnoise=11, zbonus=12, alpha=13, gpick=14, gother=15, U=16)
 
 
 def _gen(seed: int, tid: str, device) -> torch.Generator:
@@ -186,6 +189,12 @@ def make_inputs(wl: Workload, device="cpu", seed: int | None = None) -> Inputs:
         c_in = torch.from_numpy(c).to(device)
     return Inputs(wl, z, E, W, anchor, u_draft, u_acc, u_fin, h, w_conf,
                   sts_temperatures(wl).to(device), c_in, sps_table(wl).to(device))
+
+
+def rnn_recurrence(wl: Workload, device="cpu", seed: int | None = None) -> torch.Tensor:
+    """U [r, r] for the RNN head, N(0, 0.5 / sqrt(r)) in the workload's dtype."""
+    s = wl.seed if seed is None else seed
+    return _normal((wl.r, wl.r), 0.5 / math.sqrt(wl.r), wl.torch_dtype, s, "U", device)
 
 
 @dataclass

@@ -44,6 +44,14 @@
 //  * Capacity scheduling: with a capacity K (the batch the global search
 //    chose on the survival values two steps earlier) the batch is exactly the
 //    first min(max(K - R, 0), R*gamma) candidates of the current order.
+//  * RNN sequential head (named, no formula given): s_k = tanh(E[x_{k-1}] +
+//    s_{k-1} U), s_{-1} = 0, U an r x r matrix; s_k replaces the Markov row
+//    E[x_{k-1}] in the bias (bias_k = s_k W).  The confidence head keeps
+//    W1[x_{k-1}].  The state is stored in the table's type (bf16 or fp32);
+//    its pre-activation is accumulated in fp32 (the embedding, then the fused
+//    multiply-adds s_{k-1}[i] * U[i][j], i ascending) and tanh is taken in
+//    double, so the stored (quantised) state is decided in the same
+//    precision as on the GPU.
 //  * Verification: accept position j iff u_acc < p_j(x_j) / q_j(x_j)
 //    (strict); at the first rejection draw from max(0, p - q) with the
 //    request's final uniform, or from p if that mass is zero; if every
@@ -72,15 +80,47 @@ constexpr int kFixShift = 40;  // survival values summed in units of 2^-40
 // ------------------------------------------------ Markov head and softmax
 // Explainer, Markov-head panel; news article, innovation 1 (low-rank table).
 
-// bias[v] = sum_{i < r} E[prev][i] * W[i][v], i ascending; zero if prev < 0.
-void markov_bias_row(int V, int r, const double* E, const double* W, int64_t prev, double* bias) {
+// bias[v] = sum_{i < r} e[i] * W[i][v], i ascending; zero if e is null.
+void row_bias(int V, int r, const double* e, const double* W, double* bias) {
   for (int v = 0; v < V; ++v) bias[v] = 0.0;
-  if (prev < 0) return;
-  const double* e = E + (size_t)prev * r;
+  if (e == nullptr) return;
   for (int i = 0; i < r; ++i) {
     const double ei = e[i];
     const double* w = W + (size_t)i * V;
     for (int v = 0; v < V; ++v) bias[v] = bias[v] + ei * w[v];
+  }
+}
+
+// bias[v] = sum_{i < r} E[prev][i] * W[i][v], i ascending; zero if prev < 0.
+void markov_bias_row(int V, int r, const double* E, const double* W, int64_t prev, double* bias) {
+  row_bias(V, r, prev >= 0 ? E + (size_t)prev * r : nullptr, W, bias);
+}
+
+// ------------------------------------------------ RNN sequential head
+// News article, innovation 1 (an RNN head keeps a recurrent state);
+// explainer, Markov-head panel (it accumulates the prefix inside the block).
+
+// Nearest bf16 value to x (8 significant bits, ties to even), as a double.
+double round_bf16(double x) {
+  if (x == 0.0 || !std::isfinite(x)) return x;
+  if (std::fabs(x) < std::ldexp(1.0, -126))  // subnormal bf16: multiples of 2^-133
+    return std::ldexp(std::nearbyint(std::ldexp(x, 133)), -133);
+  int e;
+  const double m = std::frexp(x, &e);  // 0.5 <= |m| < 1
+  return std::ldexp(std::nearbyint(std::ldexp(m, 8)), e - 8);
+}
+
+// dt 0: bf16, 1: fp32 (the conversion rounds to nearest, ties to even).
+double round_state(double x, int dt) { return dt == 0 ? round_bf16(x) : (double)(float)x; }
+
+// s[j] = round(tanh(pre_j)); pre_j in fp32: E[prev][j] (0 if prev < 0), then
+// fmaf(s_prev[i], U[i][j], pre_j) for i = 0..r-1.
+void rnn_state(int r, int dt, const double* E, const double* U, int64_t prev,
+               const double* s_prev, double* s) {
+  for (int j = 0; j < r; ++j) {
+    float acc = prev >= 0 ? (float)E[(size_t)prev * r + j] : 0.0f;
+    for (int i = 0; i < r; ++i) acc = std::fmaf((float)s_prev[i], (float)U[(size_t)i * r + j], acc);
+    s[j] = round_state(std::tanh((double)acc), dt);
   }
 }
 
@@ -119,15 +159,31 @@ int64_t first_argmax(int V, const double* y) {
   return best;
 }
 
-// q over the vocabulary at one draft position: softmax((z_k + E[prev] W) / T).
-void draft_distribution(int V, int r, double T, const double* zk, const double* E, const double* W,
-                        int64_t prev, double* q, double* tmp) {
-  markov_bias_row(V, r, E, W, prev, tmp);
+// q over the vocabulary at one draft position: softmax((z_k + e W) / T),
+// e the bias row (null: no bias).
+void draft_distribution_row(int V, int r, double T, const double* zk, const double* e,
+                            const double* W, double* q, double* tmp) {
+  row_bias(V, r, e, W, tmp);
   for (int v = 0; v < V; ++v) tmp[v] = (zk[v] + tmp[v]) / T;
   double m;
   const double S = softmax_weights(V, tmp, q, &m);
   const double lse = m + std::log(S);
   for (int v = 0; v < V; ++v) q[v] = std::exp(tmp[v] - lse);
+}
+
+// q over the vocabulary at one draft position: softmax((z_k + E[prev] W) / T).
+void draft_distribution(int V, int r, double T, const double* zk, const double* E, const double* W,
+                        int64_t prev, double* q, double* tmp) {
+  draft_distribution_row(V, r, T, zk, prev >= 0 ? E + (size_t)prev * r : nullptr, W, q, tmp);
+}
+
+// The bias row of request n's draft position j: the RNN state S[n][j] when
+// S is given, else the Markov row E[x_{j-1}] (x_{-1} the anchor; null if < 0).
+const double* bias_row(int G, int r, const double* E, const double* S, const int64_t* anchor,
+                       const int64_t* tokens, int n, int64_t j) {
+  if (S != nullptr) return S + ((size_t)n * G + j) * r;
+  const int64_t prev = j == 0 ? anchor[n] : tokens[(size_t)n * G + j - 1];
+  return prev >= 0 ? E + (size_t)prev * r : nullptr;
 }
 
 // p over the vocabulary of one target row: softmax(row / T); returns lse.
@@ -259,6 +315,72 @@ void oc_draft_sample(int R, int G, int V, int r, double T, const double* z, cons
   }
 }
 
+// The RNN head's draft: for k = 0..gamma-1, s_k = rnn_state(x_{k-1}, s_{k-1})
+// (s_{-1} = 0, x_{-1} the anchor), y = (z_k + s_k W) / T, then as above.
+// S: [R][G][r] the states.
+void oc_draft_sample_rnn(int R, int G, int V, int r, int dt, double T, const double* z,
+                         const double* E, const double* U, const double* W,
+                         const int64_t* anchor, const double* u, int64_t* tokens, double* q_lse,
+                         double* q_tok, double* S) {
+#pragma omp parallel
+  {
+    std::vector<double> y(V), w(V), zero(r, 0.0);
+#pragma omp for schedule(dynamic, 1)
+    for (int n = 0; n < R; ++n) {
+      int64_t prev = anchor[n];
+      const double* s_prev = zero.data();
+      for (int k = 0; k < G; ++k) {
+        const size_t nk = (size_t)n * G + k;
+        double* s = S + nk * r;
+        rnn_state(r, dt, E, U, prev, s_prev, s);
+        row_bias(V, r, s, W, y.data());
+        const double* zk = z + nk * V;
+        for (int v = 0; v < V; ++v) y[v] = zk[v] + y[v];
+        int64_t x;
+        if (T == 0.0) {
+          x = first_argmax(V, y.data());
+          q_lse[nk] = y[x];
+          q_tok[nk] = 1.0;
+        } else {
+          for (int v = 0; v < V; ++v) y[v] = y[v] / T;
+          double m;
+          const double Sw = softmax_weights(V, y.data(), w.data(), &m);
+          const double lse = m + std::log(Sw);
+          x = inverse_cdf(V, w.data(), u[nk]);
+          q_lse[nk] = lse;
+          q_tok[nk] = std::exp(y[x] - lse);
+        }
+        tokens[nk] = x;
+        prev = x;
+        s_prev = s;
+      }
+    }
+  }
+}
+
+// The RNN states of given drafts (s_k from x_{k-1} and s_{k-1}): S [R][G][r].
+void oc_rnn_states(int R, int G, int r, int dt, const double* E, const double* U,
+                   const int64_t* anchor, const int64_t* tokens, double* S) {
+#pragma omp parallel
+  {
+    std::vector<double> zero(r, 0.0);
+#pragma omp for schedule(static)
+    for (int n = 0; n < R; ++n) {
+      const double* s_prev = zero.data();
+      for (int k = 0; k < G; ++k) {
+        const int64_t prev = k == 0 ? anchor[n] : tokens[(size_t)n * G + k - 1];
+        double* s = S + ((size_t)n * G + k) * r;
+        rnn_state(r, dt, E, U, prev, s_prev, s);
+        s_prev = s;
+      }
+    }
+  }
+}
+
+void oc_round_state(int64_t n, int dt, const double* x, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = round_state(x[i], dt);
+}
+
 // ------------------------------------------------------------- stage 2: confidence
 // c_{n,k} = sigmoid((w[:d] . h_{n,k} + w[d:] . E1[x_{k-1}]) / t_k); a = running
 // product of c.  With c_in given the head is skipped (d, h, w, E1 unused).
@@ -359,7 +481,7 @@ void oc_verify(int R, int G, int V, int r, double T, const double* z, const doub
                const double* W, const int64_t* anchor, const int64_t* tokens, const int64_t* ell,
                const int64_t* row_off, const double* target, int64_t n_rows, const double* u_acc,
                const double* u_fin, int64_t* n_acc, int64_t* out_tokens, double* p_lse,
-               int64_t* final_kind, int64_t* final_row) {
+               int64_t* final_kind, int64_t* final_row, const double* S) {
   for (int64_t i = 0; i < n_rows; ++i) p_lse[i] = std::numeric_limits<double>::quiet_NaN();
 #pragma omp parallel
   {
@@ -384,9 +506,9 @@ void oc_verify(int R, int G, int V, int r, double T, const double* z, const doub
           acc = first_argmax(V, row) == x;
         } else {
           target_distribution(V, T, row, p.data(), tmp.data());
-          const int64_t prev = j == 0 ? anchor[n] : tokens[(size_t)n * G + j - 1];
-          draft_distribution(V, r, T, z + ((size_t)n * G + j) * V, E, W, prev, q.data(),
-                             tmp.data());
+          draft_distribution_row(V, r, T, z + ((size_t)n * G + j) * V,
+                                 bias_row(G, r, E, S, anchor, tokens, n, j), W, q.data(),
+                                 tmp.data());
           acc = u_acc[(size_t)n * G + j] < p[x] / q[x];
         }
         if (!acc) {
@@ -408,9 +530,9 @@ void oc_verify(int R, int G, int V, int r, double T, const double* z, const doub
       } else {
         target_distribution(V, T, row, p.data(), tmp.data());
         if (rejected) {
-          const int64_t prev = na == 0 ? anchor[n] : tokens[(size_t)n * G + na - 1];
-          draft_distribution(V, r, T, z + ((size_t)n * G + na) * V, E, W, prev, q.data(),
-                             tmp.data());
+          draft_distribution_row(V, r, T, z + ((size_t)n * G + na) * V,
+                                 bias_row(G, r, E, S, anchor, tokens, n, na), W, q.data(),
+                                 tmp.data());
           double mass = 0.0;
           for (int v = 0; v < V; ++v) {
             q[v] = std::max(0.0, p[v] - q[v]);  // the residual, in place of q
@@ -434,14 +556,16 @@ void oc_verify(int R, int G, int V, int r, double T, const double* z, const doub
 
 // The distribution request n's final token is drawn from, given its target
 // row for position j+1: the residual max(0, p - q_{j+1}) when rejected there
-// (p if that mass is zero), else the bonus row's p.  z_row is z[n][j].
+// (p if that mass is zero), else the bonus row's p.  z_row is z[n][j]; the
+// bias row is s_row when given (the RNN state), else E[prev].
 void oc_final_weights(int V, int r, double T, const double* z_row, const double* E,
                       const double* W, int64_t prev, const double* target_row, int rejected,
-                      double* w) {
+                      double* w, const double* s_row) {
   std::vector<double> q(V), tmp(V);
   target_distribution(V, T, target_row, w, tmp.data());
   if (!rejected) return;
-  draft_distribution(V, r, T, z_row, E, W, prev, q.data(), tmp.data());
+  const double* e = s_row != nullptr ? s_row : (prev >= 0 ? E + (size_t)prev * r : nullptr);
+  draft_distribution_row(V, r, T, z_row, e, W, q.data(), tmp.data());
   double mass = 0.0;
   for (int v = 0; v < V; ++v) {
     tmp[v] = std::max(0.0, w[v] - q[v]);

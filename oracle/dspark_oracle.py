@@ -49,6 +49,16 @@ Readings where the pages are silent:
   global search chose on the survival values two steps earlier) is filled
   with the first min(max(K - R, 0), R * gamma) candidates of the current
   order.
+* RNN sequential head (the pages name it and give no formula): an Elman
+  recurrence over the block's prefix, s_k = tanh(E[x_{k-1}] + s_{k-1} U) with
+  s_{-1} = 0 and U an r x r matrix; s_k takes the place of the Markov row
+  E[x_{k-1}] in the bias (bias_k = s_k W), so U = 0 leaves a one-token
+  memory.  The confidence head keeps W1[x_{k-1}] as written.  The state is
+  stored in the table's type (bf16 or fp32) and its pre-activation is
+  accumulated in fp32 -- the embedding first, then the fused multiply-adds
+  s_{k-1}[i] * U[i][j] for i ascending -- and tanh is taken in float64: the
+  stored state is a quantised value, so both implementations take its
+  rounding in the same precision.
 * Verification: accept draft position j iff u_acc < p_j(x_j) / q_j(x_j)
   (strict); on the first rejection sample max(0, p - q) normalised with the
   request's final uniform, or p itself if that mass is zero; if every
@@ -152,6 +162,112 @@ def draft_distribution(z_k, E, W, prev, T):
     y = (z_k + markov_bias(E, W, prev)) / T
     e, lse = softmax_rows(y)
     return np.exp(y - lse[:, None])
+
+
+# --------------------------------------------------------------------------
+# RNN sequential head (news article section 创新一, second stage: the RNN head
+# keeps a recurrent state and so captures longer dependencies; explainer,
+# Markov-head panel: an RNN head accumulates the prefix inside the block)
+# --------------------------------------------------------------------------
+
+def round_to(x, dtype: str) -> np.ndarray:
+    """Round float64 values to the nearest bf16 ("bf16") or fp32 ("f32")
+    value, ties to even, in one step; returned as float64."""
+    x = np.asarray(x, dtype=np.float64)
+    if dtype == "f32":
+        return x.astype(np.float32).astype(np.float64)
+    m, e = np.frexp(x)  # x = m 2^e, 0.5 <= |m| < 1: 8 significant bits kept
+    out = np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
+    tiny = np.abs(x) < 2.0 ** -126  # bf16 subnormals: spacing 2^-133
+    out[tiny] = np.ldexp(np.rint(np.ldexp(x[tiny], 133)), -133)
+    return out
+
+
+def fma32(a, b, c) -> np.ndarray:
+    """fp32 fused multiply-add a * b + c with a single rounding (IEEE 754),
+    for fp32 operands.  The product is exact in float64; TwoSum gives the
+    float64 sum's rounding error, which decides the fp32 rounding when the
+    float64 sum lands exactly half-way between two fp32 values."""
+    a, b, c = (np.asarray(t, dtype=np.float32).astype(np.float64) for t in (a, b, c))
+    a, b, c = np.broadcast_arrays(a, b, c)
+    p = a * b
+    hi = p + c
+    bv = hi - p
+    lo = (p - (hi - bv)) + (c - bv)
+    f = hi.astype(np.float32)
+    d = hi - f.astype(np.float64)
+    g = np.nextafter(f, np.where(d > 0, np.float32(np.inf), np.float32(-np.inf)))
+    half = (d != 0) & (hi == (f.astype(np.float64) + g.astype(np.float64)) / 2)
+    flip = half & (lo != 0) & (np.sign(lo) == np.sign(d))
+    return np.where(flip, g, f)
+
+
+def rnn_state(E, U, prev, s_prev, dtype: str) -> np.ndarray:
+    """s = round(tanh(pre)) for a batch of requests: pre[n, j] starts from
+    E[prev[n], j] (0 when prev < 0) and adds s_prev[n, i] * U[i, j] for
+    i = 0..r-1 in fp32 fused multiply-adds; tanh in float64; rounded to the
+    state type.  E: [V, r], U: [r, r], prev: [n], s_prev: [n, r]."""
+    prev = np.asarray(prev, dtype=np.int64)
+    r = E.shape[1]
+    acc = np.zeros((prev.shape[0], r), dtype=np.float32)
+    ok = prev >= 0
+    acc[ok] = E[prev[ok]].astype(np.float32)
+    for i in range(r):
+        acc = fma32(s_prev[:, i : i + 1], U[i][None, :], acc)
+    return round_to(np.tanh(acc.astype(np.float64)), dtype)
+
+
+def rnn_states(E, U, anchor, tokens, dtype: str) -> np.ndarray:
+    """The states s_0..s_{gamma-1} of given drafts: s_k from x_{k-1} (the
+    anchor for k = 0) and s_{k-1}.  Returns [R, gamma, r] float64."""
+    tokens = np.asarray(tokens, dtype=np.int64)
+    R, G = tokens.shape
+    S = np.zeros((R, G, E.shape[1]))
+    s = np.zeros((R, E.shape[1]))
+    for k in range(G):
+        prev = np.asarray(anchor, dtype=np.int64) if k == 0 else tokens[:, k - 1]
+        s = rnn_state(E, U, prev, s, dtype)
+        S[:, k] = s
+    return S
+
+
+def draft_distribution_rows(z_k, rows, W, T):
+    """q over the vocabulary for one position with bias rows @ W:
+    softmax((z_k + rows W) / T)."""
+    y = (z_k + np.asarray(rows, dtype=np.float64) @ W) / T
+    e, lse = softmax_rows(y)
+    return np.exp(y - lse[:, None])
+
+
+def draft_sample_rnn(z, E, U, W, anchor, u_draft, T, dtype: str):
+    """Semi-autoregressive draft with the RNN head: for k = 0..gamma-1,
+    s_k = rnn_state(x_{k-1}, s_{k-1}), y = (z_k + s_k W) / T, q_k = softmax(y),
+    x_k = inverse_cdf(q_k, u_k) (greedy when T == 0).  Returns tokens,
+    q_lse, q_tok as draft_sample does, and the states S [R, gamma, r]."""
+    R, G, V = z.shape
+    tokens = np.zeros((R, G), dtype=np.int64)
+    q_lse = np.zeros((R, G))
+    q_tok = np.zeros((R, G))
+    S = np.zeros((R, G, E.shape[1]))
+    s = np.zeros((R, E.shape[1]))
+    prev = np.asarray(anchor, dtype=np.int64).copy()
+    for k in range(G):
+        s = rnn_state(E, U, prev, s, dtype)
+        S[:, k] = s
+        y = z[:, k, :] + s @ W
+        if T == 0.0:
+            x = first_argmax(y)
+            q_lse[:, k] = y[np.arange(R), x]
+            q_tok[:, k] = 1.0
+        else:
+            y = y / T
+            e, lse = softmax_rows(y)
+            x = inverse_cdf(e, u_draft[:, k])
+            q_lse[:, k] = lse
+            q_tok[:, k] = np.exp(y[np.arange(R), x] - lse)
+        tokens[:, k] = x
+        prev = x
+    return tokens, q_lse, q_tok, S
 
 
 # --------------------------------------------------------------------------
@@ -272,8 +388,11 @@ def _row_lse(target, rows, T, chunk=256):
     return out
 
 
-def verify(z, E, W, anchor, tokens, T, ell, row_off, target, u_acc, u_fin):
+def verify(z, E, W, anchor, tokens, T, ell, row_off, target, u_acc, u_fin, states=None):
     """Rejection-sampling (or greedy) verification of the scheduled prefixes.
+
+    With states ([R, gamma, r], the RNN head's) the draft distribution of
+    position j is rebuilt with the bias states[r, j] W instead of E[x_{j-1}] W.
 
     target: [B_rows, V]; the rows of request r are row_off[r] + j for
     j = 0..ell[r]; row j is the target distribution for draft position j+1
@@ -305,8 +424,11 @@ def verify(z, E, W, anchor, tokens, T, ell, row_off, target, u_acc, u_fin):
             y = trow / T
             _, lse = softmax_rows(y)
             p_x = np.exp(y[np.arange(idx.size), x] - lse)
-            prev = anchor[idx] if j == 0 else tokens[idx, j - 1]
-            q = draft_distribution(z[idx, j, :], E, W, prev, T)
+            if states is None:
+                prev = anchor[idx] if j == 0 else tokens[idx, j - 1]
+                q = draft_distribution(z[idx, j, :], E, W, prev, T)
+            else:
+                q = draft_distribution_rows(z[idx, j, :], states[idx, j, :], W, T)
             q_x = q[np.arange(idx.size), x]
             acc = u_acc[idx, j] < p_x / q_x
         rej = idx[~acc]
@@ -330,8 +452,11 @@ def verify(z, E, W, anchor, tokens, T, ell, row_off, target, u_acc, u_fin):
         ridx = np.nonzero(rejected)[0]
         if ridx.size:
             j = n_acc[ridx]
-            prev = np.where(j == 0, anchor[ridx], tokens[ridx, np.maximum(j - 1, 0)])
-            q = draft_distribution(z[ridx, j, :], E, W, prev, T)
+            if states is None:
+                prev = np.where(j == 0, anchor[ridx], tokens[ridx, np.maximum(j - 1, 0)])
+                q = draft_distribution(z[ridx, j, :], E, W, prev, T)
+            else:
+                q = draft_distribution_rows(z[ridx, j, :], states[ridx, j, :], W, T)
             res = np.maximum(0.0, p[ridx] - q)
             zero = ~(np.sum(res, axis=1) > 0.0)
             res[zero] = p[ridx[zero]]
@@ -343,16 +468,19 @@ def verify(z, E, W, anchor, tokens, T, ell, row_off, target, u_acc, u_fin):
                 final_row=final_row)
 
 
-def final_weights(z, E, W, anchor, tokens, T, target_row, j, r, rejected):
+def final_weights(z, E, W, anchor, tokens, T, target_row, j, r, rejected, states=None):
     """The distribution the final token of request r is drawn from
     (residual when rejected at position j+1, else the bonus row's p);
-    used by the tests to classify near-ties."""
+    used by the tests to classify near-ties.  states: as in verify."""
     y = target_row[None, :] / T
     e, lse = softmax_rows(y)
     p = np.exp(y - lse[:, None])
     if not rejected:
         return p[0]
-    prev = np.array([anchor[r] if j == 0 else tokens[r, j - 1]])
-    q = draft_distribution(z[r : r + 1, j, :], E, W, prev, T)
+    if states is None:
+        prev = np.array([anchor[r] if j == 0 else tokens[r, j - 1]])
+        q = draft_distribution(z[r : r + 1, j, :], E, W, prev, T)
+    else:
+        q = draft_distribution_rows(z[r : r + 1, j, :], states[r : r + 1, j, :], W, T)
     w = np.maximum(0.0, p - q)
     return w[0] if np.sum(w) > 0 else p[0]

@@ -55,8 +55,12 @@ def _lib():
             "oc_schedule": (i, [i, i, vp, vp, i64, i, i64, vp, vp, vp, vp, vp, vp, vp]),
             "oc_schedule_capacity": (None, [i, i, vp, i64, vp, vp, vp, vp, vp]),
             "oc_verify": (None, [i, i, i, i, d, vp, vp, vp, vp, vp, vp, vp, vp, i64, vp, vp,
-                                 vp, vp, vp, vp, vp]),
-            "oc_final_weights": (None, [i, i, d, vp, vp, vp, i64, vp, i, vp]),
+                                 vp, vp, vp, vp, vp, vp]),
+            "oc_final_weights": (None, [i, i, d, vp, vp, vp, i64, vp, i, vp, vp]),
+            "oc_draft_sample_rnn": (None, [i, i, i, i, i, d, vp, vp, vp, vp, vp, vp, vp, vp,
+                                           vp, vp]),
+            "oc_rnn_states": (None, [i, i, i, i, vp, vp, vp, vp, vp]),
+            "oc_round_state": (None, [i64, i, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -134,6 +138,35 @@ def draft_distribution(z_k, E, W, prev, T):
     return q
 
 
+def draft_distribution_rows(z_k, rows, W, T):
+    """softmax((z_k + rows W) / T): the rows serve as the table, row n for
+    request n."""
+    rows = _f(rows)
+    return draft_distribution(z_k, rows, W, np.arange(rows.shape[0]), T)
+
+
+def _dt(dtype):
+    if dtype not in ("bf16", "f32"):
+        raise ValueError(f"state type {dtype!r}: bf16 or f32")
+    return 0 if dtype == "bf16" else 1
+
+
+def round_to(x, dtype):
+    x = _f(x)
+    out = np.empty_like(x)
+    _lib().oc_round_state(x.size, _dt(dtype), _p(x), _p(out))
+    return out
+
+
+def rnn_states(E, U, anchor, tokens, dtype):
+    E, U, anchor, tokens = _f(E), _f(U), _i(anchor), _i(tokens)
+    R, G = tokens.shape
+    r = E.shape[1]
+    S = np.empty((R, G, r))
+    _lib().oc_rnn_states(R, G, r, _dt(dtype), _p(E), _p(U), _p(anchor), _p(tokens), _p(S))
+    return S
+
+
 # --------------------------------------------------------------- stages
 
 def draft_sample(z, E, W, anchor, u_draft, T):
@@ -146,6 +179,20 @@ def draft_sample(z, E, W, anchor, u_draft, T):
     _lib().oc_draft_sample(R, G, V, E.shape[1], float(T), _p(z), _p(E), _p(W), _p(anchor), _p(u),
                            _p(tokens), _p(q_lse), _p(q_tok))
     return tokens, q_lse, q_tok
+
+
+def draft_sample_rnn(z, E, U, W, anchor, u_draft, T, dtype):
+    z, E, U, W, anchor = _f(z), _f(E), _f(U), _f(W), _i(anchor)
+    R, G, V = z.shape
+    r = E.shape[1]
+    u = _f(u_draft) if u_draft is not None else np.zeros((R, G))
+    tokens = np.empty((R, G), dtype=np.int64)
+    q_lse = np.empty((R, G))
+    q_tok = np.empty((R, G))
+    S = np.empty((R, G, r))
+    _lib().oc_draft_sample_rnn(R, G, V, r, _dt(dtype), float(T), _p(z), _p(E), _p(U), _p(W),
+                               _p(anchor), _p(u), _p(tokens), _p(q_lse), _p(q_tok), _p(S))
+    return tokens, q_lse, q_tok, S
 
 
 def confidence(h, w, E1, anchor, tokens, sts_t, c_in=None):
@@ -197,8 +244,9 @@ def schedule_capacity(a, K):
     return dict(ell=ell, row_off=row_off, B=int(B[0]), E=float(E[0]), i_star=int(ist[0]))
 
 
-def verify(z, E, W, anchor, tokens, T, ell, row_off, target, u_acc, u_fin):
+def verify(z, E, W, anchor, tokens, T, ell, row_off, target, u_acc, u_fin, states=None):
     z, E, W = _f(z), _f(E), _f(W)
+    S = None if states is None else _f(states)
     anchor, tokens, ell, row_off = _i(anchor), _i(tokens), _i(ell), _i(row_off)
     target = _f(target)
     R, G, V = z.shape
@@ -212,18 +260,19 @@ def verify(z, E, W, anchor, tokens, T, ell, row_off, target, u_acc, u_fin):
     frow = np.empty(R, dtype=np.int64)
     _lib().oc_verify(R, G, V, E.shape[1], float(T), _p(z), _p(E), _p(W), _p(anchor), _p(tokens),
                      _p(ell), _p(row_off), _p(target), n_rows, _p(u_acc), _p(u_fin), _p(n_acc),
-                     _p(out), _p(p_lse), _p(kind), _p(frow))
+                     _p(out), _p(p_lse), _p(kind), _p(frow), _p(S))
     rows = np.concatenate([row_off[r] + np.arange(ell[r] + 1) for r in range(R)])
     return dict(n_acc=n_acc, out_tokens=out, p_lse={int(x): float(p_lse[x]) for x in rows},
                 final_kind=kind, final_row=frow)
 
 
-def final_weights(z, E, W, anchor, tokens, T, target_row, j, r, rejected):
+def final_weights(z, E, W, anchor, tokens, T, target_row, j, r, rejected, states=None):
     E, W, trow = _f(E), _f(W), _f(target_row)
+    srow = None if states is None else _f(states[r, j, :])
     V = trow.shape[0]
     prev = int(anchor[r]) if j == 0 else int(tokens[r, j - 1])
     zrow = _f(z[r, j, :]) if rejected else np.zeros(V)
     w = np.empty(V)
     _lib().oc_final_weights(V, E.shape[1], float(T), _p(zrow), _p(E), _p(W), prev, _p(trow),
-                            int(bool(rejected)), _p(w))
+                            int(bool(rejected)), _p(w), _p(srow))
     return w

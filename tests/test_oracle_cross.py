@@ -90,3 +90,41 @@ def test_cpp_oracle_threads_give_identical_results():
         cpo.set_threads(n0)
     for x, y in zip(one, many):
         assert np.array_equal(x, y)
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid_bf16", "mid_t07", "mid_greedy"])
+def test_numpy_and_cpp_oracles_agree_on_the_rnn_head(name):
+    """RNN head: tokens and states exactly (the state is quantised in the same
+    fp32 / float64 steps on both sides), q to 1e-12, and verification with the
+    states as the draft's bias rows."""
+    cpo.build()
+    wl = CASES[name]
+    inp = synth.make_inputs(wl)
+    f = synth.to_f64
+    z, E, Wm = f(inp.z), f(inp.E), f(inp.W)
+    U = f(synth.rnn_recurrence(wl))
+    anchor = inp.anchor.numpy().astype(np.int64)
+    out = {}
+    for tag, o in (("np", npo), ("cpp", cpo)):
+        tok, ql, qt, S = o.draft_sample_rnn(z, E, U, Wm, anchor, f(inp.u_draft), wl.T, wl.dtype)
+        S2 = o.rnn_states(E, U, anchor, tok, wl.dtype)
+        dense = target_logits_for(inp, tok, S)
+        G = wl.gamma
+        ell = np.arange(wl.R) % (G + 1)
+        row_off = np.concatenate([[0], np.cumsum(1 + ell)])
+        rows = np.concatenate([dense[n, : ell[n] + 1] for n in range(wl.R)])
+        ver = o.verify(z, E, Wm, anchor, tok, wl.T, ell, row_off, rows, f(inp.u_acc),
+                       f(inp.u_fin), states=S)
+        out[tag] = (tok, ql, qt, S, S2, ver)
+    a, b = out["np"], out["cpp"]
+    assert np.array_equal(a[0], b[0])
+    close(a[1], b[1])
+    close(a[2], b[2])
+    assert np.array_equal(a[3], b[3]) and np.array_equal(a[3], a[4]) and np.array_equal(b[3], b[4])
+    for k in ("n_acc", "out_tokens", "final_kind", "final_row"):
+        assert np.array_equal(a[5][k], b[5][k]), k
+
+
+def target_logits_for(inp, tok, S):
+    return target_model.target_logits(inp, torch.from_numpy(tok),
+                                      states=torch.from_numpy(S)).double().numpy()

@@ -580,3 +580,134 @@ def test_capacity_tie_order_request_then_position(orc):
     a = np.full((3, 2), 0.5)
     for K, want in [(4, [1, 0, 0]), (5, [2, 0, 0]), (6, [2, 1, 0]), (8, [2, 2, 1])]:
         assert orc.schedule_capacity(a, K)["ell"].tolist() == want
+
+
+# ---------------------------------------------------------------- RNN head
+# News article, innovation 1 (an RNN head keeps a recurrent state); the
+# form s_k = tanh(E[x_{k-1}] + s_{k-1} U) is this library's reading.
+
+def test_round_to_state_types(orc):
+    """bf16 keeps 8 significant bits, ties to even, in one rounding from the
+    double (no detour through fp32): 1/3 -> 171/512; 1 + 2^-8 (a tie) -> 1;
+    1 + 3 * 2^-8 (a tie) -> 1 + 2^-6; 1 + 2^-8 + 2^-40 (above the tie by less
+    than an fp32 ulp) -> 1 + 2^-7.  fp32: 1/3 -> 11184811 / 2^25."""
+    x = np.array([1.0 / 3.0, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, 1.0 + 2.0 ** -8 + 2.0 ** -40,
+                  -0.75, 2.0 ** -130 * 1.75])
+    want = [171.0 / 512.0, 1.0, 1.0 + 2.0 ** -6, 1.0 + 2.0 ** -7, -0.75, 2.0 ** -133 * 14.0]
+    assert orc.round_to(x, "bf16").tolist() == want
+    assert orc.round_to(np.array([1.0 / 3.0]), "f32").tolist() == [11184811.0 / 2.0 ** 25]
+
+
+def test_rnn_head_without_recurrence_is_the_markov_head_on_tanh_rows(orc):
+    """U = 0: s_k = round(tanh(E[x_{k-1}])) depends on the previous token
+    only, so the RNN draft equals the (pinned) Markov draft on the table
+    round(tanh(E)), token for token, for both state types and greedy."""
+    rng = np.random.default_rng(77)
+    R, G, V, r = 6, 5, 40, 8
+    for dtype, T in (("bf16", 1.0), ("f32", 0.7), ("bf16", 0.0)):
+        E = orc.round_to(rng.standard_normal((V, r)), dtype)
+        W = orc.round_to(rng.standard_normal((r, V)) * 0.5, dtype)
+        z = rng.standard_normal((R, G, V)) * 2.0
+        anchor = rng.integers(-1, V, size=R)
+        anchor[0] = -1
+        u = uni24(rng, (R, G))
+        tok, ql, qt, S = orc.draft_sample_rnn(z, E, np.zeros((r, r)), W, anchor, u, T, dtype)
+        Et = orc.round_to(np.tanh(E), dtype)
+        tok2, ql2, qt2 = orc.draft_sample(z, Et, W, anchor, u, T)
+        assert np.array_equal(tok, tok2)
+        assert np.allclose(ql, ql2, rtol=1e-12, atol=0) and np.allclose(qt, qt2, rtol=1e-12)
+        prev = np.concatenate([anchor[:, None], tok[:, :-1]], axis=1)
+        want = np.where((prev >= 0)[..., None], Et[np.maximum(prev, 0)], 0.0)
+        assert np.array_equal(S, want)
+
+
+def _rnn_three_token_case(U):
+    """V = 3, r = 1, fp32 states, base scores 0 (token 2 at -inf).  The anchor
+    is token 2 and the draws are forced to x_0 = 0, x_1 = 1 by the uniforms.
+    E is chosen so that the states are s_0 = 0.5, s_1 = 0.6, s_2 = 0.8 when
+    the recurrence adds s_{k-1} * U; W gives token 1 the bias s * ln 9 / 0.8,
+    so at the third position token 1 gains ln 9 over token 0: the explainer's
+    Markov-head experiment (scores 0 / 0, +ln 9: 50% / 50% becomes 90% / 10%)."""
+    E = np.array([[math.atanh(0.6) - 0.5 * U], [math.atanh(0.8) - 0.6 * U], [math.atanh(0.5)]])
+    E = E.astype(np.float32).astype(np.float64)
+    W = np.array([[0.0, math.log(9.0) / 0.8, 0.0]])
+    z = np.zeros((1, 3, 3))
+    z[..., 2] = -np.inf
+    return E, W, z
+
+
+@pytest.mark.parametrize("u_last,want", [(0.0999, 0), (0.1001, 1)])
+def test_rnn_head_explainer_ratio_through_the_recurrence(orc, u_last, want):
+    U = 0.7
+    E, W, z = _rnn_three_token_case(U)
+    u = np.array([[0.0, 0.999999, u_last]])
+    tok, ql, qt, S = orc.draft_sample_rnn(z, E, np.array([[U]]), W, np.array([2]), u, 1.0, "f32")
+    assert tok[0].tolist() == [0, 1, want]
+    assert np.allclose(S[0, :, 0], [0.5, 0.6, 0.8], atol=2e-7, rtol=0)
+    assert abs(qt[0, 2] - (0.1 if want == 0 else 0.9)) < 1e-6
+    assert abs(ql[0, 2] - math.log(10.0)) < 1e-6  # ln(e^0 + e^{ln 9})
+    # without the recurrence term the third state is not 0.8: the 90% is gone
+    _, _, qt0, _ = orc.draft_sample_rnn(z, E, np.zeros((1, 1)), W, np.array([2]), u, 1.0, "f32")
+    assert abs(qt0[0, 2] - qt[0, 2]) > 1e-2
+
+
+def test_rnn_head_remembers_the_token_two_back(orc):
+    """With U != 0 the third position's distribution depends on x_0 even with
+    x_1 fixed; with U = 0 (a one-token memory) it does not."""
+    rng = np.random.default_rng(5)
+    V, r = 4, 8
+    E = orc.round_to(rng.standard_normal((V, r)), "f32")
+    W = orc.round_to(rng.standard_normal((r, V)), "f32")
+    Um = orc.round_to(rng.standard_normal((r, r)) * 0.6, "f32")
+    z = np.zeros((2, 3, V))
+    anchor = np.array([3, 3])
+    tokens = np.array([[0, 2, 0], [1, 2, 0]])  # same x_1, different x_0
+    for U, differ in ((Um, True), (np.zeros((r, r)), False)):
+        S = orc.rnn_states(E, U, anchor, tokens, "f32")
+        q = orc.draft_distribution_rows(z[:, 2, :], S[:, 2, :], W, 1.0)
+        assert (np.max(np.abs(q[0] - q[1])) > 1e-3) == differ
+        assert np.array_equal(S[0, 0], S[1, 0])  # same anchor
+
+
+@pytest.mark.parametrize("s", [math.log(3.0), -math.log(3.0)])
+def test_verify_uses_the_rnn_state_of_the_rejected_position(orc, s):
+    """gamma = 1, V = 2, r = 1, W = (0, 1): the draft q at the first position
+    is built from the state s (not from E, which is zero here): q = (1/4, 3/4)
+    for s = ln 3 and (3/4, 1/4) for s = -ln 3.  Drafts drawn from that q and
+    verified against p = (0.6, 0.4) must emit p (forum post, lossless proof);
+    a residual built from E's zero bias (q = (1/2, 1/2)) would emit
+    (0.4, 0.6) for s = ln 3."""
+    n = 200_000
+    rng = np.random.default_rng(11)
+    q = np.array([1.0, math.exp(s)]) / (1.0 + math.exp(s))
+    x = (uni24(rng, n) >= q[0]).astype(np.int64)
+    p = np.array([0.6, 0.4])
+    rows = np.zeros((n, 2, 2))
+    rows[:, 0, :] = np.log(p)
+    states = np.full((n, 1, 1), s)
+    out = orc.verify(np.zeros((n, 1, 2)), np.zeros((2, 1)), np.array([[0.0, 1.0]]),
+                     np.full(n, 1, dtype=np.int64), x[:, None], 1.0, np.ones(n, dtype=np.int64),
+                     np.arange(n + 1, dtype=np.int64) * 2, rows.reshape(2 * n, 2),
+                     uni24(rng, (n, 1)), uni24(rng, (n,)), states=states)
+    first = out["out_tokens"][:, 0]
+    counts = np.bincount(first, minlength=2).astype(np.float64)
+    assert _chi2_two(counts, p) < 10.828
+    acc = float(np.mean(out["n_acc"] == 1))
+    a_true = float(np.minimum(p, q).sum())
+    assert abs(acc - a_true) <= 4 * math.sqrt(a_true * (1 - a_true) / n)
+    over = 0 if q[0] > p[0] else 1  # the over-drafted token is the one rejected
+    rej = out["n_acc"] == 0
+    assert np.all(x[rej] == over) and np.all(first[rej] == 1 - over)
+
+
+def test_rnn_state_row_vector_times_U(orc):
+    """The recurrence multiplies the state as a row vector, like E[x] W:
+    pre_j = E[x][j] + sum_i s_i U[i][j].  r = 2: s_0 = (0.5, 0) from the anchor
+    row (atanh 0.5, 0); the next row is 0 and U has one entry U[0][1] = c with
+    c / 2 = atanh 0.75, so s_1 = (0, 0.75).  U's transpose would give s_1 = 0."""
+    c = 2.0 * math.atanh(0.75)
+    E = np.array([[0.0, 0.0], [math.atanh(0.5), 0.0]]).astype(np.float32).astype(np.float64)
+    U = np.array([[0.0, c], [0.0, 0.0]]).astype(np.float32).astype(np.float64)
+    S = orc.rnn_states(E, U, np.array([1]), np.array([[0, 0]]), "f32")
+    assert np.allclose(S[0, 0], [0.5, 0.0], atol=1e-7, rtol=0)
+    assert np.allclose(S[0, 1], [0.0, 0.75], atol=1e-7, rtol=0)
