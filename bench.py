@@ -51,6 +51,8 @@ def algorithmic_bytes(kind, wl, B, n_rej):
     R, V, r = wl.R, wl.V, wl.r
     if kind == "verify_rows":
         return B * V * e
+    if kind == "rnn_state":  # U once, the E rows and previous states of every request
+        return r * r * e + 2 * R * r * e
     if kind in ("draft_partial", "draft_fused_tc"):
         return R * V * e + (r * V * e if kind == "draft_fused_tc" else 0)
     if kind == "draft_persistent_tc":  # all gamma positions; W read once (L2-resident)
@@ -176,8 +178,16 @@ def run_ours(args, wl, world, rank, local):
     g = dict(z=inp.z, E=inp.E, Wt=Wt, anchor=inp.anchor, ud=inp.u_draft, ua=inp.u_acc,
              uf=inp.u_fin, h=inp.h, w=inp.w_conf, sts=inp.sts_t, c_in=inp.c_in, sps=inp.sps)
     step = DSparkStep(wl.R, wl.gamma, wl.V, wl.r, wl.n_sps_eff, device=dev)
+    rnn = args.head == "rnn"
+    if rnn:
+        g["U"] = synth.rnn_recurrence(wl, device=dev)
 
     def front():
+        if rnn:  # RNN head: the draft, then the head and the scheduler
+            step.draft_rnn(g["z"], g["E"], g["U"], g["Wt"], g["anchor"], g["ud"], wl.T)
+            step.confidence(g["h"], g["w"], g["E"], g["anchor"], g["sts"], c_in=g["c_in"])
+            step.schedule(g["sps"], early_stop=bool(args.early_stop))
+            return
         # draft + confidence head + scheduler: one call (one launch here)
         step.draft_schedule(g["z"], g["E"], g["Wt"], g["anchor"], g["ud"], wl.T, g["h"], g["w"],
                             g["E"], g["sts"], g["sps"], c_in=g["c_in"],
@@ -189,13 +199,16 @@ def run_ours(args, wl, world, rank, local):
     torch.cuda.synchronize()
     Bn = int(step.B.item())
     ell = step.ell.cpu().numpy()
-    dense = target_model.target_logits(inp, step.tokens)
+    dense = target_model.target_logits(inp, step.tokens, states=step.S if rnn else None)
     rows = np.concatenate([r * (wl.gamma + 1) + np.arange(ell[r] + 1) for r in range(wl.R)])
     target = dense.reshape(-1, wl.V)[torch.from_numpy(rows).to(dev)].contiguous()
     del dense
     step.p_lse = torch.zeros((Bn,), dtype=torch.float64, device=dev)
 
     def verify():
+        if rnn:
+            step.verify_rnn(g["z"], g["Wt"], target, g["ua"], g["uf"], wl.T)
+            return
         step.verify(g["z"], g["E"], g["Wt"], g["anchor"], target, g["ua"], g["uf"], wl.T)
 
     def full_step():
@@ -269,7 +282,7 @@ def run_ours(args, wl, world, rank, local):
     del tgraph
 
     # end to end through the public calls with pinned host buffers
-    e2e = None if args.verify_only else run_e2e(args, wl, inp, g, step, target, dev, Bd)
+    e2e = None if args.verify_only or rnn else run_e2e(args, wl, inp, g, step, target, dev, Bd)
 
     peaks, psrc = read_peaks()
     kernels = {k: {"launches_per_step": v[0] / args.steps, "avg_us": 1e3 * v[1] / v[0],
@@ -285,7 +298,7 @@ def run_ours(args, wl, world, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "config": {"workload": f"{wl.name}: R={wl.R} gamma={wl.gamma} V={wl.V} r={wl.r} "
                                f"d={wl.d} T={wl.T}", "B": Bn, "mean_n_acc": mean_acc,
-                   "early_stop": bool(args.early_stop),
+                   "early_stop": bool(args.early_stop), "head": args.head,
                    "timed": "verification only" if args.verify_only else "the whole step",
                    "l2": "flushed between timed steps (512 MiB write)", "cuda_graph": True,
                    "parallelism": f"replicas x{world}"},
@@ -295,7 +308,7 @@ def run_ours(args, wl, world, rank, local):
         "roofline": roof,
         "kernels": kernels,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.verify_only:
+    if rank == 0 and world == 1 and not (args.no_cpu_baseline or args.verify_only or rnn):
         out["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
     return out
 
@@ -553,6 +566,9 @@ def main():
                     help="scheduler stop rule: 1 early stop, 0 global search")
     ap.add_argument("--verify-only", action="store_true",
                     help="time the verification alone on the scheduled batch")
+    ap.add_argument("--head", default="markov", choices=["markov", "rnn"],
+                    help="sequential head of the draft: the Markov head, or the RNN head "
+                         "(state launch + draw per position; no e2e or CPU legs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     args = ap.parse_args()

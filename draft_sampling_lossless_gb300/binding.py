@@ -40,6 +40,8 @@ SYMBOLS = (
     "dspark_draft_schedule",
     "dspark_check_wait_timeout",
     "dspark_schedule_async",
+    "dspark_draft_sample_rnn",
+    "dspark_verify_rnn",
 )
 
 
@@ -92,6 +94,13 @@ def lib() -> ctypes.CDLL:
                                             vp]
         L.dspark_schedule_async.restype = c_int
         L.dspark_schedule_async.argtypes = [c_int, c_int, vp, vp, vp, vp, vp, vp, vp, c_size, vp]
+        L.dspark_draft_sample_rnn.restype = c_int
+        L.dspark_draft_sample_rnn.argtypes = [c_int, c_int, c_int, c_int, c_float, vp, vp, vp, vp,
+                                              c_int, vp, vp, vp, vp, vp, vp, vp, c_size, vp]
+        L.dspark_verify_rnn.restype = c_int
+        L.dspark_verify_rnn.argtypes = [c_int, c_int, c_int, c_int, c_float, vp, vp, vp, c_int,
+                                        vp, vp, vp, vp, vp, vp, ctypes.c_int64, vp, vp, vp, vp,
+                                        vp, vp, c_size, vp]
         L.dspark_check_wait_timeout.restype = c_int
         L.dspark_check_wait_timeout.argtypes = [c_int, vp, c_size, vp]
         L.dspark_launch_count.restype = ctypes.c_longlong
@@ -201,6 +210,16 @@ def dspark_draft_sample(z, E, Wt, anchor, u_draft, temperature, tokens, q_lse, q
         _p(tokens), _p(q_lse), _p(q_tok), _p(ws), ws.numel(), _stream(stream)))
 
 
+def dspark_draft_sample_rnn(z, E, U, Wt, anchor, u_draft, temperature, tokens, q_lse, q_tok, S,
+                            ws, stream=None):
+    R, G, V = z.shape
+    r = E.shape[1]
+    _check("dspark_draft_sample_rnn", lib().dspark_draft_sample_rnn(
+        R, G, V, r, float(temperature), _p(z), _p(E), _p(U), _p(Wt), _dt(z), _p(anchor),
+        _p(u_draft), _p(tokens), _p(q_lse), _p(q_tok), _p(S), _p(ws), ws.numel(),
+        _stream(stream)))
+
+
 def dspark_confidence(R, gamma, hidden, w, E1, anchor, tokens, sts_t, c_in, c_out, a_out, ws,
                       stream=None):
     if c_in is None:
@@ -250,6 +269,16 @@ def dspark_verify(z, E, Wt, anchor, tokens, q_lse, q_tok, ell, row_off, target, 
         R, G, V, r, float(temperature), _p(z), _p(E), _p(Wt), _dt(z), _p(anchor), _p(tokens),
         _p(q_lse), _p(q_tok), _p(ell), _p(row_off), _p(target), target.shape[0], _p(u_acc),
         _p(u_fin), _p(n_acc), _p(out_tokens), _p(p_lse), _p(ws), ws.numel(), _stream(stream)))
+
+
+def dspark_verify_rnn(z, S, Wt, tokens, q_lse, q_tok, ell, row_off, target, u_acc, u_fin,
+                      temperature, n_acc, out_tokens, p_lse, ws, stream=None):
+    R, G, V = z.shape
+    r = S.shape[2]
+    _check("dspark_verify_rnn", lib().dspark_verify_rnn(
+        R, G, V, r, float(temperature), _p(z), _p(S), _p(Wt), _dt(z), _p(tokens), _p(q_lse),
+        _p(q_tok), _p(ell), _p(row_off), _p(target), target.shape[0], _p(u_acc), _p(u_fin),
+        _p(n_acc), _p(out_tokens), _p(p_lse), _p(ws), ws.numel(), _stream(stream)))
 
 
 def dspark_schedule_noalloc(a, sps, early_stop, max_B, ell, row_off, B_out, E_out,

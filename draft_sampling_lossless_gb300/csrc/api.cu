@@ -295,6 +295,25 @@ int dspark_draft_sample(int R, int gamma, int V, int r, float temperature, const
   return DSPARK_OK;
 }
 
+int dspark_draft_sample_rnn(int R, int gamma, int V, int r, float temperature, const void* z,
+                            const void* E, const void* U, const void* Wt, int dt,
+                            const int32_t* anchor, const float* u_draft, int32_t* tokens,
+                            double* q_lse, float* q_tok, void* S, void* ws, size_t ws_bytes,
+                            void* stream) {
+  DraftArgs a;
+  int s = draft_args(R, gamma, V, r, temperature, z, E, Wt, dt, anchor, u_draft, tokens, q_lse,
+                     q_tok, ws, ws_bytes, a);
+  if (s) return s;
+  REQUIRE(U);
+  REQUIRE(S);
+  if (((uintptr_t)S & 15) != 0) return fail(DSPARK_ERR_INVALID_ARG, "S must be 16-byte aligned");
+  a.U = U;
+  a.S = S;
+  cudaError_t e = launch_draft(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dspark_draft_sample_rnn");
+  return DSPARK_OK;
+}
+
 int dspark_confidence(int R, int gamma, int d, int r, int V, const void* hidden, const float* w,
                       const void* E1, int dt, const int32_t* anchor, const int32_t* tokens,
                       const float* sts_t, const float* c_in, float* c_out, float* a_out,
@@ -409,12 +428,19 @@ int dspark_draft_schedule(int R, int gamma, int V, int r, float temperature, con
   return DSPARK_OK;
 }
 
-int dspark_verify(int R, int gamma, int V, int r, float temperature, const void* z, const void* E,
-                  const void* Wt, int dt, const int32_t* anchor, const int32_t* tokens,
-                  const double* q_lse, const float* q_tok, const int32_t* ell,
-                  const int32_t* row_off, const void* target, int64_t n_target_rows,
-                  const float* u_acc, const float* u_fin, int32_t* n_acc, int32_t* out_tokens,
-                  double* p_lse, void* ws, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// dspark_verify and dspark_verify_rnn: with rnn set, E is the states table
+// [R][gamma][r] and anchor is unused (the bias row of position j is S[n][j]).
+int verify_call(bool rnn, int R, int gamma, int V, int r, float temperature, const void* z,
+                const void* E, const void* Wt, int dt, const int32_t* anchor,
+                const int32_t* tokens, const double* q_lse, const float* q_tok,
+                const int32_t* ell, const int32_t* row_off, const void* target,
+                int64_t n_target_rows, const float* u_acc, const float* u_fin, int32_t* n_acc,
+                int32_t* out_tokens, double* p_lse, void* ws, size_t ws_bytes, void* stream,
+                const char* name) {
   int s = check_common(R, gamma, V, r, dt);
   if (s) return s;
   if (!isfinite(temperature) || temperature < 0.0f)
@@ -433,7 +459,7 @@ int dspark_verify(int R, int gamma, int V, int r, float temperature, const void*
     REQUIRE(z);
     REQUIRE(E);
     REQUIRE(Wt);
-    REQUIRE(anchor);
+    if (!rnn) REQUIRE(anchor);
     REQUIRE(q_lse);
     REQUIRE(q_tok);
     REQUIRE(u_acc);
@@ -451,7 +477,7 @@ int dspark_verify(int R, int gamma, int V, int r, float temperature, const void*
   a.z = z;
   a.E = E;
   a.Wt = Wt;
-  a.anchor = anchor;
+  a.anchor = rnn ? nullptr : anchor;
   a.tokens = tokens;
   a.q_lse = q_lse;
   a.q_tok = q_tok;
@@ -472,8 +498,37 @@ int dspark_verify(int R, int gamma, int V, int r, float temperature, const void*
   a.prev = at<int32_t>(ws, L.prev);
   a.vcnt = at<int>(ws, L.vcnt);
   cudaError_t e = launch_verify(a, (cudaStream_t)stream);
-  if (e != cudaSuccess) return cuda_fail(e, "dspark_verify");
+  if (e != cudaSuccess) return cuda_fail(e, name);
   return DSPARK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dspark_verify(int R, int gamma, int V, int r, float temperature, const void* z, const void* E,
+                  const void* Wt, int dt, const int32_t* anchor, const int32_t* tokens,
+                  const double* q_lse, const float* q_tok, const int32_t* ell,
+                  const int32_t* row_off, const void* target, int64_t n_target_rows,
+                  const float* u_acc, const float* u_fin, int32_t* n_acc, int32_t* out_tokens,
+                  double* p_lse, void* ws, size_t ws_bytes, void* stream) {
+  return verify_call(false, R, gamma, V, r, temperature, z, E, Wt, dt, anchor, tokens, q_lse,
+                     q_tok, ell, row_off, target, n_target_rows, u_acc, u_fin, n_acc, out_tokens,
+                     p_lse, ws, ws_bytes, stream, "dspark_verify");
+}
+
+int dspark_verify_rnn(int R, int gamma, int V, int r, float temperature, const void* z,
+                      const void* S, const void* Wt, int dt, const int32_t* tokens,
+                      const double* q_lse, const float* q_tok, const int32_t* ell,
+                      const int32_t* row_off, const void* target, int64_t n_target_rows,
+                      const float* u_acc, const float* u_fin, int32_t* n_acc,
+                      int32_t* out_tokens, double* p_lse, void* ws, size_t ws_bytes,
+                      void* stream) {
+  if (S != nullptr && ((uintptr_t)S & 15) != 0)
+    return fail(DSPARK_ERR_INVALID_ARG, "S must be 16-byte aligned");
+  return verify_call(true, R, gamma, V, r, temperature, z, S, Wt, dt, nullptr, tokens, q_lse,
+                     q_tok, ell, row_off, target, n_target_rows, u_acc, u_fin, n_acc, out_tokens,
+                     p_lse, ws, ws_bytes, stream, "dspark_verify_rnn");
 }
 
 int dspark_check_wait_timeout(int limit_us, void* ws, size_t ws_bytes, void* stream) {

@@ -196,6 +196,7 @@ enum KernelKind {
   kKindDraftPersistent,
   kKindFinalTc,
   kKindWaitCheck,
+  kKindRnnState,
   kKindCount
 };
 
@@ -297,6 +298,10 @@ struct DraftArgs {
   void* stage;             // [R][r] bf16: E rows of the latest drafted tokens
   const DraftFuse* fuse = nullptr;  // confidence + scheduler in the same launch, if possible
   int* fused = nullptr;             // out: 1 when the launch included them
+  // RNN head (when U is set): U [r][r] in the table's type, S [R][gamma][r]
+  // the states; position k's bias row is S[n][k] instead of E[x_{k-1}]
+  const void* U = nullptr;
+  void* S = nullptr;
 };
 cudaError_t launch_draft(const DraftArgs& a, cudaStream_t st);
 // Whether the persistent draft can also evaluate the confidence head and the
@@ -308,10 +313,11 @@ cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st);
 // operands): the fused bias GEMM + partial pass for draft position k.
 bool draft_tc_supported(const DraftArgs& a);
 bool tc_shape_supported(int dt, int V, int r, const void* a, const void* b, const void* c);
-// bias[n][v] = E[prev[n * prev_stride]] . Wt[v] on the tensor cores.
+// bias[n][v] = E[prev[n * prev_stride]] . Wt[v] on the tensor cores; rows
+// prev >= prev_limit (or < -1) are flagged and zero.
 cudaError_t launch_bias_tc(int R, int V, int r, const void* E, const void* Wt,
-                           const int32_t* prev, int prev_stride, float* bias, uint32_t* status,
-                           cudaStream_t st);
+                           const int32_t* prev, int prev_stride, int prev_limit, float* bias,
+                           uint32_t* status, cudaStream_t st);
 cudaError_t launch_draft_partial_tc(const DraftArgs& a, int k, const int32_t* prev,
                                     int prev_stride, cudaStream_t st);
 
@@ -445,7 +451,7 @@ struct VerifyArgs {
   int R, gamma, V, r, dt;
   float T;
   const void* z;
-  const void* E;
+  const void* E;  // Markov table [V][r]; RNN head (anchor null): the states [R][gamma][r]
   const void* Wt;
   const int32_t* anchor;
   const int32_t* tokens;
@@ -477,10 +483,19 @@ cudaError_t launch_final_tc(const VerifyArgs& a, const VerifyState* vstate, long
 
 // CUDA-core Markov bias: bias[n][v] = sum_i E[prev[n]][i] * Wt[v][i] for the
 // n = 0..R-1 rows whose previous token is prev_base[n * prev_stride]
-// (negative = zero row).
+// (negative = zero row; at or above prev_limit: flagged, zero row).  With
+// prev_base null the row of request n is n * prev_stride (the RNN states).
 cudaError_t launch_bias(int R, int V, int r, int dt, const void* E, const void* Wt,
-                        const int32_t* prev_base, int prev_stride, float* bias,
+                        const int32_t* prev_base, int prev_stride, int prev_limit, float* bias,
                         uint32_t* status, cudaStream_t st);
+
+// RNN head, draft position k: S[n][k] = round(tanh(pre)), pre[j] in fp32 =
+// E[x_{k-1}][j] (0 when x_{k-1} < 0; x_{-1} the anchor, x_{k-1} = tokens[n][k-1])
+// followed by the fused multiply-adds S[n][k-1][i] * U[i][j], i ascending
+// (none at k = 0); tanh in double; rounded to the table's type (dt).
+cudaError_t launch_rnn_state(int R, int gamma, int r, int dt, int k, const void* E, const void* U,
+                             const int32_t* anchor, const int32_t* tokens, int V, void* S,
+                             uint32_t* status, cudaStream_t st);
 
 // ------------------------------------------------- integer-built doubles
 // The FP64 pipe of this part is narrow, so the hot paths build and take

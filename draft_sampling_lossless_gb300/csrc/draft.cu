@@ -23,8 +23,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) bias_kernel(int R, int V, int r, const T* __restrict__ E,
                                                    const T* __restrict__ Wt,
                                                    const int32_t* __restrict__ prev_base,
-                                                   int prev_stride, float* __restrict__ bias,
-                                                   uint32_t* status) {
+                                                   int prev_stride, int prev_limit,
+                                                   float* __restrict__ bias, uint32_t* status) {
   // Tile: 64 vocabulary columns x 32 requests, K in chunks of 32.
   __shared__ float Es[32][33];
   __shared__ float Ws[64][33];
@@ -34,9 +34,11 @@ __global__ void __launch_bounds__(256) bias_kernel(int R, int V, int r, const T*
   if (threadIdx.x < 32) {
     int n = n0 + threadIdx.x;
     int p = -1;
-    if (n < R) {
+    if (n < R && prev_base == nullptr) {
+      p = n * prev_stride;  // the RNN state of request n
+    } else if (n < R) {
       p = prev_base[(size_t)n * prev_stride];
-      if (p >= V || p < -1) {
+      if (p >= prev_limit || p < -1) {
         set_flag(status, kFlagTokenRange);
         p = -1;
       }
@@ -92,16 +94,17 @@ __global__ void __launch_bounds__(256) bias_kernel(int R, int V, int r, const T*
 }
 
 cudaError_t launch_bias(int R, int V, int r, int dt, const void* E, const void* Wt,
-                        const int32_t* prev_base, int prev_stride, float* bias, uint32_t* status,
-                        cudaStream_t st) {
+                        const int32_t* prev_base, int prev_stride, int prev_limit, float* bias,
+                        uint32_t* status, cudaStream_t st) {
   dim3 grid((V + 63) / 64, (R + 31) / 32);
   if (dt == 0)
     DSPARK_LAUNCH(kKindBias, st, bias_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
-        R, V, r, (const __nv_bfloat16*)E, (const __nv_bfloat16*)Wt, prev_base, prev_stride, bias,
-        status));
+        R, V, r, (const __nv_bfloat16*)E, (const __nv_bfloat16*)Wt, prev_base, prev_stride,
+        prev_limit, bias, status));
   else
-    DSPARK_LAUNCH(kKindBias, st, bias_kernel<float><<<grid, 256, 0, st>>>(R, V, r, (const float*)E, (const float*)Wt,
-                                             prev_base, prev_stride, bias, status));
+    DSPARK_LAUNCH(kKindBias, st, bias_kernel<float><<<grid, 256, 0, st>>>(
+        R, V, r, (const float*)E, (const float*)Wt, prev_base, prev_stride, prev_limit, bias,
+        status));
   return cudaGetLastError();
 }
 
@@ -166,7 +169,54 @@ cudaError_t launch_finish(const DraftArgs& a, int k, const BiasSrc& b, ScalePair
   return cudaGetLastError();
 }
 
+// RNN head: per position, the state kernel, then the bias and the draw with
+// the state rows S[n][k] (row n * gamma of the table S + k * r) as the bias
+// rows.
+cudaError_t launch_draft_rnn(const DraftArgs& a, cudaStream_t st) {
+  const int n_tiles = (a.V + kTileV - 1) / kTileV;
+  const bool greedy = a.T == 0.0f;
+  const ScalePair sc = make_scale(greedy ? 1.0 : 1.4426950408889634 / (double)a.T);
+  const bool tc = draft_tc_supported(a);
+  const size_t esz = a.dt == 0 ? 2 : 4;
+  for (int k = 0; k < a.gamma; ++k) {
+    cudaError_t e = launch_rnn_state(a.R, a.gamma, a.r, a.dt, k, a.E, a.U, a.anchor, a.tokens,
+                                     a.V, a.S, a.status, st);
+    if (e != cudaSuccess) return e;
+    DraftArgs b = a;
+    b.E = static_cast<const char*>(a.S) + (size_t)k * a.r * esz;  // row n * gamma: S[n][k]
+    if (tc) {
+      e = launch_draft_partial_tc(b, k, nullptr, a.gamma, st);
+      if (e != cudaSuccess) return e;
+      BiasSrc bs{nullptr, (const __nv_bfloat16*)b.E, (const __nv_bfloat16*)a.Wt, nullptr, a.gamma,
+                 a.r};
+      e = launch_finish<__nv_bfloat16, 128>(a, k, bs, sc, greedy, st);
+      if (e != cudaSuccess) return e;
+      continue;
+    }
+    e = launch_bias(a.R, a.V, a.r, a.dt, b.E, a.Wt, nullptr, a.gamma, 0, a.bias, a.status, st);
+    if (e != cudaSuccess) return e;
+    dim3 g1(n_tiles, a.R);
+    BiasSrc bs{a.bias, nullptr, nullptr, nullptr, a.gamma, a.r};
+    if (a.dt == 0) {
+      DSPARK_LAUNCH(kKindDraftPartial, st,
+                    draft_partial_kernel<__nv_bfloat16><<<g1, kTileV, 0, st>>>(
+                        a.V, a.gamma, k, n_tiles, (const __nv_bfloat16*)a.z, a.bias, sc, greedy,
+                        a.part, a.status));
+      e = launch_finish<__nv_bfloat16, kTileV>(a, k, bs, sc, greedy, st);
+    } else {
+      DSPARK_LAUNCH(kKindDraftPartial, st,
+                    draft_partial_kernel<float><<<g1, kTileV, 0, st>>>(
+                        a.V, a.gamma, k, n_tiles, (const float*)a.z, a.bias, sc, greedy, a.part,
+                        a.status));
+      e = launch_finish<float, kTileV>(a, k, bs, sc, greedy, st);
+    }
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_draft(const DraftArgs& a, cudaStream_t st) {
+  if (a.U != nullptr) return launch_draft_rnn(a, st);
   const int n_tiles = (a.V + kTileV - 1) / kTileV;
   const bool greedy = a.T == 0.0f;
   const ScalePair sc = make_scale(greedy ? 1.0 : 1.4426950408889634 / (double)a.T);
@@ -190,7 +240,7 @@ cudaError_t launch_draft(const DraftArgs& a, cudaStream_t st) {
       if (e != cudaSuccess) return e;
       continue;
     }
-    e = launch_bias(a.R, a.V, a.r, a.dt, a.E, a.Wt, prev, stride, a.bias, a.status, st);
+    e = launch_bias(a.R, a.V, a.r, a.dt, a.E, a.Wt, prev, stride, a.V, a.bias, a.status, st);
     if (e != cudaSuccess) return e;
     dim3 g1(n_tiles, a.R);
     BiasSrc b{a.bias, nullptr, nullptr, prev, stride, a.r};

@@ -81,8 +81,9 @@ struct TcParams {
   ScalePair sc;
   float c12, crest;  // log2(e)/T = c12 + crest, c12 with 12 significant bits
   const __nv_bfloat16* E;
-  const int32_t* prev;
+  const int32_t* prev;  // null: row n * prev_stride of E (the RNN states)
   int prev_stride;
+  int prev_limit;   // rows of E: larger previous-token entries are flagged
   double* part;     // [R][n_parts] partials (draft mode)
   float* sub;       // [R][n_parts][8] 16-token group sums of each partial (sampling)
   float* bias_out;  // [R][V] (bias-out mode)
@@ -491,9 +492,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x < BM) {
       const int n = r0 + threadIdx.x;
       int tok = -1;
-      if (n < p.R) {
+      if (n < p.R && p.prev == nullptr) {
+        tok = n * p.prev_stride;
+      } else if (n < p.R) {
         tok = p.prev[(size_t)n * p.prev_stride];
-        if (tok >= p.V || tok < -1) {
+        if (tok >= p.prev_limit || tok < -1) {
           set_flag(p.status, kFlagTokenRange);
           tok = -1;
         }
@@ -1261,13 +1264,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // banks.
 struct FinalParams {
   int R, V, r, nK, n_vt, n_halves, gamma, pair;
+  int prev_limit;  // rows of E
   long long n_rows;
   ScalePair sc;
   float c12, crest;  // log2(e)/T = c12 + crest, c12 with 12 significant bits
-  const __nv_bfloat16* E;
+  const __nv_bfloat16* E;       // Markov table, or the RNN states [R][gamma][r]
   const __nv_bfloat16* z;       // [R][gamma][V]
   const __nv_bfloat16* target;  // [n_rows][V]
-  const int32_t* prev;          // [R] token before the rejected position, -1 none
+  const int32_t* prev;          // [R] bias row of the rejected position (row of E), -1 none
   const VerifyState* vstate;    // [R]
   long long* fin_part;          // [R][n_halves][2]: residual, p
   uint32_t* status;
@@ -1428,7 +1432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int tok = -1;
       if (n < p.R) {
         tok = p.prev[n];
-        if (tok >= p.V || tok < -1) {
+        if (tok >= p.prev_limit || tok < -1) {
           set_flag(p.status, kFlagTokenRange);
           tok = -1;
         }
@@ -1740,6 +1744,7 @@ cudaError_t launch_draft_partial_tc(const DraftArgs& a, int k, const int32_t* pr
   p.E = static_cast<const __nv_bfloat16*>(a.E);
   p.prev = prev;
   p.prev_stride = prev_stride;
+  p.prev_limit = a.V;
   p.part = a.part;
   p.sub = a.sub;
   p.bias_out = nullptr;
@@ -1775,6 +1780,7 @@ cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st) {
   p.E = static_cast<const __nv_bfloat16*>(a.E);
   p.prev = nullptr;
   p.prev_stride = 0;
+  p.prev_limit = a.V;
   p.part = a.part;
   p.sub = a.sub;
   p.bias_out = nullptr;
@@ -1844,8 +1850,8 @@ bool draft_fuse_supported(const DraftArgs& a, const DraftFuse& f) {
 // bias[n][v] = E[prev[n * prev_stride]] . Wt[v] on the tensor cores (rows of
 // requests with prev < 0 are zero).
 cudaError_t launch_bias_tc(int R, int V, int r, const void* E, const void* Wt,
-                           const int32_t* prev, int prev_stride, float* bias, uint32_t* status,
-                           cudaStream_t st) {
+                           const int32_t* prev, int prev_stride, int prev_limit, float* bias,
+                           uint32_t* status, cudaStream_t st) {
   CUtensorMap tm_w;
   cudaError_t e = encode_w(&tm_w, Wt, V, r);
   if (e != cudaSuccess) return e;
@@ -1863,6 +1869,7 @@ cudaError_t launch_bias_tc(int R, int V, int r, const void* E, const void* Wt,
   p.E = static_cast<const __nv_bfloat16*>(E);
   p.prev = prev;
   p.prev_stride = prev_stride;
+  p.prev_limit = prev_limit;
   p.part = nullptr;
   p.sub = nullptr;
   p.bias_out = bias;
@@ -1892,6 +1899,7 @@ cudaError_t launch_final_tc(const VerifyArgs& a, const VerifyState* vstate, long
   p.z = static_cast<const __nv_bfloat16*>(a.z);
   p.target = static_cast<const __nv_bfloat16*>(a.target);
   p.prev = a.prev;
+  p.prev_limit = a.anchor == nullptr ? a.R * a.gamma : a.V;
   p.vstate = vstate;
   p.fin_part = fin_part;
   p.status = a.status;

@@ -26,7 +26,8 @@ struct NamedSync {
 
 // Where the finish gets the chosen tile's bias: the CUDA-core bias array of
 // the workspace (bias != nullptr), or recomputed on CUDA cores from E, Wt and
-// the previous token (the fused tensor-core pass stores no bias).
+// the previous token prev[n * prev_stride] (the fused tensor-core pass stores
+// no bias); with prev null, from row n * prev_stride of E (the RNN states).
 struct BiasSrc {
   const float* bias;
   const __nv_bfloat16* E;
@@ -347,10 +348,13 @@ __device__ void finish_request(FinishScratch& s, int n, int V, int gamma, int k,
   }
   if (bsrc.bias == nullptr) {
     // the previous token's E row, needed once the tile is chosen: load it now
-    int tok = __ldcg(bsrc.prev + (size_t)n * bsrc.prev_stride);
-    if (tok >= V || tok < -1) {
-      if (tid == 0) set_flag(status, kFlagTokenRange);
-      tok = -1;
+    int tok = n * bsrc.prev_stride;  // no token list: row n * stride (the RNN states)
+    if (bsrc.prev != nullptr) {
+      tok = __ldcg(bsrc.prev + (size_t)n * bsrc.prev_stride);
+      if (tok >= V || tok < -1) {
+        if (tid == 0) set_flag(status, kFlagTokenRange);
+        tok = -1;
+      }
     }
     for (int i = tid; i < bsrc.r; i += 256)
       s.erow[i] = tok >= 0 ? __bfloat162float(bsrc.E[(size_t)tok * bsrc.r + i]) : 0.f;

@@ -22,7 +22,7 @@ constexpr int kPairs = 8192;
 const char* const kNames[kKindCount] = {
     "markov_bias",       "draft_partial",  "draft_finish", "confidence",  "schedule",
     "verify_rows",    "verify_decide", "final_partial", "final_pick",
-    "draft_fused_tc",    "draft_persistent_tc", "final_tc", "wait_check",
+    "draft_fused_tc",    "draft_persistent_tc", "final_tc", "wait_check", "rnn_state",
 };
 
 std::mutex g_mu;

@@ -714,7 +714,10 @@ __device__ __noinline__ void decide_request(
   st.ip = greedy ? InvPair{0.f, 0.f, 0} : inv_fix(SpF[nacc], Spg[nacc]);
   st.iq = InvPair{0.f, 0.f, 0};
   if (st.mode == 1) {
-    st.prev = nacc == 0 ? anchor[n] : tokens[(size_t)n * gamma + nacc - 1];
+    // the bias row of the rejected position: the Markov row of the token
+    // before it, or (no anchors: the RNN head) the state S[n][nacc]
+    st.prev = anchor == nullptr ? n * gamma + nacc
+                                : (nacc == 0 ? anchor[n] : tokens[(size_t)n * gamma + nacc - 1]);
     st.iq = exp_neg_pair(q_lse[(size_t)n * gamma + nacc]);
   }
   vstate[n] = st;
@@ -1056,6 +1059,8 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t st) {
   const T* z = (const T*)a.z;
   const T* tg = (const T*)a.target;
   const long long items = (long long)a.R * (a.gamma + 1) * n_chunks;
+  // rows of E the final draw may read: tokens, or (RNN head) the states
+  const int lim = a.anchor == nullptr ? a.R * a.gamma : a.V;
   const bool staged = sizeof(T) == 2 && a.R <= kRowsSmem && a.V % 8 == 0 &&
                       ((uintptr_t)a.target & 15) == 0;
   // the staged row pass runs every request's decide itself
@@ -1107,8 +1112,8 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t st) {
     return cudaGetLastError();
   }
   e = tc_shape_supported(a.dt, a.V, a.r, a.z, a.E, a.Wt)
-          ? launch_bias_tc(a.R, a.V, a.r, a.E, a.Wt, a.prev, 1, a.bias, a.status, st)
-          : launch_bias(a.R, a.V, a.r, a.dt, a.E, a.Wt, a.prev, 1, a.bias, a.status, st);
+          ? launch_bias_tc(a.R, a.V, a.r, a.E, a.Wt, a.prev, 1, lim, a.bias, a.status, st)
+          : launch_bias(a.R, a.V, a.r, a.dt, a.E, a.Wt, a.prev, 1, lim, a.bias, a.status, st);
   if (e != cudaSuccess) return e;
   DSPARK_LAUNCH(kKindFinalPartial, st,
                 final_partial_kernel<T><<<dim3((n_tiles + 7) / 8, a.R), 256, 0, st>>>(

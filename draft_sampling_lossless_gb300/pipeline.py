@@ -32,10 +32,31 @@ class DSparkStep:
         rows = max_rows if max_rows is not None else R * (gamma + 1)
         self.p_lse = torch.zeros((rows,), dtype=f64, device=dev)
         self.ws = B.alloc_workspace(R, gamma, V, r, n_sps, device=dev)
+        self.S = None  # RNN head states, allocated by draft_rnn
 
     def draft(self, z, E, Wt, anchor, u_draft, T, stream=None):
         B.dspark_draft_sample(z, E, Wt, anchor, u_draft, T, self.tokens, self.q_lse, self.q_tok,
                               self.ws, stream)
+
+    def draft_rnn(self, z, E, U, Wt, anchor, u_draft, T, stream=None):
+        """The draft with the RNN head; the states land in self.S [R, gamma, r]
+        (allocated on first use, in E's dtype)."""
+        if self.S is None or self.S.dtype != E.dtype:
+            self.S = torch.zeros((self.R, self.gamma, self.r), dtype=E.dtype, device=E.device)
+        B.dspark_draft_sample_rnn(z, E, U, Wt, anchor, u_draft, T, self.tokens, self.q_lse,
+                                  self.q_tok, self.S, self.ws, stream)
+
+    def verify_rnn(self, z, Wt, target, u_acc, u_fin, T, S=None, tokens=None, q_lse=None,
+                   q_tok=None, ell=None, row_off=None, stream=None):
+        B.dspark_verify_rnn(z, self.S if S is None else S, Wt,
+                            self.tokens if tokens is None else tokens,
+                            self.q_lse if q_lse is None else q_lse,
+                            self.q_tok if q_tok is None else q_tok,
+                            self.ell if ell is None else ell,
+                            self.row_off if row_off is None else row_off, target, u_acc, u_fin,
+                            T, self.n_acc, self.out_tokens,
+                            self.p_lse if self.p_lse.numel() >= target.shape[0] else None,
+                            self.ws, stream)
 
     def confidence(self, hidden, w, E1, anchor, sts_t, c_in=None, tokens=None, stream=None):
         B.dspark_confidence(self.R, self.gamma, hidden, w, E1, anchor,

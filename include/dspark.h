@@ -12,6 +12,8 @@
  *   dspark_schedule      hardware-aware prefix scheduler
  *   (the target model's forward pass over the scheduled rows -- not here)
  *   dspark_verify        lossless rejection-sampling (or greedy) verification
+ *   dspark_draft_sample_rnn, dspark_verify_rnn
+ *                        the same two stages with the RNN sequential head
  *
  * Conventions shared by every call
  * --------------------------------
@@ -126,6 +128,41 @@ int dspark_draft_sample(int R, int gamma, int V, int r, float temperature,
                         const int32_t* anchor, const float* u_draft,
                         int32_t* tokens, double* q_lse, float* q_tok,
                         void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * dspark_draft_sample_rnn -- the semi-autoregressive draft with the RNN
+ * sequential head instead of the Markov head.
+ *
+ * News article "DSpark: Confidence-Scheduled Speculative Decoding with
+ * Semi-Autoregressive Generation", innovation 1, second stage (the RNN head
+ * keeps a recurrent state that captures longer dependencies); explainer
+ * "DSpark.让每一轮计算，多走几步", Markov-head panel (an RNN head accumulates
+ * the prefix inside the block).  The pages give no formula; this library's
+ * reading is an Elman recurrence in the Markov head's shapes:
+ *
+ *   s_0 = 0 (before the first position), x_0 = anchor[n]
+ *   s_k[j] = round(tanh(pre_k[j])), pre_k[j] = E[x_{k-1}][j] + sum_i s_{k-1}[i] U[i][j]
+ *   bias_k = s_k W, then y_k, x_k, q_lse, q_tok exactly as dspark_draft_sample
+ *
+ * U = 0 gives the Markov head on the table round(tanh(E)).  pre_k is
+ * accumulated in fp32 in a fixed order -- the E entry first, then one fused
+ * multiply-add per i, i ascending (s_0 = 0 still runs the chain) -- tanh is
+ * taken in double and rounded once to dt: the states are bit-reproducible.
+ * An anchor of -1 (or a token outside [0, V), flagged) contributes a zero E
+ * row.  Runs one state launch and one draw per position (no persistent
+ * launch).
+ *
+ *   z, E, Wt, anchor, u_draft, tokens, q_lse, q_tok: as dspark_draft_sample
+ *   U        [r][r] dt          recurrence matrix, r <= 1024
+ *   S        [R][gamma][r] dt   out: the states s_1..s_gamma (S[n][k-1] = s_k,
+ *                               the bias row of position k); 16-byte aligned;
+ *                               dspark_verify_rnn takes it in place of E
+ */
+int dspark_draft_sample_rnn(int R, int gamma, int V, int r, float temperature,
+                            const void* z, const void* E, const void* U, const void* Wt,
+                            int dt, const int32_t* anchor, const float* u_draft,
+                            int32_t* tokens, double* q_lse, float* q_tok, void* S,
+                            void* ws, size_t ws_bytes, void* stream);
 
 /*
  * dspark_confidence -- confidence head with sequential temperature scaling
@@ -287,6 +324,24 @@ int dspark_verify(int R, int gamma, int V, int r, float temperature,
                   const void* target, int64_t n_target_rows, const float* u_acc,
                   const float* u_fin, int32_t* n_acc, int32_t* out_tokens,
                   double* p_lse, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * dspark_verify_rnn -- dspark_verify for drafts made with the RNN head
+ * (dspark_draft_sample_rnn): the draft distribution of position j is rebuilt
+ * with the bias row S[n][j-1] (the state that drafted it) instead of
+ * E[x_{j-1}], for the accept tests and the residual max(0, p - q).  Same
+ * pages and rules as dspark_verify; anchor is not needed.
+ *
+ *   S        [R][gamma][r] dt   the states written by dspark_draft_sample_rnn
+ *   every other argument: as dspark_verify (S replaces E; no anchor)
+ */
+int dspark_verify_rnn(int R, int gamma, int V, int r, float temperature, const void* z,
+                      const void* S, const void* Wt, int dt, const int32_t* tokens,
+                      const double* q_lse, const float* q_tok, const int32_t* ell,
+                      const int32_t* row_off, const void* target, int64_t n_target_rows,
+                      const float* u_acc, const float* u_fin, int32_t* n_acc,
+                      int32_t* out_tokens, double* p_lse, void* ws, size_t ws_bytes,
+                      void* stream);
 
 /*
  * dspark_schedule_noalloc -- dspark_schedule for callers that cannot allocate

@@ -80,8 +80,10 @@ class Case:
     """Inputs of one workload on both sides (float64 numpy for the oracle,
     torch on the GPU for the library)."""
 
-    def __init__(self, wl: synth.Workload, seed=None, gen_device="cpu", sample=None):
+    def __init__(self, wl: synth.Workload, seed=None, gen_device="cpu", sample=None,
+                 head="markov"):
         self.wl = wl
+        self.head = head
         self.inp = synth.make_inputs(wl, device=gen_device, seed=seed)
         self.seed = seed
         R = wl.R
@@ -109,32 +111,55 @@ class Case:
                       sts=self.inp.sts_t.to(d),
                       c_in=None if self.inp.c_in is None else self.inp.c_in.to(d),
                       sps=self.inp.sps.to(d))
+        self.S_o = None
+        if head == "rnn":
+            U = synth.rnn_recurrence(wl, device=gen_device, seed=seed)
+            self.U64 = f(U)
+            self.g["U"] = U.to(d)
         wlr = wl
         self.step = DSparkStep(wlr.R, wlr.gamma, wlr.V, wlr.r, wlr.n_sps_eff)
 
     # ------------------------------------------------------------ draft
     def draft(self, st: Stats):
         wl, g = self.wl, self.g
-        self.step.draft(g["z"], g["E"], g["Wt"], g["anchor"], g["u_draft"], wl.T)
+        rnn = self.head == "rnn"
+        if rnn:
+            self.step.draft_rnn(g["z"], g["E"], g["U"], g["Wt"], g["anchor"], g["u_draft"], wl.T)
+        else:
+            self.step.draft(g["z"], g["E"], g["Wt"], g["anchor"], g["u_draft"], wl.T)
         torch.cuda.synchronize()
         assert self.step.status() == 0, f"device status {self.step.status():#x}"
         tok_g = self.step.tokens.cpu().numpy()[self.sample]
         qlse_g = self.step.q_lse.cpu().numpy()[self.sample]
         qtok_g = self.step.q_tok.cpu().numpy()[self.sample]
-        tok_o, qlse_o, qtok_o = oracle.draft_sample(self.z64, self.E64, self.W64, self.anchor,
-                                                    self.u_draft, wl.T)
+        if rnn:
+            S_g = synth.to_f64(self.step.S)[self.sample]
+            tok_o, qlse_o, qtok_o, S_o = oracle.draft_sample_rnn(
+                self.z64, self.E64, self.U64, self.W64, self.anchor, self.u_draft, wl.T, wl.dtype)
+            self.S_o = S_o
+        else:
+            tok_o, qlse_o, qtok_o = oracle.draft_sample(self.z64, self.E64, self.W64,
+                                                        self.anchor, self.u_draft, wl.T)
         self.tok_o, self.qlse_o, self.qtok_o = tok_o, qlse_o, qtok_o
         n_s, G = tok_o.shape
         for i in range(n_s):
             prev = self.anchor[i]
             for k in range(G):
                 st.decisions += 1
+                if rnn:  # the state that drafts position k: bit for bit (by value)
+                    assert np.array_equal(S_g[i, k], S_o[i, k]), (
+                        f"state of request {self.sample[i]} position {k} differs in "
+                        f"{int(np.sum(S_g[i, k] != S_o[i, k]))} entries")
                 st.rel("q_lse", qlse_g[i, k], qlse_o[i, k])
                 if tok_g[i, k] == tok_o[i, k]:
                     st.rel("q_tok", qtok_g[i, k], qtok_o[i, k])
                     prev = tok_o[i, k]
                     continue
-                y = self.z64[i, k] + oracle.markov_bias(self.E64, self.W64, np.array([prev]))[0]
+                if rnn:
+                    y = self.z64[i, k] + S_o[i, k] @ self.W64
+                else:
+                    y = self.z64[i, k] + oracle.markov_bias(self.E64, self.W64,
+                                                            np.array([prev]))[0]
                 if wl.T == 0.0:
                     tie = argmax_near_tie(y, int(tok_g[i, k]), int(tok_o[i, k]))
                 else:
@@ -199,7 +224,13 @@ class Case:
         wl, g = self.wl, self.g
         R, G, V = wl.R, wl.gamma, wl.V
         tok_full = self.oracle_tokens_full()
-        dense = target_model.target_logits(self.inp, torch.from_numpy(tok_full), seed=self.seed)
+        S_full = None
+        if self.head == "rnn":  # oracle states of the sampled requests, zeros elsewhere
+            S_full = np.zeros((R, G, wl.r))
+            S_full[self.sample] = self.S_o
+            S_full = torch.from_numpy(S_full).to(wl.torch_dtype)
+        dense = target_model.target_logits(self.inp, torch.from_numpy(tok_full), seed=self.seed,
+                                           states=S_full)
         ell = np.zeros(R, dtype=np.int64)
         ell[self.sample] = ell_s
         row_off = np.concatenate([[0], np.cumsum(1 + ell)])
@@ -212,10 +243,16 @@ class Case:
         qtok[self.sample] = self.qtok_o
         c = lambda x, dt: torch.from_numpy(np.ascontiguousarray(x)).to(dt).cuda()
         self.step.p_lse = torch.zeros((packed.shape[0],), dtype=torch.float64, device="cuda")
-        self.step.verify(g["z"], g["E"], g["Wt"], g["anchor"], packed.cuda(), g["u_acc"],
-                         g["u_fin"], wl.T, tokens=c(tok_full, torch.int32),
-                         q_lse=c(qlse, torch.float64), q_tok=c(qtok, torch.float32),
-                         ell=c(ell, torch.int32), row_off=c(row_off, torch.int32))
+        if S_full is not None:
+            self.step.verify_rnn(g["z"], g["Wt"], packed.cuda(), g["u_acc"], g["u_fin"], wl.T,
+                                 S=S_full.cuda(), tokens=c(tok_full, torch.int32),
+                                 q_lse=c(qlse, torch.float64), q_tok=c(qtok, torch.float32),
+                                 ell=c(ell, torch.int32), row_off=c(row_off, torch.int32))
+        else:
+            self.step.verify(g["z"], g["E"], g["Wt"], g["anchor"], packed.cuda(), g["u_acc"],
+                             g["u_fin"], wl.T, tokens=c(tok_full, torch.int32),
+                             q_lse=c(qlse, torch.float64), q_tok=c(qtok, torch.float32),
+                             ell=c(ell, torch.int32), row_off=c(row_off, torch.int32))
         torch.cuda.synchronize()
         assert self.step.status() == 0, f"device status {self.step.status():#x}"
         nacc_g = self.step.n_acc.cpu().numpy()[self.sample]
@@ -226,7 +263,7 @@ class Case:
         tgt64 = synth.to_f64(packed[torch.from_numpy(s_rows).to(packed.device)])
         ro_s = np.concatenate([[0], np.cumsum(1 + ell_s)])
         o = oracle.verify(self.z64, self.E64, self.W64, self.anchor, self.tok_o, wl.T, ell_s,
-                          ro_s, tgt64, self.u_acc, self.u_fin)
+                          ro_s, tgt64, self.u_acc, self.u_fin, states=self.S_o)
         # p_lse of every verified row
         want = np.array([o["p_lse"][i] for i in range(len(s_rows))])
         st.rel("p_lse", plse_g[s_rows], want)
@@ -251,7 +288,7 @@ class Case:
                 tie = argmax_near_tie(trow, fg, fo)
             else:
                 w = oracle.final_weights(self.z64, self.E64, self.W64, self.anchor, self.tok_o,
-                                         wl.T, trow, na_o, i, na_o < ell_s[i])
+                                         wl.T, trow, na_o, i, na_o < ell_s[i], states=self.S_o)
                 tie = cdf_near_tie(w, self.u_fin[i], fg, fo)
             if tie:
                 st.tie("final")
@@ -268,6 +305,11 @@ class Case:
         y = trow / wl.T
         e, lse = oracle.softmax_rows(y[None, :])
         p_x = float(np.exp(y[x] - lse[0]))
-        prev = np.array([self.anchor[i] if j == 0 else self.tok_o[i, j - 1]])
-        q = oracle.draft_distribution(self.z64[i:i + 1, j, :], self.E64, self.W64, prev, wl.T)[0]
+        if self.S_o is not None:
+            q = oracle.draft_distribution_rows(self.z64[i:i + 1, j, :], self.S_o[i:i + 1, j, :],
+                                               self.W64, wl.T)[0]
+        else:
+            prev = np.array([self.anchor[i] if j == 0 else self.tok_o[i, j - 1]])
+            q = oracle.draft_distribution(self.z64[i:i + 1, j, :], self.E64, self.W64, prev,
+                                          wl.T)[0]
         return abs(self.u_acc[i, j] - p_x / q[x]) <= TIE

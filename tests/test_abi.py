@@ -168,3 +168,25 @@ def test_schedule_async_rejects_bad_arguments_without_launching(lib):
     assert "capacity is NULL" in _err(L)
     assert L.dspark_schedule_async(*args(ws=n)) == 1
     assert L.dspark_schedule_async(*args(nb=256)) == 4
+
+
+def test_rnn_calls_reject_bad_arguments_without_launching(lib):
+    L = lib.lib()
+    f, n = _fake(), _null()
+    ws_n = 1 << 30
+    # R, G, V, r, T, z, E, U, Wt, dt, anchor, u, tokens, q_lse, q_tok, S, ws, ws_bytes, stream
+    args = lambda U=f, S=f, r=16, T=1.0: (4, 4, 1024, r, T, f, f, U, f, 1, f, f, f, f, f, S, f,
+                                           ws_n, n)
+    assert L.dspark_draft_sample_rnn(*args(U=n)) == 1
+    assert "U is NULL" in _err(L)
+    assert L.dspark_draft_sample_rnn(*args(S=n)) == 1
+    assert L.dspark_draft_sample_rnn(*args(S=ctypes.c_void_p(0x1008))) == 1  # not 16-byte aligned
+    assert L.dspark_draft_sample_rnn(*args(r=2000)) == 1  # rank above 1024
+    # verify: R, G, V, r, T, z, S, Wt, dt, tokens, q_lse, q_tok, ell, row_off, target,
+    # n_rows, u_acc, u_fin, n_acc, out_tokens, p_lse, ws, ws_bytes, stream
+    v = lambda S=f, rows=20, ua=f: (4, 4, 1024, 16, 1.0, f, S, f, 1, f, f, f, f, f, f, rows, ua,
+                                    f, f, f, n, f, ws_n, n)
+    assert L.dspark_verify_rnn(*v(S=n)) == 1  # the states are needed when T > 0
+    assert L.dspark_verify_rnn(*v(S=ctypes.c_void_p(0x1008))) == 1
+    assert L.dspark_verify_rnn(*v(rows=0)) == 1
+    assert L.dspark_verify_rnn(*v(ua=n)) == 1
