@@ -719,6 +719,9 @@ struct PersistParams {
 // lane quadrant (hence every epilogue warp) holding live rows.
 constexpr uint32_t kPairBlk = 64 * 128;  // 64 rows x 128 bytes
 static_assert(sizeof(FinishScratch) <= kPairBlk, "finish scratch must fit one A block");
+// two finish scratches (more requests than CTAs: unpaired layout) on A(0)
+static_assert(2 * sizeof(FinishScratch) <= kABytesPerChunk, "two finish scratches must fit A(0)");
+static_assert(sizeof(FinishScratch) % 16 == 0, "finish scratch alignment");
 
 __host__ __device__ inline uint32_t persist_a_bytes(int nK, int pair) {
   return pair ? (uint32_t)(2 * nK + 1) * kPairBlk : (uint32_t)nK * kABytesPerChunk;
@@ -910,6 +913,10 @@ __device__ __noinline__ void fused_cut(const PersistParams& pp, uint8_t* buf, in
                            f.row_off, f.B_out, f.E_out);
 }
 
+// kGrouped: more than 7 requests a CTA; each CTA runs two finishes at once
+// (a separate instantiation: the grouped finish's registers would otherwise
+// weigh on the epilogue of every launch).
+template <bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 1)
     draft_persistent_kernel(const __grid_constant__ CUtensorMap tm_w,
                             const __grid_constant__ CUtensorMap tm_z,
@@ -1208,10 +1215,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       // done: order their async-proxy reads before these generic writes)
       fence_proxy_async_smem();
       const BiasSrc b{nullptr, p.E, pp.Wt, prev, stride, p.r};
-      for (int nn = cta; nn < p.R; nn += n_ctas)
-        finish_request<__nv_bfloat16, kHalf, NamedSync<3, 256>, true>(
-            fs, nn, p.V, p.gamma, k, p.n_parts, pp.z, b, p.sc, p.greedy, p.part, pp.u, pp.tokens,
-            pp.q_lse, pp.q_tok, p.status, k + 1 < p.gamma ? pp.stage : nullptr, p.sub);
+      if constexpr (kGrouped) {
+        // many requests a CTA: two finishes at once, four warps each
+        // (request cta, cta + 2 n_ctas, ... on warps 0-3; cta + n_ctas, ...
+        // on warps 4-7), each on its own scratch and named barrier
+        const int grp = warp >> 2;
+        FinishScratch& fg = (&fs)[grp];
+        for (int nn = cta + grp * (int)n_ctas; nn < p.R; nn += 2 * (int)n_ctas)
+          finish_request<__nv_bfloat16, kHalf, GroupSync<4, 4>, true>(
+              fg, nn, p.V, p.gamma, k, p.n_parts, pp.z, b, p.sc, p.greedy, p.part, pp.u,
+              pp.tokens, pp.q_lse, pp.q_tok, p.status, k + 1 < p.gamma ? pp.stage : nullptr,
+              p.sub);
+        NamedSync<3, 256>::sync();  // both groups done (the log pass reads their q_lse)
+      } else {
+        for (int nn = cta; nn < p.R; nn += n_ctas)
+          finish_request<__nv_bfloat16, kHalf, NamedSync<3, 256>, true>(
+              fs, nn, p.V, p.gamma, k, p.n_parts, pp.z, b, p.sc, p.greedy, p.part, pp.u,
+              pp.tokens, pp.q_lse, pp.q_tok, p.status, k + 1 < p.gamma ? pp.stage : nullptr,
+              p.sub);
+      }
       if (k + 1 < p.gamma) {
         // the finish scratch (generic) is overwritten by the next A's TMA;
         // every CTA needs every staged row before it loads the next A
@@ -1802,16 +1824,18 @@ cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st) {
                                   (size_t)persist_z_slots(pair) * kZBytes)
     pp.fuse = 0;
   if (pp.fuse) pp.f = *a.fuse;
-  e = ensure_smem_attr((const void*)draft_persistent_kernel, (int)tc_smem_bytes(4));
-  if (e != cudaSuccess) return e;
-  const size_t smem = persist_smem_bytes(p.nK, pair);
-  if (blocks_per_sm((const void*)draft_persistent_kernel, kThreads, smem) < 1)
-    return cudaErrorNotSupported;
   const int n_rt = (a.R + BM - 1) / BM;
   const int n_units = pair ? (p.n_vt + 1) / 2 : p.n_vt;
   int gx = sm_count() / n_rt;
   if (gx < 1) return cudaErrorNotSupported;
   if (gx > n_units) gx = n_units;
+  const bool grouped = a.R > 7 * gx * n_rt;
+  const void* kern = grouped ? (const void*)draft_persistent_kernel<true>
+                             : (const void*)draft_persistent_kernel<false>;
+  e = ensure_smem_attr(kern, (int)tc_smem_bytes(4));
+  if (e != cudaSuccess) return e;
+  const size_t smem = persist_smem_bytes(p.nK, pair);
+  if (blocks_per_sm(kern, kThreads, smem) < 1) return cudaErrorNotSupported;
   e = cudaMemsetAsync(a.grid_counter, 0, 2 * sizeof(unsigned), st);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1824,8 +1848,13 @@ cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  DSPARK_LAUNCH(kKindDraftPersistent, st,
-                e = cudaLaunchKernelEx(&cfg, draft_persistent_kernel, tm_w, tm_z, tm_a, pp));
+  if (grouped)
+    DSPARK_LAUNCH(kKindDraftPersistent, st,
+                  e = cudaLaunchKernelEx(&cfg, draft_persistent_kernel<true>, tm_w, tm_z, tm_a, pp));
+  else
+    DSPARK_LAUNCH(kKindDraftPersistent, st,
+                  e = cudaLaunchKernelEx(&cfg, draft_persistent_kernel<false>, tm_w, tm_z, tm_a,
+                                         pp));
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e == cudaSuccess && a.fused != nullptr) *a.fused = pp.fuse;

@@ -13,15 +13,34 @@
 
 namespace dspark {
 
+// The threads that run one finish and how they synchronise: kWarps warps,
+// tid() the thread's index among them.  BlockSync: a 256-thread block;
+// NamedSync: threads 0 .. kThreads-1 of a larger block, on barrier kId;
+// GroupSync: the block's warps in groups of NW, group g on barrier kBase + g
+// (several finishes at once, one per group).
 struct BlockSync {
+  static constexpr int kWarps = 8;
   __device__ __forceinline__ static void sync() { __syncthreads(); }
+  __device__ __forceinline__ static int tid() { return threadIdx.x; }
 };
 
 template <int kId, int kThreads>
 struct NamedSync {
+  static constexpr int kWarps = kThreads / 32;
   __device__ __forceinline__ static void sync() {
     asm volatile("bar.sync %0, %1;" ::"n"(kId), "n"(kThreads) : "memory");
   }
+  __device__ __forceinline__ static int tid() { return threadIdx.x; }
+};
+
+template <int kBase, int NW>
+struct GroupSync {
+  static constexpr int kWarps = NW;
+  __device__ __forceinline__ static void sync() {
+    const int id = kBase + (int)(threadIdx.x >> 5) / NW;
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(NW * 32) : "memory");
+  }
+  __device__ __forceinline__ static int tid() { return (int)threadIdx.x % (NW * 32); }
 };
 
 // Where the finish gets the chosen tile's bias: the CUDA-core bias array of
@@ -53,7 +72,7 @@ struct FinishScratch {
   float erow[1024];
 };
 
-// ---- reductions over 256 threads (8 warps), every thread gets the result
+// ---- reductions over the S::kWarps warps of a finish, every thread gets the result
 
 // Warp maximum of floats that are never NaN (-inf allowed), as one integer
 // reduction instruction on an order-preserving image of the bits (a negative
@@ -65,10 +84,10 @@ __device__ __forceinline__ float warp_max_nonan(float a) {
   return __int_as_float(k >= 0 ? k : (k ^ 0x7fffffff));
 }
 
-// Inclusive scan over the 256 threads; *total receives the sum of all.
+// Inclusive scan over the finish's threads; *total receives the sum of all.
 template <class S>
 __device__ __forceinline__ long long g_scan_ll(long long v, long long* sh, long long* total) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int lane = S::tid() & 31, wid = S::tid() >> 5;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const long long n = __shfl_up_sync(0xffffffffu, v, o);
@@ -79,7 +98,7 @@ __device__ __forceinline__ long long g_scan_ll(long long v, long long* sh, long 
   S::sync();
   long long off = 0, tot = 0;
 #pragma unroll
-  for (int w = 0; w < 8; ++w) {
+  for (int w = 0; w < S::kWarps; ++w) {
     const long long x = sh[w];
     if (w < wid) off += x;
     tot += x;
@@ -92,7 +111,7 @@ __device__ __forceinline__ long long g_scan_ll(long long v, long long* sh, long 
 template <class S>
 __device__ __forceinline__ void g_scan_ll2(long long& a, long long& b, long long* sha,
                                            long long* shb, long long* ta, long long* tb) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int lane = S::tid() & 31, wid = S::tid() >> 5;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const long long na = __shfl_up_sync(0xffffffffu, a, o);
@@ -110,7 +129,7 @@ __device__ __forceinline__ void g_scan_ll2(long long& a, long long& b, long long
   S::sync();
   long long oa = 0, ob = 0, sa = 0, sb = 0;
 #pragma unroll
-  for (int w = 0; w < 8; ++w) {
+  for (int w = 0; w < S::kWarps; ++w) {
     const long long xa = sha[w], xb = shb[w];
     if (w < wid) {
       oa += xa;
@@ -127,54 +146,54 @@ __device__ __forceinline__ void g_scan_ll2(long long& a, long long& b, long long
 
 template <class S>
 __device__ __forceinline__ int g_min_i(int v, int* sh) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int lane = S::tid() & 31, wid = S::tid() >> 5;
   v = __reduce_min_sync(0xffffffffu, v);  // one warp-wide reduction instruction
   S::sync();
   if (lane == 0) sh[wid] = v;
   S::sync();
   int r = sh[0];
 #pragma unroll
-  for (int w = 1; w < 8; ++w) r = min(r, sh[w]);
+  for (int w = 1; w < S::kWarps; ++w) r = min(r, sh[w]);
   return r;
 }
 
 template <class S>
 __device__ __forceinline__ int g_max_i(int v, int* sh) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int lane = S::tid() & 31, wid = S::tid() >> 5;
   v = __reduce_max_sync(0xffffffffu, v);
   S::sync();
   if (lane == 0) sh[wid] = v;
   S::sync();
   int r = sh[0];
 #pragma unroll
-  for (int w = 1; w < 8; ++w) r = max(r, sh[w]);
+  for (int w = 1; w < S::kWarps; ++w) r = max(r, sh[w]);
   return r;
 }
 
 // (v never NaN)
 template <class S>
 __device__ __forceinline__ float g_max_f(float v, float* sh) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int lane = S::tid() & 31, wid = S::tid() >> 5;
   v = warp_max_nonan(v);
   S::sync();
   if (lane == 0) sh[wid] = v;
   S::sync();
   float r = sh[0];
 #pragma unroll
-  for (int w = 1; w < 8; ++w) r = fmaxf(r, sh[w]);
+  for (int w = 1; w < S::kWarps; ++w) r = fmaxf(r, sh[w]);
   return r;
 }
 
 template <class S>
 __device__ __forceinline__ ArgMax g_argmax(ArgMax a, ArgMax* sh) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int lane = S::tid() & 31, wid = S::tid() >> 5;
   a = warp_argmax(a);
   S::sync();
   if (lane == 0) sh[wid] = a;
   S::sync();
   ArgMax r = sh[0];
 #pragma unroll
-  for (int w = 1; w < 8; ++w) r = better(r, sh[w]);
+  for (int w = 1; w < S::kWarps; ++w) r = better(r, sh[w]);
   return r;
 }
 
@@ -194,8 +213,8 @@ __device__ __forceinline__ long long rel_fix(float a, float ref, float* w_out) {
 template <int TW, class S>
 __device__ __forceinline__ void tile_bias_recompute(const BiasSrc& b, int V, int v0,
                                                     const float* erow, float* bias) {
-  constexpr int CPW = TW / 8;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int CPW = TW / S::kWarps;
+  const int warp = S::tid() >> 5, lane = S::tid() & 31;
   const int j = lane * 8;
   const bool lane_on = j < b.r;
   uint4 raw[CPW];
@@ -232,7 +251,7 @@ __device__ __forceinline__ void stage_row(FinishScratch& s, __nv_bfloat16* stage
                                           const BiasSrc& b, int n) {
   if (stage == nullptr) return;
   const int tok = s.tok;
-  const int tid = threadIdx.x;
+  const int tid = S::tid();
   if (tid < b.r / 8) {
     uint4 v = make_uint4(0, 0, 0, 0);
     if (tok >= 0) v = *reinterpret_cast<const uint4*>(b.E + (size_t)tok * b.r + tid * 8);
@@ -303,8 +322,8 @@ __device__ __forceinline__ void load_groups(const float* sub, float (&gs)[8]) {
   gs[4] = b.x; gs[5] = b.y; gs[6] = b.z; gs[7] = b.w;
 }
 
-// The finish of request n at draft position k, by 256 threads
-// (threadIdx.x < 256).  part: [R][n_tiles] tile partials (doubles; greedy:
+// The finish of request n at draft position k, by the S::kWarps warps of
+// one finish group (S::tid() their thread index).  part: [R][n_tiles] tile partials (doubles; greedy:
 // ArgMax pairs) of width TW.  Writes tokens / q_lse / q_tok [n][k].
 // With sub ([R][n_tiles][8] group sums of 128-token partials) the draw is
 // placed in a 16-token group first and only that group is recomputed;
@@ -317,13 +336,14 @@ __device__ void finish_request(FinishScratch& s, int n, int V, int gamma, int k,
                                int greedy, const double* part, const float* __restrict__ u,
                                int32_t* tokens, double* q_lse, float* q_tok, uint32_t* status,
                                __nv_bfloat16* stage = nullptr, const float* sub = nullptr) {
-  const int tid = threadIdx.x;
+  constexpr int NT = S::kWarps * 32;
+  const int tid = S::tid();
   const size_t out = (size_t)n * gamma + k;
   const float u_out = greedy ? 0.0f : u[out];  // issued early: needed after the scan
   if (greedy) {
     const ArgMax* P = reinterpret_cast<const ArgMax*>(part) + (size_t)n * n_tiles;
     ArgMax best{-INFINITY, 0x7fffffff};
-    for (int t = tid; t < n_tiles; t += 256) {
+    for (int t = tid; t < n_tiles; t += NT) {
       const long long raw = __ldcg(reinterpret_cast<const long long*>(P + t));
       ArgMax am;
       am.v = __int_as_float((int)(raw & 0xffffffffll));
@@ -356,18 +376,18 @@ __device__ void finish_request(FinishScratch& s, int n, int V, int gamma, int k,
         tok = -1;
       }
     }
-    for (int i = tid; i < bsrc.r; i += 256)
+    for (int i = tid; i < bsrc.r; i += NT)
       s.erow[i] = tok >= 0 ? __bfloat162float(bsrc.E[(size_t)tok * bsrc.r + i]) : 0.f;
   }
   // The partials are exact doubles; they are summed exactly as integers in
   // units of 2^g, g chosen from the largest partial's exponent so that the
   // sum of all n_tiles partials stays below 2^62.  Thread tid owns the
-  // contiguous tiles [t0, t0 + seg); up to kMaxSeg of them (V <= 2^18 on
-  // the tensor-core path) are loaded once into registers, longer segments
-  // are re-read from L2 in each pass.
+  // contiguous tiles [t0, t0 + seg); up to kMaxSeg of them (2048 tiles in
+  // all: V <= 2^18 on the tensor-core path) are loaded once into registers,
+  // longer segments are re-read from L2 in each pass.
   constexpr int kMaxSeg = 8;
   const double* S_ = part + (size_t)n * n_tiles;
-  const int seg = (n_tiles + 255) / 256;
+  const int seg = (n_tiles + NT - 1) / NT;
   const bool fast = seg <= kMaxSeg;
   const int t0 = min(n_tiles, tid * seg), t1 = min(n_tiles, t0 + seg);
   double pv[kMaxSeg];
@@ -523,7 +543,8 @@ __device__ __forceinline__ void finish_group(FinishScratch& s, int n, int V, int
                                           const BiasSrc& bsrc, ScalePair sc, const float* sub,
                                           int n_tiles, int32_t* tokens, double* q_lse,
                                           float* q_tok, __nv_bfloat16* stage) {
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  constexpr int TPW = 16 / S::kWarps;  // the group's tokens per warp
+  const int tid = S::tid(), lane = tid & 31, w = tid >> 5;
   const int grp0 = s.grp;
   if (fallback || grp0 < 0) {
     // the last group with mass, its last token with mass
@@ -542,13 +563,13 @@ __device__ __forceinline__ void finish_group(FinishScratch& s, int n, int V, int
   }
   const int gv0 = tsel * 128 + s.grp * 16;
   const float f2 = s.f2;
-  // bias of tokens gv0 + 2w + c; the E rows of the same tokens ride along
+  // bias of tokens gv0 + TPW w + c; the E rows of the same tokens ride along
   const int j = lane * 8;
   const bool lane_on = j < bsrc.r;
-  uint4 wr[2], er[2];
+  uint4 wr[TPW], er[TPW];
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    const int v = gv0 + 2 * w + c;
+  for (int c = 0; c < TPW; ++c) {
+    const int v = gv0 + TPW * w + c;
     const bool ok = lane_on && v < V;
     wr[c] = ok ? *reinterpret_cast<const uint4*>(bsrc.Wt + (size_t)v * bsrc.r + j)
                : make_uint4(0, 0, 0, 0);
@@ -562,7 +583,7 @@ __device__ __forceinline__ void finish_group(FinishScratch& s, int n, int V, int
 #pragma unroll
   for (int i = 0; i < 8; ++i) e8[i] = lane_on ? s.erow[j + i] : 0.f;
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {
+  for (int c = 0; c < TPW; ++c) {
     const uint32_t w4[4] = {wr[c].x, wr[c].y, wr[c].z, wr[c].w};
     float acc = 0.f;
 #pragma unroll
@@ -571,7 +592,7 @@ __device__ __forceinline__ void finish_group(FinishScratch& s, int n, int V, int
       acc = fmaf(__uint_as_float(w4[e] & 0xffff0000u), e8[2 * e + 1], acc);
     }
     acc = warp_sum(acc);
-    if (lane == 0) s.bias[2 * w + c] = acc;
+    if (lane == 0) s.bias[TPW * w + c] = acc;
   }
   S::sync();
   if (w == 0) {
@@ -613,8 +634,13 @@ __device__ __forceinline__ void finish_group(FinishScratch& s, int n, int V, int
   S::sync();
   if (stage != nullptr) {
     const int isel = s.tok;
-    if (w == (isel >> 1) && lane_on)
-      *reinterpret_cast<uint4*>(stage + (size_t)n * bsrc.r + j) = (isel & 1) ? er[1] : er[0];
+    if (w == isel / TPW && lane_on) {
+      uint4 row = er[0];
+#pragma unroll
+      for (int c = 1; c < TPW; ++c)
+        if (isel % TPW == c) row = er[c];
+      *reinterpret_cast<uint4*>(stage + (size_t)n * bsrc.r + j) = row;
+    }
     sm100::fence_proxy_async_all();
     S::sync();
   }
