@@ -913,10 +913,10 @@ __device__ __noinline__ void fused_cut(const PersistParams& pp, uint8_t* buf, in
                            f.row_off, f.B_out, f.E_out);
 }
 
-// kGrouped: more than 7 requests a CTA; each CTA runs two finishes at once
-// (a separate instantiation: the grouped finish's registers would otherwise
-// weigh on the epilogue of every launch).
-template <bool kGrouped>
+// kGroups: finishes a CTA runs at once (8 / kGroups warps each) when it has
+// many requests to finish; separate instantiations, so that the grouped
+// finishes' registers do not weigh on the epilogue of every launch.
+template <int kGroups>
 __global__ void __launch_bounds__(kThreads, 1)
     draft_persistent_kernel(const __grid_constant__ CUtensorMap tm_w,
                             const __grid_constant__ CUtensorMap tm_z,
@@ -1215,14 +1215,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // done: order their async-proxy reads before these generic writes)
       fence_proxy_async_smem();
       const BiasSrc b{nullptr, p.E, pp.Wt, prev, stride, p.r};
-      if constexpr (kGrouped) {
-        // many requests a CTA: two finishes at once, four warps each
-        // (request cta, cta + 2 n_ctas, ... on warps 0-3; cta + n_ctas, ...
-        // on warps 4-7), each on its own scratch and named barrier
-        const int grp = warp >> 2;
+      if constexpr (kGroups > 1) {
+        // many requests a CTA: kGroups finishes at once (group g on warps
+        // g * 8 / kGroups .., requests cta + g n_ctas, cta + (g + kGroups)
+        // n_ctas, ...), each on its own scratch and named barrier
+        constexpr int kNW = 8 / kGroups;
+        const int grp = warp / kNW;
         FinishScratch& fg = (&fs)[grp];
-        for (int nn = cta + grp * (int)n_ctas; nn < p.R; nn += 2 * (int)n_ctas)
-          finish_request<__nv_bfloat16, kHalf, GroupSync<4, 4>, true>(
+        for (int nn = cta + grp * (int)n_ctas; nn < p.R; nn += kGroups * (int)n_ctas)
+          finish_request<__nv_bfloat16, kHalf, GroupSync<4, kNW>, true>(
               fg, nn, p.V, p.gamma, k, p.n_parts, pp.z, b, p.sc, p.greedy, p.part, pp.u,
               pp.tokens, pp.q_lse, pp.q_tok, p.status, k + 1 < p.gamma ? pp.stage : nullptr,
               p.sub);
@@ -1829,9 +1830,12 @@ cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st) {
   int gx = sm_count() / n_rt;
   if (gx < 1) return cudaErrorNotSupported;
   if (gx > n_units) gx = n_units;
-  const bool grouped = a.R > 7 * gx * n_rt;
-  const void* kern = grouped ? (const void*)draft_persistent_kernel<true>
-                             : (const void*)draft_persistent_kernel<false>;
+  // two concurrent finishes a CTA once a CTA has eight or more requests (at
+  // four, the greedy workload, they measured slower)
+  const int per_cta = (a.R + gx * n_rt - 1) / (gx * n_rt);
+  const int groups = per_cta >= 8 ? 2 : 1;
+  const void* kern = groups == 2 ? (const void*)draft_persistent_kernel<2>
+                                 : (const void*)draft_persistent_kernel<1>;
   e = ensure_smem_attr(kern, (int)tc_smem_bytes(4));
   if (e != cudaSuccess) return e;
   const size_t smem = persist_smem_bytes(p.nK, pair);
@@ -1848,13 +1852,12 @@ cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (grouped)
+  if (groups == 2)
     DSPARK_LAUNCH(kKindDraftPersistent, st,
-                  e = cudaLaunchKernelEx(&cfg, draft_persistent_kernel<true>, tm_w, tm_z, tm_a, pp));
+                  e = cudaLaunchKernelEx(&cfg, draft_persistent_kernel<2>, tm_w, tm_z, tm_a, pp));
   else
     DSPARK_LAUNCH(kKindDraftPersistent, st,
-                  e = cudaLaunchKernelEx(&cfg, draft_persistent_kernel<false>, tm_w, tm_z, tm_a,
-                                         pp));
+                  e = cudaLaunchKernelEx(&cfg, draft_persistent_kernel<1>, tm_w, tm_z, tm_a, pp));
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e == cudaSuccess && a.fused != nullptr) *a.fused = pp.fuse;

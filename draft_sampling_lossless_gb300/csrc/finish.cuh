@@ -563,19 +563,23 @@ __device__ __forceinline__ void finish_group(FinishScratch& s, int n, int V, int
   }
   const int gv0 = tsel * 128 + s.grp * 16;
   const float f2 = s.f2;
-  // bias of tokens gv0 + TPW w + c; the E rows of the same tokens ride along
+  // bias of tokens gv0 + TPW w + c; with up to two tokens a warp their E
+  // rows ride along (the drawn token's is staged from registers), with more
+  // the drawn token's row is read once it is known (fewer live registers)
+  constexpr bool kRide = TPW <= 2;
   const int j = lane * 8;
   const bool lane_on = j < bsrc.r;
-  uint4 wr[TPW], er[TPW];
+  uint4 wr[TPW], er[kRide ? TPW : 1];
 #pragma unroll
   for (int c = 0; c < TPW; ++c) {
     const int v = gv0 + TPW * w + c;
     const bool ok = lane_on && v < V;
     wr[c] = ok ? *reinterpret_cast<const uint4*>(bsrc.Wt + (size_t)v * bsrc.r + j)
                : make_uint4(0, 0, 0, 0);
-    er[c] = (ok && stage != nullptr)
-                ? *reinterpret_cast<const uint4*>(bsrc.E + (size_t)v * bsrc.r + j)
-                : make_uint4(0, 0, 0, 0);
+    if constexpr (kRide)
+      er[c] = (ok && stage != nullptr)
+                  ? *reinterpret_cast<const uint4*>(bsrc.E + (size_t)v * bsrc.r + j)
+                  : make_uint4(0, 0, 0, 0);
   }
   const int vz = gv0 + lane;
   const float zv = (w == 0 && lane < 16 && vz < V) ? ldf(z, out * V + vz) : 0.f;
@@ -634,12 +638,17 @@ __device__ __forceinline__ void finish_group(FinishScratch& s, int n, int V, int
   S::sync();
   if (stage != nullptr) {
     const int isel = s.tok;
-    if (w == isel / TPW && lane_on) {
-      uint4 row = er[0];
+    if constexpr (kRide) {
+      if (w == isel / TPW && lane_on) {
+        uint4 row = er[0];
 #pragma unroll
-      for (int c = 1; c < TPW; ++c)
-        if (isel % TPW == c) row = er[c];
-      *reinterpret_cast<uint4*>(stage + (size_t)n * bsrc.r + j) = row;
+        for (int c = 1; c < TPW; ++c)
+          if (isel % TPW == c) row = er[c];
+        *reinterpret_cast<uint4*>(stage + (size_t)n * bsrc.r + j) = row;
+      }
+    } else if (w == 0 && lane_on && gv0 + isel < V) {
+      *reinterpret_cast<uint4*>(stage + (size_t)n * bsrc.r + j) =
+          *reinterpret_cast<const uint4*>(bsrc.E + (size_t)(gv0 + isel) * bsrc.r + j);
     }
     sm100::fence_proxy_async_all();
     S::sync();
