@@ -994,6 +994,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpW) {
     if (lane == 0) {
       const uint64_t pol = policy_evict_last();
+      // W is not in L2 at the first position: ask for the tiles of this
+      // CTA's later units now, so that they arrive while the first unit's
+      // tiles stream through the ring (32 KiB prefetches of whole rows)
+      for (int u = blockIdx.x + gridDim.x; u < n_units; u += gridDim.x)
+        for (int pass = 0; pass < passes; ++pass) {
+          const int t = pair ? 2 * u + pass : u;
+          if (t >= p.n_vt) continue;
+          const char* base = reinterpret_cast<const char*>(pp.Wt) + (size_t)t * BN * p.r * 2;
+          const uint32_t bytes = (uint32_t)(min(BN, p.V - t * BN) * p.r * 2);
+          for (uint32_t o = 0; o < bytes; o += 32768)
+            prefetch_l2_bulk(base + o, min(32768u, bytes - o));
+        }
       RingPos rb;
       for (int k = 0; k < p.gamma; ++k)
         for (int u = blockIdx.x; u < n_units; u += gridDim.x)
