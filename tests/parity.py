@@ -38,10 +38,13 @@ class Stats:
     value_checks: int = 0
     worst_rel: dict = field(default_factory=dict)
     tie_kinds: dict = field(default_factory=dict)  # near-ties by decision kind
+    tie_details: list = field(default_factory=list)  # (kind, details) of each near-tie
 
-    def tie(self, kind):
+    def tie(self, kind, detail=None):
         self.near_ties += 1
         self.tie_kinds[kind] = self.tie_kinds.get(kind, 0) + 1
+        if detail is not None:
+            self.tie_details.append((kind, detail))
 
     def rel(self, name, got, want, tol=REL):
         got = np.asarray(got, dtype=np.float64)
@@ -57,6 +60,7 @@ class Stats:
         self.decisions += o.decisions
         self.near_ties += o.near_ties
         self.unexplained += o.unexplained
+        self.tie_details += o.tie_details
         self.value_checks += o.value_checks
         for k, v in o.tie_kinds.items():
             self.tie_kinds[k] = self.tie_kinds.get(k, 0) + v
@@ -70,6 +74,17 @@ def cdf_near_tie(w: np.ndarray, u: float, g: int, o: int) -> bool:
     thr = u * S
     lo, hi = min(g, o), max(g, o)
     return abs(C[lo] - thr) <= TIE * S and abs(C[hi - 1] - thr) <= TIE * S
+
+
+def cdf_tie_detail(w: np.ndarray, u: float, g: int, o: int) -> dict:
+    """Where a differing draw sits: the normalised distance of u from the
+    oracle's boundaries between the two tokens, their probabilities."""
+    C = np.cumsum(w)
+    S = C[-1]
+    lo, hi = min(g, o), max(g, o)
+    return dict(gpu=g, oracle=o, d_lo=float((C[lo] - u * S) / S),
+                d_hi=float((C[hi - 1] - u * S) / S), p_gpu=float(w[g] / S),
+                p_oracle=float(w[o] / S), u=float(u))
 
 
 def argmax_near_tie(y: np.ndarray, g: int, o: int) -> bool:
@@ -167,7 +182,9 @@ class Case:
                     tie = cdf_near_tie(np.exp(yy - yy.max()), self.u_draft[i, k],
                                        int(tok_g[i, k]), int(tok_o[i, k]))
                 if tie:
-                    st.tie("draft")
+                    st.tie("draft", None if wl.T == 0.0 else dict(
+                        k=k, **cdf_tie_detail(np.exp(yy - yy.max()), self.u_draft[i, k],
+                                              int(tok_g[i, k]), int(tok_o[i, k]))))
                 else:
                     st.unexplained.append(("draft", int(self.sample[i]), k, int(tok_g[i, k]),
                                            int(tok_o[i, k])))
@@ -291,7 +308,7 @@ class Case:
                                          wl.T, trow, na_o, i, na_o < ell_s[i], states=self.S_o)
                 tie = cdf_near_tie(w, self.u_fin[i], fg, fo)
             if tie:
-                st.tie("final")
+                st.tie("final", None if wl.T == 0.0 else cdf_tie_detail(w, self.u_fin[i], fg, fo))
             else:
                 st.unexplained.append(("final", int(self.sample[i]), na_o, fg, fo))
         return o

@@ -85,5 +85,8 @@ def test_near_tie_rate_at_full_size(name):
         f"decisions={st.decisions} near_ties={st.near_ties} {st.tie_kinds} "
         f"rate={st.near_ties / max(1, st.decisions):.2e} (budget {budget:.0e}: "
         f"{budget * st.decisions:.1f}) unexplained={len(st.unexplained)}")
+    for kind, d in st.tie_details[:12]:
+        conftest.SUMMARY.append(f"  near-tie {name} {kind}: " + " ".join(
+            f"{a}={v:.3g}" if isinstance(v, float) else f"{a}={v}" for a, v in d.items()))
     assert st.unexplained == [], st.unexplained[:10]
     assert st.near_ties <= budget * st.decisions, (st.near_ties, st.decisions)
