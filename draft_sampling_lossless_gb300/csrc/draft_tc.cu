@@ -241,8 +241,8 @@ __device__ __forceinline__ void epi_half_greedy(const uint32_t (&b)[32], const u
 // in the draft epilogue: x c = P + x' (P = x_hi c12 exact for a bf16 x_hi;
 // x' the rest), n = rint(P + bq c12 + e) clamped at -125, the fraction
 // f = (P - rint(P + bq c12)) + bq c12 + (x_hi + bq) crest in [-1/2, 1/2]
-// to ex2, 2^n from the magic number's bits.  xx: the bf16 values (z, or the
-// target logits with bb = 0); bb: the Markov bias (or zero).
+// to ex2, 2^n from the magic number's bits.  xx: the bf16 values (z);
+// bb: the Markov bias.
 __device__ __forceinline__ unsigned long long pow2_split2(unsigned long long xx,
                                                           unsigned long long bb,
                                                           unsigned long long c12,
@@ -258,6 +258,48 @@ __device__ __forceinline__ unsigned long long pow2_split2(unsigned long long xx,
   F = fma2(xx, cr2, fma2(bb, cr2, F));
   float fa, fb;
   unpack2(F, fa, fb);
+  const float sa = __uint_as_float(__float_as_uint(qa) * 8388608u + 0x3f800000u);  // 2^n
+  const float sb = __uint_as_float(__float_as_uint(qb) * 8388608u + 0x3f800000u);
+  return pack2(ex2_approx(fa) * sa, ex2_approx(fb) * sb);
+}
+
+// The same with the bias scaled by cf = c rounded to fp32 (one fused
+// multiply-add fewer: bq c12 + bq crest becomes bq cf, whose rounding moves
+// f by about 2^-24 |bq| c, far below ex2's own error).  The final draw's
+// residual weights use it.
+__device__ __forceinline__ unsigned long long pow2_split2_cf(unsigned long long xx,
+                                                             unsigned long long bb,
+                                                             unsigned long long c12,
+                                                             unsigned long long cf2,
+                                                             unsigned long long cr2,
+                                                             unsigned long long k2, float klo) {
+  const unsigned long long P = mul2(xx, c12);
+  float qa, qb;
+  unpack2(add2(fma2(bb, cf2, P), k2), qa, qb);  // 1.5 * 2^23 + n
+  qa = fmaxf(qa, klo);
+  qb = fmaxf(qb, klo);
+  const unsigned long long M = sub2(pack2(qa, qb), k2);
+  float fa, fb;
+  unpack2(fma2(xx, cr2, fma2(bb, cf2, sub2(P, M))), fa, fb);
+  const float sa = __uint_as_float(__float_as_uint(qa) * 8388608u + 0x3f800000u);  // 2^n
+  const float sb = __uint_as_float(__float_as_uint(qb) * 8388608u + 0x3f800000u);
+  return pack2(ex2_approx(fa) * sa, ex2_approx(fb) * sb);
+}
+
+// The same without a bias (the target logits): n = rint(P + e) clamped at
+// -125, f = (P - rint(P)) + x_hi crest.
+__device__ __forceinline__ unsigned long long pow2_split2_nb(unsigned long long xx,
+                                                             unsigned long long c12,
+                                                             unsigned long long cr2,
+                                                             unsigned long long k2, float klo) {
+  const unsigned long long P = mul2(xx, c12);
+  float qa, qb;
+  unpack2(add2(P, k2), qa, qb);  // 1.5 * 2^23 + n
+  qa = fmaxf(qa, klo);
+  qb = fmaxf(qb, klo);
+  const unsigned long long M = sub2(pack2(qa, qb), k2);
+  float fa, fb;
+  unpack2(fma2(xx, cr2, sub2(P, M)), fa, fb);
   const float sa = __uint_as_float(__float_as_uint(qa) * 8388608u + 0x3f800000u);  // 2^n
   const float sb = __uint_as_float(__float_as_uint(qb) * 8388608u + 0x3f800000u);
   return pack2(ex2_approx(fa) * sa, ex2_approx(fb) * sb);
@@ -1347,10 +1389,12 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
 // A NaN group is left out (the pick's recompute flags it).
 __device__ __forceinline__ void fin_block(const uint32_t (&b)[32], const uint4 (&zq)[4],
                                           const uint4 (&tq)[4], int lim, bool resid, float c12,
-                                          float crest, InvPair ip, InvPair iq, float (&acc)[4]) {
+                                          float cf, float crest, InvPair ip, InvPair iq,
+                                          float (&acc)[4]) {
   if (ip.hi == 0.f) return;  // no target normaliser: no mass
   const bool qlive = resid && iq.hi != 0.f;
   const unsigned long long c2 = pack2(c12, c12), cr2 = pack2(crest, crest);
+  const unsigned long long cf2 = pack2(cf, cf);
   const float kp = 12582912.0f + (float)ip.e, kq = 12582912.0f + (float)iq.e;
   const unsigned long long kp2 = pack2(kp, kp), kq2 = pack2(kq, kq);
   const float klo = 12582912.0f - 125.0f;
@@ -1364,7 +1408,7 @@ __device__ __forceinline__ void fin_block(const uint32_t (&b)[32], const uint4 (
       const int k = gg * 8 + e;  // the token pair (2k, 2k + 1)
       const uint32_t tw = (&tq[0].x)[k];
       const unsigned long long wp =
-          pow2_split2(pack2(bf_lo(tw), bf_hi(tw)), 0ull, c2, cr2, kp2, klo);
+          pow2_split2_nb(pack2(bf_lo(tw), bf_hi(tw)), c2, cr2, kp2, klo);
       unsigned long long pp = fma2(wp, iph, mul2(wp, ipl));
       float pa, pb;
       unpack2(pp, pa, pb);
@@ -1374,9 +1418,9 @@ __device__ __forceinline__ void fin_block(const uint32_t (&b)[32], const uint4 (
       if (qlive) {
         const uint32_t zw = (&zq[0].x)[k];
         const unsigned long long wq =
-            pow2_split2(pack2(bf_lo(zw), bf_hi(zw)),
-                        pack2(__uint_as_float(b[2 * k]), __uint_as_float(b[2 * k + 1])), c2, cr2,
-                        kq2, klo);
+            pow2_split2_cf(pack2(bf_lo(zw), bf_hi(zw)),
+                           pack2(__uint_as_float(b[2 * k]), __uint_as_float(b[2 * k + 1])), c2,
+                           cf2, cr2, kq2, klo);
         float qa, qb;
         unpack2(fma2(wq, iqh, mul2(wq, iql)), qa, qb);
         r2[e] = pack2(fmaxf(0.0f, pa - qa), fmaxf(0.0f, pb - qb));
@@ -1640,7 +1684,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(b_emptyZ + 8 * (half * 4 + zs));
         tmem_wait_ld_regs(b);
         if (valid)
-          fin_block(b, zq, tq, min(32, p.V - v0), resid, p.c12, p.crest, st.ip, st.iq, facc);
+          fin_block(b, zq, tq, min(32, p.V - v0), resid, p.c12, p.sc.hi, p.crest, st.ip, st.iq,
+                    facc);
       }
       tc_fence_before();
       __syncwarp();
