@@ -19,40 +19,13 @@
 // double tanh implementations landing on a rounding boundary, about 2^-45 a
 // value).
 #include "common.cuh"
+#include "rnn.cuh"
 
 namespace dspark {
 
 namespace {
 
 constexpr int kRnnMaxR = 1024;  // largest rank
-
-// One rounding from double to bf16 (8 significant bits, ties to even).
-__device__ __forceinline__ __nv_bfloat16 bf16_from_double(double x) {
-  if (x == 0.0 || isnan(x)) return __float2bfloat16_rn((float)x);
-  double y;
-  if (fabs(x) < 0x1p-126) {
-    y = ldexp(rint(ldexp(x, 133)), -133);  // bf16 subnormals: multiples of 2^-133
-  } else {
-    int e;
-    const double m = frexp(x, &e);  // 0.5 <= |m| < 1
-    y = ldexp(rint(ldexp(m, 8)), e - 8);
-  }
-  return __float2bfloat16_rn((float)y);  // y is a bf16 value: exact
-}
-
-// round_bf16(tanh(x)).  The fp32 tanhf (a few ulp of fp32 from the exact
-// value) already decides the bf16 rounding unless its result lies within 8
-// fp32 ulps of a bf16 rounding midpoint (low 16 bits near 0x8000, about one
-// value in 4000); only then is tanh taken in double (GB300's double rate is
-// a small fraction of its fp32 rate).
-__device__ __forceinline__ void store_state(__nv_bfloat16* p, float x) {
-  const float t = tanhf(x);
-  const int low = (int)(__float_as_uint(t) & 0xffffu);
-  *p = abs(low - 0x8000) > 8 ? __float2bfloat16_rn(t) : bf16_from_double(tanh((double)x));
-}
-__device__ __forceinline__ void store_state(float* p, float x) {
-  *p = __double2float_rn(tanh((double)x));
-}
 
 constexpr int kRnnCols = 32;  // columns of S a block computes (one per lane)
 constexpr int kRnnReqs = 8;   // requests a block computes (one per warp)
@@ -150,7 +123,7 @@ __global__ void __launch_bounds__(256) rnn_state_kernel(int R, int gamma, int r,
   // multiply-add each
 #pragma unroll 8
   for (int i = 0; i < r; ++i) acc = fmaf(s[i], to_f32<T>(Us[i * kRnnCols + lane]), acc);
-  store_state(S + ((size_t)n * gamma + k) * r + j, acc);
+  rnn::store_state(S + ((size_t)n * gamma + k) * r + j, acc);
 }
 
 }  // namespace
