@@ -84,7 +84,7 @@ __global__ void confidence_kernel(int gamma, int d, int r, int V, int vec,
   const int n = blockIdx.x;
   const int k = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t idx = (size_t)n * gamma + k;
-  const bool one_pass = sizeof(T) == 2 && vec && d <= 32 * 8 * kHLoads && r <= 256;
+  const bool one_pass = sizeof(T) == 2 && vec && d <= kHMaxD && r <= 256;
   uint4 hq[kHLoads];
   if (one_pass && k < gamma && c_in == nullptr) {
     // h does not depend on the draft: request it before waiting for the tokens
@@ -103,7 +103,9 @@ __global__ void confidence_kernel(int gamma, int d, int r, int V, int vec,
       }
       if (one_pass) {
         const uint4 eq = conf_load_e1(reinterpret_cast<const __nv_bfloat16*>(E1), prev, r);
-        c = conf_sigma(conf_h_lane(hq, w, d), eq, prev, r, w + d, sts[k]);
+        c = conf_sigma(
+            conf_h_lane_all(hq, reinterpret_cast<const __nv_bfloat16*>(h) + idx * d, w, d), eq,
+            prev, r, w + d, sts[k]);
       } else {
         float s = warp_dot<T>(w, h + idx * d, d, vec);
         if (prev >= 0) s += warp_dot<T>(w + d, E1 + (size_t)prev * r, r, vec);

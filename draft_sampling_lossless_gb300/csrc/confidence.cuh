@@ -13,11 +13,14 @@ namespace dspark {
 namespace conf {
 
 // One warp per (request, position): c = sigmoid((w_h . h + w_e . E1[prev]) / sts).
-// bf16 with vector loads (the common case): the lane's whole share of h
-// (up to kHLoads 16-byte loads) and the previous token are requested
-// together, then the E1 row once the token is known, so a dot product costs
-// about two memory round trips; w (shared by every warp) is read through L1.
-constexpr int kHLoads = 16;  // d <= 32 * 8 * kHLoads = 4096 on the one-pass path
+// bf16 with vector loads (the common case): the lane's share of h (up to
+// kHLoads 16-byte loads at once, a second batch for d above 4096) and the
+// previous token are requested together, then the E1 row once the token is
+// known, so a dot product costs about two memory round trips (three with a
+// second batch); w (shared by every warp) is read through L1.
+constexpr int kHLoads = 16;   // 16-byte loads a lane holds at once
+constexpr int kHBatches = 2;  // d <= 32 * 8 * kHLoads * kHBatches = 8192 on the one-pass path
+constexpr int kHMaxD = 32 * 8 * kHLoads * kHBatches;
 
 __device__ __forceinline__ float dot8_bf16(const uint4 q, const float* __restrict__ w) {
   const float4 w0 = __ldg(reinterpret_cast<const float4*>(w));
@@ -37,24 +40,40 @@ __device__ __forceinline__ float dot8_bf16(const uint4 q, const float* __restric
 // The lane's partial of w_h . h for one (request, position) on the one-pass
 // bf16 path: the lane's 16-byte loads of h (issued by conf_load_h) times w,
 // accumulated in load order.
+// Batch b of a lane's loads: steps i = 16 b .. 16 b + 15 (elements
+// (i * 32 + lane) * 8 .. + 7); a lane's partial adds the steps in order,
+// batch after batch, so the sum does not depend on how the loads are grouped.
 __device__ __forceinline__ void conf_load_h(const __nv_bfloat16* __restrict__ hp, int d,
-                                            uint4 (&hq)[kHLoads]) {
+                                            uint4 (&hq)[kHLoads], int batch = 0) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int i = 0; i < kHLoads; ++i) {
-    const int j = (i * 32 + lane) * 8;
+    const int j = ((batch * kHLoads + i) * 32 + lane) * 8;
     hq[i] = j < d ? __ldcs(reinterpret_cast<const uint4*>(hp + j)) : make_uint4(0, 0, 0, 0);
   }
 }
 
 __device__ __forceinline__ float conf_h_lane(const uint4 (&hq)[kHLoads],
-                                             const float* __restrict__ w, int d) {
+                                             const float* __restrict__ w, int d, int batch = 0,
+                                             float s = 0.f) {
   const int lane = threadIdx.x & 31;
-  float s = 0.f;
 #pragma unroll
   for (int i = 0; i < kHLoads; ++i) {
-    const int j = (i * 32 + lane) * 8;
+    const int j = ((batch * kHLoads + i) * 32 + lane) * 8;
     if (j < d) s += dot8_bf16(hq[i], w + j);
+  }
+  return s;
+}
+
+// The lane's whole partial of w . h: the first batch from hq (already
+// loaded), the second (d > 4096) loaded and added here.
+__device__ __forceinline__ float conf_h_lane_all(uint4 (&hq)[kHLoads],
+                                                 const __nv_bfloat16* __restrict__ hp,
+                                                 const float* __restrict__ w, int d) {
+  float s = conf_h_lane(hq, w, d, 0);
+  if (d > 32 * 8 * kHLoads) {
+    conf_load_h(hp, d, hq, 1);
+    s = conf_h_lane(hq, w, d, 1, s);
   }
   return s;
 }

@@ -29,9 +29,13 @@ CASES = {
     # more candidates than the fused launch takes (R * gamma > 8192): three launches
     "many_candidates": W["stress"].scaled(name="many_candidates", R=520, gamma=16, V=512, r=16,
                                           n_sps=0),
-    # a hidden size past the head's one-pass form (d > 4096): three launches
+    # a hidden size past the fused head (d > 4096): three launches, the
+    # confidence kernel's one-pass form with a second batch of h loads
     "wide_hidden": W["qwen3_4b"].scaled(name="wide_hidden", R=4, gamma=3, V=1024, r=64, d=4104,
                                         n_sps=0),
+    # past the one-pass form (d > 8192): three launches, the general dot products
+    "wider_hidden": W["qwen3_4b"].scaled(name="wider_hidden", R=4, gamma=3, V=1024, r=64,
+                                         d=8200, n_sps=0),
 }
 
 OUTPUTS = ("tokens", "q_lse", "q_tok", "c", "a", "ell", "row_off", "B", "E")
