@@ -359,11 +359,15 @@ __device__ __forceinline__ void sum16(unsigned long long (&v)[8], float& hi, flo
 // The sums are compensated: plain packed adds form four-token partials,
 // TwoSum the levels above; a group's high part is converted to 2^-40 units
 // exactly with integer operations.
+// kRagged: the block holds the vocabulary's end (its last block only), so
+// tokens at or past lim are masked; a template parameter, so that the
+// unrolled pairs of the common case carry no branch.
+template <bool kRagged>
 __device__ __forceinline__ void epi_half(const uint32_t (&b)[32], const uint4 (&zq)[4], int h,
                                          int lim, const TcParams& p, Part& s, float (&gs)[4],
                                          float& lo) {
   const int t0 = h * 32;
-  const bool ragged = lim < t0 + 32;  // warp-uniform: only the vocabulary's last block
+  constexpr bool ragged = kRagged;
   float mx[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
@@ -435,6 +439,7 @@ __device__ __forceinline__ void epi_half(const uint32_t (&b)[32], const uint4 (&
 // b0 must hold the first half's load, already issued at column tcol.  Every
 // lane of the warp calls this (the loads are warp-collective); `valid`
 // lanes compute.
+template <bool kGreedy>
 __device__ __forceinline__ void epi_block(uint32_t (&b0)[32], uint32_t (&b1)[32], uint32_t tcol,
                                           const uint4 (&z0)[4], const uint4 (&z1)[4], int v0,
                                           int lim, bool valid, const TcParams& p, Part& s,
@@ -442,19 +447,24 @@ __device__ __forceinline__ void epi_block(uint32_t (&b0)[32], uint32_t (&b1)[32]
   float lo = 0.f;
   tmem_wait_ld_regs(b0);
   if (valid) {
-    if (p.greedy)
+    if (kGreedy)
       epi_half_greedy(b0, z0, 0, v0, lim, s);
+    else if (lim < 64)
+      epi_half<true>(b0, z0, 0, lim, p, s, gs, lo);
     else
-      epi_half(b0, z0, 0, lim, p, s, gs, lo);
+      epi_half<false>(b0, z0, 0, lim, p, s, gs, lo);
   }
   __syncwarp();
   tmem_ld_32x32b_x32(tcol + 32, b1);
   tmem_wait_ld_regs(b1);
   if (valid) {
-    if (p.greedy) {
+    if (kGreedy) {
       epi_half_greedy(b1, z1, 1, v0, lim, s);
     } else {
-      epi_half(b1, z1, 1, lim, p, s, gs, lo);
+      if (lim < 64)
+        epi_half<true>(b1, z1, 1, lim, p, s, gs, lo);
+      else
+        epi_half<false>(b1, z1, 1, lim, p, s, gs, lo);
       s.acc += __float2ll_rn(lo * 1099511627776.0f);  // one 64-bit conversion a block
     }
   }
@@ -695,7 +705,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(b_emptyZ + 8 * (half * 4 + zs));
         float gs[4] = {0.f, 0.f, 0.f, 0.f};
-        epi_block(b0, b1, tcol, z0, z1, v0, min(64, p.V - v0), valid, p, s, gs);
+        if (p.greedy)
+          epi_block<true>(b0, b1, tcol, z0, z1, v0, min(64, p.V - v0), valid, p, s, gs);
+        else
+          epi_block<false>(b0, b1, tcol, z0, z1, v0, min(64, p.V - v0), valid, p, s, gs);
         if (own && !p.greedy) store_groups(p.sub + o * 8, jj, gs, s.ref, ref0);
       }
       tc_fence_before();
@@ -958,12 +971,14 @@ __device__ __noinline__ void fused_cut(const PersistParams& pp, uint8_t* buf, in
 // kGroups: finishes a CTA runs at once (8 / kGroups warps each) when it has
 // many requests to finish; separate instantiations, so that the grouped
 // finishes' registers do not weigh on the epilogue of every launch.
-template <int kGroups>
+// kGreedy: T = 0 (argmax draws), its own instantiation for the same reason.
+template <int kGroups, bool kGreedy>
 __global__ void __launch_bounds__(kThreads, 1)
     draft_persistent_kernel(const __grid_constant__ CUtensorMap tm_w,
                             const __grid_constant__ CUtensorMap tm_z,
                             const __grid_constant__ CUtensorMap tm_a, const PersistParams pp) {
   const TcParams& p = pp.p;
+  constexpr int greedy = kGreedy ? 1 : 0;  // p.greedy
   const bool pair = pp.pair != 0;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_abort;
@@ -1250,15 +1265,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(b_emptyZ + 8 * (half * 4 + zs));
           float gs[4] = {0.f, 0.f, 0.f, 0.f};
-          epi_block(b0, b1, tcol, z0, z1, v0, min(64, p.V - v0), valid, p, s, gs);
-          if (own && !p.greedy) store_groups(p.sub + o * 8, jj, gs, s.ref, ref0);
+          epi_block<kGreedy>(b0, b1, tcol, z0, z1, v0, min(64, p.V - v0), valid, p, s, gs);
+          if (own && !greedy) store_groups(p.sub + o * 8, jj, gs, s.ref, ref0);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(b_accEmpty + 8 * a);
         if (own) {
           if (s.bad) set_flag(p.status, kFlagNonFinite);
-          if (p.greedy)
+          if (greedy)
             reinterpret_cast<ArgMax*>(p.part)[o] = s.best;
           else
             p.part[o] = (s.ref == INT_MIN) ? 0.0 : fix_to_double(s.acc, s.ref - kFixRel);
@@ -1278,14 +1293,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         FinishScratch& fg = (&fs)[grp];
         for (int nn = cta + grp * (int)n_ctas; nn < p.R; nn += kGroups * (int)n_ctas)
           finish_request<__nv_bfloat16, kHalf, GroupSync<4, kNW>, true>(
-              fg, nn, p.V, p.gamma, k, p.n_parts, pp.z, b, p.sc, p.greedy, p.part, pp.u,
+              fg, nn, p.V, p.gamma, k, p.n_parts, pp.z, b, p.sc, greedy, p.part, pp.u,
               pp.tokens, pp.q_lse, pp.q_tok, p.status, k + 1 < p.gamma ? pp.stage : nullptr,
               p.sub);
         NamedSync<3, 256>::sync();  // both groups done (the log pass reads their q_lse)
       } else {
         for (int nn = cta; nn < p.R; nn += n_ctas)
           finish_request<__nv_bfloat16, kHalf, NamedSync<3, 256>, true>(
-              fs, nn, p.V, p.gamma, k, p.n_parts, pp.z, b, p.sc, p.greedy, p.part, pp.u,
+              fs, nn, p.V, p.gamma, k, p.n_parts, pp.z, b, p.sc, greedy, p.part, pp.u,
               pp.tokens, pp.q_lse, pp.q_tok, p.status, k + 1 < p.gamma ? pp.stage : nullptr,
               p.sub);
       }
@@ -1306,7 +1321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // The finishes left each q_lse entry holding its normaliser; take the
     // logarithms here, off the per-position path (same CTA, same requests).
-    if (!p.greedy) {
+    if (!greedy) {
       const int mine = p.R > cta ? (p.R - cta + (int)n_ctas - 1) / (int)n_ctas : 0;
       for (int i = threadIdx.x; i < mine * p.gamma; i += 256) {
         const size_t o = (size_t)(cta + (i / p.gamma) * (int)n_ctas) * p.gamma + i % p.gamma;
@@ -1387,6 +1402,7 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
 // fp32 rounding of t c or of z + b at the magnitude of the logits) and the
 // 16-token sums are TwoSum trees; acc holds (residual hi, lo, p hi, lo).
 // A NaN group is left out (the pick's recompute flags it).
+template <bool kRagged, bool kQ>
 __device__ __forceinline__ void fin_block(const uint32_t (&b)[32], const uint4 (&zq)[4],
                                           const uint4 (&tq)[4], int lim, bool resid, float c12,
                                           float cf, float crest, InvPair ip, InvPair iq,
@@ -1409,21 +1425,26 @@ __device__ __forceinline__ void fin_block(const uint32_t (&b)[32], const uint4 (
       const uint32_t tw = (&tq[0].x)[k];
       const unsigned long long wp =
           pow2_split2_nb(pack2(bf_lo(tw), bf_hi(tw)), c2, cr2, kp2, klo);
-      unsigned long long pp = fma2(wp, iph, mul2(wp, ipl));
+      p2[e] = fma2(wp, iph, mul2(wp, ipl));
       float pa, pb;
-      unpack2(pp, pa, pb);
-      if (2 * k >= lim) pa = 0.f;
-      if (2 * k + 1 >= lim) pb = 0.f;
-      p2[e] = pack2(pa, pb);
-      if (qlive) {
+      unpack2(p2[e], pa, pb);
+      if (kRagged) {
+        pa = 2 * k < lim ? pa : 0.f;
+        pb = 2 * k + 1 < lim ? pb : 0.f;
+        p2[e] = pack2(pa, pb);
+      }
+      if (kQ) {
+        // q for every lane of a warp with a residual (finite: a bonus lane's
+        // z and bias are zero), the residual taken by select, so the
+        // unrolled pairs have no branch
         const uint32_t zw = (&zq[0].x)[k];
         const unsigned long long wq =
             pow2_split2_cf(pack2(bf_lo(zw), bf_hi(zw)),
                            pack2(__uint_as_float(b[2 * k]), __uint_as_float(b[2 * k + 1])), c2,
                            cf2, cr2, kq2, klo);
-        float qa, qb;
-        unpack2(fma2(wq, iqh, mul2(wq, iql)), qa, qb);
-        r2[e] = pack2(fmaxf(0.0f, pa - qa), fmaxf(0.0f, pb - qb));
+        float da, db;  // p - q
+        unpack2(sub2(p2[e], fma2(wq, iqh, mul2(wq, iql))), da, db);
+        r2[e] = pack2(qlive ? fmaxf(0.0f, da) : pa, qlive ? fmaxf(0.0f, db) : pb);
       } else {
         r2[e] = p2[e];
       }
@@ -1648,6 +1669,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (n < p.R) st = p.vstate[n];
     const bool live = n < p.R && st.mode >= 0;
     const bool resid = st.mode == 1;
+    // a warp whose requests all draw a bonus token computes no q
+    const bool warp_q = __any_sync(0xffffffffu, live && resid && st.iq.hi != 0.f);
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     uint32_t acc_it = 0, zit = 0, cpar = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++acc_it, zit += kFinSteps) {
@@ -1683,9 +1706,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(b_emptyZ + 8 * (half * 4 + zs));
         tmem_wait_ld_regs(b);
-        if (valid)
-          fin_block(b, zq, tq, min(32, p.V - v0), resid, p.c12, p.sc.hi, p.crest, st.ip, st.iq,
-                    facc);
+        const int lim = min(32, p.V - v0);
+        if (valid && lim < 32)  // only the vocabulary's last block
+          fin_block<true, true>(b, zq, tq, lim, resid, p.c12, p.sc.hi, p.crest, st.ip, st.iq,
+                                facc);
+        else if (valid && warp_q)
+          fin_block<false, true>(b, zq, tq, lim, resid, p.c12, p.sc.hi, p.crest, st.ip, st.iq,
+                                 facc);
+        else if (valid)
+          fin_block<false, false>(b, zq, tq, lim, resid, p.c12, p.sc.hi, p.crest, st.ip, st.iq,
+                                  facc);
       }
       tc_fence_before();
       __syncwarp();
@@ -1890,9 +1920,11 @@ cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st) {
   // two concurrent finishes a CTA once a CTA has eight or more requests (at
   // four, the greedy workload, they measured slower)
   const int per_cta = (a.R + gx * n_rt - 1) / (gx * n_rt);
-  const int groups = per_cta >= 8 ? 2 : 1;
-  const void* kern = groups == 2 ? (const void*)draft_persistent_kernel<2>
-                                 : (const void*)draft_persistent_kernel<1>;
+  // (greedy draws always finish one request at a time: the argmax finish is short)
+  const int groups = per_cta >= 8 && !p.greedy ? 2 : 1;
+  const void* kern = p.greedy      ? (const void*)draft_persistent_kernel<1, true>
+                     : groups == 2 ? (const void*)draft_persistent_kernel<2, false>
+                                   : (const void*)draft_persistent_kernel<1, false>;
   e = ensure_smem_attr(kern, (int)tc_smem_bytes(4));
   if (e != cudaSuccess) return e;
   const size_t smem = persist_smem_bytes(p.nK, pair);
@@ -1909,12 +1941,18 @@ cudaError_t launch_draft_persistent_tc(const DraftArgs& a, cudaStream_t st) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (groups == 2)
+  if (p.greedy)
     DSPARK_LAUNCH(kKindDraftPersistent, st,
-                  e = cudaLaunchKernelEx(&cfg, draft_persistent_kernel<2>, tm_w, tm_z, tm_a, pp));
+                  e = cudaLaunchKernelEx(&cfg, draft_persistent_kernel<1, true>, tm_w, tm_z, tm_a,
+                                         pp));
+  else if (groups == 2)
+    DSPARK_LAUNCH(kKindDraftPersistent, st,
+                  e = cudaLaunchKernelEx(&cfg, draft_persistent_kernel<2, false>, tm_w, tm_z,
+                                         tm_a, pp));
   else
     DSPARK_LAUNCH(kKindDraftPersistent, st,
-                  e = cudaLaunchKernelEx(&cfg, draft_persistent_kernel<1>, tm_w, tm_z, tm_a, pp));
+                  e = cudaLaunchKernelEx(&cfg, draft_persistent_kernel<1, false>, tm_w, tm_z,
+                                         tm_a, pp));
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e == cudaSuccess && a.fused != nullptr) *a.fused = pp.fuse;
