@@ -1452,8 +1452,10 @@ __device__ __forceinline__ void fin_block(const uint32_t (&b)[32], const uint4 (
     float ph, pl, rh, rl;
     sum16(p2, ph, pl);
     sum16(r2, rh, rl);
-    if (ph == ph) add_pair(acc[2], acc[3], ph, pl);
-    if (rh == rh) add_pair(acc[0], acc[1], rh, rl);
+    // a NaN group is left out, by select (no branch between the groups)
+    const bool okp = ph == ph, okr = rh == rh;
+    add_pair(acc[2], acc[3], okp ? ph : 0.f, okp ? pl : 0.f);
+    add_pair(acc[0], acc[1], okr ? rh : 0.f, okr ? rl : 0.f);
   }
 }
 

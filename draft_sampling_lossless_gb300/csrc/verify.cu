@@ -320,11 +320,16 @@ __host__ __device__ constexpr size_t rows_tma_smem(int R) {
   return kRowsTmaSmem + (size_t)(4 * R + 1) * sizeof(int);  // rings; r0, pre, items, winners
 }
 
+//
+// kGreedy (T = 0: arg-max items) is a template parameter, so that each
+// instantiation's sub-chunk loop holds one kind of reduction.
+template <bool kGreedy>
 __global__ void __launch_bounds__(256, 4) verify_rows_tma_kernel(
     int R, int gamma, int V, int n_chunks, long long n_rows,
     const __nv_bfloat16* __restrict__ target, const int32_t* __restrict__ ell,
-    const int32_t* __restrict__ row_off, ScalePair sc, int greedy, double* __restrict__ row_part,
+    const int32_t* __restrict__ row_off, ScalePair sc, double* __restrict__ row_part,
     uint32_t* status, const DecideOut dec) {
+  constexpr int greedy = kGreedy ? 1 : 0;
   extern __shared__ __align__(16) uint8_t rows_ring[];
   int* s_r0 = reinterpret_cast<int*>(rows_ring + kRowsTmaSmem);  // [R]
   int* s_pre = s_r0 + R;                                          // [R + 1]
@@ -426,6 +431,11 @@ __global__ void __launch_bounds__(256, 4) verify_rows_tma_kernel(
         const int v0 = c * kRowChunk + sb * kRowSub, lim = V - v0;
         RowRaw<__nv_bfloat16> x;
         const uint8_t* sl = ring + slot * kRowSlot;
+        if (lim >= kRowSub) {  // every sub-chunk but the vocabulary's last
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            x.q[i] = *reinterpret_cast<const uint4*>(sl + (i * 256 + lane * 8) * 2);
+        } else {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int e0 = i * 256 + lane * 8;
@@ -442,6 +452,7 @@ __global__ void __launch_bounds__(256, 4) verify_rows_tma_kernel(
             }
             x.q[i] = make_uint4(w[0], w[1], w[2], w[3]);
           }
+        }
         }
         st.add(x, v0, V, sc, greedy);
       }
@@ -1070,16 +1081,15 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t st) {
     // the opt-in for the largest list, once per device; the resident grid
     // for this list size (cached per device and size)
     const size_t dyn = rows_tma_smem(a.R);
-    cudaError_t ea = ensure_smem_attr((const void*)verify_rows_tma_kernel,
-                                      (int)rows_tma_smem(kRowsSmem));
+    auto kern = greedy ? verify_rows_tma_kernel<true> : verify_rows_tma_kernel<false>;
+    cudaError_t ea = ensure_smem_attr((const void*)kern, (int)rows_tma_smem(kRowsSmem));
     if (ea != cudaSuccess) return ea;
-    const int grid = row_grid(verify_rows_tma_kernel, 1ll << 40, dyn);
+    const int grid = row_grid(kern, 1ll << 40, dyn);
     const int g = (int)(grid < (items + 7) / 8 ? grid : (items + 7) / 8);
     DSPARK_LAUNCH(kKindVerifyRows, st,
-                  launch_pdl(verify_rows_tma_kernel, dim3(g), dim3(256), dyn, st, a.R,
-                             a.gamma, a.V, n_chunks, a.n_rows,
-                             reinterpret_cast<const __nv_bfloat16*>(tg), a.ell, a.row_off, sc,
-                             (int)greedy, a.row_part, a.status, dec));
+                  launch_pdl(kern, dim3(g), dim3(256), dyn, st, a.R, a.gamma, a.V, n_chunks,
+                             a.n_rows, reinterpret_cast<const __nv_bfloat16*>(tg), a.ell,
+                             a.row_off, sc, a.row_part, a.status, dec));
   } else {
     DSPARK_LAUNCH(kKindVerifyRows, st,
                   launch_pdl(verify_rows_wide_kernel<T>,
