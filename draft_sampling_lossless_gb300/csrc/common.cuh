@@ -87,6 +87,13 @@ struct ArgMax {
   int i;
 };
 
+// max(a, b) that returns NaN when either operand is NaN.
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
 __device__ __forceinline__ ArgMax better(ArgMax a, ArgMax b) {
   if (b.v > a.v || (b.v == a.v && b.i < a.i)) return b;
   return a;

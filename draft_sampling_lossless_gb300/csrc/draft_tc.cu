@@ -175,12 +175,6 @@ struct Part {
   ArgMax best;    // greedy
 };
 
-// max(a, b) that returns NaN when either operand is NaN.
-__device__ __forceinline__ float fmax_nan(float a, float b) {
-  float r;
-  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-  return r;
-}
 
 // TwoSum (Knuth): s = RN(a + b) and the exact error a + b - s, for any
 // order of magnitudes; the packed form does two pairs at once.
@@ -211,30 +205,46 @@ __device__ __forceinline__ long long fix40(float x) {
 // Greedy: the arg-max of y = z + b over 32 consecutive tokens of one
 // request row (one 32-column accumulator load b and the z words zq), half h
 // (tokens v0 + 32h ..) of a 64-token block; `lim` = number of the block's
-// tokens below V.  NaN and +inf set s.bad.
+// tokens below V.  The half's maximum first (NaN-propagating, so a NaN shows
+// in it; then the maximum of the other values is taken again), then its
+// first index, then one comparison with the running best (lowest index on
+// ties: the halves come in token order).  NaN and +inf set s.bad.
+template <bool kRagged>
 __device__ __forceinline__ void epi_half_greedy(const uint32_t (&b)[32], const uint4 (&zq)[4],
                                                 int h, int v0, int lim, Part& s) {
   const int t0 = h * 32;
-  ArgMax t[16];
-  float chk = -INFINITY;
+  float y[32];
 #pragma unroll
   for (int k = 0; k < 16; ++k) {
     const uint32_t zw = (&zq[0].x)[k];
-    float ya, yb;
     unpack2(add2(pack2(bf_lo(zw), bf_hi(zw)),
                  pack2(__uint_as_float(b[2 * k]), __uint_as_float(b[2 * k + 1]))),
-            ya, yb);
-    if (t0 + 2 * k >= lim) ya = -INFINITY;
-    if (t0 + 2 * k + 1 >= lim) yb = -INFINITY;
-    t[k] = better(ArgMax{ya, v0 + t0 + 2 * k}, ArgMax{yb, v0 + t0 + 2 * k + 1});
-    chk = fmax_nan(chk, fmax_nan(ya, yb));
+            y[2 * k], y[2 * k + 1]);
+    if (kRagged) {
+      if (t0 + 2 * k >= lim) y[2 * k] = -INFINITY;
+      if (t0 + 2 * k + 1 >= lim) y[2 * k + 1] = -INFINITY;
+    }
   }
+  float mx[8];
 #pragma unroll
-  for (int w = 8; w > 0; w >>= 1)
+  for (int e = 0; e < 8; ++e) mx[e] = fmax_nan(fmax_nan(y[e], y[e + 8]), fmax_nan(y[e + 16], y[e + 24]));
 #pragma unroll
-    for (int e = 0; e < w; ++e) t[e] = better(t[e], t[e + w]);
-  s.best = better(s.best, t[0]);
-  if (!(chk < INFINITY)) s.bad = 1;
+  for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+    for (int e = 0; e < w; ++e) mx[e] = fmax_nan(mx[e], mx[e + w]);
+  float m = mx[0];
+  if (!(m < INFINITY)) {  // NaN or +inf: flagged; the maximum of the non-NaN values
+    s.bad = 1;
+    if (m != m) {
+      m = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) m = fmaxf(m, y[k]);
+    }
+  }
+  int idx = 31;  // the first token holding the maximum (all NaN: the last, -inf weight)
+#pragma unroll
+  for (int k = 30; k >= 0; --k) idx = y[k] == m ? k : idx;
+  s.best = better(s.best, ArgMax{m, v0 + t0 + idx});
 }
 
 // One weight 2^(x c + e) for two tokens at once, with the exponent split as
@@ -447,8 +457,10 @@ __device__ __forceinline__ void epi_block(uint32_t (&b0)[32], uint32_t (&b1)[32]
   float lo = 0.f;
   tmem_wait_ld_regs(b0);
   if (valid) {
-    if (kGreedy)
-      epi_half_greedy(b0, z0, 0, v0, lim, s);
+    if (kGreedy && lim < 64)
+      epi_half_greedy<true>(b0, z0, 0, v0, lim, s);
+    else if (kGreedy)
+      epi_half_greedy<false>(b0, z0, 0, v0, lim, s);
     else if (lim < 64)
       epi_half<true>(b0, z0, 0, lim, p, s, gs, lo);
     else
@@ -459,7 +471,10 @@ __device__ __forceinline__ void epi_block(uint32_t (&b0)[32], uint32_t (&b1)[32]
   tmem_wait_ld_regs(b1);
   if (valid) {
     if (kGreedy) {
-      epi_half_greedy(b1, z1, 1, v0, lim, s);
+      if (lim < 64)
+        epi_half_greedy<true>(b1, z1, 1, v0, lim, s);
+      else
+        epi_half_greedy<false>(b1, z1, 1, v0, lim, s);
     } else {
       if (lim < 64)
         epi_half<true>(b1, z1, 1, lim, p, s, gs, lo);

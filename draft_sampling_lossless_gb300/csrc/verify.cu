@@ -170,16 +170,19 @@ struct RowState {
                                       int greedy) {
     const int lane = threadIdx.x & 31;
     if (greedy) {
+      // the 32 values' maximum (NaN ignored), its first index in token order,
+      // then one comparison with the item's best.  Values past V were loaded
+      // as -inf, so they never come before a token of the row.
+      const float m = raw.max();
+      int idx = 31;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 3; i >= 0; --i) {
         float x[8];
         raw.get(i, x);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int v = v0 + i * 256 + lane * 8 + e;
-          if (v < V) am = better(am, ArgMax{x[e], v});
-        }
+        for (int e = 7; e >= 0; --e) idx = x[e] == m ? i * 8 + e : idx;
       }
+      am = better(am, ArgMax{m, v0 + (idx >> 3) * 256 + lane * 8 + (idx & 7)});
       return;
     }
     const float m = raw.max() * sc.hi;
