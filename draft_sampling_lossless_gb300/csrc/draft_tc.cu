@@ -1403,6 +1403,15 @@ __device__ __forceinline__ uint32_t row_granule(int m, int g) {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+// The same, issued only when `on` is nonzero (a predicate inside the
+// instruction, so that a run of them carries no branch).
+__device__ __forceinline__ void cp_async16_if(uint32_t dst, const void* src, uint32_t on) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t"
+      "@q cp.async.cg.shared.global [%0], [%1], 16;\n\t}" ::"r"(dst),
+      "l"(src), "r"(on)
+      : "memory");
+}
 // Arrive on `bar` once this thread's earlier cp.async copies have landed
 // (counts as one of the barrier's expected arrivals).
 __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
@@ -1627,27 +1636,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           zr[c] = p.z + ((size_t)n * p.gamma + st.n_acc) * p.V;
       }
     }
-    uint32_t it = 0;
+    // per lane, once: the slot offsets of its granules and which rows it
+    // copies (a missing row: a valid dummy address, its copies not issued)
+    uint32_t off[16], ton = 0, zon = 0;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      off[c] = row_granule(8 * c + sub, g);
+      ton |= (tr[c] != nullptr ? 1u : 0u) << c;
+      zon |= (zr[c] != nullptr ? 1u : 0u) << c;
+      if (tr[c] == nullptr) tr[c] = p.target;
+      if (zr[c] == nullptr) zr[c] = p.z;
+    }
+    uint32_t it = 0, s = 0;
     ZRing zring;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x)
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      // slot rows 0-63 read tile t0, rows 64-127 tile t1 (paired; else both t0)
+      const int t0 = pair ? 2 * u : u, t1 = pair ? 2 * u + 1 : u;
       for (int j = 0; j < kFinSteps; ++j, ++it) {
-        const int s = it % kFinSlots, h = j / (kFinSteps / 2);
-        zring.acquire(b_emptyZ, s, h, &s_abort, p.status);
+        const int h = j / (kFinSteps / 2);
+        zring.acquire(b_emptyZ, (int)s, h, &s_abort, p.status);
         fence_proxy_async_smem();
         const uint32_t zdst = smem_u32(sZ + s * kRowSlot), tdst = zdst + kRowPart;
+        // V is a multiple of 8: a granule is all in or out
+        const int v0 = t0 * BN + j * 32 + g * 8, v1 = t1 * BN + j * 32 + g * 8;
+        const uint32_t in0 = v0 < p.V ? 0xffffu : 0u, in1 = v1 < p.V ? 0xffffu : 0u;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const int m = 8 * c + sub;
-          const int t = pair ? 2 * u + (m >> 6) : u;
-          const int v = t * BN + j * 32 + g * 8;  // V is a multiple of 8: a granule is all in or out
-          if (v < p.V) {
-            const uint32_t off = row_granule(m, g);
-            if (tr[c] != nullptr) cp_async16(tdst + off, tr[c] + v);
-            if (zr[c] != nullptr) cp_async16(zdst + off, zr[c] + v);
-          }
+          const int v = c < 8 ? v0 : v1;
+          const uint32_t in = c < 8 ? in0 : in1;
+          cp_async16_if(tdst + off[c], tr[c] + v, (ton & in) & (1u << c));
+          cp_async16_if(zdst + off[c], zr[c] + v, (zon & in) & (1u << c));
         }
         cp_async_arrive(b_fullZ + 8 * (h * 4 + s));
+        if (++s == kFinSlots) s = 0;
       }
+    }
   } else if (warp == kWarpMma) {
     if (lane == 0) {
       const uint64_t da0 = desc_kmajor_sw128(smem_u32(sA));
