@@ -500,7 +500,8 @@ __device__ __forceinline__ void store_groups(float* dst, int jj, const float (&g
   *reinterpret_cast<float4*>(dst + jj * 4) = make_float4(gs[0] * sc, gs[1] * sc, gs[2] * sc, gs[3] * sc);
 }
 
-template <bool kBiasOut>
+// kGreedy: T = 0, its own instantiation (one kind of epilogue a kernel).
+template <bool kBiasOut, bool kGreedy>
 __global__ void __launch_bounds__(kThreads, 1)
     draft_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_w,
                           const __grid_constant__ CUtensorMap tm_z, const TcParams p) {
@@ -720,18 +721,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(b_emptyZ + 8 * (half * 4 + zs));
         float gs[4] = {0.f, 0.f, 0.f, 0.f};
-        if (p.greedy)
-          epi_block<true>(b0, b1, tcol, z0, z1, v0, min(64, p.V - v0), valid, p, s, gs);
-        else
-          epi_block<false>(b0, b1, tcol, z0, z1, v0, min(64, p.V - v0), valid, p, s, gs);
-        if (own && !p.greedy) store_groups(p.sub + o * 8, jj, gs, s.ref, ref0);
+        epi_block<kGreedy>(b0, b1, tcol, z0, z1, v0, min(64, p.V - v0), valid, p, s, gs);
+        if (own && !kGreedy) store_groups(p.sub + o * 8, jj, gs, s.ref, ref0);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_accEmpty + 8 * a);
       if (own) {
         if (s.bad) set_flag(p.status, kFlagNonFinite);
-        if (p.greedy)
+        if (kGreedy)
           reinterpret_cast<ArgMax*>(p.part)[o] = s.best;
         else
           p.part[o] = (s.ref == INT_MIN) ? 0.0 : fix_to_double(s.acc, s.ref - kFixRel);
@@ -1844,16 +1842,19 @@ cudaError_t encode_stage(CUtensorMap* m, const void* stage, int R, int r, int bo
 template <bool kBiasOut>
 cudaError_t launch_tc(const CUtensorMap& tm_w, const CUtensorMap& tm_z, const TcParams& p,
                       cudaStream_t st) {
-  cudaError_t e = ensure_smem_attr((const void*)draft_fused_tc_kernel<kBiasOut>,
-                                   (int)tc_smem_bytes(4));
+  // the bias-only pass has no epilogue draws: one instantiation
+  auto kern = draft_fused_tc_kernel<kBiasOut, false>;
+  if constexpr (!kBiasOut) {
+    if (p.greedy) kern = draft_fused_tc_kernel<false, true>;
+  }
+  cudaError_t e = ensure_smem_attr((const void*)kern, (int)tc_smem_bytes(4));
   if (e != cudaSuccess) return e;
   const int n_rt = (p.R + BM - 1) / BM;
   int gx = sm_count() / n_rt;
   if (gx < 1) gx = 1;
   if (gx > p.n_vt) gx = p.n_vt;
   DSPARK_LAUNCH(kKindDraftFusedTc, st,
-                draft_fused_tc_kernel<kBiasOut>
-                <<<dim3(gx, n_rt), kThreads, tc_smem_bytes(p.nK), st>>>(tm_w, tm_z, p));
+                kern<<<dim3(gx, n_rt), kThreads, tc_smem_bytes(p.nK), st>>>(tm_w, tm_z, p));
   return cudaGetLastError();
 }
 
