@@ -634,29 +634,14 @@ __device__ __noinline__ void decide_request(
   __shared__ long long SpF[kMaxGamma + 1];  // target row totals F * 2^g
   __shared__ int Spg[kMaxGamma + 1];
   __shared__ ArgMax am_s[kMaxGamma + 1];
-  __shared__ int bad_s;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int L = ell[n];
   const long long r0 = row_off[n];
-  int x_pre = -1;
-  float tx_pre = 0.f, qx_pre = 1.f, u_pre = 1.f;
-  if (wid == 0 && lane < L && L <= gamma && r0 >= 0 && r0 + L < n_rows) {
-    x_pre = tokens[(size_t)n * gamma + lane];
-    if (x_pre >= 0 && x_pre < V) {
-      tx_pre = to_f32<T>(target[(size_t)(r0 + lane) * V + x_pre]);
-      if (!greedy) {
-        qx_pre = q_tok[(size_t)n * gamma + lane];
-        u_pre = u_acc[(size_t)n * gamma + lane];
-      }
-    }
-  }
-  if (tid == 0) {
-    bad_s = (L < 0 || L > gamma || r0 < 0 || r0 + L >= n_rows);
-    if (bad_s) set_flag(status, kFlagRowRange);
-  }
-  __syncthreads();
+  // the same for every thread of the block
+  const bool bad = L < 0 || L > gamma || r0 < 0 || r0 + L >= n_rows;
   int32_t* ot = out_tokens + (size_t)n * (gamma + 1);
-  if (bad_s) {
+  if (bad) {
+    if (tid == 0) set_flag(status, kFlagRowRange);
     for (int j = tid; j <= gamma; j += blockDim.x) ot[j] = -1;
     if (tid == 0) {
       n_acc_out[n] = 0;
@@ -666,6 +651,23 @@ __device__ __noinline__ void decide_request(
     }
     return;
   }
+  // warp 0, lane j < L: drafted token j, its target logit, q, u and q_lse
+  // (the q_lse and the previous token of the rejected position are taken
+  // from these registers later); lane 0 also the anchor.  Issued before the
+  // row totals' loads, which do not wait for them.
+  int x_pre = -1, anc = -1;
+  float tx_pre = 0.f, qx_pre = 1.f, u_pre = 1.f;
+  double ql_pre = 0.0;
+  if (wid == 0 && lane < L) {
+    x_pre = tokens[(size_t)n * gamma + lane];
+    if (!greedy) {
+      qx_pre = q_tok[(size_t)n * gamma + lane];
+      u_pre = u_acc[(size_t)n * gamma + lane];
+      ql_pre = q_lse[(size_t)n * gamma + lane];
+    }
+    if (x_pre >= 0 && x_pre < V) tx_pre = to_f32<T>(target[(size_t)(r0 + lane) * V + x_pre]);
+  }
+  if (wid == 0 && lane == 0 && anchor != nullptr) anc = anchor[n];
   const double* part = row_part + (size_t)n * (gamma + 1) * n_chunks;
   for (int j = wid; j <= L; j += blockDim.x >> 5) {
     const double* pj = part + (size_t)j * n_chunks;
@@ -682,9 +684,9 @@ __device__ __noinline__ void decide_request(
       }
     } else {
       int g;
-      bool bad = false;
-      const long long F = warp_fix_total(pj, n_chunks, &g, &bad);
-      if (bad) set_flag(status, kFlagNonFinite);
+      bool nonfinite = false;
+      const long long F = warp_fix_total(pj, n_chunks, &g, &nonfinite);
+      if (nonfinite) set_flag(status, kFlagNonFinite);
       if (lane == 0) {
         SpF[j] = F;
         Spg[j] = g;
@@ -718,6 +720,10 @@ __device__ __noinline__ void decide_request(
     else if (j == nacc && greedy) v = am_s[nacc].i;
     ot[j] = v;
   }
+  // the rejected position's q_lse and the token before it (nacc < L when a
+  // position is rejected, so both are in lanes below L)
+  const double ql_rej = __shfl_sync(0xffffffffu, ql_pre, nacc & 31);
+  const int x_before = __shfl_sync(0xffffffffu, x_pre, nacc > 0 ? (nacc - 1) & 31 : 0);
   if (lane != 0) return;
   n_acc_out[n] = nacc;
   VerifyState st;
@@ -730,9 +736,8 @@ __device__ __noinline__ void decide_request(
   if (st.mode == 1) {
     // the bias row of the rejected position: the Markov row of the token
     // before it, or (no anchors: the RNN head) the state S[n][nacc]
-    st.prev = anchor == nullptr ? n * gamma + nacc
-                                : (nacc == 0 ? anchor[n] : tokens[(size_t)n * gamma + nacc - 1]);
-    st.iq = exp_neg_pair(q_lse[(size_t)n * gamma + nacc]);
+    st.prev = anchor == nullptr ? n * gamma + nacc : (nacc == 0 ? anc : x_before);
+    st.iq = exp_neg_pair(ql_rej);
   }
   vstate[n] = st;
   prev_out[n] = st.prev;
