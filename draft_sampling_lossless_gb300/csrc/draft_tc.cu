@@ -1424,6 +1424,9 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
 // fp32 rounding of t c or of z + b at the magnitude of the logits) and the
 // 16-token sums are TwoSum trees; acc holds (residual hi, lo, p hi, lo).
 // A NaN group is left out (the pick's recompute flags it).
+// kRagged: the block holds the vocabulary's end (tokens at or past lim
+// weigh 0); kQ: some lane of the warp draws from a residual (else no q is
+// formed).  Template parameters, so that the unrolled pairs carry no branch.
 template <bool kRagged, bool kQ>
 __device__ __forceinline__ void fin_block(const uint32_t (&b)[32], const uint4 (&zq)[4],
                                           const uint4 (&tq)[4], int lim, bool resid, float c12,
